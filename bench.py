@@ -1,0 +1,441 @@
+"""Benchmark of the Fathom decode step on GB300.
+
+One step = one decode step over all layers of the workload: per layer, the
+per-query-group plan, the gather of the planned plane runs (host-resident
+regime), the scan + top-k and the exact sparse attention over the winners,
+for every (sequence, KV head) unit of the layer.  The reported value is
+microseconds per layer-step (whole job: time / (steps * layers * sessions));
+the JSON line also carries the scanned-bytes rate, the roofline of the
+dominant kernel, the end-to-end figure through the C ABI with host buffers,
+the clocks seen and the CPU oracle baseline.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload host_1m]
+                    [--budget 48] [--impl fathom|reference] [--fixed]
+
+Multi-GPU: one process per GPU (torchrun); every rank serves its own session
+(its own seeded store), no data-path collective ("scaling": "weak").
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from bit_plane_kv_gb300 import synth  # noqa: E402
+
+METRIC = "decode-step µs/layer and scan GB/s (% of PCIe/HBM roofline) at 1M tokens"
+CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+# ---------------------------------------------------------------- distributed
+def dist_setup(n_gpus):
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend)
+    if torch.cuda.is_available():
+        torch.cuda.set_device(local)
+    return rank, world
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    def __init__(self):
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={CLOCK_FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", "200"], stdout=self.fh, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self, device_index=0):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        rows = []
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9 or not f[0].isdigit() or int(f[0]) != device_index:
+                continue
+            rows.append(f)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ---------------------------------------------------------------- workload
+class Setup:
+    """Builds the store and rows of one session on this rank (untimed)."""
+
+    def __init__(self, w: synth.Workload, budget: int, rank: int, steps_total: int, fixed: bool):
+        from bit_plane_kv_gb300 import binding as B
+        self.B = B
+        self.w, self.budget, self.fixed = w, budget, fixed
+        # each rank serves its own session: a different seed
+        self.ws_ = synth.shrink(w, seed=w.seed + 1000003 * rank) if rank else w
+        w = self.ws_
+        self.L, self.H = w.layers, w.units_per_layer()
+        self.n, self.G, self.D, self.k = w.n, w.G, w.D, w.k
+        self.nb = B.nblocks(self.n)
+        self.host = w.regime == "host"
+        self.shape = B.make_shape(self.H, self.n, self.D, self.G, self.k, w.n_sink, w.n_recent)
+        dev = "cuda"
+        L, H, n, D, nb = self.L, self.H, self.n, self.D, self.nb
+        t0 = time.time()
+        alloc = (lambda *s, dtype: torch.empty(*s, dtype=dtype, pin_memory=True)) if self.host else \
+                (lambda *s, dtype: torch.empty(*s, dtype=dtype, device=dev))
+        self.planes = alloc(L, H, D, 4, nb, dtype=torch.int64)
+        self.scales = alloc(L, H, D, nb, dtype=torch.int16)
+        self.krows = alloc(L, H, n, D, dtype=torch.bfloat16)
+        self.vrows = alloc(L, H, n, D, dtype=torch.bfloat16)
+        self.var = torch.empty(L, H, D, dtype=torch.float32, device=dev)
+        for l in range(L):
+            units = w.layer_units(l)
+            keys = torch.stack([synth.unit_keys(w, u, dev) for u in units]).to(torch.bfloat16)
+            p, s = B.fathom_quantize_pack(self.shape, keys)
+            calib = torch.stack([synth.unit_calib(w, u, dev) for u in units])
+            _, self.var[l] = B.fathom_calibrate(calib)
+            self.planes[l].copy_(p)
+            self.scales[l].copy_(s)
+            self.krows[l].copy_(keys)
+            del keys, p, s
+            vals = torch.stack([synth.unit_values(w, u, dev) for u in units]).to(torch.bfloat16)
+            self.vrows[l].copy_(vals)
+            del vals
+        torch.cuda.synchronize()
+        log(f"[bench] store built in {time.time() - t0:.1f}s "
+            f"({'pinned host' if self.host else 'HBM'}: store {self.planes.numel() * 8 / 2**30:.2f} GiB "
+            f"+ {self.scales.numel() * 2 / 2**30:.2f} GiB, rows {2 * self.krows.numel() * 2 / 2**30:.2f} GiB)")
+        # queries of every step and layer (device) and their pinned host copy
+        self.Q = torch.stack([torch.stack([torch.stack([synth.unit_query(w, u, dev, step=s + 1) for u in w.layer_units(l)])
+                                           for l in range(L)]) for s in range(steps_total)]).contiguous()
+        self.Qh = torch.empty(self.Q.shape, dtype=self.Q.dtype, pin_memory=True)
+        self.Qh.copy_(self.Q)
+        self.budget_t = torch.full((H,), budget, dtype=torch.int32, device=dev)
+        bmax = 128 if fixed else budget
+        self.stage_w = max(2, min(bmax, 4 * D) * nb + (min(bmax, 4 * D) * nb) % 2)
+        self.stage_s = max(8, (min(bmax, D) * nb + 7) // 8 * 8)
+        self.stage_p = torch.zeros(H, self.stage_w, dtype=torch.int64, device=dev)
+        self.stage_sc = torch.zeros(H, self.stage_s, dtype=torch.int16, device=dev)
+        self.ws = B.alloc_workspace(self.shape, B.WS_SCAN_TOPK)
+        self.aws = B.alloc_workspace(self.shape, B.WS_SPARSE_ATTN)
+        self.depth = torch.empty(H, D, dtype=torch.uint8, device=dev)
+        self.theta = torch.empty(H, dtype=torch.float64, device=dev)
+        self.runs = torch.empty(H, D, 6, dtype=torch.int32, device=dev)
+        self.idx = torch.empty(H, self.G, self.k, dtype=torch.int32, device=dev)
+        self.sel = torch.empty(H, self.G, self.k, dtype=torch.float32, device=dev)
+        self.out = torch.empty(L, H, self.G, D, dtype=torch.float32, device=dev)
+        self.outh = torch.empty(L, H, self.G, D, dtype=torch.float32, pin_memory=True)
+        self.qcur = torch.empty(L, H, self.G, D, dtype=torch.float32, device=dev)
+
+    def layer(self, l, q, ev=None):
+        """One layer of the decode step; ev = optional (start, end) events around the gather
+        (host regime) or the scan (HBM regime)."""
+        B = self.B
+        if self.fixed:
+            B.fathom_plan_fixed(self.shape, q, self.var[l], 32, 4, depth=self.depth, runs=self.runs)
+        else:
+            B.fathom_plan(self.shape, q, self.var[l], self.budget_t, depth=self.depth, theta=self.theta,
+                          runs=self.runs)
+        if self.host:
+            if ev:
+                ev[0].record()
+            B.fathom_gather(self.shape, self.planes[l], self.scales[l], self.runs, self.stage_p, self.stage_sc)
+            if ev:
+                ev[1].record()
+            B.fathom_scan_topk(self.shape, self.stage_p, self.stage_sc, self.runs, q, self.ws,
+                               source=B.SRC_STAGING, topk_idx=self.idx, topk_score=self.sel)
+        else:
+            if ev:
+                ev[0].record()
+            B.fathom_scan_topk(self.shape, self.planes[l], self.scales[l], self.runs, q, self.ws,
+                               topk_idx=self.idx, topk_score=self.sel)
+            if ev:
+                ev[1].record()
+        B.fathom_sparse_attn(self.shape, self.krows[l], self.vrows[l], q, self.idx, self.aws, out=self.out[l])
+
+    def step(self, s, evs=None):
+        for l in range(self.L):
+            self.layer(l, self.Q[s, l], evs[l] if evs else None)
+
+    def step_e2e(self, s):
+        """The same step through the public calls with host buffers: the step's
+        queries come from pinned host memory and the attention outputs go back."""
+        self.qcur.copy_(self.Qh[s], non_blocking=True)
+        for l in range(self.L):
+            self.layer(l, self.qcur[l])
+        self.outh.copy_(self.out, non_blocking=True)
+
+    def planned_bytes(self):
+        """Scanned bytes of the current plan per layer (code planes + active scales), summed over units."""
+        d = self.depth.to(torch.int64)
+        return int(d.sum().item()) * self.nb * 8 + int((d > 0).sum().item()) * self.nb * 2
+
+
+def measure_link_peak():
+    """Pinned host -> device copy bandwidth (copy engine), best of 10 over 1 GiB."""
+    sz = 1 << 30
+    h = torch.empty(sz, dtype=torch.uint8, pin_memory=True)
+    d = torch.empty(sz, dtype=torch.uint8, device="cuda")
+    for _ in range(3):
+        d.copy_(h, non_blocking=True)
+    torch.cuda.synchronize()
+    best = 1e9
+    for _ in range(10):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        d.copy_(h, non_blocking=True)
+        e1.record()
+        torch.cuda.synchronize()
+        best = min(best, e0.elapsed_time(e1) / 1e3)
+    del h, d
+    return sz / best / 1e9
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        return json.load(open(p)), "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}, "fallback"
+
+
+# ---------------------------------------------------------------- CPU oracle baseline
+def oracle_layer_sample(w: synth.Workload, budget: int, unit: int):
+    """Time the CPU oracle on one unit of the workload (the whole per-unit step:
+    plan, gather, scores, selection, attention); returns seconds."""
+    from oracle import oracle as O
+    O.build()
+    n = w.n
+    keys = synth.unit_keys(w, unit, "cpu").to(torch.bfloat16)
+    k32 = keys.float().numpy()
+    kb = keys.view(torch.int16).numpy().view(np.uint16)
+    vb = synth.unit_values(w, unit, "cpu").to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    q = synth.unit_query(w, unit, "cpu", step=1).numpy()
+    _, var = O.calibrate(synth.unit_calib(w, unit, "cpu").numpy())
+    P, S, _ = O.quantize_pack(k32)            # store build: not part of the step
+    t0 = time.perf_counter()
+    depth, theta, _ = O.plan(q, var.astype(np.float32), budget)
+    runs = O.runs(depth, n)
+    if w.regime == "host":
+        nb = (n + 63) // 64
+        sp, ss = O.gather(runs, P, S, int(depth.sum()) * nb, int((depth > 0).sum()) * nb)
+        s = O.scores_staged(runs, sp, ss, depth, q, n)
+    else:
+        s = O.scores(P[None], S[None], depth[None], q[None], n)[0]
+    idx, _ = O.select(s, w.k, w.n_sink, w.n_recent)
+    O.attention(kb, vb, q, idx)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(w, budget, reps=1):
+    secs = [oracle_layer_sample(w, budget, u) for u in w.layer_units(0)[:reps]]
+    per_unit = statistics.mean(secs)
+    us_layer = per_unit * w.units_per_layer() * 1e6
+    return {"value": us_layer, "unit": "µs/layer", "cores": 1, "kind": "oracle",
+            "sample": f"{reps} unit(s) of layer 0 at n={w.n} (plan, gather, scores, top-k, attention; "
+                      f"single-threaded C), scaled x{w.units_per_layer()} units per layer"}
+
+
+# ---------------------------------------------------------------- main
+def run_reference(args, w, rank, world):
+    """The CPU oracle on the same workload, as the reference arm."""
+    if rank != 0:
+        return
+    for _ in range(args.warmup):
+        oracle_layer_sample(w, args.budget, w.layer_units(0)[0])
+    secs = []
+    units = w.layer_units(0)
+    for s in range(args.steps):
+        secs.append(oracle_layer_sample(w, args.budget, units[s % len(units)]))
+    per_unit = statistics.mean(secs)
+    us_layer = per_unit * w.units_per_layer() * 1e6
+    line = {"impl": "reference", "metric": METRIC, "value": us_layer, "unit": "µs/layer",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": us_layer * w.layers / 1e3,
+            "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded Qwen3-8B-shaped keys/queries/values)",
+            "config": {"workload": w.name, "n": w.n, "layers": w.layers, "kv_heads": w.kv_heads, "G": w.G,
+                       "D": w.D, "k": w.k, "budget": args.budget, "regime": w.regime},
+            "cpu_baseline": {"value": us_layer, "unit": "µs/layer", "cores": 1, "kind": "oracle",
+                             "sample": f"one unit per step at n={w.n}, scaled x{w.units_per_layer()} units per layer"},
+            "e2e": {"value": us_layer, "unit": "µs/layer", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--workload", default="host_1m", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--budget", type=int, default=48)
+    ap.add_argument("--fixed", action="store_true", help="the 136-bit fixed-depth comparison plan")
+    ap.add_argument("--impl", default="fathom", choices=["fathom", "reference"])
+    ap.add_argument("--layers", type=int, default=0, help="override the layer count (0: workload's)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    rank, world = dist_setup(args.gpus)
+    w = synth.WORKLOADS[args.workload]
+    if args.layers:
+        w = synth.shrink(w, layers=args.layers)
+    if args.impl == "reference":
+        run_reference(args, w, rank, world)
+        return
+
+    from bit_plane_kv_gb300 import binding as B
+    import __graft_entry__
+    __graft_entry__.build()
+    total_steps = args.warmup + 2 * args.steps
+    st = Setup(w, args.budget, rank, total_steps, args.fixed)
+    link_gbs = measure_link_peak() if st.host else None
+    peaks, peak_src = measured_peaks()
+
+    # warm-up
+    for s in range(args.warmup):
+        st.step(s)
+    torch.cuda.synchronize()
+    plan_bytes = [0] * st.L
+    for l in range(st.L):
+        st.layer(l, st.Q[0, l])
+        torch.cuda.synchronize()
+        plan_bytes[l] = st.planned_bytes()
+
+    # timed region: K steps, events around the dominant kernel of every layer
+    evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(st.L)]
+           for _ in range(args.steps)]
+    clocks = ClockSampler()
+    clocks.start()
+    barrier(world)
+    torch.cuda.synchronize()
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_start.record()
+    for s in range(args.steps):
+        st.step(args.warmup + s, evs[s])
+    t_end.record()
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop(torch.cuda.current_device())
+    elapsed = t_start.elapsed_time(t_end) / 1e3
+    elapsed = max_over_ranks(elapsed, world)
+    kern = [e[0].elapsed_time(e[1]) / 1e3 for row in evs for e in row]
+    kern_avg = statistics.mean(kern)
+
+    # end to end through the public calls with host buffers
+    barrier(world)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for s in range(args.steps):
+        st.step_e2e(args.warmup + args.steps + s)
+    e1.record()
+    torch.cuda.synchronize()
+    e2e_elapsed = max_over_ranks(e0.elapsed_time(e1) / 1e3, world)
+
+    L, H = st.L, st.H
+    layer_steps = args.steps * L * world
+    us_layer = elapsed * 1e6 / layer_steps         # whole job: all ranks' layer-steps
+    e2e_us_layer = e2e_elapsed * 1e6 / layer_steps
+    scanned = statistics.mean(plan_bytes)          # bytes scanned per layer (all units of the layer)
+    bits_per_token = scanned * 8 / (H * st.n)
+    scan_gbs = scanned / (elapsed / (args.steps * L)) / 1e9
+    launches_per_layer = 5                         # plan, gather|-, scan, merge, attention
+    if not st.host:
+        launches_per_layer = 4
+    if st.host:
+        link = link_gbs
+        achieved = scanned / kern_avg / 1e9
+        roof = {"bound": "link", "achieved": achieved, "peak": link, "unit": "GB/s", "frac": achieved / link,
+                "traffic": None, "kernel": "gather_kernel",
+                "peak_source": "measured in this run: pinned host->device copy, 1 GiB, best of 10",
+                "note": "host-link bytes per gather launch (planned plane runs + active-channel scales) / launch time"}
+    else:
+        hbm = peaks["hbm_gbs"]
+        achieved = scanned / kern_avg / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                "traffic": None, "kernel": "scan_kernel+merge_kernel",
+                "peak_source": f"{peak_src} HBM copy peak (MEASURED_PEAKS.json hbm_gbs)"}
+    line = {
+        "metric": METRIC, "value": us_layer, "unit": "µs/layer", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": elapsed / args.steps * 1e3, "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "fp32 (u64 bit planes, fp16 scales, bf16 rows)",
+        "data": "synthetic (seeded Qwen3-8B-shaped keys/queries/values, no trained weights)",
+        "config": {"workload": w.name, "n": w.n, "layers": L, "kv_heads": w.kv_heads, "sessions_per_gpu": w.seqs,
+                   "G": w.G, "D": w.D, "k": w.k, "n_sink": w.n_sink, "n_recent": w.n_recent,
+                   "budget": "fixed 32ch x 4 planes" if args.fixed else args.budget, "regime": w.regime,
+                   "l2": "inputs larger than L2 (store and rows of all layers > 129 MB)"},
+        "scan_gbs": scan_gbs,
+        "scanned_bytes_per_layer": scanned,
+        "scanned_bits_per_token": bits_per_token,
+        "roofline": roof,
+        "e2e": {"value": e2e_us_layer, "unit": "µs/layer",
+                "h2d_bytes_per_step": int(st.Q[0].numel() * 4), "d2h_bytes_per_step": int(st.out.numel() * 4)},
+        "gpu_launches": launches_per_layer * L * args.steps,
+        "clocks": clk,
+    }
+    if st.host:
+        line["link_gbs_peak"] = link_gbs
+        line["link_roofline_frac_of_step"] = (scanned / (link_gbs * 1e9)) / (elapsed / (args.steps * L))
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, args.budget)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,250 @@
+"""Thin Python binding of libfathom (include/fathom.h).
+
+Argument marshalling only: every function takes torch tensors, checks dtype,
+device and contiguity, passes raw pointers and the current CUDA stream to the
+C ABI of the same name, and raises ``FathomError`` on a non-zero status.  All
+computation runs in the CUDA kernels of libfathom; there is no fallback: if
+the library is missing or CUDA is unavailable the call fails.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_build", "libfathom.so")
+
+F32, BF16 = 0, 1
+WS_SCAN_TOPK, WS_SPARSE_ATTN = 0, 1
+SRC_STORE, SRC_STAGING = 0, 1
+MAX_D, MAX_G, MAX_K = 128, 8, 2048
+
+# (name, restype, argtypes) of every symbol include/fathom.h declares
+_vp, _i32, _sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
+
+
+class Shape(ctypes.Structure):
+    _fields_ = [("units", ctypes.c_int32), ("n", ctypes.c_int32), ("D", ctypes.c_int32),
+                ("G", ctypes.c_int32), ("k", ctypes.c_int32), ("n_sink", ctypes.c_int32),
+                ("n_recent", ctypes.c_int32)]
+
+    def __repr__(self):
+        return (f"Shape(units={self.units}, n={self.n}, D={self.D}, G={self.G}, k={self.k}, "
+                f"n_sink={self.n_sink}, n_recent={self.n_recent})")
+
+
+RUN_FIELDS = ("src_word", "n_words", "dst_word", "src_scale", "n_scales", "dst_scale")
+RUN_BYTES = 24
+
+SIGNATURES = {
+    "fathom_calibrate": (ctypes.c_int, [_i32, _i32, _i32, _vp, _vp, _vp, _vp]),
+    "fathom_quantize_pack": (ctypes.c_int, [ctypes.POINTER(Shape), _vp, ctypes.c_int, _vp, _vp, _vp]),
+    "fathom_plan": (ctypes.c_int, [ctypes.POINTER(Shape), _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
+    "fathom_plan_fixed": (ctypes.c_int, [ctypes.POINTER(Shape), _vp, _vp, _i32, _i32, _vp, _vp, _vp]),
+    "fathom_gather": (ctypes.c_int, [ctypes.POINTER(Shape), _vp, _vp, _vp, _vp, _vp, _sz, _sz, _vp]),
+    "fathom_scan_topk": (ctypes.c_int, [ctypes.POINTER(Shape), _vp, _vp, ctypes.c_int, _sz, _sz, _vp,
+                                        _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "fathom_sparse_attn": (ctypes.c_int, [ctypes.POINTER(Shape), _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "fathom_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(Shape), ctypes.c_int]),
+    "fathom_last_error": (ctypes.c_char_p, []),
+    "fathom_version": (ctypes.c_char_p, []),
+}
+
+
+class FathomError(RuntimeError):
+    def __init__(self, name, status, msg):
+        super().__init__(f"{name} failed with status {status}: {msg}")
+        self.status = status
+
+
+_lib = None
+
+
+def lib():
+    """Load libfathom.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"libfathom is not built ({LIB_PATH} missing): run "
+                               "`python -c 'import __graft_entry__ as g; g.build()'`")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(L, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = L
+    return _lib
+
+
+def _call(name, *args):
+    rc = getattr(lib(), name)(*args)
+    if rc != 0:
+        raise FathomError(name, rc, lib().fathom_last_error().decode())
+    return rc
+
+
+def _p(t):
+    if t is None:
+        return None
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(t, name, dtypes, shape=None, dev=True):
+    if t is None:
+        raise ValueError(f"{name} is required")
+    if dtypes and t.dtype not in dtypes:
+        raise TypeError(f"{name}: dtype {t.dtype} not in {dtypes}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dev and not (t.is_cuda or t.is_pinned()):
+        raise ValueError(f"{name} must be a CUDA tensor or pinned host memory")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: shape {tuple(t.shape)} != {tuple(shape)}")
+    return t
+
+
+def make_shape(units, n, D=128, G=4, k=1, n_sink=4, n_recent=32) -> Shape:
+    return Shape(units, n, D, G, k, n_sink, n_recent)
+
+
+def nblocks(n: int) -> int:
+    return (n + 63) // 64
+
+
+def version() -> str:
+    return lib().fathom_version().decode()
+
+
+def workspace_size(shape: Shape, which: int) -> int:
+    return int(lib().fathom_workspace_size(ctypes.byref(shape), which))
+
+
+def alloc_workspace(shape: Shape, which: int, device="cuda") -> torch.Tensor:
+    nbytes = workspace_size(shape, which)
+    if nbytes == 0:
+        raise FathomError("fathom_workspace_size", 1, lib().fathom_last_error().decode())
+    return torch.zeros(nbytes, dtype=torch.uint8, device=device)
+
+
+# ------------------------------------------------------------------ calls
+def fathom_calibrate(calib, mean=None, var=None, stream=None):
+    """calib [U][m][D] fp32 -> (mean [U][D], var [U][D]) fp32 (ddof = 1)."""
+    _check(calib, "calib", (torch.float32,))
+    U, m, D = calib.shape
+    if var is None:
+        var = torch.empty(U, D, dtype=torch.float32, device=calib.device)
+    if mean is None:
+        mean = torch.empty(U, D, dtype=torch.float32, device=calib.device)
+    _call("fathom_calibrate", U, m, D, _p(calib), _p(mean), _p(var), _stream(stream))
+    return mean, var
+
+
+def fathom_quantize_pack(shape: Shape, keys, planes=None, scales=None, stream=None):
+    """keys [U][n][D] fp32 or bf16 -> planes [U][D][4][nb] (int64 storage of u64),
+    scales [U][D][nb] (int16 storage of fp16 bits)."""
+    _check(keys, "keys", (torch.float32, torch.bfloat16, torch.int16))
+    dt = F32 if keys.dtype == torch.float32 else BF16
+    nb = nblocks(shape.n)
+    dev = keys.device
+    if planes is None:
+        planes = torch.empty(shape.units, shape.D, 4, nb, dtype=torch.int64, device=dev)
+    if scales is None:
+        scales = torch.empty(shape.units, shape.D, nb, dtype=torch.int16, device=dev)
+    _call("fathom_quantize_pack", ctypes.byref(shape), _p(keys), dt, _p(planes), _p(scales),
+          _stream(stream))
+    return planes, scales
+
+
+def fathom_plan(shape: Shape, q, var, budget, bracket=None, depth=None, theta=None, runs=None,
+                stream=None):
+    """-> depth [U][D] u8, theta [U] f64, runs [U][D][6] (int32 storage of u32)."""
+    _check(q, "q", (torch.float32,), (shape.units, shape.G, shape.D))
+    _check(var, "var", (torch.float32,), (shape.units, shape.D))
+    _check(budget, "budget", (torch.int32,), (shape.units,))
+    if bracket is not None:
+        _check(bracket, "bracket", (torch.float64,), (shape.units, 2))
+    dev = q.device
+    if depth is None:
+        depth = torch.empty(shape.units, shape.D, dtype=torch.uint8, device=dev)
+    if theta is None:
+        theta = torch.empty(shape.units, dtype=torch.float64, device=dev)
+    if runs is None:
+        runs = torch.empty(shape.units, shape.D, 6, dtype=torch.int32, device=dev)
+    _call("fathom_plan", ctypes.byref(shape), _p(q), _p(var), _p(budget), _p(bracket), _p(depth),
+          _p(theta), _p(runs), _stream(stream))
+    return depth, theta, runs
+
+
+def fathom_plan_fixed(shape: Shape, q, var, n_channels, depth_each, depth=None, runs=None,
+                      stream=None):
+    _check(q, "q", (torch.float32,), (shape.units, shape.G, shape.D))
+    _check(var, "var", (torch.float32,), (shape.units, shape.D))
+    dev = q.device
+    if depth is None:
+        depth = torch.empty(shape.units, shape.D, dtype=torch.uint8, device=dev)
+    if runs is None:
+        runs = torch.empty(shape.units, shape.D, 6, dtype=torch.int32, device=dev)
+    _call("fathom_plan_fixed", ctypes.byref(shape), _p(q), _p(var), int(n_channels), int(depth_each),
+          _p(depth), _p(runs), _stream(stream))
+    return depth, runs
+
+
+def fathom_gather(shape: Shape, store_planes, store_scales, runs, stage_planes, stage_scales,
+                  stream=None):
+    """stage_planes [U][W] int64, stage_scales [U][S] int16 (per-unit strides W, S)."""
+    _check(store_planes, "store_planes", (torch.int64,))
+    _check(store_scales, "store_scales", (torch.int16,))
+    _check(runs, "runs", (torch.int32,), (shape.units, shape.D, 6))
+    _check(stage_planes, "stage_planes", (torch.int64,))
+    _check(stage_scales, "stage_scales", (torch.int16,))
+    W = stage_planes.shape[-1]
+    S = stage_scales.shape[-1]
+    _call("fathom_gather", ctypes.byref(shape), _p(store_planes), _p(store_scales), _p(runs),
+          _p(stage_planes), _p(stage_scales), W, S, _stream(stream))
+    return stage_planes, stage_scales
+
+
+def fathom_scan_topk(shape: Shape, planes, scales, runs, q, workspace, source=SRC_STORE,
+                     topk_idx=None, topk_score=None, scores=None, stream=None):
+    """-> topk_idx [U][G][k] int32 ascending, topk_score [U][G][k] fp32 (scores, if given,
+    receives every token's score [U][G][n])."""
+    _check(planes, "planes", (torch.int64,))
+    _check(scales, "scales", (torch.int16,))
+    _check(runs, "runs", (torch.int32,), (shape.units, shape.D, 6))
+    _check(q, "q", (torch.float32,), (shape.units, shape.G, shape.D))
+    _check(workspace, "workspace", (torch.uint8,))
+    dev = q.device
+    if topk_idx is None:
+        topk_idx = torch.empty(shape.units, shape.G, shape.k, dtype=torch.int32, device=dev)
+    if topk_score is None:
+        topk_score = torch.empty(shape.units, shape.G, shape.k, dtype=torch.float32, device=dev)
+    if scores is not None:
+        _check(scores, "scores", (torch.float32,), (shape.units, shape.G, shape.n))
+    W = planes.shape[-1] if source == SRC_STAGING else 0
+    S = scales.shape[-1] if source == SRC_STAGING else 0
+    _call("fathom_scan_topk", ctypes.byref(shape), _p(planes), _p(scales), int(source), W, S,
+          _p(runs), _p(q), _p(topk_idx), _p(topk_score), _p(scores), _p(workspace),
+          workspace.numel(), _stream(stream))
+    return topk_idx, topk_score
+
+
+def fathom_sparse_attn(shape: Shape, k_rows, v_rows, q, topk_idx, workspace, out=None, stream=None):
+    """k_rows, v_rows [U][n][D] bf16 (device or pinned host) -> out [U][G][D] fp32."""
+    _check(k_rows, "k_rows", (torch.bfloat16, torch.int16), (shape.units, shape.n, shape.D))
+    _check(v_rows, "v_rows", (torch.bfloat16, torch.int16), (shape.units, shape.n, shape.D))
+    _check(q, "q", (torch.float32,), (shape.units, shape.G, shape.D))
+    _check(topk_idx, "topk_idx", (torch.int32,), (shape.units, shape.G, shape.k))
+    _check(workspace, "workspace", (torch.uint8,))
+    if out is None:
+        out = torch.empty(shape.units, shape.G, shape.D, dtype=torch.float32, device=q.device)
+    _call("fathom_sparse_attn", ctypes.byref(shape), _p(k_rows), _p(v_rows), _p(q), _p(topk_idx),
+          _p(out), _p(workspace), workspace.numel(), _stream(stream))
+    return out

@@ -1,0 +1,273 @@
+// api.cu -- the extern "C" boundary of libfathom: argument checks, error
+// reporting and workspace layouts.  All arithmetic lives in the kernels.
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "fathom_internal.cuh"
+
+namespace fathom {
+
+static thread_local char g_err[512] = "";
+
+void set_error(const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof(g_err), fmt, ap);
+    va_end(ap);
+}
+
+int launch_status(const char *what) {
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) {
+        set_error("%s: %s", what, cudaGetErrorString(e));
+        return FATHOM_ECUDA;
+    }
+    return FATHOM_OK;
+}
+
+static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+bool smem_attr_needed(const void *func, size_t bytes) {
+    struct Entry { const void *f; int dev; size_t bytes; };
+    static std::mutex mu;
+    static Entry table[64];
+    static int used = 0;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < used; ++i) {
+        if (table[i].f == func && table[i].dev == dev) {
+            if (table[i].bytes >= bytes) return false;
+            table[i].bytes = bytes;
+            return true;
+        }
+    }
+    if (used < 64) table[used++] = Entry{func, dev, bytes};
+    return true;
+}
+
+ScanGrid scan_grid(int units, int n) {
+    // About four resident CTAs per SM on a 152-SM part; at least one 32-block
+    // sub-chunk per CTA.
+    const int target_ctas = 4 * 152;
+    int nb = num_blocks(n);
+    int max_chunks = (nb + kSubBlocks - 1) / kSubBlocks;
+    int chunks = (target_ctas + units - 1) / units;
+    if (chunks > max_chunks) chunks = max_chunks;
+    if (chunks < 1) chunks = 1;
+    int cb = (nb + chunks - 1) / chunks;
+    cb = (cb + kSubBlocks - 1) / kSubBlocks * kSubBlocks;
+    ScanGrid g;
+    g.chunk_blocks = cb;
+    g.chunks = (nb + cb - 1) / cb;
+    return g;
+}
+
+int scan_cand_cap(const fathom_shape &s) {
+    Forced f = forced_range(s.n, s.n_sink, s.n_recent);
+    int k_sel = s.k - f.nf;
+    if (k_sel < 0) k_sel = 0;
+    int cap = k_sel + kPruneSlack + 2 * kSubTokens;
+    return (cap + 255) / 256 * 256;
+}
+
+ScanWorkspace scan_workspace_layout(const fathom_shape &s) {
+    ScanGrid g = scan_grid(s.units, s.n);
+    Forced f = forced_range(s.n, s.n_sink, s.n_recent);
+    ScanWorkspace w;
+    size_t ctas = (size_t)s.units * g.chunks;
+    w.cand_off = 0;
+    w.cnt_off = align256(w.cand_off + ctas * s.G * 2 * (size_t)scan_cand_cap(s) * sizeof(uint64_t));
+    w.forced_off = align256(w.cnt_off + ctas * s.G * sizeof(int32_t));
+    w.total = align256(w.forced_off + (size_t)s.units * s.G * (f.nf > 0 ? f.nf : 1) * sizeof(float));
+    return w;
+}
+
+AttnWorkspace attn_workspace_layout(const fathom_shape &s) {
+    AttnWorkspace w;
+    int rows = s.G * s.k;
+    w.splits = (rows + kAttnRows - 1) / kAttnRows;
+    if (w.splits < 1) w.splits = 1;
+    w.part_off = 0;
+    w.ticket_off = align256((size_t)s.units * w.splits * s.G * (s.D + 2) * sizeof(float));
+    w.total = align256(w.ticket_off + (size_t)s.units * sizeof(uint32_t));
+    return w;
+}
+
+}  // namespace fathom
+
+using namespace fathom;
+
+static int check_shape(const fathom_shape *s, bool need_select) {
+    if (!s) { set_error("shape is NULL"); return FATHOM_EINVAL; }
+    if (s->units < 1) { set_error("units must be >= 1 (got %d)", s->units); return FATHOM_EINVAL; }
+    if (s->n < 1 || s->n > (1 << 28)) { set_error("n must be in [1, 2^28] (got %d)", s->n); return FATHOM_EINVAL; }
+    if (s->D < 1 || s->D > FATHOM_MAX_D) { set_error("D must be in [1, %d] (got %d)", FATHOM_MAX_D, s->D); return FATHOM_EINVAL; }
+    if (!(s->G == 1 || s->G == 2 || s->G == 4 || s->G == 8)) { set_error("G must be 1, 2, 4 or 8 (got %d)", s->G); return FATHOM_EINVAL; }
+    if ((size_t)s->units * s->D * FATHOM_PLANES * (size_t)num_blocks(s->n) >= ((size_t)1 << 40)) {
+        set_error("store too large"); return FATHOM_EINVAL;
+    }
+    if (need_select) {
+        if (s->n_sink < 0 || s->n_recent < 0) { set_error("n_sink and n_recent must be >= 0"); return FATHOM_EINVAL; }
+        if (s->k < 1 || s->k > s->n || s->k > FATHOM_MAX_K) {
+            set_error("k must be in [1, min(n, %d)] (got k=%d, n=%d)", FATHOM_MAX_K, s->k, s->n);
+            return FATHOM_EINVAL;
+        }
+        Forced f = forced_range(s->n, s->n_sink, s->n_recent);
+        if (f.nf > s->k) {
+            set_error("k=%d is smaller than the %d forced tokens", s->k, f.nf);
+            return FATHOM_EINVAL;
+        }
+    }
+    return FATHOM_OK;
+}
+
+#define NONNULL(p)                                               \
+    do {                                                         \
+        if (!(p)) { set_error("%s is NULL", #p); return FATHOM_EINVAL; } \
+    } while (0)
+
+extern "C" {
+
+const char *fathom_last_error(void) { return g_err; }
+
+const char *fathom_version(void) { return "fathom-gb300 0.1 (sm_103a)"; }
+
+int fathom_calibrate(int32_t units, int32_t m, int32_t D, const float *calib, float *mean_out,
+                     float *var_out, void *stream) {
+    g_err[0] = 0;
+    if (units < 1 || m < 2 || D < 1 || D > FATHOM_MAX_D) {
+        set_error("calibrate: need units >= 1, m >= 2, 1 <= D <= %d", FATHOM_MAX_D);
+        return FATHOM_EINVAL;
+    }
+    NONNULL(calib);
+    NONNULL(var_out);
+    return launch_calibrate(units, m, D, calib, mean_out, var_out, (cudaStream_t)stream);
+}
+
+int fathom_quantize_pack(const fathom_shape *shape, const void *keys, int keys_dtype,
+                         uint64_t *planes, uint16_t *scales, void *stream) {
+    g_err[0] = 0;
+    int rc = check_shape(shape, false);
+    if (rc) return rc;
+    if (keys_dtype != FATHOM_F32 && keys_dtype != FATHOM_BF16) {
+        set_error("keys_dtype must be FATHOM_F32 or FATHOM_BF16"); return FATHOM_EINVAL;
+    }
+    NONNULL(keys);
+    NONNULL(planes);
+    NONNULL(scales);
+    return launch_quantize(*shape, keys, keys_dtype, planes, scales, (cudaStream_t)stream);
+}
+
+int fathom_plan(const fathom_shape *shape, const float *q, const float *var, const int32_t *budget,
+                const double *bracket, uint8_t *depth, double *theta, fathom_run *runs,
+                void *stream) {
+    g_err[0] = 0;
+    int rc = check_shape(shape, false);
+    if (rc) return rc;
+    NONNULL(q);
+    NONNULL(var);
+    NONNULL(budget);
+    NONNULL(depth);
+    NONNULL(theta);
+    NONNULL(runs);
+    return launch_plan(*shape, q, var, budget, bracket, depth, theta, runs, (cudaStream_t)stream);
+}
+
+int fathom_plan_fixed(const fathom_shape *shape, const float *q, const float *var,
+                      int32_t n_channels, int32_t depth_each, uint8_t *depth, fathom_run *runs,
+                      void *stream) {
+    g_err[0] = 0;
+    int rc = check_shape(shape, false);
+    if (rc) return rc;
+    if (n_channels < 1 || n_channels > shape->D || depth_each < 1 || depth_each > 4) {
+        set_error("plan_fixed: need 1 <= n_channels <= D and 1 <= depth_each <= 4");
+        return FATHOM_EINVAL;
+    }
+    NONNULL(q);
+    NONNULL(var);
+    NONNULL(depth);
+    NONNULL(runs);
+    return launch_plan_fixed(*shape, q, var, n_channels, depth_each, depth, runs,
+                             (cudaStream_t)stream);
+}
+
+int fathom_gather(const fathom_shape *shape, const uint64_t *store_planes,
+                  const uint16_t *store_scales, const fathom_run *runs, uint64_t *stage_planes,
+                  uint16_t *stage_scales, size_t stage_words, size_t stage_scales_n, void *stream) {
+    g_err[0] = 0;
+    int rc = check_shape(shape, false);
+    if (rc) return rc;
+    NONNULL(store_planes);
+    NONNULL(store_scales);
+    NONNULL(runs);
+    NONNULL(stage_planes);
+    NONNULL(stage_scales);
+    if (stage_words < 1 || stage_scales_n < 1) { set_error("empty staging area"); return FATHOM_EINVAL; }
+    return launch_gather(*shape, store_planes, store_scales, runs, stage_planes, stage_scales,
+                         stage_words, stage_scales_n, (cudaStream_t)stream);
+}
+
+size_t fathom_workspace_size(const fathom_shape *shape, int which) {
+    if (check_shape(shape, true)) return 0;
+    if (which == FATHOM_WS_SCAN_TOPK) return scan_workspace_layout(*shape).total;
+    if (which == FATHOM_WS_SPARSE_ATTN) return attn_workspace_layout(*shape).total;
+    return 0;
+}
+
+int fathom_scan_topk(const fathom_shape *shape, const uint64_t *planes, const uint16_t *scales,
+                     int source, size_t stage_words, size_t stage_scales_n, const fathom_run *runs,
+                     const float *q, int32_t *topk_idx, float *topk_score, float *scores_opt,
+                     void *workspace, size_t workspace_bytes, void *stream) {
+    g_err[0] = 0;
+    int rc = check_shape(shape, true);
+    if (rc) return rc;
+    if (source != FATHOM_SRC_STORE && source != FATHOM_SRC_STAGING) {
+        set_error("source must be FATHOM_SRC_STORE or FATHOM_SRC_STAGING"); return FATHOM_EINVAL;
+    }
+    if (source == FATHOM_SRC_STAGING && (stage_words < 1 || stage_scales_n < 1)) {
+        set_error("staging strides must be >= 1"); return FATHOM_EINVAL;
+    }
+    NONNULL(planes);
+    NONNULL(scales);
+    NONNULL(runs);
+    NONNULL(q);
+    NONNULL(topk_idx);
+    NONNULL(topk_score);
+    NONNULL(workspace);
+    size_t need = scan_workspace_layout(*shape).total;
+    if (workspace_bytes < need) {
+        set_error("scan_topk workspace too small: %zu < %zu bytes", workspace_bytes, need);
+        return FATHOM_ENOMEM;
+    }
+    if (((uintptr_t)workspace & 255) != 0) { set_error("workspace must be 256-byte aligned"); return FATHOM_EINVAL; }
+    return launch_scan_topk(*shape, planes, scales, source, stage_words, stage_scales_n, runs, q,
+                            topk_idx, topk_score, scores_opt, workspace, (cudaStream_t)stream);
+}
+
+int fathom_sparse_attn(const fathom_shape *shape, const uint16_t *k_rows, const uint16_t *v_rows,
+                       const float *q, const int32_t *topk_idx, float *out, void *workspace,
+                       size_t workspace_bytes, void *stream) {
+    g_err[0] = 0;
+    int rc = check_shape(shape, true);
+    if (rc) return rc;
+    NONNULL(k_rows);
+    NONNULL(v_rows);
+    NONNULL(q);
+    NONNULL(topk_idx);
+    NONNULL(out);
+    NONNULL(workspace);
+    size_t need = attn_workspace_layout(*shape).total;
+    if (workspace_bytes < need) {
+        set_error("sparse_attn workspace too small: %zu < %zu bytes", workspace_bytes, need);
+        return FATHOM_ENOMEM;
+    }
+    if (((uintptr_t)workspace & 255) != 0) { set_error("workspace must be 256-byte aligned"); return FATHOM_EINVAL; }
+    return launch_sparse_attn(*shape, k_rows, v_rows, q, topk_idx, out, workspace,
+                              (cudaStream_t)stream);
+}
+
+}  // extern "C"

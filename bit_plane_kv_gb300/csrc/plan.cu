@@ -1,0 +1,195 @@
+// plan.cu -- per-query-group read plan (Fathom §3.3 per-query read depth,
+// §3.6 fixed-size run list).
+//
+// One warp per unit; lane l owns channels l, l+32, l+64, l+96.
+//   g_j  = (sum_h q_hj^2) * var_j              (fp64, h ascending)
+//   t_j(theta) = #{m in 0..3 : g_j >= theta * 2^(2m+1)}
+// which is clip(round(log4(g_j / theta)), 0, 4) with ties rounding up, written
+// with compares against exact power-of-two multiples of theta so that no
+// logarithm (and no rounding of one) enters a decision.  theta comes from 30
+// steps of geometric bisection mid = sqrt(lo * hi) that keep hi feasible
+// (sum_j t_j(hi) <= B); the plan is t(hi).  Every fp64 operation is an
+// explicitly rounded IEEE operation (no contraction), so the result is
+// reproducible bit for bit on any IEEE machine.  The whole plan stays on the
+// device: the run list has one slot per channel (zero length when t_j = 0),
+// so nothing needs to come back to the host.
+#include "fathom_internal.cuh"
+
+namespace fathom {
+
+constexpr int kPlanWarps = 4;
+constexpr int kCh = FATHOM_MAX_D / 32;   // channels per lane
+
+__device__ __forceinline__ int depth_of(double g, double theta) {
+    int t = 0;
+#pragma unroll
+    for (int m = 0; m < 4; ++m) t += (g >= __dmul_rn(theta, (double)(2 << (2 * m)))) ? 1 : 0;
+    return t;
+}
+
+__device__ __forceinline__ int warp_sum(int v) {
+#pragma unroll
+    for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+__device__ __forceinline__ void importance(int u, int lane, int D, int G, const float *q,
+                                           const float *var, double (&g)[kCh]) {
+#pragma unroll
+    for (int c = 0; c < kCh; ++c) {
+        const int j = lane + 32 * c;
+        double gj = 0.0;
+        if (j < D) {
+            double s = 0.0;
+            for (int h = 0; h < G; ++h) {
+                const double x = (double)q[((size_t)u * G + h) * D + j];
+                s = __dadd_rn(s, __dmul_rn(x, x));
+            }
+            gj = __dmul_rn(s, (double)var[(size_t)u * D + j]);
+        }
+        g[c] = gj;
+    }
+}
+
+// Writes depth and the run list of one unit from per-lane depths t[c].
+__device__ __forceinline__ void write_plan(int u, int lane, int D, int nb, const int (&t)[kCh],
+                                           uint8_t *depth, fathom_run *runs) {
+    uint32_t carry_w = 0, carry_s = 0;
+#pragma unroll
+    for (int c = 0; c < kCh; ++c) {
+        const int j = lane + 32 * c;
+        const int tj = (j < D) ? t[c] : 0;
+        const int act = tj > 0 ? 1 : 0;
+        // inclusive warp scans of t and of "active"
+        int st = tj, sa = act;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int yt = __shfl_up_sync(0xffffffffu, st, o);
+            const int ya = __shfl_up_sync(0xffffffffu, sa, o);
+            if (lane >= o) { st += yt; sa += ya; }
+        }
+        if (j < D) {
+            depth[(size_t)u * D + j] = (uint8_t)tj;
+            fathom_run r;
+            r.src_word = (uint32_t)j * FATHOM_PLANES * nb;
+            r.n_words = (uint32_t)tj * nb;
+            r.dst_word = (carry_w + (uint32_t)(st - tj)) * nb;
+            r.src_scale = (uint32_t)j * nb;
+            r.n_scales = act ? (uint32_t)nb : 0u;
+            r.dst_scale = (carry_s + (uint32_t)(sa - act)) * nb;
+            runs[(size_t)u * D + j] = r;
+        }
+        carry_w += (uint32_t)__shfl_sync(0xffffffffu, st, 31);
+        carry_s += (uint32_t)__shfl_sync(0xffffffffu, sa, 31);
+    }
+}
+
+__global__ void __launch_bounds__(32 * kPlanWarps)
+plan_kernel(int units, int n, int D, int G, const float *__restrict__ q,
+            const float *__restrict__ var, const int32_t *__restrict__ budget,
+            const double *__restrict__ bracket, uint8_t *__restrict__ depth,
+            double *__restrict__ theta_out, fathom_run *__restrict__ runs) {
+    const int u = blockIdx.x * kPlanWarps + threadIdx.x / 32;
+    const int lane = threadIdx.x & 31;
+    if (u >= units) return;
+    const int nb = num_blocks(n);
+    double g[kCh];
+    importance(u, lane, D, G, q, var, g);
+    const int B = budget[u];
+
+    auto total = [&](double th) {
+        int s = 0;
+#pragma unroll
+        for (int c = 0; c < kCh; ++c) s += depth_of(g[c], th);
+        return warp_sum(s);
+    };
+
+    double lo, hi;
+    bool bisect = true;
+    if (bracket) {
+        lo = bracket[2 * (size_t)u];
+        hi = bracket[2 * (size_t)u + 1];
+    } else {
+        double gmax = 0.0, gmin = CUDART_INF;
+#pragma unroll
+        for (int c = 0; c < kCh; ++c) {
+            gmax = fmax(gmax, g[c]);
+            if (g[c] > 0.0) gmin = fmin(gmin, g[c]);
+        }
+#pragma unroll
+        for (int o = 16; o; o >>= 1) {
+            gmax = fmax(gmax, __shfl_xor_sync(0xffffffffu, gmax, o));
+            gmin = fmin(gmin, __shfl_xor_sync(0xffffffffu, gmin, o));
+        }
+        if (gmax == 0.0) {                       // nothing worth reading
+            int t0[kCh] = {0};
+            write_plan(u, lane, D, nb, t0, depth, runs);
+            if (lane == 0) theta_out[u] = 0.0;
+            return;
+        }
+        hi = gmax;
+        lo = __dmul_rn(gmin, 1.0 / 512.0);        // exact power-of-two scaling
+        if (total(lo) <= B) { hi = lo; bisect = false; }   // budget not binding
+    }
+    if (bisect) {
+        for (int it = 0; it < 30; ++it) {
+            const double mid = __dsqrt_rn(__dmul_rn(lo, hi));
+            if (total(mid) <= B) hi = mid; else lo = mid;
+        }
+    }
+    int t[kCh];
+#pragma unroll
+    for (int c = 0; c < kCh; ++c) t[c] = depth_of(g[c], hi);
+    write_plan(u, lane, D, nb, t, depth, runs);
+    if (lane == 0) theta_out[u] = hi;
+}
+
+// Fixed-depth comparison plan: the n_sel channels of largest g (ties: lower
+// index) at depth t_fixed.
+__global__ void __launch_bounds__(32 * kPlanWarps)
+plan_fixed_kernel(int units, int n, int D, int G, const float *__restrict__ q,
+                  const float *__restrict__ var, int n_sel, int t_fixed,
+                  uint8_t *__restrict__ depth, fathom_run *__restrict__ runs) {
+    __shared__ double gs[kPlanWarps][FATHOM_MAX_D];
+    const int w = threadIdx.x / 32;
+    const int u = blockIdx.x * kPlanWarps + w;
+    const int lane = threadIdx.x & 31;
+    if (u >= units) return;   // whole warps exit together; no block barrier below
+    const int nb = num_blocks(n);
+    double g[kCh];
+    importance(u, lane, D, G, q, var, g);
+#pragma unroll
+    for (int c = 0; c < kCh; ++c) gs[w][lane + 32 * c] = g[c];
+    __syncwarp();
+    int t[kCh];
+#pragma unroll
+    for (int c = 0; c < kCh; ++c) {
+        const int j = lane + 32 * c;
+        int better = 0;
+        for (int i = 0; i < D; ++i) {
+            const double gi = gs[w][i];
+            better += (gi > g[c] || (gi == g[c] && i < j)) ? 1 : 0;
+        }
+        t[c] = (j < D && better < n_sel) ? t_fixed : 0;
+    }
+    write_plan(u, lane, D, nb, t, depth, runs);
+}
+
+int launch_plan(const fathom_shape &s, const float *q, const float *var, const int32_t *budget,
+                const double *bracket, uint8_t *depth, double *theta, fathom_run *runs,
+                cudaStream_t st) {
+    const int grid = (s.units + kPlanWarps - 1) / kPlanWarps;
+    plan_kernel<<<grid, 32 * kPlanWarps, 0, st>>>(s.units, s.n, s.D, s.G, q, var, budget, bracket,
+                                                  depth, theta, runs);
+    return launch_status("plan_kernel");
+}
+
+int launch_plan_fixed(const fathom_shape &s, const float *q, const float *var, int n_sel,
+                      int t_fixed, uint8_t *depth, fathom_run *runs, cudaStream_t st) {
+    const int grid = (s.units + kPlanWarps - 1) / kPlanWarps;
+    plan_fixed_kernel<<<grid, 32 * kPlanWarps, 0, st>>>(s.units, s.n, s.D, s.G, q, var, n_sel,
+                                                        t_fixed, depth, runs);
+    return launch_status("plan_fixed_kernel");
+}
+
+}  // namespace fathom

@@ -1,0 +1,214 @@
+/*
+ * fathom.h -- C ABI of libfathom, a GB300 (sm_103a) implementation of the
+ * Fathom variable-depth bit-plane key scan for top-k sparse decode attention.
+ *
+ * Source of the method: the review page "Fathom: 쿼리마다 깊이를 바꾸는
+ * 스캔으로 1M 토큰 디코딩을 1.67배 빠르게 하다" (jaehun.me, a summary of the
+ * Fathom paper).  Section numbers below are the paper's, as that page cites
+ * them (§2 evaluation protocol, §3.2 bit-plane K cache, §3.3 per-query read
+ * depth, §3.5 rotated basis, §3.6 host-resident store, Appx. A toy example).
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * - A "unit" is one independent (sequence, layer, KV head) triple; units are
+ *   packed row-major in that order and every array below has the unit as its
+ *   outermost index.
+ * - n tokens per unit, nb = ceil(n / 64) blocks of 64 tokens, D channels
+ *   (1..128), G query heads sharing the KV head (1, 2, 4 or 8).
+ * - Pointers are raw addresses.  "device" means device memory or any memory
+ *   the GPU can load from directly (pinned host memory registered with CUDA:
+ *   with unified addressing its host pointer is also its device pointer).
+ *   The caller owns and allocates every buffer; the library never allocates.
+ * - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *   stream).  Every call only enqueues work on that stream: no host
+ *   synchronisation, no host read of device results.  Results are valid once
+ *   the stream reaches them.
+ * - Every call returns a fathom_status.  Argument errors return FATHOM_EINVAL
+ *   before anything is enqueued; CUDA launch errors return FATHOM_ECUDA.
+ *   fathom_last_error() returns the calling thread's last message.  Nothing
+ *   throws across this ABI and nothing aborts the process.
+ * - Inputs are never modified.  Outputs may not alias inputs.
+ */
+#ifndef FATHOM_H
+#define FATHOM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define FATHOM_MAX_D 128
+#define FATHOM_MAX_G 8
+#define FATHOM_MAX_K 2048
+#define FATHOM_PLANES 4
+#define FATHOM_BLOCK 64
+
+typedef enum {
+    FATHOM_OK = 0,
+    FATHOM_EINVAL = 1,   /* bad argument; nothing was enqueued */
+    FATHOM_ECUDA = 2,    /* a CUDA call or launch failed */
+    FATHOM_ENOMEM = 3,   /* a caller-provided buffer is too small */
+    FATHOM_ETIMEOUT = 4  /* reserved for bounded device waits */
+} fathom_status;
+
+typedef enum { FATHOM_F32 = 0, FATHOM_BF16 = 1 } fathom_dtype;
+
+typedef enum { FATHOM_WS_SCAN_TOPK = 0, FATHOM_WS_SPARSE_ATTN = 1 } fathom_workspace_kind;
+
+/* Which copy of the bit-plane store a scan reads. */
+typedef enum {
+    FATHOM_SRC_STORE = 0,   /* the store in place, layout [U][D][4][nb] (HBM-resident regime) */
+    FATHOM_SRC_STAGING = 1  /* the staging area written by fathom_gather (host-resident regime) */
+} fathom_source;
+
+/* One slot of the fixed-size run list (§3.6): one per channel, zero length
+ * when the channel is inactive.  Offsets count 64-bit plane words or fp16
+ * scales, relative to the unit's store (src) and the unit's staging area
+ * (dst).  Destinations are contiguous in ascending channel order. */
+typedef struct {
+    uint32_t src_word;   /* = j * 4 * nb: first plane word of channel j in the store */
+    uint32_t n_words;    /* = t_j * nb: channel j's first t_j planes, one contiguous run */
+    uint32_t dst_word;   /* = sum_{j' < j} t_j' * nb */
+    uint32_t src_scale;  /* = j * nb */
+    uint32_t n_scales;   /* = nb if t_j > 0 else 0 */
+    uint32_t dst_scale;  /* = nb * #{j' < j : t_j' > 0} */
+} fathom_run;
+
+typedef struct {
+    int32_t units;    /* >= 1 */
+    int32_t n;        /* tokens per unit, 1 .. 2^28 */
+    int32_t D;        /* channels, 1 .. 128 */
+    int32_t G;        /* query heads per KV head: 1, 2, 4 or 8 */
+    int32_t k;        /* tokens kept per query head, |forced| <= k <= min(n, 2048) */
+    int32_t n_sink;   /* first tokens always kept (the pages use 4) */
+    int32_t n_recent; /* last tokens always kept (the pages use 32) */
+} fathom_shape;
+
+/* ---------------------------------------------------------------------- */
+
+/* Calibration statistics (§3.3: Var(k_j) is measured once on calibration
+ * keys).  For each unit and channel: mean and unbiased (ddof = 1) variance
+ * over m calibration rows, accumulated in fp64 in row order and rounded to
+ * fp32 once.
+ *   calib [units][m][D] fp32 (device); mean_out (may be NULL), var_out
+ *   [units][D] fp32 (device).  m >= 2. */
+int fathom_calibrate(int32_t units, int32_t m, int32_t D, const float *calib,
+                     float *mean_out, float *var_out, void *stream);
+
+/* Quantise and pack the K store (§3.2).  Per unit, channel j and 64-token
+ * block beta: a = max_{i in beta} |k_ij| stored as fp16 (round to nearest
+ * even, saturating at 65504); s = a / 8; code c = clip(floor(k / s), -8, 7) + 8
+ * in [0, 16) (floor of the exact quotient; a == 0 gives code 8); bit p
+ * (p = 0 the MSB) of the 64 codes of the block forms plane word P[beta][j][p],
+ * token 64*beta + i at bit i.  Tail tokens past n have all-zero bits and do
+ * not enter a.  Reading the first t planes of a channel then gives the t-bit
+ * mid-rise code c >> (4 - t).
+ *   keys   [units][n][D], fp32 or bf16 (keys_dtype), device
+ *   planes [units][D][4][nb] uint64 (out, device): channel j's planes 0..3
+ *          each contiguous over the sequence (§3.6)
+ *   scales [units][D][nb] fp16 bit patterns (out, device)
+ * Uses shape->units, n, D. */
+int fathom_quantize_pack(const fathom_shape *shape, const void *keys, int keys_dtype,
+                         uint64_t *planes, uint16_t *scales, void *stream);
+
+/* Per-query-group read plan (§3.3, §3.6).  Per unit:
+ *   g_j = (sum_h q_hj^2) * var_j  (fp64, h ascending);
+ *   depth t_j(theta) = #{m in 0..3 : g_j >= theta * 2^(2m+1)}
+ *                    = clip(round(log4(g_j / theta)), 0, 4)  (ties round up);
+ *   theta from 30 steps of geometric bisection mid = sqrt(lo * hi) on
+ *   [lo, hi], keeping hi feasible (sum_j t_j(hi) <= budget), and the result is
+ *   t(hi), theta = hi: the smallest probed theta that fits the budget.
+ *   bracket NULL: hi = max_j g_j, lo = min_{g_j > 0} g_j / 512; if t(lo) fits
+ *   the budget the bisection is skipped and theta = lo (budget not binding);
+ *   if every g_j is 0, all depths are 0 and theta = 0.
+ *   bracket non-NULL: [units][2] {lo, hi} fp64 used as given (hi must fit).
+ * Every decision uses only IEEE-exact fp64 operations in a fixed order, so the
+ * plan is reproducible bit for bit.
+ *   q [units][G][D] fp32, var [units][D] fp32, budget [units] int32 >= 0
+ *   depth [units][D] uint8 (out), theta [units] fp64 (out),
+ *   runs [units][D] fathom_run (out; see fathom_run).
+ * All pointers device. */
+int fathom_plan(const fathom_shape *shape, const float *q, const float *var,
+                const int32_t *budget, const double *bracket, uint8_t *depth,
+                double *theta, fathom_run *runs, void *stream);
+
+/* Fixed-depth comparison plan: the n_channels channels of largest g_j (ties:
+ * lower j) at depth depth_each, all others 0 (32 channels x 4 planes is the
+ * byte-equivalent of a 136-bit scan).  Outputs as fathom_plan; theta is not
+ * written.  1 <= n_channels <= D, 1 <= depth_each <= 4. */
+int fathom_plan_fixed(const fathom_shape *shape, const float *q, const float *var,
+                      int32_t n_channels, int32_t depth_each, uint8_t *depth,
+                      fathom_run *runs, void *stream);
+
+/* Gather (§3.6): for every unit and every channel, copy run[j].n_words plane
+ * words from store_planes + src_word to stage_planes + dst_word and
+ * run[j].n_scales scales likewise; zero-length runs copy nothing, so the run
+ * list needs no host synchronisation.  The store is typically pinned host
+ * memory read over the host link; staging is device memory.
+ *   store_planes/store_scales: the store as written by fathom_quantize_pack
+ *   runs [units][D] from fathom_plan / fathom_plan_fixed
+ *   stage_planes [units][stage_words], stage_scales [units][stage_nscales]
+ *   (device): per-unit strides in words / scales
+ * Runs whose destination would pass the unit's stage_words / stage_nscales
+ * are clipped at that end (a plan that fits its budget B never is when
+ * stage_words >= B * nb and stage_nscales >= min(B, D) * nb). */
+int fathom_gather(const fathom_shape *shape, const uint64_t *store_planes,
+                  const uint16_t *store_scales, const fathom_run *runs,
+                  uint64_t *stage_planes, uint16_t *stage_scales, size_t stage_words,
+                  size_t stage_nscales, void *stream);
+
+/* Scan and select (§3.2, §3.3, §2).  For every unit, query head h and token i:
+ *   s_h(i) = sum_{j : t_j > 0} q_hj * (c_t + 0.5 - 2^(t-1)) * a / 2^(t-1)
+ * with t = t_j, c_t the code prefix read from channel j's first t planes and
+ * a its block scale, accumulated in fp32 (one pass over the planned planes
+ * serves all G heads).  Then per head the kept set is the first n_sink and
+ * the last n_recent tokens plus the k - |forced| other tokens of largest
+ * s_h (ties: lower index), written in ascending token order with their
+ * scores.
+ *   planes/scales: source (FATHOM_SRC_STORE: the store [U][D][4][nb] /
+ *   [U][D][nb]; FATHOM_SRC_STAGING: staging [U][stage_words] /
+ *   [U][stage_nscales] laid out by the run list; the strides are ignored
+ *   for FATHOM_SRC_STORE)
+ *   runs [units][D], q [units][G][D] fp32
+ *   topk_idx [units][G][k] int32 (out), topk_score [units][G][k] fp32 (out)
+ *   scores_opt NULL, or [units][G][n] fp32 (out): every token's score
+ *   workspace: device scratch of at least
+ *   fathom_workspace_size(shape, FATHOM_WS_SCAN_TOPK) bytes, 256-byte
+ *   aligned, zero-filled before its first use; each call leaves it ready for
+ *   the next call.  Calls that share a workspace must not overlap in time. */
+int fathom_scan_topk(const fathom_shape *shape, const uint64_t *planes,
+                     const uint16_t *scales, int source, size_t stage_words,
+                     size_t stage_nscales, const fathom_run *runs, const float *q,
+                     int32_t *topk_idx, float *topk_score, float *scores_opt,
+                     void *workspace, size_t workspace_bytes, void *stream);
+
+/* Exact sparse attention over the winners (§1, §2, §3.1).  Per unit, the
+ * union of the G heads' kept sets is fetched once at full precision (bf16 K
+ * and V rows; at most G * k rows), and per head
+ *   o_h = sum_{i in S_h} softmax_i(q_h . k_i / sqrt(D)) v_i
+ * with fp32 accumulation and no mass for unselected tokens.
+ *   k_rows, v_rows [units][n][D] bf16 bit patterns (device or pinned host)
+ *   q [units][G][D] fp32, topk_idx [units][G][k] int32, each row ascending
+ *   out [units][G][D] fp32 (out)
+ *   workspace: at least fathom_workspace_size(shape, FATHOM_WS_SPARSE_ATTN)
+ *   bytes, same rules as fathom_scan_topk's. */
+int fathom_sparse_attn(const fathom_shape *shape, const uint16_t *k_rows,
+                       const uint16_t *v_rows, const float *q, const int32_t *topk_idx,
+                       float *out, void *workspace, size_t workspace_bytes, void *stream);
+
+/* Workspace bytes a call needs for this shape (0 if the shape is invalid). */
+size_t fathom_workspace_size(const fathom_shape *shape, int which);
+
+/* The calling thread's last error message ("" if none). */
+const char *fathom_last_error(void);
+
+/* Library version string. */
+const char *fathom_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FATHOM_H */

@@ -1,0 +1,94 @@
+"""The C-ABI library loads and exports every symbol include/fathom.h declares,
+and argument validation rejects bad calls before any CUDA work (no GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from bit_plane_kv_gb300 import binding as B
+from bit_plane_kv_gb300 import build as BUILD
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "fathom.h")
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fathom_[a-z_]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    BUILD.build()
+    return B.lib()
+
+
+def test_every_declared_symbol_is_exported(lib):
+    syms = declared_symbols()
+    assert len(syms) >= 10, syms
+    for s in syms:
+        assert hasattr(lib, s), s
+    # and the binding knows every one of them
+    assert sorted(B.SIGNATURES) == syms
+
+
+def test_version_and_struct_sizes(lib):
+    assert "sm_103a" in B.version()
+    assert ctypes.sizeof(B.Shape) == 7 * 4
+    assert B.RUN_BYTES == 24
+
+
+def rc_msg(lib, rc):
+    return rc, lib.fathom_last_error().decode()
+
+
+@pytest.mark.parametrize("field,value,frag", [
+    ("units", 0, "units"), ("n", 0, "n must"), ("D", 0, "D must"), ("D", 129, "D must"),
+    ("G", 3, "G must"), ("k", 0, "k must"), ("k", 5000, "k must"), ("n_sink", -1, "n_sink"),
+])
+def test_shape_validation(lib, field, value, frag):
+    s = B.make_shape(2, 4096, 128, 4, 64)
+    setattr(s, field, value)
+    dummy = ctypes.c_void_p(16)   # never dereferenced: validation fails first
+    rc = lib.fathom_scan_topk(ctypes.byref(s), dummy, dummy, 0, 0, 0, dummy, dummy, dummy, dummy,
+                              None, dummy, 1 << 30, None)
+    rc, msg = rc_msg(lib, rc)
+    assert rc == 1 and frag in msg, msg
+
+
+def test_forced_exceeds_k(lib):
+    s = B.make_shape(1, 4096, 128, 4, 20, 4, 32)
+    assert lib.fathom_workspace_size(ctypes.byref(s), 0) == 0
+    assert "forced" in lib.fathom_last_error().decode()
+
+
+def test_null_pointers_and_small_workspace(lib):
+    s = B.make_shape(1, 4096, 128, 4, 64)
+    dummy = ctypes.c_void_p(256)
+    rc = lib.fathom_quantize_pack(ctypes.byref(s), None, 0, dummy, dummy, None)
+    assert rc_msg(lib, rc) == (1, "keys is NULL")
+    need = lib.fathom_workspace_size(ctypes.byref(s), B.WS_SCAN_TOPK)
+    assert need > 0
+    rc = lib.fathom_scan_topk(ctypes.byref(s), dummy, dummy, 0, 0, 0, dummy, dummy, dummy, dummy,
+                              None, dummy, need - 1, None)
+    rc, msg = rc_msg(lib, rc)
+    assert rc == 3 and "workspace too small" in msg
+    rc = lib.fathom_scan_topk(ctypes.byref(s), dummy, dummy, 7, 0, 0, dummy, dummy, dummy, dummy,
+                              None, dummy, need, None)
+    assert rc_msg(lib, rc)[0] == 1
+    rc = lib.fathom_plan_fixed(ctypes.byref(s), dummy, dummy, 0, 4, dummy, dummy, None)
+    assert rc_msg(lib, rc)[0] == 1
+    rc = lib.fathom_calibrate(1, 1, 128, dummy, None, dummy, None)
+    assert rc_msg(lib, rc)[0] == 1
+    rc = lib.fathom_sparse_attn(ctypes.byref(s), dummy, dummy, dummy, dummy, dummy, dummy,
+                                lib.fathom_workspace_size(ctypes.byref(s), 1) - 1, None)
+    assert rc_msg(lib, rc)[0] == 3
+
+
+def test_workspace_sizes_scale_with_shape(lib):
+    small = B.make_shape(1, 4096, 128, 4, 64)
+    big = B.make_shape(8, 1 << 20, 128, 4, 512)
+    assert 0 < B.workspace_size(small, 0) < B.workspace_size(big, 0)
+    assert 0 < B.workspace_size(small, 1) <= B.workspace_size(big, 1)
+    assert B.workspace_size(big, 2) == 0

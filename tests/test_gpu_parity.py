@@ -1,0 +1,267 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle on the
+same seeded inputs.  Needs an sm_103a GPU and the built library."""
+import dataclasses
+import json
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from bit_plane_kv_gb300 import binding as B
+from bit_plane_kv_gb300 import synth
+from oracle import oracle as O
+
+from fathom_cases import Inputs, check_unit, run_gpu, u16, u32, u64
+
+pytestmark = pytest.mark.gpu
+
+GOLD = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "toy_appx_a.json")))
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    B.lib()
+
+
+def W(name, **kw):
+    return synth.shrink(synth.WORKLOADS[name], **kw)
+
+
+# ------------------------------------------------------------------ toy (Appx. A)
+class ToyInputs:
+    """The page's 6 x 4 toy: channel 2 as printed, the other channels seeded."""
+
+    def __init__(self):
+        rng = np.random.default_rng(20260000)
+        keys = rng.normal(size=(6, 4)).astype(np.float32)
+        keys[:, 2] = GOLD["channel2"]["values"]
+        self.w = synth.Workload("toy", 0, n=6, G=2, D=4, k=2, n_sink=0, n_recent=0, keys_dtype="f32")
+        self.units, self.n = [0], 6
+        self.keys_in = torch.tensor(keys[None], device="cuda")
+        self.keys32 = self.keys_in
+        self.krows = self.keys_in.to(torch.bfloat16)
+        self.vrows = torch.tensor(rng.normal(size=(1, 6, 4)), dtype=torch.bfloat16, device="cuda")
+        self.q = torch.tensor([[GOLD["q_A"], GOLD["q_B"]]], dtype=torch.float32, device="cuda")
+        # calibration rows whose unbiased variance is close to the printed Var
+        cal = rng.normal(size=(1024, 4)) * np.sqrt(GOLD["var"])
+        self.calib = torch.tensor(cal[None], dtype=torch.float32, device="cuda")
+
+
+def test_toy_plan_with_printed_bracket_and_var():
+    toy = ToyInputs()
+    shape = B.make_shape(1, 6, 4, 2, 2, 0, 0)
+    var = torch.tensor([GOLD["var"]], dtype=torch.float32, device="cuda")
+    for Bud, ref in ((8, GOLD["B8"]["depth"]), (6, GOLD["B6"]["depth"])):
+        bud = torch.tensor([Bud], dtype=torch.int32, device="cuda")
+        br = torch.tensor([GOLD["bracket"]], dtype=torch.float64, device="cuda")
+        depth, theta, runs = B.fathom_plan(shape, toy.q, var, bud, bracket=br)
+        assert depth[0].tolist() == ref
+        od, oth, _ = O.plan(toy.q[0].cpu().numpy(), np.array(GOLD["var"], np.float32), Bud,
+                            bracket=GOLD["bracket"])
+        assert theta[0].item() == oth
+        np.testing.assert_array_equal(u32(runs[0]), O.runs(od, 6))
+    assert abs(theta[0].item() - 0.11796875) < 1e-7   # B = 6 stops at g1 / 32
+
+
+def test_toy_channel2_codes_and_full_path():
+    toy = ToyInputs()
+    r = run_gpu(toy, k=2, budget=8, n_sink=0, n_recent=0)
+    # printed codes of channel 2 via the plane words (token i at bit i)
+    words = u64(r["planes"][0, 2, :, 0])
+    codes = [sum(((int(words[p]) >> i) & 1) << (3 - p) for p in range(4)) for i in range(6)]
+    assert codes == GOLD["channel2"]["codes"]
+    assert u16(r["scales"][0, 2])[0] == np.float16(0.5).view(np.uint16)
+    check_unit(toy, r, 0, 2, 8, n_sink=0, n_recent=0)
+
+
+# ------------------------------------------------------------------ store / calibration
+@pytest.mark.parametrize("n,dtype", [(4096, "f32"), (4096 + 37, "bf16"), (64, "bf16"), (1, "f32")])
+def test_quantize_bit_exact(n, dtype):
+    w = W("qwen3_32k", keys_dtype=dtype)
+    inp = Inputs(w, [0, 5, 17], n)
+    shape = B.make_shape(3, n, 128, 4, 1, 0, 0)
+    planes, scales = B.fathom_quantize_pack(shape, inp.keys_in)
+    torch.cuda.synchronize()
+    for ui in range(3):
+        P, S, _ = O.quantize_pack(inp.keys32[ui].cpu().numpy())
+        np.testing.assert_array_equal(u64(planes[ui]), P)
+        np.testing.assert_array_equal(u16(scales[ui]), S)
+
+
+def test_quantize_edge_values():
+    # zeros, exact cell edges, values above the fp16-rounded maximum, huge and tiny blocks
+    rng = np.random.default_rng(3)
+    n, D = 256, 16
+    k = rng.normal(size=(n, D)).astype(np.float32)
+    k[:64, 0] = 0.0                                  # a == 0 block
+    k[64:128, 1] = np.float32(0.5) * np.arange(-32, 32) / 4   # exact multiples of s
+    k[128:192, 2] = 1e-9                             # subnormal-range fp16 scale
+    k[192:, 3] = 7e4                                 # saturating scale
+    k[192, 3] = -7.1e4
+    k[:, 4] = np.float32(1.00048828125)              # rounds down in fp16: |k| > a16
+    keys = torch.tensor(k[None], device="cuda")
+    shape = B.make_shape(1, n, D, 4, 1, 0, 0)
+    planes, scales = B.fathom_quantize_pack(shape, keys)
+    torch.cuda.synchronize()
+    P, S, _ = O.quantize_pack(k)
+    np.testing.assert_array_equal(u64(planes[0]), P)
+    np.testing.assert_array_equal(u16(scales[0]), S)
+
+
+def test_calibrate_bit_exact():
+    w = W("qwen3_32k")
+    calib = torch.stack([synth.unit_calib(w, u, "cuda") for u in range(5)])
+    mean, var = B.fathom_calibrate(calib)
+    torch.cuda.synchronize()
+    for u in range(5):
+        m64, v64 = O.calibrate(calib[u].cpu().numpy())
+        np.testing.assert_array_equal(var[u].cpu().numpy(), v64.astype(np.float32))
+        np.testing.assert_array_equal(mean[u].cpu().numpy(), m64.astype(np.float32))
+
+
+# ------------------------------------------------------------------ plan
+@pytest.mark.parametrize("G", [1, 2, 4, 8])
+def test_plan_bit_exact_over_budgets(G):
+    w = W("qwen3_32k", G=G)
+    U = 64
+    q = torch.stack([synth.unit_query(w, u, "cuda") for u in range(U)])
+    calib = torch.stack([synth.unit_calib(w, u, "cuda") for u in range(U)])
+    _, var = B.fathom_calibrate(calib)
+    q[3] = 0.0                       # no live channel
+    q[4, :, 5:] = 0.0                # few live channels
+    budgets = np.array([0, 1, 7, 24, 32, 40, 48, 56, 64, 96, 128, 300, 512, 600] * 5, np.int32)[:U]
+    shape = B.make_shape(U, 32768, 128, G, 1, 0, 0)
+    depth, theta, runs = B.fathom_plan(shape, q, var, torch.tensor(budgets, device="cuda"))
+    torch.cuda.synchronize()
+    qn, vn = q.cpu().numpy(), var.cpu().numpy()
+    for u in range(U):
+        od, oth, _ = O.plan(qn[u], vn[u], int(budgets[u]))
+        np.testing.assert_array_equal(depth[u].cpu().numpy(), od)
+        assert theta[u].item() == oth
+        np.testing.assert_array_equal(u32(runs[u]), O.runs(od, 32768))
+        assert od.sum() <= max(budgets[u], 0)
+
+
+def test_plan_explicit_bracket_and_fixed():
+    w = W("qwen3_32k")
+    U = 16
+    q = torch.stack([synth.unit_query(w, u, "cuda") for u in range(U)])
+    _, var = B.fathom_calibrate(torch.stack([synth.unit_calib(w, u, "cuda") for u in range(U)]))
+    shape = B.make_shape(U, 1 << 20, 128, 4, 1, 0, 0)
+    br = torch.tensor([[1e-3, 1e3]] * U, dtype=torch.float64, device="cuda")
+    bud = torch.full((U,), 48, dtype=torch.int32, device="cuda")
+    depth, theta, runs = B.fathom_plan(shape, q, var, bud, bracket=br)
+    fdepth, fruns = B.fathom_plan_fixed(shape, q, var, 32, 4)
+    torch.cuda.synchronize()
+    for u in range(U):
+        qn, vn = q[u].cpu().numpy(), var[u].cpu().numpy()
+        od, oth, _ = O.plan(qn, vn, 48, bracket=[1e-3, 1e3])
+        np.testing.assert_array_equal(depth[u].cpu().numpy(), od)
+        assert theta[u].item() == oth
+        fd = O.plan_fixed(qn, vn, 32, 4)
+        np.testing.assert_array_equal(fdepth[u].cpu().numpy(), fd)
+        np.testing.assert_array_equal(u32(fruns[u]), O.runs(fd, 1 << 20))
+
+
+# ------------------------------------------------------------------ whole path, small
+@pytest.mark.parametrize("regime", ["hbm", "host"])
+def test_single_layer_4k_full_parity(regime):
+    w = synth.WORKLOADS["single_4k"]
+    inp = Inputs(w, [0], w.n)
+    r = run_gpu(inp, k=w.k, budget=48, regime=regime)
+    check_unit(inp, r, 0, w.k, 48)
+
+
+def test_ragged_multi_tile_multi_unit():
+    # several sub-chunks and chunks per unit, a ragged tail block, bf16 keys
+    w = W("qwen3_32k", n=6481)
+    inp = Inputs(w, [0, 1, 2], 6481)
+    r = run_gpu(inp, k=300, budget=[40, 48, 56])
+    for ui in range(3):
+        check_unit(inp, r, ui, 300, [40, 48, 56])
+
+
+def test_long_chunks_exercise_pruning():
+    # 152 units x 64k tokens: 4 chunks per unit of 8 sub-chunks -> in-CTA prunes
+    w = W("qwen3_32k", n=65536)
+    U = 152
+    inp = Inputs(w, range(U), 65536)
+    r = run_gpu(inp, k=512, budget=48, want_scores=True)
+    for ui in (0, 77, 151):
+        check_unit(inp, r, ui, 512, 48, check_attn=(ui == 0))
+
+
+@pytest.mark.parametrize("G", [1, 2, 8])
+def test_other_group_sizes(G):
+    w = W("qwen3_32k", G=G, n=5000)
+    inp = Inputs(w, [3, 4], 5000)
+    r = run_gpu(inp, k=128, budget=64)
+    for ui in range(2):
+        check_unit(inp, r, ui, 128, 64)
+
+
+def test_dense_budget_and_small_D():
+    w = W("qwen3_32k", D=24, n=3000)
+    inp = Inputs(w, [1], 3000)
+    r = run_gpu(inp, k=100, budget=4 * 24)        # every channel at depth 4
+    assert int(r["depth"].min()) == 4
+    check_unit(inp, r, 0, 100, 4 * 24)
+
+
+@pytest.mark.parametrize("k,ns,nr", [(36, 4, 32), (2000, 4, 32), (2000, 0, 0), (7, 0, 0), (40, 20, 20),
+                                     (2048, 0, 0)])
+def test_selection_edges(k, ns, nr):
+    n = 2000 if k <= 2000 else 2600
+    w = W("qwen3_32k", n=n)
+    inp = Inputs(w, [2], n)
+    r = run_gpu(inp, k=k, budget=48, n_sink=ns, n_recent=nr)
+    check_unit(inp, r, 0, k, 48, n_sink=ns, n_recent=nr)
+
+
+def test_tiny_sequences():
+    for n, k, ns, nr in ((1, 1, 0, 0), (5, 5, 4, 32), (40, 36, 4, 32), (70, 40, 4, 32)):
+        w = W("qwen3_32k", n=n)
+        inp = Inputs(w, [0], n)
+        r = run_gpu(inp, k=k, budget=48, n_sink=ns, n_recent=nr)
+        check_unit(inp, r, 0, k, 48, n_sink=ns, n_recent=nr)
+
+
+def test_all_ties_break_by_index():
+    w = W("qwen3_32k", n=4096)
+    inp = Inputs(w, [0], 4096)
+    inp.q.zero_()                      # every score is 0: lowest free indices win
+    r = run_gpu(inp, k=64, budget=48)
+    assert int(r["depth"].sum()) == 0
+    idx = r["idx"][0].cpu().numpy()
+    for h in range(4):
+        assert idx[h].tolist() == list(range(4)) + list(range(4, 32)) + list(range(4064, 4096))
+
+
+def test_staged_equals_in_place_and_fixed_plan():
+    w = W("host_256k", n=20000)
+    inp = Inputs(w, [0, 1], 20000)
+    a = run_gpu(inp, k=256, budget=64, regime="hbm")
+    b = run_gpu(inp, k=256, budget=64, regime="host")
+    assert torch.equal(a["idx"], b["idx"]) and torch.equal(a["scores"], b["scores"])
+    c = run_gpu(inp, k=256, budget=0, regime="host", fixed=(32, 4))
+    check_unit(inp, c, 1, 256, 0, fixed=(32, 4))
+
+
+def test_workspace_reuse_across_calls():
+    w = W("qwen3_32k", n=8192)
+    inp = Inputs(w, [0, 1, 2, 3], 8192)
+    shape = B.make_shape(4, 8192, 128, 4, 256)
+    r = run_gpu(inp, k=256, budget=48)
+    ws = B.alloc_workspace(shape, B.WS_SCAN_TOPK)
+    aws = B.alloc_workspace(shape, B.WS_SPARSE_ATTN)
+    outs = []
+    for _ in range(3):
+        idx, _ = B.fathom_scan_topk(shape, r["planes"], r["scales"], r["runs"], inp.q, ws)
+        outs.append((idx.clone(), B.fathom_sparse_attn(shape, inp.krows, inp.vrows, inp.q, idx, aws).clone()))
+    torch.cuda.synchronize()
+    for idx, out in outs[1:]:
+        assert torch.equal(idx, outs[0][0]) and torch.equal(out, outs[0][1])
+    assert torch.equal(outs[0][0], r["idx"])
