@@ -66,12 +66,20 @@ def barrier(world):
 
 
 def max_over_ranks(x, world):
+    """The largest of the ranks' values (the job's time is its slowest rank's)."""
     if world == 1:
         return x
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def rank_workload(w: synth.Workload, rank: int) -> synth.Workload:
+    """Every rank serves its own session: the same shapes with a rank-specific seed
+    (rank 0 keeps the workload's own seed).  Units are never split across ranks."""
+    return synth.shrink(w, seed=w.seed + 1000003 * rank) if rank else w
 
 
 # ---------------------------------------------------------------- clocks
@@ -124,9 +132,7 @@ class Setup:
         from bit_plane_kv_gb300 import binding as B
         self.B = B
         self.w, self.budget, self.fixed = w, budget, fixed
-        # each rank serves its own session: a different seed
-        self.ws_ = synth.shrink(w, seed=w.seed + 1000003 * rank) if rank else w
-        w = self.ws_
+        w = rank_workload(w, rank)
         self.L, self.H = w.layers, w.units_per_layer()
         self.n, self.G, self.D, self.k = w.n, w.G, w.D, w.k
         self.nb = B.nblocks(self.n)
@@ -206,6 +212,28 @@ class Setup:
             if ev:
                 ev[1].record()
         B.fathom_sparse_attn(self.shape, self.krows[l], self.vrows[l], q, self.idx, self.aws, out=self.out[l])
+
+    def layer_stages(self, l, q):
+        """One layer with CUDA events between the calls: per-stage milliseconds."""
+        B = self.B
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+        ev[0].record()
+        B.fathom_plan(self.shape, q, self.var[l], self.budget_t, depth=self.depth, theta=self.theta,
+                      runs=self.runs)
+        ev[1].record()
+        if self.host:
+            B.fathom_gather(self.shape, self.planes[l], self.scales[l], self.runs, self.stage_p, self.stage_sc)
+            ev[2].record()
+            B.fathom_scan_topk(self.shape, self.stage_p, self.stage_sc, self.runs, q, self.ws,
+                               source=B.SRC_STAGING, topk_idx=self.idx, topk_score=self.sel)
+        else:
+            ev[2].record()
+            B.fathom_scan_topk(self.shape, self.planes[l], self.scales[l], self.runs, q, self.ws,
+                               topk_idx=self.idx, topk_score=self.sel)
+        ev[3].record()
+        B.fathom_sparse_attn(self.shape, self.krows[l], self.vrows[l], q, self.idx, self.aws, out=self.out[l])
+        ev[4].record()
+        return ev
 
     def step(self, s, evs=None):
         for l in range(self.L):
@@ -324,6 +352,8 @@ def main():
     ap.add_argument("--fixed", action="store_true", help="the 136-bit fixed-depth comparison plan")
     ap.add_argument("--impl", default="fathom", choices=["fathom", "reference"])
     ap.add_argument("--layers", type=int, default=0, help="override the layer count (0: workload's)")
+    ap.add_argument("--regime", default="", choices=["", "hbm", "host"],
+                    help="override where the store and rows live (default: the workload's)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
@@ -331,6 +361,8 @@ def main():
     w = synth.WORKLOADS[args.workload]
     if args.layers:
         w = synth.shrink(w, layers=args.layers)
+    if args.regime:
+        w = synth.shrink(w, regime=args.regime)
     if args.impl == "reference":
         run_reference(args, w, rank, world)
         return
@@ -384,6 +416,16 @@ def main():
     torch.cuda.synchronize()
     e2e_elapsed = max_over_ranks(e0.elapsed_time(e1) / 1e3, world)
 
+    # per-stage breakdown (separate pass, events between the calls)
+    stage_ev = []
+    for s in range(args.steps):
+        for l in range(st.L):
+            stage_ev.append(st.layer_stages(l, st.Q[args.warmup + s, l]))
+    torch.cuda.synchronize()
+    names = ["plan", "gather", "scan_topk", "sparse_attn"]
+    stages = {nm: statistics.mean(e[i].elapsed_time(e[i + 1]) * 1e3 for e in stage_ev) for i, nm in enumerate(names)}
+    log("[bench] per-layer stages (µs): " + ", ".join(f"{k} {v:.1f}" for k, v in stages.items()))
+
     L, H = st.L, st.H
     layer_steps = args.steps * L * world
     us_layer = elapsed * 1e6 / layer_steps         # whole job: all ranks' layer-steps
@@ -423,6 +465,7 @@ def main():
         "e2e": {"value": e2e_us_layer, "unit": "µs/layer",
                 "h2d_bytes_per_step": int(st.Q[0].numel() * 4), "d2h_bytes_per_step": int(st.out.numel() * 4)},
         "gpu_launches": launches_per_layer * L * args.steps,
+        "stages_us_per_layer": stages,
         "clocks": clk,
     }
     if st.host:

@@ -71,25 +71,39 @@ int scan_cand_cap(const fathom_shape &s) {
     int k_sel = s.k - f.nf;
     if (k_sel < 0) k_sel = 0;
     int cap = k_sel + kPruneSlack + 2 * kSubTokens;
-    return (cap + 255) / 256 * 256;
+    return (cap + 255) / 256 * 256;   // <= 6400 for k <= 2048
+}
+
+int merge_parts(int chunks, int k_sel) {
+    long long keys = (long long)chunks * (k_sel > 0 ? k_sel : 1);
+    int p = (int)((keys + 4095) / 4096);
+    if (p > chunks) p = chunks;
+    if (p > FATHOM_MERGE_MAX_LISTS) p = FATHOM_MERGE_MAX_LISTS;
+    return p < 1 ? 1 : p;
 }
 
 ScanWorkspace scan_workspace_layout(const fathom_shape &s) {
     ScanGrid g = scan_grid(s.units, s.n);
     Forced f = forced_range(s.n, s.n_sink, s.n_recent);
+    int k_sel = s.k - f.nf;
+    if (k_sel < 1) k_sel = 1;
     ScanWorkspace w;
-    size_t ctas = (size_t)s.units * g.chunks;
+    w.parts = merge_parts(g.chunks, k_sel);
+    const size_t ctas = (size_t)s.units * g.chunks;
+    const size_t uh = (size_t)s.units * s.G;
     w.cand_off = 0;
-    w.cnt_off = align256(w.cand_off + ctas * s.G * 2 * (size_t)scan_cand_cap(s) * sizeof(uint64_t));
+    w.cnt_off = align256(w.cand_off + ctas * s.G * (size_t)scan_cand_cap(s) * sizeof(uint64_t));
     w.forced_off = align256(w.cnt_off + ctas * s.G * sizeof(int32_t));
-    w.total = align256(w.forced_off + (size_t)s.units * s.G * (f.nf > 0 ? f.nf : 1) * sizeof(float));
+    w.part_keys_off = align256(w.forced_off + uh * (f.nf > 0 ? f.nf : 1) * sizeof(float));
+    w.part_cnt_off = align256(w.part_keys_off + uh * w.parts * (size_t)k_sel * sizeof(uint64_t));
+    w.ticket_off = align256(w.part_cnt_off + uh * w.parts * sizeof(int32_t));
+    w.total = align256(w.ticket_off + uh * sizeof(uint32_t));
     return w;
 }
 
 AttnWorkspace attn_workspace_layout(const fathom_shape &s) {
     AttnWorkspace w;
-    int rows = s.G * s.k;
-    w.splits = (rows + kAttnRows - 1) / kAttnRows;
+    w.splits = s.G * ((s.k + kAttnRows - 1) / kAttnRows);
     if (w.splits < 1) w.splits = 1;
     w.part_off = 0;
     w.ticket_off = align256((size_t)s.units * w.splits * s.G * (s.D + 2) * sizeof(float));

@@ -48,12 +48,18 @@ constexpr int kSubTokens = kSubBlocks * 64;  // 2048
 constexpr int kPruneSlack = 256;             // a pruned list keeps <= k' + slack keys
 
 // Candidate list capacity per (CTA, head): after a prune a list holds at most
-// k' + slack keys and a sub-chunk appends at most kSubTokens, so two
+// k' + slack keys and a sub-chunk appends at most kSubTokens, so at least two
 // sub-chunks fit between prunes.
 int scan_cand_cap(const fathom_shape &s);
 
+#define FATHOM_MERGE_MAX_LISTS 1024
+
+// Merge parts per (unit, head): about 4096 candidate keys per part.
+int merge_parts(int chunks, int k_sel);
+
 struct ScanWorkspace {
-    size_t cand_off, cnt_off, forced_off, total;
+    int parts;
+    size_t cand_off, cnt_off, forced_off, part_keys_off, part_cnt_off, ticket_off, total;
 };
 ScanWorkspace scan_workspace_layout(const fathom_shape &s);
 

@@ -20,10 +20,23 @@ namespace fathom {
 constexpr int kPlanWarps = 4;
 constexpr int kCh = FATHOM_MAX_D / 32;   // channels per lane
 
+// t(g, theta) = #{m in 0..3 : g >= theta * 2^(2m+1)}.  For a normal positive
+// theta, theta * 2^e is the double whose bit pattern is bits(theta) + e * 2^52
+// (no rounding: only the exponent changes), and positive doubles order like
+// their bit patterns, so each compare is one exact 64-bit integer compare
+// (negative or zero g compares below every positive threshold, as in fp64).
+// Zero or subnormal theta takes the fp64 route.
 __device__ __forceinline__ int depth_of(double g, double theta) {
+    const long long tb = __double_as_longlong(theta);
     int t = 0;
+    if ((tb >> 52) > 0 && (tb >> 52) < 0x7ff) {
+        const long long gb = __double_as_longlong(g);
 #pragma unroll
-    for (int m = 0; m < 4; ++m) t += (g >= __dmul_rn(theta, (double)(2 << (2 * m)))) ? 1 : 0;
+        for (int m = 0; m < 4; ++m) t += (gb >= tb + ((long long)(2 * m + 1) << 52)) ? 1 : 0;
+    } else {
+#pragma unroll
+        for (int m = 0; m < 4; ++m) t += (g >= __dmul_rn(theta, (double)(2 << (2 * m)))) ? 1 : 0;
+    }
     return t;
 }
 

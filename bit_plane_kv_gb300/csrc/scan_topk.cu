@@ -20,31 +20,48 @@
 //   q_hj * (c_t + 0.5 - 2^(t-1)) * a_j / 2^(t-1), i.e. q_hj times the t-bit
 //   mid-rise value, with no rounding before the multiply.
 //
-// Selection never materialises all scores.  Each CTA keeps, per head, a
-// candidate list of 64-bit keys (score, ~index) in the workspace and a
-// threshold key tau: a token is appended only if its key >= tau.  When a
-// list could overflow, an in-CTA radix select finds a key T such that at
-// least k' (and at most k' + slack) keys are >= T, keeps those and sets
-// tau = T.  Any token of the CTA's top-k' is always kept, so the union of the
-// CTAs' lists contains the unit's top-k'.  A second kernel, one CTA per
-// (unit, head), selects the exact top-k' from that union, adds the forced
-// tokens and writes the kept set in ascending index order.
+// Selection never materialises all scores.  Tokens are ordered by a 64-bit
+// key (score, ~index).  Each CTA keeps, per head, a candidate list of keys in
+// the workspace and a threshold key tau; a token is appended only if its key
+// >= tau.  tau starts as the exact k'-th key of the CTA's first sub-chunk
+// (selected straight from registers for all heads at once); when a list could
+// overflow it is pruned (loaded into registers once, radix-selected, written
+// back) to at least k' and at most k' + slack keys and tau rises to the new
+// bound; at the end every list is cut to its exact top-k'.  A token of the
+// CTA's top-k' is never dropped, so the union of the CTAs' lists holds the
+// unit's top-k'.  The merge kernel streams those lists through shared memory
+// (P CTAs per (unit, head), the last of which, by an atomic ticket, merges
+// the P partial results), selects the exact top-k', adds the forced tokens
+// and writes the kept set in ascending index order.
+#include <type_traits>
+
 #include "fathom_internal.cuh"
 
 namespace fathom {
 
-constexpr int kPG = 64;                 // plane words staged per group
+constexpr int kCHG = 32;                // channels per staged group (fixed runs of the sorted order)
+constexpr int kPG = kCHG * FATHOM_PLANES;   // plane words staged per group, at most
 constexpr int kPWStride = kPG + 2;      // padded row (uint2 units) -> distinct banks per block
 constexpr int NT = kScanThreads;
 
 template <int G>
 struct ScanCfg {
-    static constexpr int CHG = (G <= 4) ? 64 : 32;     // channels per staged group
-    static constexpr int WStride = CHG * G + 4;        // padded weight row (floats)
+    static constexpr int WStride = kCHG * G + 4;       // padded weight row (floats)
 };
 
 struct GroupDesc {
     int a0, p0, n4, n3, n2, n1;   // first active channel, first plane slot, channels per depth
+};
+
+// Scratch of up to S simultaneous CTA-wide threshold selections.
+constexpr int kMaxWarps = 16;
+template <int S>
+struct SelScratch {
+    unsigned hist[S][256];
+    unsigned long long red[2][S][kMaxWarps];
+    int red_n[S][kMaxWarps];
+    int digit[S], above[S], bucket[S];
+    int new_cnt;
 };
 
 template <int G>
@@ -56,17 +73,13 @@ struct ScanSmem {
     float qs[FATHOM_MAX_D][G];                          // q_hj * 2^-t_j, active channels
     int ch_t[FATHOM_MAX_D];                             // depth of active channel (sorted)
     int raw_t[FATHOM_MAX_D];
-    GroupDesc grp[FATHOM_MAX_D];
-    int n_groups, n_active;
+    GroupDesc grp[FATHOM_MAX_D / kCHG];
+    int wcnt[FATHOM_PLANES + 1][FATHOM_MAX_D / 32];   // channels of each depth per warp
+    int n_groups;
     int cnt[G];
-    int cur[G];
     uint64_t tau[G];
-    float tau_s[G];
-    // radix select scratch
-    unsigned hist[256];
-    unsigned lane_sum[32];
-    int sel_digit, sel_above, sel_bucket;
-    int new_cnt;
+    SelScratch<G> selg;   // first-sub-chunk selection, all heads at once
+    SelScratch<1> sel1;   // list prunes
 };
 
 // ---------------------------------------------------------------------------
@@ -116,29 +129,103 @@ __device__ __forceinline__ void accum_depth(const uint2 *__restrict__ pwrow,
 }
 
 // ---------------------------------------------------------------------------
-// CTA-wide radix select over `count` keys at `src`.  Finds T with
-// #{keys >= T} in [target, target + slack] (slack = 0: exactly target) and
-// returns #{keys >= T}.  target >= 1 and count >= target.
-template <typename Sm>
-__device__ uint64_t radix_threshold(Sm &sm, const uint64_t *src, int count, int target, int slack,
-                                    int *kept) {
-    const int tid = threadIdx.x;
-    const int lane = tid & 31, warp = tid >> 5;
-    uint64_t prefix = 0, pmask = 0;
-    int above = 0;   // keys strictly above the current bucket
-    for (int shift = 56; shift >= 0; shift -= 8) {
-        for (int i = tid; i < 256; i += blockDim.x) sm.hist[i] = 0;
-        __syncthreads();
-        for (int e = tid; e < count; e += blockDim.x) {
-            const uint64_t key = src[e];
-            if ((key & pmask) == prefix) atomicAdd(&sm.hist[(key >> shift) & 255], 1u);
+// CTA-wide threshold selection, S selections at once.
+//
+// For every selection s, finds T[s] such that #{keys of s >= T[s]} lies in
+// [target, target + slack] (slack = 0: T[s] is exactly the target-th largest
+// key); a selection with fewer than `target` keys gets T[s] = 0 (keep all).
+// Keys are unique within a selection.  visit(f) calls f(s, valid, key) for
+// every key from every thread in lock step (invalid entries pass
+// valid = false), so warp collectives inside f are safe.
+//
+// MSD radix select that starts at the highest bit in which the selection's
+// keys differ (a min/max reduction finds it), so the first 8-bit digit
+// already splits the live range of scores rather than the sign and exponent
+// bits every candidate shares; histogram increments are aggregated per warp
+// (lanes with equal digits add once).
+// Compile-time loop: f(integral_constant<int, I>) for I in [B, E).
+template <int B, int E, typename F>
+__device__ __forceinline__ void static_for(F &&f) {
+    if constexpr (B < E) {
+        f(std::integral_constant<int, B>{});
+        static_for<B + 1, E>(f);
+    }
+}
+
+template <int S, typename Visit>
+__device__ void select_thresholds(SelScratch<S> &sm, Visit visit, int target, int slack,
+                                  uint64_t (&T)[S], int (&kept)[S]) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
+    unsigned long long kmin[S], kmax[S];
+    int cnt[S];
+    static_for<0, S>([&](auto s) { kmin[s] = ~0ull; kmax[s] = 0ull; cnt[s] = 0; });
+    visit([&](auto s, bool valid, uint64_t key) {
+        if (valid) {
+            kmin[s] = min(kmin[s], (unsigned long long)key);
+            kmax[s] = max(kmax[s], (unsigned long long)key);
+            ++cnt[s];
         }
+    });
+    static_for<0, S>([&](auto s) {
+#pragma unroll
+        for (int o = 16; o; o >>= 1) {
+            kmin[s] = min(kmin[s], __shfl_xor_sync(0xffffffffu, kmin[s], o));
+            kmax[s] = max(kmax[s], __shfl_xor_sync(0xffffffffu, kmax[s], o));
+            cnt[s] += __shfl_xor_sync(0xffffffffu, cnt[s], o);
+        }
+        if (lane == 0) { sm.red[0][s][warp] = kmin[s]; sm.red[1][s][warp] = kmax[s]; sm.red_n[s][warp] = cnt[s]; }
+    });
+    __syncthreads();
+    uint64_t prefix[S], pmask[S];
+    int hi_bit[S], above[S];
+    bool done[S];
+    static_for<0, S>([&](auto s) {
+        unsigned long long mn = ~0ull, mx = 0ull;
+        int c = 0;
+        for (int w = 0; w < nw; ++w) { mn = min(mn, sm.red[0][s][w]); mx = max(mx, sm.red[1][s][w]); c += sm.red_n[s][w]; }
+        above[s] = 0;
+        prefix[s] = 0; pmask[s] = 0; hi_bit[s] = 0;
+        if (c < target || c == 0) { T[s] = 0; kept[s] = c; done[s] = true; }
+        else if (mn == mx) { T[s] = mn; kept[s] = 1; done[s] = true; }
+        else {
+            done[s] = false;
+            hi_bit[s] = 63 - __clzll((long long)(mn ^ mx));
+            pmask[s] = (hi_bit[s] == 63) ? 0ull : ~((2ull << hi_bit[s]) - 1ull);
+            prefix[s] = mn & pmask[s];
+            T[s] = 0; kept[s] = c;
+        }
+    });
+    __syncthreads();
+    while (true) {
+        bool all_done = true;
+        static_for<0, S>([&](auto s) { all_done = all_done && done[s]; });
+        if (all_done) break;
+        int lo[S];
+        uint64_t dmask[S];
+        static_for<0, S>([&](auto s) {
+            lo[s] = hi_bit[s] >= 7 ? hi_bit[s] - 7 : 0;
+            dmask[s] = (2ull << (hi_bit[s] - lo[s])) - 1ull;    // digit bits [hi_bit .. lo]
+        });
+        for (int i = tid; i < S * 256; i += blockDim.x) (&sm.hist[0][0])[i] = 0;
         __syncthreads();
-        if (warp == 0) {
+        visit([&](auto s, bool valid, uint64_t key) {
+            const bool in = valid && !done[s] && ((key & pmask[s]) == prefix[s]);
+            const unsigned bin = in ? (unsigned)((key >> lo[s]) & dmask[s]) : 256u + lane;
+            const unsigned peers = __match_any_sync(0xffffffffu, bin);
+            if (in && lane == __ffs(peers) - 1) atomicAdd(&sm.hist[s][bin], (unsigned)__popc(peers));
+        });
+        __syncthreads();
+        bool warp_live = false;   // this warp searches selection `warp`
+        int need_w = 0;
+        static_for<0, S>([&](auto s) {
+            if (warp == s && !done[s]) { warp_live = true; need_w = target - above[s]; }
+        });
+        if (warp_live) {
+            const int s = warp;
             // lane l owns bins 255-8l .. 248-8l (descending)
             unsigned loc = 0;
 #pragma unroll
-            for (int i = 0; i < 8; ++i) loc += sm.hist[255 - 8 * lane - i];
+            for (int i = 0; i < 8; ++i) loc += sm.hist[s][255 - 8 * lane - i];
             unsigned incl = loc;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
@@ -146,16 +233,17 @@ __device__ uint64_t radix_threshold(Sm &sm, const uint64_t *src, int count, int 
                 if (lane >= o) incl += y;
             }
             const unsigned excl = incl - loc;
-            const unsigned need = (unsigned)(target - above);
+            const unsigned need = (unsigned)need_w;
+            if (lane == 31 && incl < need) { sm.digit[s] = -1; sm.above[s] = 0; sm.bucket[s] = 0; }
             if (excl < need && need <= incl) {
                 unsigned c = excl;
                 for (int i = 0; i < 8; ++i) {
                     const int bin = 255 - 8 * lane - i;
-                    const unsigned hb = sm.hist[bin];
+                    const unsigned hb = sm.hist[s][bin];
                     if (c + hb >= need) {
-                        sm.sel_digit = bin;
-                        sm.sel_above = (int)c;
-                        sm.sel_bucket = (int)hb;
+                        sm.digit[s] = bin;
+                        sm.above[s] = (int)c;
+                        sm.bucket[s] = (int)hb;
                         break;
                     }
                     c += hb;
@@ -163,47 +251,86 @@ __device__ uint64_t radix_threshold(Sm &sm, const uint64_t *src, int count, int 
             }
         }
         __syncthreads();
-        const int d = sm.sel_digit;
-        above += sm.sel_above;
-        const int hb = sm.sel_bucket;
-        prefix |= (uint64_t)d << shift;
-        pmask |= (uint64_t)255 << shift;
-        __syncthreads();   // everyone has read sel_* before the next pass rewrites them
-        if (above + hb == target || above + hb <= target + slack || shift == 0) {
-            *kept = above + hb;
-            return prefix;
-        }
+        static_for<0, S>([&](auto s) {
+            if (done[s]) return;
+            const int d = sm.digit[s];
+            if (d < 0) {                      // cannot happen for unique keys; keep everything
+                T[s] = 0; done[s] = true;
+                return;
+            }
+            above[s] += sm.above[s];
+            const int hb = sm.bucket[s];
+            prefix[s] |= (uint64_t)d << lo[s];
+            pmask[s] |= dmask[s] << lo[s];
+            if (above[s] + hb == target || above[s] + hb <= target + slack || lo[s] == 0) {
+                T[s] = prefix[s];
+                kept[s] = above[s] + hb;
+                done[s] = true;
+            } else {
+                hi_bit[s] = lo[s] - 1;
+            }
+        });
+        __syncthreads();   // everyone has read the results before the next pass rewrites them
     }
-    *kept = target;
-    return prefix;
 }
 
-// Keep the keys >= T of list (count) by copying them to dst; returns new count.
-template <typename Sm>
-__device__ int compact_keys(Sm &sm, const uint64_t *src, int count, uint64_t T, uint64_t *dst,
-                            int dst_cap) {
-    const int tid = threadIdx.x, lane = tid & 31;
-    if (tid == 0) sm.new_cnt = 0;
-    __syncthreads();
-    for (int e0 = 0; e0 < count; e0 += blockDim.x) {
-        const int e = e0 + tid;
-        uint64_t key = 0;
-        bool keep = false;
-        if (e < count) { key = src[e]; keep = key >= T; }
-        const unsigned bal = __ballot_sync(0xffffffffu, keep);
+// Appends the valid keys >= T (one per thread) to dst at a shared counter.
+template <int S>
+__device__ __forceinline__ void append_if(SelScratch<S> &sm, bool keep, uint64_t key, uint64_t *dst,
+                                          int dst_cap) {
+    const int lane = threadIdx.x & 31;
+    const unsigned bal = __ballot_sync(0xffffffffu, keep);
+    if (bal) {
         int base = 0;
-        if (lane == 0 && bal) base = atomicAdd(&sm.new_cnt, __popc(bal));
-        base = __shfl_sync(0xffffffffu, base, 0);
+        if (lane == __ffs(bal) - 1) base = atomicAdd(&sm.new_cnt, __popc(bal));
+        base = __shfl_sync(0xffffffffu, base, __ffs(bal) - 1);
         const int pos = base + __popc(bal & ((1u << lane) - 1u));
         if (keep && pos < dst_cap) dst[pos] = key;
     }
+}
+
+// Prunes a list of `count` keys (global or shared memory) in place to the
+// keys >= T found by select_thresholds(target, slack): the keys are read into
+// registers once (KPT per thread, KPT * blockDim.x >= count), so the radix
+// passes never go back to memory.  Returns the new count and T.
+template <int KPT>
+__device__ int prune_list(SelScratch<1> &sm, uint64_t *lst, int count, int target, int slack,
+                          uint64_t *T_out) {
+    const int tid = threadIdx.x;
+    // only the first `used` register slots hold keys (a block-uniform bound)
+    const int used = (count + (int)blockDim.x - 1) / (int)blockDim.x;
+    uint64_t r[KPT];
+#pragma unroll
+    for (int i = 0; i < KPT; ++i) {
+        const int e = i * (int)blockDim.x + tid;
+        r[i] = (i < used && e < count) ? lst[e] : 0ull;
+    }
+    uint64_t T[1];
+    int kept[1];
+    select_thresholds<1>(sm, [&](auto f) {
+#pragma unroll
+        for (int i = 0; i < KPT; ++i)
+            if (i < used) f(std::integral_constant<int, 0>{}, i * (int)blockDim.x + tid < count, r[i]);
+    }, target, slack, T, kept);
+    if (tid == 0) sm.new_cnt = 0;
+    __syncthreads();   // all keys are in registers: the list may be overwritten
+#pragma unroll
+    for (int i = 0; i < KPT; ++i) {
+        if (i < used) {
+            const bool keep = (i * (int)blockDim.x + tid < count) && r[i] >= T[0];
+            append_if<1>(sm, keep, r[i], lst, count);
+        }
+    }
     __syncthreads();
-    return min(sm.new_cnt, dst_cap);
+    *T_out = T[0];
+    return min(sm.new_cnt, count);
 }
 
 // ---------------------------------------------------------------------------
+constexpr int kListKPT = 26;   // register keys per thread for list prunes (cap <= 26 * 256)
+
 template <int G>
-__global__ void __launch_bounds__(NT)
+__global__ void __launch_bounds__(NT, (G <= 4) ? 3 : 1)
 scan_kernel(int n, int D, int chunk_blocks, int source, size_t stage_words, size_t stage_scales,
             const uint64_t *__restrict__ planes, const uint16_t *__restrict__ scales,
             const fathom_run *__restrict__ runs, const float *__restrict__ q, int k_sel, int ns,
@@ -211,7 +338,7 @@ scan_kernel(int n, int D, int chunk_blocks, int source, size_t stage_words, size
             int *__restrict__ cand_cnt, float *__restrict__ forced_scores) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     ScanSmem<G> &sm = *reinterpret_cast<ScanSmem<G> *>(smem_raw);
-    const int tid = threadIdx.x, lane = tid & 31;
+    const int tid = threadIdx.x;
     const int u = blockIdx.y;
     const int chunk = blockIdx.x;
     const int nb = num_blocks(n);
@@ -219,10 +346,16 @@ scan_kernel(int n, int D, int chunk_blocks, int source, size_t stage_words, size
     const int b_end = min(nb, b_begin + chunk_blocks);
     const size_t cta = (size_t)u * gridDim.x + chunk;
 
-    // ---- prologue: active channels sorted by depth (desc), ties by channel
+    // ---- prologue: active channels sorted by depth (desc), ties by channel:
+    // a stable partition by depth from per-warp ballots over the D <= 128
+    // channels; plane slots and the fixed 32-channel staging groups follow
+    // arithmetically from the per-depth totals.
+    const int lane = tid & 31, wid = tid >> 5;
+    int t = 0;
+    fathom_run rr = {0, 0, 0, 0, 0, 0};
     if (tid < D) {
-        const fathom_run rr = runs[(size_t)u * D + tid];
-        int t = (int)(rr.n_words / (uint32_t)nb);
+        rr = runs[(size_t)u * D + tid];
+        t = (int)(rr.n_words / (uint32_t)nb);
         t = t > FATHOM_PLANES ? FATHOM_PLANES : t;
         // a channel whose staged run or scales would pass the unit's staging
         // stride (a plan larger than the staging area) is not read at all
@@ -231,103 +364,105 @@ scan_kernel(int n, int D, int chunk_blocks, int source, size_t stage_words, size
              (uint64_t)rr.dst_scale + (t > 0 ? (uint64_t)nb : 0) > stage_scales))
             t = 0;
         if (source == FATHOM_SRC_STORE && rr.src_word != (uint32_t)tid * FATHOM_PLANES * nb) t = 0;
-        sm.raw_t[tid] = t;
     }
-    if (tid == 0) { sm.sel_digit = 0; sm.sel_above = 0; sm.sel_bucket = 0; }
+    unsigned my_mask = 0;   // lanes of this warp with the same depth as this thread
+    if (tid < FATHOM_MAX_D) {
+#pragma unroll
+        for (int v = 1; v <= FATHOM_PLANES; ++v) {
+            const unsigned m = __ballot_sync(0xffffffffu, t == v);
+            if (t == v) my_mask = m;
+            if (lane == 0) sm.wcnt[v][wid] = __popc(m);
+        }
+    }
     if (tid < G) {
         sm.cnt[tid] = 0;
-        sm.cur[tid] = 0;
         sm.tau[tid] = 0;
-        sm.tau_s[tid] = -CUDART_INF_F;
     }
     __syncthreads();
-    if (tid < D) {
-        const int t = sm.raw_t[tid];
-        if (t > 0) {
-            int pos = 0;
-            for (int i = 0; i < D; ++i) {
-                const int ti = sm.raw_t[i];
-                pos += (ti > t || (ti == t && i < tid)) ? 1 : 0;
-            }
-            const fathom_run rr = runs[(size_t)u * D + tid];
-            const uint64_t wbase = (source == FATHOM_SRC_STORE)
-                                       ? ((uint64_t)u * D + tid) * FATHOM_PLANES * nb
-                                       : (uint64_t)u * stage_words + rr.dst_word;
-            const uint64_t sbase = (source == FATHOM_SRC_STORE)
-                                       ? ((uint64_t)u * D + tid) * nb
-                                       : (uint64_t)u * stage_scales + rr.dst_scale;
-            sm.ch_t[pos] = t;
-            sm.ch_scale[pos] = sbase;
-            const float sc = ldexpf(1.0f, -t);
-            for (int h = 0; h < G; ++h) sm.qs[pos][h] = q[((size_t)u * G + h) * D + tid] * sc;
-            // plane slots are assigned after the sort; stash the base for now
-            sm.plane_src[pos] = wbase;
+    int tot[FATHOM_PLANES + 1], start[FATHOM_PLANES + 1];   // per depth: count, first sorted index
+    {
+        int acc_start = 0;
+#pragma unroll
+        for (int v = FATHOM_PLANES; v >= 1; --v) {
+            int c = 0;
+#pragma unroll
+            for (int w2 = 0; w2 < FATHOM_MAX_D / 32; ++w2) c += sm.wcnt[v][w2];
+            tot[v] = c;
+            start[v] = acc_start;
+            acc_start += c;
         }
+        tot[0] = start[0] = 0;
     }
-    __syncthreads();
-    if (tid == 0) {
-        int A = 0;
-        for (int i = 0; i < D; ++i) A += sm.raw_t[i] > 0 ? 1 : 0;
-        sm.n_active = A;
-        // expand plane slots (in place from the back: slot index >= channel index)
-        int P = 0;
-        for (int a = 0; a < A; ++a) P += sm.ch_t[a];
-        int slot = P;
-        for (int a = A - 1; a >= 0; --a) {
-            const int t = sm.ch_t[a];
-            const uint64_t base = sm.plane_src[a];
-            slot -= t;
-            for (int p = t - 1; p >= 0; --p) sm.plane_src[slot + p] = base + (uint64_t)p * nb;
+    const int A = tot[1] + tot[2] + tot[3] + tot[4];
+    // first plane slot of sorted channel a: planes of all channels before it
+    auto slot_of = [&](int a) {
+        int sl = 0;
+#pragma unroll
+        for (int v = 1; v <= FATHOM_PLANES; ++v) {
+            const int lo = start[v], hi = start[v] + tot[v];
+            const int ov = max(0, min(a, hi) - lo);
+            sl += v * ov;
         }
-        // groups of consecutive channels: <= kPG planes and <= CHG channels
-        int ng = 0, a = 0, p0 = 0;
-        while (a < A) {
-            GroupDesc g;
-            g.a0 = a;
-            g.p0 = p0;
-            g.n4 = g.n3 = g.n2 = g.n1 = 0;
-            int planes_in = 0, chans = 0;
-            while (a < A && planes_in + sm.ch_t[a] <= kPG && chans < ScanCfg<G>::CHG) {
-                const int t = sm.ch_t[a];
-                if (t == 4) ++g.n4; else if (t == 3) ++g.n3; else if (t == 2) ++g.n2; else ++g.n1;
-                planes_in += t;
-                ++chans;
-                ++a;
-            }
-            p0 += planes_in;
-            sm.grp[ng++] = g;
-        }
-        sm.n_groups = ng;
+        return sl;
+    };
+    if (tid < D && t > 0) {
+        int pos = start[t] + __popc(my_mask & ((1u << lane) - 1u));
+        for (int w2 = 0; w2 < wid; ++w2) pos += sm.wcnt[t][w2];
+        const uint64_t wbase = (source == FATHOM_SRC_STORE)
+                                   ? ((uint64_t)u * D + tid) * FATHOM_PLANES * nb
+                                   : (uint64_t)u * stage_words + rr.dst_word;
+        const uint64_t sbase = (source == FATHOM_SRC_STORE)
+                                   ? ((uint64_t)u * D + tid) * nb
+                                   : (uint64_t)u * stage_scales + rr.dst_scale;
+        sm.ch_t[pos] = t;
+        sm.ch_scale[pos] = sbase;
+        const float sc = ldexpf(1.0f, -t);
+        for (int h = 0; h < G; ++h) sm.qs[pos][h] = q[((size_t)u * G + h) * D + tid] * sc;
+        const int sl = slot_of(pos);
+        for (int p = 0; p < t; ++p) sm.plane_src[sl + p] = wbase + (uint64_t)p * nb;
     }
+    const int n_groups = (A + kCHG - 1) / kCHG;
+    if (tid < n_groups) {
+        GroupDesc g;
+        g.a0 = tid * kCHG;
+        const int a1 = min(A, g.a0 + kCHG);
+        g.p0 = slot_of(g.a0);
+        int nv[FATHOM_PLANES + 1];
+#pragma unroll
+        for (int v = 1; v <= FATHOM_PLANES; ++v)
+            nv[v] = max(0, min(a1, start[v] + tot[v]) - max(g.a0, start[v]));
+        g.n4 = nv[4]; g.n3 = nv[3]; g.n2 = nv[2]; g.n1 = nv[1];
+        sm.grp[tid] = g;
+    }
+    if (tid == 0) sm.n_groups = n_groups;
     __syncthreads();
 
     const int ng = sm.n_groups;
     const int bl = tid >> 3;                 // block within the sub-chunk
     const uint32_t r = (uint32_t)(tid & 7);  // token offset within a byte lane
 
+    uint64_t tau[G];                         // per-head thresholds (same in every thread)
+#pragma unroll
+    for (int h = 0; h < G; ++h) tau[h] = 0;
+    bool first = true;
+
     for (int sb = b_begin; sb < b_end; sb += kSubBlocks) {
         const int nblk = min(kSubBlocks, b_end - sb);
         // make room in every head's candidate list before this sub-chunk
         if (k_sel > 0) {
+#pragma unroll 1
             for (int h = 0; h < G; ++h) {
-                if (sm.cnt[h] + kSubTokens > cap) {
-                    uint64_t *base = cand + (cta * G + h) * 2 * (size_t)cap;
-                    const uint64_t *srcl = base + (size_t)sm.cur[h] * cap;
-                    uint64_t *dstl = base + (size_t)(1 - sm.cur[h]) * cap;
-                    int kept;
-                    const int cnt_h = min(sm.cnt[h], cap);
-                    const uint64_t T = radix_threshold(sm, srcl, cnt_h, k_sel, kPruneSlack, &kept);
-                    const int c = compact_keys(sm, srcl, cnt_h, T, dstl, cap);
-                    if (tid == 0) {
-                        sm.cnt[h] = c;
-                        sm.cur[h] = 1 - sm.cur[h];
-                        sm.tau[h] = T;
-                        const uint32_t hi = (uint32_t)(T >> 32);
-                        sm.tau_s[h] = (hi <= 0x00800000u) ? -CUDART_INF_F : unorder_f32(hi);
-                    }
+                const int c = sm.cnt[h];
+                if (c + kSubTokens > cap) {
+                    uint64_t *lst = cand + (cta * G + h) * (size_t)cap;
+                    uint64_t T;
+                    const int nc = prune_list<kListKPT>(sm.sel1, lst, min(c, cap), k_sel, kPruneSlack, &T);
+                    if (tid == 0) { sm.cnt[h] = nc; sm.tau[h] = T; }
                     __syncthreads();
                 }
             }
+#pragma unroll
+            for (int h = 0; h < G; ++h) tau[h] = sm.tau[h];
         }
 
         float acc[8][G];
@@ -375,220 +510,227 @@ scan_kernel(int n, int D, int chunk_blocks, int source, size_t stage_words, size
             }
         }
 
-        // ---- epilogue: debug scores, forced tokens, candidates
+        // ---- epilogue: debug scores, forced tokens, then order words of the scores
         const int beta = sb + bl;
-        uint64_t pass = 0;   // bit m * G + h
+        uint32_t okey[8][G];                     // order_f32(score): the high word of a key
+        unsigned cvm = 0;                        // bit m: a candidate (valid, not forced)
 #pragma unroll
         for (int m = 0; m < 8; ++m) {
             const int i = beta * 64 + (int)r + 8 * (m & 3) + 32 * (m >> 2);
             const bool valid = (bl < nblk) && (i < n);
-            if (!valid) continue;
-            if (scores_opt) {
+            const bool forced = (i < ns || i >= r0);
+            if (valid && !forced) cvm |= 1u << m;
+            if (valid && scores_opt) {
 #pragma unroll
                 for (int h = 0; h < G; ++h) scores_opt[((size_t)u * G + h) * n + i] = acc[m][h];
             }
-            if (i < ns || i >= r0) {
+            if (valid && forced) {
                 const int slot = (i < ns) ? i : ns + (i - r0);
 #pragma unroll
                 for (int h = 0; h < G; ++h) forced_scores[((size_t)u * G + h) * nf + slot] = acc[m][h];
-            } else if (k_sel > 0) {
+            }
+#pragma unroll
+            for (int h = 0; h < G; ++h) okey[m][h] = order_f32(acc[m][h]);
+        }
+        auto key_of = [&](int m, int h) -> uint64_t {
+            const uint32_t i = (uint32_t)(beta * 64 + (int)r + 8 * (m & 3) + 32 * (m >> 2));
+            return ((uint64_t)okey[m][h] << 32) | (uint64_t)(0xffffffffu - i);
+        };
+        if (k_sel > 0) {
+            if (first) {
+                // exact top-k' of this first sub-chunk, all heads at once, from registers
+                uint64_t T[G];
+                int kept[G];
+                select_thresholds<G>(sm.selg, [&](auto f) {
+#pragma unroll
+                    for (int m = 0; m < 8; ++m)
+                        static_for<0, G>([&](auto h) { f(h, (cvm >> m) & 1u, key_of(m, h)); });
+                }, k_sel, 0, T, kept);
+#pragma unroll
+                for (int h = 0; h < G; ++h) tau[h] = T[h];
+                if (tid < G) sm.tau[tid] = T[tid];
+                first = false;
+            }
+            bool any = false;   // cheap pre-check on the high words
+#pragma unroll
+            for (int m = 0; m < 8; ++m)
 #pragma unroll
                 for (int h = 0; h < G; ++h)
-                    if (acc[m][h] >= sm.tau_s[h]) pass |= 1ull << (m * G + h);
-            }
-        }
-        if (__any_sync(0xffffffffu, pass != 0)) {
+                    any |= ((cvm >> m) & 1u) && okey[m][h] >= (uint32_t)(tau[h] >> 32);
+            if (__any_sync(0xffffffffu, any)) {
+                static_for<0, G>([&](auto h) {
+                    uint64_t *lst = cand + (cta * G + h) * (size_t)cap;
 #pragma unroll
-            for (int h = 0; h < G; ++h) {
-                uint64_t *lst = cand + (cta * G + h) * 2 * (size_t)cap + (size_t)sm.cur[h] * cap;
-                const uint64_t tau = sm.tau[h];
-#pragma unroll
-                for (int m = 0; m < 8; ++m) {
-                    const int i = beta * 64 + (int)r + 8 * (m & 3) + 32 * (m >> 2);
-                    uint64_t key = 0;
-                    bool p = (pass >> (m * G + h)) & 1ull;
-                    if (p) {
-                        key = make_key(acc[m][h], (uint32_t)i);
-                        p = key >= tau;
+                    for (int m = 0; m < 8; ++m) {
+                        const uint64_t kk = key_of(m, h);
+                        const bool p = ((cvm >> m) & 1u) && kk >= tau[h];
+                        const unsigned bal = __ballot_sync(0xffffffffu, p);
+                        if (bal) {
+                            int base = 0;
+                            const int leader = __ffs(bal) - 1;
+                            if (lane == leader) base = atomicAdd(&sm.cnt[h], __popc(bal));
+                            base = __shfl_sync(0xffffffffu, base, leader);
+                            const int pos = base + __popc(bal & ((1u << lane) - 1u));
+                            if (p && pos < cap) lst[pos] = kk;
+                        }
                     }
-                    const unsigned bal = __ballot_sync(0xffffffffu, p);
-                    if (bal) {
-                        int base = 0;
-                        const int leader = __ffs(bal) - 1;
-                        if (lane == leader) base = atomicAdd(&sm.cnt[h], __popc(bal));
-                        base = __shfl_sync(0xffffffffu, base, leader);
-                        const int pos = base + __popc(bal & ((1u << lane) - 1u));
-                        if (p && pos < cap) lst[pos] = key;
-                    }
-                }
+                });
             }
         }
         __syncthreads();
     }
 
-    // ---- final prune to at most k' + slack keys per head, then publish
+    // ---- cut every list to its exact top-k', then publish the counts
     if (k_sel > 0) {
+#pragma unroll 1
         for (int h = 0; h < G; ++h) {
-            if (sm.cnt[h] > k_sel + kPruneSlack) {
-                uint64_t *base = cand + (cta * G + h) * 2 * (size_t)cap;
-                const uint64_t *srcl = base + (size_t)sm.cur[h] * cap;
-                uint64_t *dstl = base + (size_t)(1 - sm.cur[h]) * cap;
-                int kept;
-                const int cnt_h = min(sm.cnt[h], cap);
-                const uint64_t T = radix_threshold(sm, srcl, cnt_h, k_sel, kPruneSlack, &kept);
-                const int c = compact_keys(sm, srcl, cnt_h, T, dstl, cap);
-                if (tid == 0) {
-                    sm.cnt[h] = c;
-                    sm.cur[h] = 1 - sm.cur[h];
-                }
+            const int c = min(sm.cnt[h], cap);
+            if (c > k_sel) {
+                uint64_t *lst = cand + (cta * G + h) * (size_t)cap;
+                uint64_t T;
+                const int nc = prune_list<kListKPT>(sm.sel1, lst, c, k_sel, 0, &T);
+                if (tid == 0) sm.cnt[h] = nc;
                 __syncthreads();
             }
         }
     }
-    if (tid < G) cand_cnt[cta * G + tid] = min(sm.cnt[tid], cap) | (sm.cur[tid] << 30);
+    if (tid < G) cand_cnt[cta * G + tid] = min(sm.cnt[tid], cap);
 }
 
 // ---------------------------------------------------------------------------
-// Merge: one CTA per (head, unit).  Exact top-k' of the chunks' candidate
-// lists, plus the forced tokens, ascending by index.
+// Merge: grid (parts, G, units).  Part p of (unit, head) streams the
+// candidate lists of chunks [p S / P, (p + 1) S / P) through a shared-memory
+// buffer, pruning it to the exact top-k' whenever the next window would not
+// fit; it writes its top-k' to the workspace and takes a ticket.  The last
+// part to finish streams the P partial lists the same way, sorts the exact
+// top-k' by token index and writes it between the forced sink and recent
+// tokens.  With P = 1 the single part finishes directly.
 constexpr int kMThreads = 512;
+constexpr int kMBuf = 8192;                  // keys in the shared-memory buffer
+constexpr int kMKPT = kMBuf / kMThreads;     // register keys per thread for a buffer prune
 
 struct MergeSmem {
-    unsigned hist[256];
-    unsigned lane_sum[32];
-    int sel_digit, sel_above, sel_bucket;
-    int new_cnt;
-    int total;
-    uint64_t sel[FATHOM_MAX_K];
+    SelScratch<1> sel;
+    uint64_t buf[kMBuf];
+    int off[FATHOM_MERGE_MAX_LISTS + 1];     // prefix sums of the streamed lists' counts
+    int count;
+    int is_last;
 };
 
-// radix select over the union of `chunks` lists (exact).
-__device__ uint64_t merge_threshold(MergeSmem &sm, const uint64_t *cand, const int *cnts, int chunks,
-                                    size_t list_stride, size_t cap, int target) {
+// Streams `nl` lists (list l: base(l), count(l)) into sm.buf and leaves the
+// exact top-k' (or everything, if fewer) in sm.buf[0 .. sm.count).
+template <typename Base, typename Count>
+__device__ void stream_select(MergeSmem &sm, int nl, Base base, Count count, int k_sel) {
     const int tid = threadIdx.x;
-    const int lane = tid & 31, warp = tid >> 5;
-    uint64_t prefix = 0, pmask = 0;
-    int above = 0;
-    for (int shift = 56; shift >= 0; shift -= 8) {
-        for (int i = tid; i < 256; i += blockDim.x) sm.hist[i] = 0;
-        __syncthreads();
-        for (int c = 0; c < chunks; ++c) {
-            const int cc = cnts[(size_t)c * list_stride];
-            const int cnt = min(cc & 0x3fffffff, (int)cap), half = (cc >> 30) & 1;
-            const uint64_t *lst = cand + (size_t)c * list_stride * 2 * cap + (size_t)half * cap;
-            for (int e = tid; e < cnt; e += blockDim.x) {
-                const uint64_t key = lst[e];
-                if ((key & pmask) == prefix) atomicAdd(&sm.hist[(key >> shift) & 255], 1u);
-            }
-        }
-        __syncthreads();
-        if (warp == 0) {
-            unsigned loc = 0;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) loc += sm.hist[255 - 8 * lane - i];
-            unsigned incl = loc;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const unsigned y = __shfl_up_sync(0xffffffffu, incl, o);
-                if (lane >= o) incl += y;
-            }
-            const unsigned excl = incl - loc;
-            const unsigned need = (unsigned)(target - above);
-            if (excl < need && need <= incl) {
-                unsigned c = excl;
-                for (int i = 0; i < 8; ++i) {
-                    const int bin = 255 - 8 * lane - i;
-                    const unsigned hb = sm.hist[bin];
-                    if (c + hb >= need) {
-                        sm.sel_digit = bin;
-                        sm.sel_above = (int)c;
-                        sm.sel_bucket = (int)hb;
-                        break;
-                    }
-                    c += hb;
-                }
-            }
-        }
-        __syncthreads();
-        const int d = sm.sel_digit;
-        above += sm.sel_above;
-        const int hb = sm.sel_bucket;
-        prefix |= (uint64_t)d << shift;
-        pmask |= (uint64_t)255 << shift;
-        __syncthreads();
-        if (above + hb == target || shift == 0) return prefix;
+    if (tid == 0) {
+        int o = 0;
+        for (int l = 0; l < nl; ++l) { sm.off[l] = o; o += count(l); }
+        sm.off[nl] = o;
+        sm.count = 0;
     }
-    return prefix;
+    __syncthreads();
+    const int total = sm.off[nl];
+    int done = 0;
+    while (done < total) {
+        int room = kMBuf - sm.count;
+        if (room < kMThreads) {              // make room: cut the buffer to its exact top-k'
+            uint64_t T;
+            const int nc = prune_list<kMKPT>(sm.sel, sm.buf, sm.count, k_sel, 0, &T);
+            __syncthreads();
+            if (tid == 0) sm.count = nc;
+            __syncthreads();
+            room = kMBuf - nc;
+        }
+        const int take = min(room, total - done);
+        const int c0 = sm.count;
+        for (int e = tid; e < take; e += blockDim.x) {
+            const int g = done + e;
+            int lo = 0, hi = nl;              // list holding flattened index g
+            while (hi - lo > 1) {
+                const int mid = (lo + hi) >> 1;
+                if (sm.off[mid] <= g) lo = mid; else hi = mid;
+            }
+            sm.buf[c0 + e] = base(lo)[g - sm.off[lo]];
+        }
+        __syncthreads();
+        if (tid == 0) sm.count = c0 + take;
+        __syncthreads();
+        done += take;
+    }
+    if (sm.count > k_sel) {
+        uint64_t T;
+        const int nc = prune_list<kMKPT>(sm.sel, sm.buf, sm.count, k_sel, 0, &T);
+        __syncthreads();
+        if (tid == 0) sm.count = nc;
+    }
+    __syncthreads();
 }
 
 __global__ void __launch_bounds__(kMThreads)
-merge_kernel(int n, int G, int k, int k_sel, int ns, int r0, int nf, int chunks, int cap,
+merge_kernel(int n, int G, int k, int k_sel, int ns, int r0, int nf, int chunks, int parts, int cap,
              const uint64_t *__restrict__ cand, const int *__restrict__ cand_cnt,
-             const float *__restrict__ forced_scores, int32_t *__restrict__ out_idx,
+             const float *__restrict__ forced_scores, uint64_t *__restrict__ part_keys,
+             int *__restrict__ part_cnt, unsigned *__restrict__ ticket, int32_t *__restrict__ out_idx,
              float *__restrict__ out_score) {
     extern __shared__ __align__(16) unsigned char msmem_raw[];
     MergeSmem &sm = *reinterpret_cast<MergeSmem *>(msmem_raw);
-    const int h = blockIdx.x, u = blockIdx.y;
-    const int tid = threadIdx.x, lane = tid & 31;
-    int32_t *oi = out_idx + ((size_t)u * G + h) * k;
-    float *os = out_score + ((size_t)u * G + h) * k;
-    const float *fs = forced_scores + ((size_t)u * G + h) * nf;
-    // forced tokens: sinks first, recent last
-    for (int e = tid; e < ns; e += blockDim.x) { oi[e] = e; os[e] = fs[e]; }
-    for (int e = tid; e < n - r0; e += blockDim.x) {
-        oi[ns + k_sel + e] = r0 + e;
-        os[ns + k_sel + e] = fs[ns + e];
+    const int p = blockIdx.x, h = blockIdx.y, u = blockIdx.z;
+    const int tid = threadIdx.x;
+    const size_t uh = (size_t)u * G + h;
+    int32_t *oi = out_idx + uh * k;
+    float *os = out_score + uh * k;
+    if (p == 0) {
+        // forced tokens: sinks first, recent last
+        const float *fs = forced_scores + uh * nf;
+        for (int e = tid; e < ns; e += blockDim.x) { oi[e] = e; os[e] = fs[e]; }
+        for (int e = tid; e < n - r0; e += blockDim.x) {
+            oi[ns + k_sel + e] = r0 + e;
+            os[ns + k_sel + e] = fs[ns + e];
+        }
     }
     if (k_sel == 0) return;
 
-    if (tid == 0) { sm.sel_digit = 0; sm.sel_above = 0; sm.sel_bucket = 0; }
-    for (int e = tid; e < FATHOM_MAX_K; e += blockDim.x) sm.sel[e] = 0;
-    __syncthreads();
-    const uint64_t *c0 = cand + ((size_t)u * chunks * G + h) * 2 * (size_t)cap;
-    const int *n0 = cand_cnt + (size_t)u * chunks * G + h;
-    const uint64_t T = merge_threshold(sm, c0, n0, chunks, (size_t)G, (size_t)cap, k_sel);
-
-    // gather the k' keys >= T
-    if (tid == 0) sm.new_cnt = 0;
-    __syncthreads();
-    for (int c = 0; c < chunks; ++c) {
-        const int cc = n0[(size_t)c * G];
-        const int cnt = min(cc & 0x3fffffff, cap), half = (cc >> 30) & 1;
-        const uint64_t *lst = c0 + (size_t)c * G * 2 * cap + (size_t)half * cap;
-        for (int e0 = 0; e0 < cnt; e0 += blockDim.x) {
-            const int e = e0 + tid;
-            uint64_t key = 0;
-            bool keep = false;
-            if (e < cnt) { key = lst[e]; keep = key >= T; }
-            const unsigned bal = __ballot_sync(0xffffffffu, keep);
-            int base = 0;
-            if (lane == 0 && bal) base = atomicAdd(&sm.new_cnt, __popc(bal));
-            base = __shfl_sync(0xffffffffu, base, 0);
-            const int pos = base + __popc(bal & ((1u << lane) - 1u));
-            if (keep && pos < k_sel) sm.sel[pos] = key;
-        }
+    const int c_lo = (int)((long long)p * chunks / parts);
+    const int c_hi = (int)((long long)(p + 1) * chunks / parts);
+    stream_select(sm, c_hi - c_lo,
+                  [&](int l) { return cand + (((size_t)u * chunks + c_lo + l) * G + h) * (size_t)cap; },
+                  [&](int l) { return min(cand_cnt[((size_t)u * chunks + c_lo + l) * G + h], cap); },
+                  k_sel);
+    if (parts > 1) {
+        uint64_t *pk = part_keys + (uh * parts + p) * (size_t)k_sel;
+        for (int e = tid; e < sm.count; e += blockDim.x) pk[e] = sm.buf[e];
+        if (tid == 0) part_cnt[uh * parts + p] = sm.count;
+        __threadfence();
+        __syncthreads();
+        if (tid == 0) sm.is_last = (atomicAdd(ticket + uh, 1u) == (unsigned)parts - 1u) ? 1 : 0;
+        __syncthreads();
+        if (!sm.is_last) return;
+        __threadfence();
+        stream_select(sm, parts,
+                      [&](int l) { return (const uint64_t *)(part_keys + (uh * parts + l) * (size_t)k_sel); },
+                      [&](int l) { return __ldcg(part_cnt + uh * parts + l); }, k_sel);
+        if (tid == 0) ticket[uh] = 0u;   // ready for the next call
     }
+    // bitonic sort of the k' winners by token index; padding keys 0 (index 0xffffffff) sort last
+    int P2 = 1;
+    while (P2 < k_sel) P2 <<= 1;
+    for (int e = sm.count + tid; e < P2; e += blockDim.x) sm.buf[e] = 0;
     __syncthreads();
-    // bitonic sort by token index ascending (key_index); pad with index 0xffffffff
-    int P = 1;
-    while (P < k_sel) P <<= 1;
-    for (int e = k_sel + tid; e < P; e += blockDim.x) sm.sel[e] = 0;   // key 0 -> index 0xffffffff
-    __syncthreads();
-    for (int size = 2; size <= P; size <<= 1) {
+    for (int size = 2; size <= P2; size <<= 1) {
         for (int stride = size >> 1; stride > 0; stride >>= 1) {
-            for (int e = tid; e < P / 2; e += blockDim.x) {
+            for (int e = tid; e < P2 / 2; e += blockDim.x) {
                 const int lo = 2 * stride * (e / stride) + (e % stride);
                 const int hi = lo + stride;
                 const bool up = ((lo & size) == 0);
-                const uint64_t a = sm.sel[lo], b = sm.sel[hi];
+                const uint64_t a = sm.buf[lo], b = sm.buf[hi];
                 const bool swap = up ? (key_index(a) > key_index(b)) : (key_index(a) < key_index(b));
-                if (swap) { sm.sel[lo] = b; sm.sel[hi] = a; }
+                if (swap) { sm.buf[lo] = b; sm.buf[hi] = a; }
             }
             __syncthreads();
         }
     }
     for (int e = tid; e < k_sel; e += blockDim.x) {
-        const uint64_t key = sm.sel[e];
+        const uint64_t key = sm.buf[e];
         oi[ns + e] = (int32_t)key_index(key);
         os[ns + e] = key_score(key);
     }
@@ -605,10 +747,14 @@ static int launch_g(const fathom_shape &s, const uint64_t *planes, const uint16_
     const ScanWorkspace wl = scan_workspace_layout(s);
     const int k_sel = s.k - f.nf;
     const int cap = scan_cand_cap(s);
+    if (cap > kListKPT * NT) { set_error("scan: candidate capacity %d too large", cap); return FATHOM_EINVAL; }
     char *w = (char *)ws;
     uint64_t *cand = (uint64_t *)(w + wl.cand_off);
     int *cnt = (int *)(w + wl.cnt_off);
     float *forced = (float *)(w + wl.forced_off);
+    uint64_t *pkeys = (uint64_t *)(w + wl.part_keys_off);
+    int *pcnt = (int *)(w + wl.part_cnt_off);
+    unsigned *ticket = (unsigned *)(w + wl.ticket_off);
     const size_t smem = sizeof(ScanSmem<G>);
     if (s.units > 65535) { set_error("scan: too many units for one launch"); return FATHOM_EINVAL; }
     ensure_smem(scan_kernel<G>, smem);
@@ -620,9 +766,9 @@ static int launch_g(const fathom_shape &s, const uint64_t *planes, const uint16_
     if (rc) return rc;
     const size_t msmem = sizeof(MergeSmem);
     ensure_smem(merge_kernel, msmem);
-    merge_kernel<<<dim3(s.G, s.units), kMThreads, msmem, st>>>(s.n, s.G, s.k, k_sel, f.ns, f.r0,
-                                                               f.nf > 0 ? f.nf : 1, sg.chunks, cap,
-                                                               cand, cnt, forced, idx, score);
+    merge_kernel<<<dim3(wl.parts, s.G, s.units), kMThreads, msmem, st>>>(
+        s.n, s.G, s.k, k_sel, f.ns, f.r0, f.nf > 0 ? f.nf : 1, sg.chunks, wl.parts, cap, cand, cnt,
+        forced, pkeys, pcnt, ticket, idx, score);
     return launch_status("merge_kernel");
 }
 

@@ -3,11 +3,11 @@
 // precision; §2: each head attends exactly over its own selected set, with no
 // mass redistribution for the rest).
 //
-// Grid: (splits, units).  Every CTA rebuilds the unit's union in shared
-// memory from the G sorted index lists (an entry is owned by the first head
-// that lists it; its head mask comes from binary searches in the other
-// lists), then takes a slice of kAttnRows union rows.  Each warp streams rows
-// (K and V, bf16, loaded once for all heads that selected the row), computes
+// Grid: (G * ceil(k / kAttnRows), units).  A CTA takes a slice of one head's
+// sorted kept list and handles the rows that head owns (the first head, in
+// order, that lists the token), so the union of the heads' winners is fetched
+// exactly once; a row's head mask comes from binary searches in the other
+// lists.  Each warp keeps several rows in flight (K and V, bf16), computes
 // q_h . k / sqrt(D) for the heads in the row's mask and keeps an online
 // softmax state (running max, sum, weighted V) per head.  Warp states are
 // merged per CTA and written to the workspace; the last CTA of the unit (an
@@ -19,26 +19,23 @@ namespace fathom {
 constexpr int NA = kAttnThreads;
 constexpr int kWarps = NA / 32;
 
-// Shared memory: a fixed header, then wo[warps][G][D] floats, lists[G*k] and
-// uidx[G*k] ints and umask[G*k] bytes, laid out by attn_smem_layout.
+// Shared memory: a fixed header, then wo[warps][G][D] floats and the G
+// index lists (G * k ints), laid out by attn_smem_layout.
 struct AttnHeader {
-    int wsum[kWarps];
     int is_last;
     float wm[kWarps][FATHOM_MAX_G];
     float wl[kWarps][FATHOM_MAX_G];
 };
 
 struct AttnLayout {
-    size_t wo, lists, uidx, umask, total;
+    size_t wo, lists, total;
 };
 
 __host__ __device__ inline AttnLayout attn_smem_layout(int G, int k, int D) {
     AttnLayout L;
     L.wo = (sizeof(AttnHeader) + 15) & ~(size_t)15;
     L.lists = L.wo + (size_t)kWarps * G * D * sizeof(float);
-    L.uidx = L.lists + (size_t)G * k * sizeof(int);
-    L.umask = L.uidx + (size_t)G * k * sizeof(int);
-    L.total = (L.umask + (size_t)G * k + 15) & ~(size_t)15;
+    L.total = (L.lists + (size_t)G * k * sizeof(int) + 15) & ~(size_t)15;
     return L;
 }
 
@@ -51,10 +48,21 @@ __device__ __forceinline__ bool contains(const int *lst, int k, int x) {
     return lo < k && lst[lo] == x;
 }
 
-__device__ __forceinline__ float bf16f(uint16_t b) { return __uint_as_float(((uint32_t)b) << 16); }
+__device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
+constexpr int kRowsInFlight = 4;   // rows a warp loads before using them
+
+// Grid: (G * chunks_per_head, units).  CTA (h, c) takes entries [c R, c R + R)
+// of head h's sorted list and handles the rows that h owns, i.e. that no lower
+// head lists: every row of the union is fetched exactly once.  The row's head
+// mask (which heads attend to it) comes from binary searches in the other
+// heads' lists.  Lane l holds channels 4l .. 4l+3 (D = 128: one 8-byte load of
+// K and one of V per row); other D take the general path with channel
+// j = l + 32 e.
+template <bool kVec>
 __global__ void __launch_bounds__(NA)
-attn_kernel(int n, int D, int G, int k, int splits, const uint16_t *__restrict__ krows,
+attn_kernel(int n, int D, int G, int k, int cph, int splits, const uint16_t *__restrict__ krows,
             const uint16_t *__restrict__ vrows, const float *__restrict__ q,
             const int32_t *__restrict__ topk, float *__restrict__ out, float *__restrict__ part,
             unsigned *__restrict__ ticket) {
@@ -63,60 +71,18 @@ attn_kernel(int n, int D, int G, int k, int splits, const uint16_t *__restrict__
     const AttnLayout lay = attn_smem_layout(G, k, D);
     float *wo = reinterpret_cast<float *>(asmem_raw + lay.wo);          // [warp][h][D]
     int *lists = reinterpret_cast<int *>(asmem_raw + lay.lists);
-    int *uidx = reinterpret_cast<int *>(asmem_raw + lay.uidx);
-    unsigned char *umask = asmem_raw + lay.umask;
     const int s = blockIdx.x, u = blockIdx.y;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int GK = G * k;
+    const int hown = s / cph;
+    const int e_begin = (s % cph) * kAttnRows;
+    const int e_end = min(k, e_begin + kAttnRows);
 
     for (int e = tid; e < GK; e += NA) lists[e] = topk[(size_t)u * GK + e];
     __syncthreads();
 
-    // ---- union: entry e = (h, r) is owned if no lower head lists the same token
-    // pass 1: counts per warp (entries processed in chunks of NA, in order)
-    int running = 0;
-    for (int e0 = 0; e0 < GK; e0 += NA) {
-        const int e = e0 + tid;
-        bool own = false;
-        unsigned char mask = 0;
-        int x = 0;
-        if (e < GK) {
-            const int h = e / k;
-            x = lists[e];
-            own = true;
-            mask = (unsigned char)(1u << h);
-            for (int h2 = 0; h2 < G; ++h2) {
-                if (h2 == h) continue;
-                if (contains(lists + h2 * k, k, x)) {
-                    mask |= (unsigned char)(1u << h2);
-                    if (h2 < h) own = false;
-                }
-            }
-        }
-        const unsigned bal = __ballot_sync(0xffffffffu, own);
-        if (lane == 0) sm.wsum[warp] = __popc(bal);
-        __syncthreads();
-        int before = running;
-        for (int w = 0; w < warp; ++w) before += sm.wsum[w];
-        int chunk_total = 0;
-        for (int w = 0; w < kWarps; ++w) chunk_total += sm.wsum[w];
-        if (own) {
-            const int pos = before + __popc(bal & ((1u << lane) - 1u));
-            uidx[pos] = x;
-            umask[pos] = mask;
-        }
-        running += chunk_total;
-        __syncthreads();
-    }
-    const int nu = running;
-
-    // ---- this CTA's slice of union rows
-    const int r_begin = s * kAttnRows;
-    const int r_end = min(nu, r_begin + kAttnRows);
     const float scale = 1.0f / sqrtf((float)D);   // 1/sqrt(D), correctly rounded
-    const int EPL = (D + 31) / 32;          // elements per lane (<= 4)
-    float m_h[FATHOM_MAX_G], l_h[FATHOM_MAX_G], o_h[FATHOM_MAX_G][4];
-    float qv[FATHOM_MAX_G][4];
+    float m_h[FATHOM_MAX_G], l_h[FATHOM_MAX_G], o_h[FATHOM_MAX_G][4], qv[FATHOM_MAX_G][4];
 #pragma unroll
     for (int h = 0; h < FATHOM_MAX_G; ++h) {
         m_h[h] = -CUDART_INF_F;
@@ -124,41 +90,76 @@ attn_kernel(int n, int D, int G, int k, int splits, const uint16_t *__restrict__
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
             o_h[h][e] = 0.0f;
-            const int j = lane + 32 * e;
-            qv[h][e] = (h < G && e < EPL && j < D) ? q[((size_t)u * G + h) * D + j] : 0.0f;
+            const int j = kVec ? 4 * lane + e : lane + 32 * e;
+            qv[h][e] = (h < G && j < D) ? q[((size_t)u * G + h) * D + j] : 0.0f;
         }
     }
-    for (int rr = r_begin + warp; rr < r_end; rr += kWarps) {
-        const int i = uidx[rr];
-        if (i < 0 || i >= n) continue;    // not a token of this unit: contributes nothing
-        const unsigned mask = umask[rr];
-        const uint16_t *kr = krows + ((size_t)u * n + i) * D;
-        const uint16_t *vr = vrows + ((size_t)u * n + i) * D;
-        float kv[4], vv[4];
+    const int *own = lists + (size_t)hown * k;
+    for (int e0 = e_begin + warp * kRowsInFlight; e0 < e_end; e0 += kWarps * kRowsInFlight) {
+        int row[kRowsInFlight];
+        unsigned mask[kRowsInFlight];
+        float kv[kRowsInFlight][4], vv[kRowsInFlight][4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const int j = lane + 32 * e;
-            const bool ok = e < EPL && j < D;
-            kv[e] = ok ? bf16f(__ldg(kr + j)) : 0.0f;
-            vv[e] = ok ? bf16f(__ldg(vr + j)) : 0.0f;
+        for (int r = 0; r < kRowsInFlight; ++r) {
+            const int e = e0 + r;
+            int i = -1;
+            unsigned m = 0;
+            if (e < e_end) {
+                i = own[e];
+                m = 1u << hown;
+                for (int h2 = 0; h2 < G; ++h2) {
+                    if (h2 == hown) continue;
+                    if (contains(lists + (size_t)h2 * k, k, i)) {
+                        if (h2 < hown) { m = 0; break; }   // a lower head owns this row
+                        m |= 1u << h2;
+                    }
+                }
+                if (i < 0 || i >= n) m = 0;                 // not a token of this unit
+            }
+            row[r] = i;
+            mask[r] = m;
+            const uint16_t *kr = krows + ((size_t)u * n + (m ? i : 0)) * D;
+            const uint16_t *vr = vrows + ((size_t)u * n + (m ? i : 0)) * D;
+            if (kVec) {
+                uint2 a = make_uint2(0u, 0u), b = make_uint2(0u, 0u);
+                if (m) {
+                    a = __ldg(reinterpret_cast<const uint2 *>(kr) + lane);
+                    b = __ldg(reinterpret_cast<const uint2 *>(vr) + lane);
+                }
+                kv[r][0] = bf16lo(a.x); kv[r][1] = bf16hi(a.x); kv[r][2] = bf16lo(a.y); kv[r][3] = bf16hi(a.y);
+                vv[r][0] = bf16lo(b.x); vv[r][1] = bf16hi(b.x); vv[r][2] = bf16lo(b.y); vv[r][3] = bf16hi(b.y);
+            } else {
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const int j = lane + 32 * c;
+                    const bool ok = m && j < D;
+                    kv[r][c] = ok ? __uint_as_float(((uint32_t)__ldg(kr + j)) << 16) : 0.0f;
+                    vv[r][c] = ok ? __uint_as_float(((uint32_t)__ldg(vr + j)) << 16) : 0.0f;
+                }
+            }
         }
 #pragma unroll
-        for (int h = 0; h < FATHOM_MAX_G; ++h) {
-            if (h >= G || !((mask >> h) & 1u)) continue;
-            float d = 0.0f;
+        for (int r = 0; r < kRowsInFlight; ++r) {
+            if (!mask[r]) continue;                         // warp-uniform
 #pragma unroll
-            for (int e = 0; e < 4; ++e) d = fmaf(qv[h][e], kv[e], d);
+            for (int h = 0; h < FATHOM_MAX_G; ++h) {
+                if (h >= G || !((mask[r] >> h) & 1u)) continue;
+                float d = 0.0f;
 #pragma unroll
-            for (int o = 16; o; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
-            const float logit = d * scale;
-            const float mn = fmaxf(m_h[h], logit);
-            const float corr = expf(m_h[h] - mn);
-            const float p = expf(logit - mn);
-            l_h[h] = l_h[h] * corr + p;
+                for (int c = 0; c < 4; ++c) d = fmaf(qv[h][c], kv[r][c], d);
 #pragma unroll
-            for (int e = 0; e < 4; ++e) o_h[h][e] = o_h[h][e] * corr + p * vv[e];
-            m_h[h] = mn;
+                for (int o = 16; o; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
+                const float logit = d * scale;
+                const float mn = fmaxf(m_h[h], logit);
+                const float corr = expf(m_h[h] - mn);
+                const float p = expf(logit - mn);
+                l_h[h] = l_h[h] * corr + p;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) o_h[h][c] = o_h[h][c] * corr + p * vv[r][c];
+                m_h[h] = mn;
+            }
         }
+        (void)row;
     }
     // ---- merge warps
 #pragma unroll
@@ -166,9 +167,9 @@ attn_kernel(int n, int D, int G, int k, int splits, const uint16_t *__restrict__
         if (h >= G) continue;
         if (lane == 0) { sm.wm[warp][h] = m_h[h]; sm.wl[warp][h] = l_h[h]; }
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const int j = lane + 32 * e;
-            if (e < EPL && j < D) wo[((size_t)warp * G + h) * D + j] = o_h[h][e];
+        for (int c = 0; c < 4; ++c) {
+            const int j = kVec ? 4 * lane + c : lane + 32 * c;
+            if (j < D) wo[((size_t)warp * G + h) * D + j] = o_h[h][c];
         }
     }
     __syncthreads();
@@ -224,9 +225,17 @@ int launch_sparse_attn(const fathom_shape &s, const uint16_t *krows, const uint1
     unsigned *ticket = (unsigned *)(w + wl.ticket_off);
     if (s.units > 65535) { set_error("sparse_attn: too many units for one launch"); return FATHOM_EINVAL; }
     const size_t smem = attn_smem_layout(s.G, s.k, s.D).total;
-    ensure_smem(attn_kernel, smem);
-    attn_kernel<<<dim3(wl.splits, s.units), NA, smem, st>>>(s.n, s.D, s.G, s.k, wl.splits, krows,
-                                                           vrows, q, idx, out, part, ticket);
+    const int cph = (s.k + kAttnRows - 1) / kAttnRows;   // CTAs per head
+    const bool vec = s.D == 128 && ((uintptr_t)krows % 8 == 0) && ((uintptr_t)vrows % 8 == 0);
+    if (vec) {
+        ensure_smem(attn_kernel<true>, smem);
+        attn_kernel<true><<<dim3(wl.splits, s.units), NA, smem, st>>>(
+            s.n, s.D, s.G, s.k, cph, wl.splits, krows, vrows, q, idx, out, part, ticket);
+    } else {
+        ensure_smem(attn_kernel<false>, smem);
+        attn_kernel<false><<<dim3(wl.splits, s.units), NA, smem, st>>>(
+            s.n, s.D, s.G, s.k, cph, wl.splits, krows, vrows, q, idx, out, part, ticket);
+    }
     return launch_status("attn_kernel");
 }
 
