@@ -47,6 +47,7 @@ SIGNATURES = {
     "fathom_scan_topk": (ctypes.c_int, [ctypes.POINTER(Shape), _vp, _vp, ctypes.c_int, _sz, _sz, _vp,
                                         _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "fathom_sparse_attn": (ctypes.c_int, [ctypes.POINTER(Shape), _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "fathom_sparse_attn_noalloc": (ctypes.c_int, [ctypes.POINTER(Shape), _vp, _vp, _vp, _vp, _vp, _vp]),
     "fathom_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(Shape), ctypes.c_int]),
     "fathom_last_error": (ctypes.c_char_p, []),
     "fathom_version": (ctypes.c_char_p, []),
@@ -234,6 +235,20 @@ def fathom_scan_topk(shape: Shape, planes, scales, runs, q, workspace, source=SR
           _p(runs), _p(q), _p(topk_idx), _p(topk_score), _p(scores), _p(workspace),
           workspace.numel(), _stream(stream))
     return topk_idx, topk_score
+
+
+def fathom_sparse_attn_noalloc(shape: Shape, k_rows, v_rows, q, topk_idx, out, stream=None):
+    """fathom_sparse_attn with the library's own fixed scratch (no workspace, no
+    allocation inside the call): for callers that may not allocate device memory.
+    `out` [U][G][D] fp32 must be provided by the caller."""
+    _check(k_rows, "k_rows", (torch.bfloat16, torch.int16), (shape.units, shape.n, shape.D))
+    _check(v_rows, "v_rows", (torch.bfloat16, torch.int16), (shape.units, shape.n, shape.D))
+    _check(q, "q", (torch.float32,), (shape.units, shape.G, shape.D))
+    _check(topk_idx, "topk_idx", (torch.int32,), (shape.units, shape.G, shape.k))
+    _check(out, "out", (torch.float32,), (shape.units, shape.G, shape.D))
+    _call("fathom_sparse_attn_noalloc", ctypes.byref(shape), _p(k_rows), _p(v_rows), _p(q),
+          _p(topk_idx), _p(out), _stream(stream))
+    return out
 
 
 def fathom_sparse_attn(shape: Shape, k_rows, v_rows, q, topk_idx, workspace, out=None, stream=None):

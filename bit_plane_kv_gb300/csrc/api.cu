@@ -284,4 +284,18 @@ int fathom_sparse_attn(const fathom_shape *shape, const uint16_t *k_rows, const 
                               (cudaStream_t)stream);
 }
 
+int fathom_sparse_attn_noalloc(const fathom_shape *shape, const uint16_t *k_rows,
+                               const uint16_t *v_rows, const float *q, const int32_t *topk_idx,
+                               float *out, void *stream) {
+    g_err[0] = 0;
+    int rc = check_shape(shape, true);
+    if (rc) return rc;
+    NONNULL(k_rows);
+    NONNULL(v_rows);
+    NONNULL(q);
+    NONNULL(topk_idx);
+    NONNULL(out);
+    return launch_sparse_attn_noalloc(*shape, k_rows, v_rows, q, topk_idx, out, (cudaStream_t)stream);
+}
+
 }  // extern "C"

@@ -120,5 +120,7 @@ int launch_scan_topk(const fathom_shape &s, const uint64_t *planes, const uint16
                      cudaStream_t st);
 int launch_sparse_attn(const fathom_shape &s, const uint16_t *krows, const uint16_t *vrows,
                        const float *q, const int32_t *idx, float *out, void *ws, cudaStream_t st);
+int launch_sparse_attn_noalloc(const fathom_shape &s, const uint16_t *krows, const uint16_t *vrows,
+                               const float *q, const int32_t *idx, float *out, cudaStream_t st);
 
 }  // namespace fathom

@@ -12,6 +12,8 @@
 // softmax state (running max, sum, weighted V) per head.  Warp states are
 // merged per CTA and written to the workspace; the last CTA of the unit (an
 // atomic ticket, no waiting) merges the splits and writes o_h.
+#include <mutex>
+
 #include "fathom_internal.cuh"
 
 namespace fathom {
@@ -237,6 +239,65 @@ int launch_sparse_attn(const fathom_shape &s, const uint16_t *krows, const uint1
             s.n, s.D, s.G, s.k, cph, wl.splits, krows, vrows, q, idx, out, part, ticket);
     }
     return launch_status("attn_kernel");
+}
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant.  Some callers cannot hand the library a workspace
+// of their own: a host framework that owns every byte of device memory and
+// forbids plug-ins from calling cudaMalloc (it would also synchronise the
+// device and fragment the framework's pool), or a latency-critical decode loop
+// that must not allocate at all.  For them the scratch (partial softmax
+// states and per-unit tickets) lives in this file-scope device array, which
+// every GPU that loads the library keeps until the process exits.
+constexpr size_t kNoAllocScratchBytes = (size_t)8 << 20;   // 8 MiB
+static __device__ __align__(256) unsigned char g_attn_scratch[kNoAllocScratchBytes];
+
+// The array's device address, looked up once per device with that device
+// current (in host code the symbol is only a host-side stand-in).
+static void *noalloc_scratch_ptr(int *status) {
+    static std::mutex mu;
+    static void *ptrs[64] = {nullptr};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess || dev < 0 || dev >= 64) {
+        set_error("sparse_attn_noalloc: cudaGetDevice: %s", cudaGetErrorString(e));
+        *status = FATHOM_ECUDA;
+        return nullptr;
+    }
+    std::lock_guard<std::mutex> lock(mu);
+    if (!ptrs[dev]) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_attn_scratch);
+        if (e != cudaSuccess || !p) {
+            set_error("sparse_attn_noalloc: cudaGetSymbolAddress: %s", cudaGetErrorString(e));
+            *status = FATHOM_ECUDA;
+            return nullptr;
+        }
+        ptrs[dev] = p;
+    }
+    *status = FATHOM_OK;
+    return ptrs[dev];
+}
+
+int launch_sparse_attn_noalloc(const fathom_shape &s, const uint16_t *krows, const uint16_t *vrows,
+                               const float *q, const int32_t *idx, float *out, cudaStream_t st) {
+    const AttnWorkspace wl = attn_workspace_layout(s);
+    if (wl.total > kNoAllocScratchBytes) {
+        set_error("sparse_attn_noalloc: this shape needs %zu bytes of scratch, more than the "
+                  "library's fixed %zu (use fathom_sparse_attn with a workspace)",
+                  wl.total, kNoAllocScratchBytes);
+        return FATHOM_EINVAL;
+    }
+    int rc = FATHOM_OK;
+    char *scratch = (char *)noalloc_scratch_ptr(&rc);
+    if (rc) return rc;
+    // the tickets must start at zero; the partial states are written before they are read
+    cudaError_t e = cudaMemsetAsync(scratch + wl.ticket_off, 0, wl.total - wl.ticket_off, st);
+    if (e != cudaSuccess) {
+        set_error("sparse_attn_noalloc: cudaMemsetAsync: %s", cudaGetErrorString(e));
+        return FATHOM_ECUDA;
+    }
+    return launch_sparse_attn(s, krows, vrows, q, idx, out, scratch, st);
 }
 
 }  // namespace fathom

@@ -198,6 +198,26 @@ int fathom_sparse_attn(const fathom_shape *shape, const uint16_t *k_rows,
                        const uint16_t *v_rows, const float *q, const int32_t *topk_idx,
                        float *out, void *workspace, size_t workspace_bytes, void *stream);
 
+/* fathom_sparse_attn without a workspace argument, for callers that cannot
+ * allocate device memory for the library: a host framework that owns all
+ * device memory and does not let plug-ins call cudaMalloc (which would also
+ * synchronise the device), or a decode loop that must never allocate.  The
+ * paper has no counterpart to this call; it is a packaging choice of this
+ * library.  Same arguments, same results as fathom_sparse_attn.
+ *   Scratch: a fixed 8 MiB array inside the library, held by every GPU that
+ *   loads the library until the process exits; shapes whose
+ *   fathom_workspace_size(shape, FATHOM_WS_SPARSE_ATTN) exceeds 8 MiB are
+ *   rejected with FATHOM_EINVAL and nothing is enqueued.
+ *   The first call on a device looks up the array's device address (with
+ *   that device current); make that first call before any stream capture.
+ *   Every call clears the array's ticket words on `stream` and then uses the
+ *   one shared array, so calls whose work overlaps on the GPU (other streams,
+ *   other threads) race and must be serialised by the caller.
+ *   Allocates nothing: no cudaMalloc, no cudaFree, no allocating library call. */
+int fathom_sparse_attn_noalloc(const fathom_shape *shape, const uint16_t *k_rows,
+                               const uint16_t *v_rows, const float *q, const int32_t *topk_idx,
+                               float *out, void *stream);
+
 /* Workspace bytes a call needs for this shape (0 if the shape is invalid). */
 size_t fathom_workspace_size(const fathom_shape *shape, int which);
 
