@@ -74,9 +74,17 @@ int scan_cand_cap(const fathom_shape &s) {
     return (cap + 255) / 256 * 256;   // <= 6400 for k <= 2048
 }
 
-int merge_parts(int chunks, int k_sel) {
-    long long keys = (long long)chunks * (k_sel > 0 ? k_sel : 1);
-    int p = (int)((keys + 4095) / 4096);
+int scan_m_sel(int chunks, int k_sel) {
+    if (k_sel <= 0) return 0;
+    int m = (4 * k_sel + chunks - 1) / chunks;
+    m = m < 64 ? 64 : m;
+    return m > k_sel ? k_sel : m;
+}
+
+int merge_parts(int chunks, int m_sel) {
+    // lists hold about 2m keys after the scan's final shrink
+    long long keys = (long long)chunks * 2 * (m_sel > 0 ? m_sel : 1);
+    int p = (int)((keys + 8191) / 8192);
     if (p > chunks) p = chunks;
     if (p > FATHOM_MERGE_MAX_LISTS) p = FATHOM_MERGE_MAX_LISTS;
     return p < 1 ? 1 : p;
@@ -88,16 +96,19 @@ ScanWorkspace scan_workspace_layout(const fathom_shape &s) {
     int k_sel = s.k - f.nf;
     if (k_sel < 1) k_sel = 1;
     ScanWorkspace w;
-    w.parts = merge_parts(g.chunks, k_sel);
+    w.parts = merge_parts(g.chunks, scan_m_sel(g.chunks, k_sel));
     const size_t ctas = (size_t)s.units * g.chunks;
     const size_t uh = (size_t)s.units * s.G;
     w.cand_off = 0;
     w.cnt_off = align256(w.cand_off + ctas * s.G * (size_t)scan_cand_cap(s) * sizeof(uint64_t));
-    w.forced_off = align256(w.cnt_off + ctas * s.G * sizeof(int32_t));
+    w.tau_off = align256(w.cnt_off + ctas * s.G * sizeof(int32_t));
+    w.flags_off = align256(w.tau_off + ctas * s.G * sizeof(uint64_t));
+    w.forced_off = align256(w.flags_off + ctas * s.G * sizeof(int32_t));
     w.part_keys_off = align256(w.forced_off + uh * (f.nf > 0 ? f.nf : 1) * sizeof(float));
     w.part_cnt_off = align256(w.part_keys_off + uh * w.parts * (size_t)k_sel * sizeof(uint64_t));
     w.ticket_off = align256(w.part_cnt_off + uh * w.parts * sizeof(int32_t));
-    w.total = align256(w.ticket_off + uh * sizeof(uint32_t));
+    w.dirty_off = align256(w.ticket_off + uh * sizeof(uint32_t));
+    w.total = align256(w.dirty_off + uh * sizeof(int32_t));
     return w;
 }
 

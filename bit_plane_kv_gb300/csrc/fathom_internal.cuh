@@ -54,12 +54,16 @@ int scan_cand_cap(const fathom_shape &s);
 
 #define FATHOM_MERGE_MAX_LISTS 1024
 
-// Merge parts per (unit, head): about 4096 candidate keys per part.
-int merge_parts(int chunks, int k_sel);
+// Per-CTA candidate target m: about four times a chunk's share of k', at
+// least 64, at most k'.  Each chunk keeps its top-m per head in the first pass.
+int scan_m_sel(int chunks, int k_sel);
+// Merge parts per (unit, head): about 8192 expected candidate keys per part.
+int merge_parts(int chunks, int m_sel);
 
 struct ScanWorkspace {
     int parts;
-    size_t cand_off, cnt_off, forced_off, part_keys_off, part_cnt_off, ticket_off, total;
+    size_t cand_off, cnt_off, tau_off, flags_off, forced_off, part_keys_off, part_cnt_off,
+        ticket_off, dirty_off, total;
 };
 ScanWorkspace scan_workspace_layout(const fathom_shape &s);
 

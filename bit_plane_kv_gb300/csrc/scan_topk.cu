@@ -33,6 +33,7 @@
 // (P CTAs per (unit, head), the last of which, by an atomic ticket, merges
 // the P partial results), selects the exact top-k', adds the forced tokens
 // and writes the kept set in ascending index order.
+#include <cstddef>
 #include <type_traits>
 
 #include "fathom_internal.cuh"
@@ -81,6 +82,15 @@ struct ScanSmem {
     SelScratch<G> selg;   // first-sub-chunk selection, all heads at once
     SelScratch<1> sel1;   // list prunes
 };
+// After scoring, pw and w (adjacent, in that order) hold each thread's 8 * G
+// order words at a stride of 8 * G + 1 words (no bank conflicts).
+template <int G>
+constexpr bool order_words_fit() {
+    return sizeof(ScanSmem<G>::pw) + sizeof(ScanSmem<G>::w) >= (size_t)kScanThreads * (8 * G + 1) * 4 &&
+           offsetof(ScanSmem<G>, w) == sizeof(ScanSmem<G>::pw);
+}
+static_assert(order_words_fit<1>() && order_words_fit<2>() && order_words_fit<4>() && order_words_fit<8>(),
+              "staged order words must fit in the plane-word and weight staging areas");
 
 // ---------------------------------------------------------------------------
 // Inner loop: channels [a_lo, a_hi) of depth T of the current group.
@@ -141,8 +151,8 @@ __device__ __forceinline__ void accum_depth(const uint2 *__restrict__ pwrow,
 // MSD radix select that starts at the highest bit in which the selection's
 // keys differ (a min/max reduction finds it), so the first 8-bit digit
 // already splits the live range of scores rather than the sign and exponent
-// bits every candidate shares; histogram increments are aggregated per warp
-// (lanes with equal digits add once).
+// bits every candidate shares.  (Plain shared-memory atomics for the
+// histogram measured faster here than aggregating equal digits per warp.)
 // Compile-time loop: f(integral_constant<int, I>) for I in [B, E).
 template <int B, int E, typename F>
 __device__ __forceinline__ void static_for(F &&f) {
@@ -209,10 +219,8 @@ __device__ void select_thresholds(SelScratch<S> &sm, Visit visit, int target, in
         for (int i = tid; i < S * 256; i += blockDim.x) (&sm.hist[0][0])[i] = 0;
         __syncthreads();
         visit([&](auto s, bool valid, uint64_t key) {
-            const bool in = valid && !done[s] && ((key & pmask[s]) == prefix[s]);
-            const unsigned bin = in ? (unsigned)((key >> lo[s]) & dmask[s]) : 256u + lane;
-            const unsigned peers = __match_any_sync(0xffffffffu, bin);
-            if (in && lane == __ffs(peers) - 1) atomicAdd(&sm.hist[s][bin], (unsigned)__popc(peers));
+            if (valid && !done[s] && ((key & pmask[s]) == prefix[s]))
+                atomicAdd(&sm.hist[s][(unsigned)((key >> lo[s]) & dmask[s])], 1u);
         });
         __syncthreads();
         bool warp_live = false;   // this warp searches selection `warp`
@@ -326,16 +334,51 @@ __device__ int prune_list(SelScratch<1> &sm, uint64_t *lst, int count, int targe
     return min(sm.new_cnt, count);
 }
 
+// Prunes the G lists of one CTA at once (keys in registers, KPT per head per
+// thread; every count <= KPT * blockDim.x): one selection for all heads
+// instead of G in a row.  lists: head h's list at lists + h * cap.
+template <int G, int KPT>
+__device__ void prune_lists_multi(SelScratch<G> &sm, uint64_t *lists, size_t cap, const int (&count)[G],
+                                  int target, int slack, uint64_t (&T)[G], int *cnt_out) {
+    const int tid = threadIdx.x, nt = blockDim.x;
+    uint64_t r[G][KPT];
+#pragma unroll
+    for (int i = 0; i < KPT; ++i)
+        static_for<0, G>([&](auto h) {
+            const int e = i * nt + tid;
+            r[h][i] = e < count[h] ? lists[h * cap + e] : 0ull;
+        });
+    int kept[G];
+    select_thresholds<G>(sm, [&](auto f) {
+#pragma unroll
+        for (int i = 0; i < KPT; ++i)
+            static_for<0, G>([&](auto h) { f(h, i * nt + tid < count[h], r[h][i]); });
+    }, target, slack, T, kept);
+    if (tid < G) cnt_out[tid] = 0;
+    __syncthreads();   // all keys are in registers: the lists may be overwritten
+#pragma unroll
+    for (int i = 0; i < KPT; ++i)
+        static_for<0, G>([&](auto h) {
+            if (i * nt + tid < count[h] && r[h][i] >= T[h]) {
+                const int pos = atomicAdd(&cnt_out[h], 1);
+                lists[h * cap + pos] = r[h][i];
+            }
+        });
+    __syncthreads();
+}
+
 // ---------------------------------------------------------------------------
 constexpr int kListKPT = 26;   // register keys per thread for list prunes (cap <= 26 * 256)
+constexpr int kMultiKPT = 4;   // register keys per thread and head for the joint final shrink
 
 template <int G>
 __global__ void __launch_bounds__(NT, (G <= 4) ? 3 : 1)
 scan_kernel(int n, int D, int chunk_blocks, int source, size_t stage_words, size_t stage_scales,
             const uint64_t *__restrict__ planes, const uint16_t *__restrict__ scales,
-            const fathom_run *__restrict__ runs, const float *__restrict__ q, int k_sel, int ns,
-            int r0, int nf, int cap, float *__restrict__ scores_opt, uint64_t *__restrict__ cand,
-            int *__restrict__ cand_cnt, float *__restrict__ forced_scores) {
+            const fathom_run *__restrict__ runs, const float *__restrict__ q, int k_sel, int m_sel,
+            int fixup, int ns, int r0, int nf, int cap, float *__restrict__ scores_opt,
+            uint64_t *__restrict__ cand, int *__restrict__ cand_cnt, uint64_t *__restrict__ cand_tau,
+            int *__restrict__ flags, float *__restrict__ forced_scores) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     ScanSmem<G> &sm = *reinterpret_cast<ScanSmem<G> *>(smem_raw);
     const int tid = threadIdx.x;
@@ -345,6 +388,13 @@ scan_kernel(int n, int D, int chunk_blocks, int source, size_t stage_words, size
     const int b_begin = chunk * chunk_blocks;
     const int b_end = min(nb, b_begin + chunk_blocks);
     const size_t cta = (size_t)u * gridDim.x + chunk;
+    if (fixup) {
+        // second pass: only chunks the merge flagged run again, keeping their exact top-k'
+        bool any = false;
+        for (int h = 0; h < G; ++h) any |= flags[cta * G + h] != 0;
+        if (!any) return;
+        m_sel = k_sel;
+    }
 
     // ---- prologue: active channels sorted by depth (desc), ties by channel:
     // a stable partition by depth from per-warp ballots over the D <= 128
@@ -456,7 +506,7 @@ scan_kernel(int n, int D, int chunk_blocks, int source, size_t stage_words, size
                 if (c + kSubTokens > cap) {
                     uint64_t *lst = cand + (cta * G + h) * (size_t)cap;
                     uint64_t T;
-                    const int nc = prune_list<kListKPT>(sm.sel1, lst, min(c, cap), k_sel, kPruneSlack, &T);
+                    const int nc = prune_list<kListKPT>(sm.sel1, lst, min(c, cap), m_sel, kPruneSlack, &T);
                     if (tid == 0) { sm.cnt[h] = nc; sm.tau[h] = T; }
                     __syncthreads();
                 }
@@ -538,63 +588,98 @@ scan_kernel(int n, int D, int chunk_blocks, int source, size_t stage_words, size
         };
         if (k_sel > 0) {
             if (first) {
-                // exact top-k' of this first sub-chunk, all heads at once, from registers
+                // a threshold from this first sub-chunk, all heads at once, from registers:
+                // between m and 2m of its keys are >= it
                 uint64_t T[G];
                 int kept[G];
                 select_thresholds<G>(sm.selg, [&](auto f) {
 #pragma unroll
                     for (int m = 0; m < 8; ++m)
                         static_for<0, G>([&](auto h) { f(h, (cvm >> m) & 1u, key_of(m, h)); });
-                }, k_sel, 0, T, kept);
+                }, m_sel, m_sel, T, kept);
 #pragma unroll
                 for (int h = 0; h < G; ++h) tau[h] = T[h];
                 if (tid < G) sm.tau[tid] = T[tid];
                 first = false;
             }
-            bool any = false;   // cheap pre-check on the high words
+            // append every key >= tau (few once tau is set): a mask of the passing
+            // (token, head) pairs from the high words alone; the thread's order words
+            // go to shared memory (the plane-word staging area is free now), so the
+            // loop over set bits reads them by index instead of selecting registers
+            uint32_t thi[G];
+#pragma unroll
+            for (int h = 0; h < G; ++h) thi[h] = (uint32_t)(tau[h] >> 32);
+            uint64_t pm = 0;   // bit m * G + h
 #pragma unroll
             for (int m = 0; m < 8; ++m)
 #pragma unroll
                 for (int h = 0; h < G; ++h)
-                    any |= ((cvm >> m) & 1u) && okey[m][h] >= (uint32_t)(tau[h] >> 32);
-            if (__any_sync(0xffffffffu, any)) {
-                static_for<0, G>([&](auto h) {
-                    uint64_t *lst = cand + (cta * G + h) * (size_t)cap;
+                    if (((cvm >> m) & 1u) && okey[m][h] >= thi[h]) pm |= 1ull << (m * G + h);
+            __syncthreads();   // every warp is done reading the staged plane words
+            uint32_t *ok_s = reinterpret_cast<uint32_t *>(&sm.pw[0][0]) + (size_t)tid * (8 * G + 1);
+            if (pm) {
 #pragma unroll
-                    for (int m = 0; m < 8; ++m) {
-                        const uint64_t kk = key_of(m, h);
-                        const bool p = ((cvm >> m) & 1u) && kk >= tau[h];
-                        const unsigned bal = __ballot_sync(0xffffffffu, p);
-                        if (bal) {
-                            int base = 0;
-                            const int leader = __ffs(bal) - 1;
-                            if (lane == leader) base = atomicAdd(&sm.cnt[h], __popc(bal));
-                            base = __shfl_sync(0xffffffffu, base, leader);
-                            const int pos = base + __popc(bal & ((1u << lane) - 1u));
-                            if (p && pos < cap) lst[pos] = kk;
-                        }
-                    }
-                });
+                for (int m = 0; m < 8; ++m)
+#pragma unroll
+                    for (int h = 0; h < G; ++h) ok_s[m * G + h] = okey[m][h];
+            }
+            while (pm) {
+                const int b = __ffsll((long long)pm) - 1;
+                pm &= pm - 1;
+                const int m = b / G, h = b % G;
+                const uint32_t i = (uint32_t)(beta * 64 + (int)r + 8 * (m & 3) + 32 * (m >> 2));
+                const uint64_t kk = ((uint64_t)ok_s[b] << 32) | (uint64_t)(0xffffffffu - i);
+                if (kk >= sm.tau[h]) {
+                    const int pos = atomicAdd(&sm.cnt[h], 1);
+                    if (pos < cap) cand[(cta * G + h) * (size_t)cap + pos] = kk;
+                }
             }
         }
         __syncthreads();
     }
 
-    // ---- cut every list to its exact top-k', then publish the counts
-    if (k_sel > 0) {
+    // ---- shrink long lists to about m keys (exactly k' in the second pass), then
+    // publish counts and thresholds: every key this CTA dropped is < its threshold
+    bool joint = false;
+    if (k_sel > 0 && !fixup) {
+        // usually every list is short: shrink all heads in one selection
+        int cs[G];
+        bool fits = true, any_long = false;
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+            cs[h] = min(sm.cnt[h], cap);
+            fits = fits && cs[h] <= kMultiKPT * NT;
+            any_long = any_long || cs[h] > 4 * m_sel;
+        }
+        if (fits && any_long) {
+            uint64_t T[G];
+            prune_lists_multi<G, kMultiKPT>(sm.selg, cand + cta * G * (size_t)cap, (size_t)cap, cs,
+                                           m_sel, m_sel, T, sm.cnt);
+            // a list that kept everything (T = 0) keeps its earlier threshold
+            if (tid < G) sm.tau[tid] = max((unsigned long long)sm.tau[tid], (unsigned long long)T[tid]);
+            __syncthreads();
+        }
+        joint = fits;
+    }
+    if (k_sel > 0 && !joint) {
 #pragma unroll 1
         for (int h = 0; h < G; ++h) {
             const int c = min(sm.cnt[h], cap);
-            if (c > k_sel) {
+            const bool cut = fixup ? (c > k_sel) : (c > 4 * m_sel);
+            if (cut) {
                 uint64_t *lst = cand + (cta * G + h) * (size_t)cap;
                 uint64_t T;
-                const int nc = prune_list<kListKPT>(sm.sel1, lst, c, k_sel, 0, &T);
-                if (tid == 0) sm.cnt[h] = nc;
+                const int nc = prune_list<kListKPT>(sm.sel1, lst, c, m_sel, fixup ? 0 : m_sel, &T);
+                if (tid == 0) { sm.cnt[h] = nc; sm.tau[h] = T; }
                 __syncthreads();
             }
         }
     }
-    if (tid < G) cand_cnt[cta * G + tid] = min(sm.cnt[tid], cap);
+    if (tid < G) {
+        cand_cnt[cta * G + tid] = min(sm.cnt[tid], cap);
+        cand_tau[cta * G + tid] = sm.tau[tid];
+        if (fixup) flags[cta * G + tid] = 0;   // handled
+    }
 }
 
 // ---------------------------------------------------------------------------
@@ -615,6 +700,7 @@ struct MergeSmem {
     int off[FATHOM_MERGE_MAX_LISTS + 1];     // prefix sums of the streamed lists' counts
     int count;
     int is_last;
+    uint64_t thresh;                         // the k'-th key of what was streamed (0: fewer keys)
 };
 
 // Streams `nl` lists (list l: base(l), count(l)) into sm.buf and leaves the
@@ -661,14 +747,20 @@ __device__ void stream_select(MergeSmem &sm, int nl, Base base, Count count, int
         uint64_t T;
         const int nc = prune_list<kMKPT>(sm.sel, sm.buf, sm.count, k_sel, 0, &T);
         __syncthreads();
-        if (tid == 0) sm.count = nc;
+        if (tid == 0) { sm.count = nc; sm.thresh = T; }
+    } else if (tid == 0) {
+        // k' keys or fewer: the threshold is the smallest of them
+        unsigned long long mn = ~0ull;
+        for (int e = 0; e < sm.count; ++e) mn = min(mn, (unsigned long long)sm.buf[e]);
+        sm.thresh = (sm.count == k_sel) ? mn : 0ull;
     }
     __syncthreads();
 }
 
 __global__ void __launch_bounds__(kMThreads)
 merge_kernel(int n, int G, int k, int k_sel, int ns, int r0, int nf, int chunks, int parts, int cap,
-             const uint64_t *__restrict__ cand, const int *__restrict__ cand_cnt,
+             int second, const uint64_t *__restrict__ cand, const int *__restrict__ cand_cnt,
+             const uint64_t *__restrict__ cand_tau, int *__restrict__ flags, int *__restrict__ dirty,
              const float *__restrict__ forced_scores, uint64_t *__restrict__ part_keys,
              int *__restrict__ part_cnt, unsigned *__restrict__ ticket, int32_t *__restrict__ out_idx,
              float *__restrict__ out_score) {
@@ -677,9 +769,10 @@ merge_kernel(int n, int G, int k, int k_sel, int ns, int r0, int nf, int chunks,
     const int p = blockIdx.x, h = blockIdx.y, u = blockIdx.z;
     const int tid = threadIdx.x;
     const size_t uh = (size_t)u * G + h;
+    if (second && !dirty[uh]) return;        // nothing was flagged for this (unit, head)
     int32_t *oi = out_idx + uh * k;
     float *os = out_score + uh * k;
-    if (p == 0) {
+    if (p == 0 && !second) {
         // forced tokens: sinks first, recent last
         const float *fs = forced_scores + uh * nf;
         for (int e = tid; e < ns; e += blockDim.x) { oi[e] = e; os[e] = fs[e]; }
@@ -710,6 +803,20 @@ merge_kernel(int n, int G, int k, int k_sel, int ns, int r0, int nf, int chunks,
                       [&](int l) { return (const uint64_t *)(part_keys + (uh * parts + l) * (size_t)k_sel); },
                       [&](int l) { return __ldcg(part_cnt + uh * parts + l); }, k_sel);
         if (tid == 0) ticket[uh] = 0u;   // ready for the next call
+    }
+    // exactness: a chunk whose threshold lies above the k'-th key T may have
+    // dropped keys >= T; flag it for the second pass (which rescans it exactly)
+    if (!second) {
+        const uint64_t T = sm.thresh;
+        int any = 0;
+        for (int c = tid; c < chunks; c += blockDim.x) {
+            const size_t ch = ((size_t)u * chunks + c) * G + h;
+            if (cand_tau[ch] > T) { flags[ch] = 1; any = 1; }
+        }
+        any = __syncthreads_or(any);
+        if (tid == 0 && any) dirty[uh] = 1;
+    } else if (tid == 0) {
+        dirty[uh] = 0;
     }
     // bitonic sort of the k' winners by token index; padding keys 0 (index 0xffffffff) sort last
     int P2 = 1;
@@ -755,21 +862,32 @@ static int launch_g(const fathom_shape &s, const uint64_t *planes, const uint16_
     uint64_t *pkeys = (uint64_t *)(w + wl.part_keys_off);
     int *pcnt = (int *)(w + wl.part_cnt_off);
     unsigned *ticket = (unsigned *)(w + wl.ticket_off);
+    const int m_sel = scan_m_sel(sg.chunks, k_sel);
+    uint64_t *ctau = (uint64_t *)(w + wl.tau_off);
+    int *flags = (int *)(w + wl.flags_off);
+    int *dirty = (int *)(w + wl.dirty_off);
     const size_t smem = sizeof(ScanSmem<G>);
     if (s.units > 65535) { set_error("scan: too many units for one launch"); return FATHOM_EINVAL; }
     ensure_smem(scan_kernel<G>, smem);
-    dim3 grid(sg.chunks, s.units);
-    scan_kernel<G><<<grid, NT, smem, st>>>(s.n, s.D, sg.chunk_blocks, source, stage_words,
-                                           stage_scales, planes, scales, runs, q, k_sel, f.ns, f.r0,
-                                           f.nf > 0 ? f.nf : 1, cap, scores_opt, cand, cnt, forced);
-    int rc = launch_status("scan_kernel");
-    if (rc) return rc;
     const size_t msmem = sizeof(MergeSmem);
     ensure_smem(merge_kernel, msmem);
-    merge_kernel<<<dim3(wl.parts, s.G, s.units), kMThreads, msmem, st>>>(
-        s.n, s.G, s.k, k_sel, f.ns, f.r0, f.nf > 0 ? f.nf : 1, sg.chunks, wl.parts, cap, cand, cnt,
-        forced, pkeys, pcnt, ticket, idx, score);
-    return launch_status("merge_kernel");
+    const int nf = f.nf > 0 ? f.nf : 1;
+    dim3 grid(sg.chunks, s.units);
+    for (int pass = 0; pass < 2; ++pass) {
+        scan_kernel<G><<<grid, NT, smem, st>>>(s.n, s.D, sg.chunk_blocks, source, stage_words,
+                                               stage_scales, planes, scales, runs, q, k_sel, m_sel, pass,
+                                               f.ns, f.r0, nf, cap, pass ? nullptr : scores_opt, cand,
+                                               cnt, ctau, flags, forced);
+        int rc = launch_status("scan_kernel");
+        if (rc) return rc;
+        merge_kernel<<<dim3(wl.parts, s.G, s.units), kMThreads, msmem, st>>>(
+            s.n, s.G, s.k, k_sel, f.ns, f.r0, nf, sg.chunks, wl.parts, cap, pass, cand, cnt, ctau,
+            flags, dirty, forced, pkeys, pcnt, ticket, idx, score);
+        rc = launch_status("merge_kernel");
+        if (rc) return rc;
+        if (k_sel == 0) break;   // nothing selected: no second pass needed
+    }
+    return FATHOM_OK;
 }
 
 int launch_scan_topk(const fathom_shape &s, const uint64_t *planes, const uint16_t *scales,

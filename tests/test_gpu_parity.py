@@ -265,3 +265,20 @@ def test_workspace_reuse_across_calls():
     for idx, out in outs[1:]:
         assert torch.equal(idx, outs[0][0]) and torch.equal(out, outs[0][1])
     assert torch.equal(outs[0][0], r["idx"])
+
+
+def test_concentrated_winners_force_the_exact_second_pass():
+    # one unit of 64k tokens is split into 32 chunks that each keep only their
+    # top-64 in the first pass; amplifying the keys of one 2048-token stretch
+    # puts all k' = 476 winners in one chunk, which the merge must flag and the
+    # second pass must rescan exactly
+    w = W("qwen3_32k", n=65536)
+    inp = Inputs(w, [0, 1], 65536)
+    for t in (inp.keys_in, inp.keys32, inp.krows):
+        t[:, 40960:43008] *= 4
+    r = run_gpu(inp, k=512, budget=48)
+    for ui in range(2):
+        check_unit(inp, r, ui, 512, 48)
+    idx = r["idx"][0].cpu().numpy()
+    free = idx[:, 4:-32]
+    assert np.mean((free >= 40960) & (free < 43008)) > 0.9
