@@ -94,7 +94,7 @@ class ClockSampler:
             os.close(fd)
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={CLOCK_FIELDS}", "--format=csv,noheader,nounits",
-                                          "-lms", "200"], stdout=self.fh, stderr=subprocess.DEVNULL)
+                                          "-lms", "50"], stdout=self.fh, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
 
@@ -128,7 +128,8 @@ class ClockSampler:
 class Setup:
     """Builds the store and rows of one session on this rank (untimed)."""
 
-    def __init__(self, w: synth.Workload, budget: int, rank: int, steps_total: int, fixed: bool):
+    def __init__(self, w: synth.Workload, budget: int, rank: int, steps_total: int, fixed: bool,
+                 path: str = "pipelined", groups: int = 4):
         from bit_plane_kv_gb300 import binding as B
         self.B = B
         self.w, self.budget, self.fixed = w, budget, fixed
@@ -178,6 +179,16 @@ class Setup:
         self.stage_sc = torch.zeros(H, self.stage_s, dtype=torch.int16, device=dev)
         self.ws = B.alloc_workspace(self.shape, B.WS_SCAN_TOPK)
         self.aws = B.alloc_workspace(self.shape, B.WS_SPARSE_ATTN)
+        self.path = path if self.host else "hbm"
+        n_groups = max(1, min(groups, H))
+        edges = [round(i * H / n_groups) for i in range(n_groups + 1)]
+        self.groups = [(edges[i], edges[i + 1]) for i in range(n_groups) if edges[i + 1] > edges[i]]
+        gsize = self.groups[0][1] - self.groups[0][0]
+        assert all(b - a == gsize for a, b in self.groups), "unit groups must be equal"
+        self.gshape = B.make_shape(gsize, self.n, self.D, self.G, self.k, w.n_sink, w.n_recent)
+        self.gws = B.alloc_workspace(self.gshape, B.WS_SCAN_TOPK)
+        self.gstream = torch.cuda.Stream()
+        self.gev = [torch.cuda.Event() for _ in self.groups]
         self.depth = torch.empty(H, D, dtype=torch.uint8, device=dev)
         self.theta = torch.empty(H, dtype=torch.float64, device=dev)
         self.runs = torch.empty(H, D, 6, dtype=torch.int32, device=dev)
@@ -188,15 +199,17 @@ class Setup:
         self.qcur = torch.empty(L, H, self.G, D, dtype=torch.float32, device=dev)
 
     def layer(self, l, q, ev=None):
-        """One layer of the decode step; ev = optional (start, end) events around the gather
-        (host regime) or the scan (HBM regime)."""
+        """One layer of the decode step; ev = optional (start, end) events around the
+        dominant stage (host regime: the gather, or the fused scan; HBM regime: the scan)."""
         B = self.B
         if self.fixed:
             B.fathom_plan_fixed(self.shape, q, self.var[l], 32, 4, depth=self.depth, runs=self.runs)
         else:
             B.fathom_plan(self.shape, q, self.var[l], self.budget_t, depth=self.depth, theta=self.theta,
                           runs=self.runs)
-        if self.host:
+        if self.host and self.path == "pipelined":
+            self._gather_scan_pipelined(l, q, ev)
+        elif self.host and self.path == "staged":
             if ev:
                 ev[0].record()
             B.fathom_gather(self.shape, self.planes[l], self.scales[l], self.runs, self.stage_p, self.stage_sc)
@@ -205,6 +218,8 @@ class Setup:
             B.fathom_scan_topk(self.shape, self.stage_p, self.stage_sc, self.runs, q, self.ws,
                                source=B.SRC_STAGING, topk_idx=self.idx, topk_score=self.sel)
         else:
+            # HBM regime, or the fused host path: the scan stages the planned runs
+            # straight from the store (pinned host memory) into shared memory
             if ev:
                 ev[0].record()
             B.fathom_scan_topk(self.shape, self.planes[l], self.scales[l], self.runs, q, self.ws,
@@ -213,19 +228,46 @@ class Setup:
                 ev[1].record()
         B.fathom_sparse_attn(self.shape, self.krows[l], self.vrows[l], q, self.idx, self.aws, out=self.out[l])
 
+    def _gather_scan_pipelined(self, l, q, ev=None):
+        """Gathers of unit groups on a second stream, each group's scan on the main stream
+        as soon as its runs have landed in HBM staging: the link stays busy while the SMs scan."""
+        B = self.B
+        main = torch.cuda.current_stream()
+        gs = self.gstream
+        plan_done = torch.cuda.Event()
+        plan_done.record(main)             # also orders this layer's gathers after the last layer's scans
+        gs.wait_event(plan_done)
+        n_g = len(self.groups)
+        if ev:
+            ev[0].record(gs)
+        for g, (a, b) in enumerate(self.groups):
+            with torch.cuda.stream(gs):
+                B.fathom_gather(self.gshape, self.planes[l, a:b], self.scales[l, a:b], self.runs[a:b],
+                                self.stage_p[a:b], self.stage_sc[a:b])
+                if ev and g == n_g - 1:
+                    ev[1].record(gs)
+                self.gev[g].record(gs)
+            main.wait_event(self.gev[g])
+            B.fathom_scan_topk(self.gshape, self.stage_p[a:b], self.stage_sc[a:b], self.runs[a:b], q[a:b],
+                               self.gws, source=B.SRC_STAGING, topk_idx=self.idx[a:b], topk_score=self.sel[a:b])
+
     def layer_stages(self, l, q):
-        """One layer with CUDA events between the calls: per-stage milliseconds."""
+        """One layer with CUDA events between the calls: per-stage milliseconds (the
+        pipelined path reports its overlapped gather + scan as one stage)."""
         B = self.B
         ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
         ev[0].record()
         B.fathom_plan(self.shape, q, self.var[l], self.budget_t, depth=self.depth, theta=self.theta,
                       runs=self.runs)
         ev[1].record()
-        if self.host:
+        if self.host and self.path == "staged":
             B.fathom_gather(self.shape, self.planes[l], self.scales[l], self.runs, self.stage_p, self.stage_sc)
             ev[2].record()
             B.fathom_scan_topk(self.shape, self.stage_p, self.stage_sc, self.runs, q, self.ws,
                                source=B.SRC_STAGING, topk_idx=self.idx, topk_score=self.sel)
+        elif self.host and self.path == "pipelined":
+            ev[2].record()
+            self._gather_scan_pipelined(l, q)
         else:
             ev[2].record()
             B.fathom_scan_topk(self.shape, self.planes[l], self.scales[l], self.runs, q, self.ws,
@@ -234,6 +276,24 @@ class Setup:
         B.fathom_sparse_attn(self.shape, self.krows[l], self.vrows[l], q, self.idx, self.aws, out=self.out[l])
         ev[4].record()
         return ev
+
+    def capture(self, evs):
+        """One decode step (all layers) as a CUDA graph reading the queries from
+        self.qcur; evs[l] = events (recorded inside the graph) around layer l's
+        dominant stage."""
+        g = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):          # warm the calls on the capture stream's side
+            for l in range(self.L):
+                self.layer(l, self.qcur[l])
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g):
+            for l in range(self.L):
+                self.layer(l, self.qcur[l], evs[l] if evs else None)
+        torch.cuda.synchronize()
+        return g
 
     def step(self, s, evs=None):
         for l in range(self.L):
@@ -350,6 +410,11 @@ def main():
     ap.add_argument("--workload", default="host_1m", choices=sorted(synth.WORKLOADS))
     ap.add_argument("--budget", type=int, default=48)
     ap.add_argument("--fixed", action="store_true", help="the 136-bit fixed-depth comparison plan")
+    ap.add_argument("--path", default="pipelined", choices=["pipelined", "staged", "fused"],
+                    help="host regime: gathers overlapped with scans (default), gather then scan, "
+                         "or the scan reading the pinned store directly")
+    ap.add_argument("--groups", type=int, default=4, help="unit groups of the pipelined path")
+    ap.add_argument("--eager", action="store_true", help="time eager launches instead of a CUDA graph per step")
     ap.add_argument("--impl", default="fathom", choices=["fathom", "reference"])
     ap.add_argument("--layers", type=int, default=0, help="override the layer count (0: workload's)")
     ap.add_argument("--regime", default="", choices=["", "hbm", "host"],
@@ -371,7 +436,7 @@ def main():
     import __graft_entry__
     __graft_entry__.build()
     total_steps = args.warmup + 2 * args.steps
-    st = Setup(w, args.budget, rank, total_steps, args.fixed)
+    st = Setup(w, args.budget, rank, total_steps, args.fixed, args.path, args.groups)
     link_gbs = measure_link_peak() if st.host else None
     peaks, peak_src = measured_peaks()
 
@@ -385,24 +450,63 @@ def main():
         torch.cuda.synchronize()
         plan_bytes[l] = st.planned_bytes()
 
-    # timed region: K steps, events around the dominant kernel of every layer
+    # CPU time to issue one eager step (the Python binding's per-call cost)
+    torch.cuda.synchronize()
+    c0 = time.perf_counter()
+    st.step(0)
+    issue_s = time.perf_counter() - c0
+    torch.cuda.synchronize()
+
+    # timed region: K steps, each one replay of the step's CUDA graph (queries
+    # copied into the graph's input buffer first), with events captured around
+    # the dominant stage of every layer
+    use_graph = not args.eager
+    try:
+        gevs = [(torch.cuda.Event(enable_timing=True, external=True),
+                 torch.cuda.Event(enable_timing=True, external=True)) for _ in range(st.L)] if use_graph else None
+        graph = st.capture(gevs) if use_graph else None
+    except Exception as exc:               # no graph capture: time the eager step
+        log(f"[bench] CUDA graph capture unavailable ({exc}); timing eager launches")
+        use_graph, graph = False, None
+    if use_graph:
+        for s in range(args.warmup):            # the first replays upload the graph
+            st.qcur.copy_(st.Q[s], non_blocking=True)
+            graph.replay()
+        torch.cuda.synchronize()
     evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(st.L)]
            for _ in range(args.steps)]
+    step_ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
     clocks = ClockSampler()
     clocks.start()
     barrier(world)
     torch.cuda.synchronize()
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    kern = []
     t_start.record()
+    step_ev[0].record()
     for s in range(args.steps):
-        st.step(args.warmup + s, evs[s])
+        if use_graph:
+            st.qcur.copy_(st.Q[args.warmup + s], non_blocking=True)
+            graph.replay()
+        else:
+            st.step(args.warmup + s, evs[s])
+        step_ev[s + 1].record()
     t_end.record()
     torch.cuda.synchronize()
     barrier(world)
     clk = clocks.stop(torch.cuda.current_device())
     elapsed = t_start.elapsed_time(t_end) / 1e3
+    step_ms = [step_ev[i].elapsed_time(step_ev[i + 1]) for i in range(args.steps)]
     elapsed = max_over_ranks(elapsed, world)
-    kern = [e[0].elapsed_time(e[1]) / 1e3 for row in evs for e in row]
+    if use_graph:
+        # the captured events hold the last replay's stage times; one more replay per step for the average
+        for s in range(args.steps):
+            st.qcur.copy_(st.Q[args.warmup + s], non_blocking=True)
+            graph.replay()
+            torch.cuda.synchronize()
+            kern += [a.elapsed_time(b) / 1e3 for a, b in gevs]
+    else:
+        kern = [e[0].elapsed_time(e[1]) / 1e3 for row in evs for e in row]
     kern_avg = statistics.mean(kern)
 
     # end to end through the public calls with host buffers
@@ -433,22 +537,33 @@ def main():
     scanned = statistics.mean(plan_bytes)          # bytes scanned per layer (all units of the layer)
     bits_per_token = scanned * 8 / (H * st.n)
     scan_gbs = scanned / (elapsed / (args.steps * L)) / 1e9
-    launches_per_layer = 5                         # plan, gather|-, scan, merge, attention
-    if not st.host:
-        launches_per_layer = 4
+    # our kernel launches per layer: plan, attention, and scan_topk's four (scan,
+    # merge, exact second-pass scan, second merge), plus one gather per group
+    if st.host and st.path == "pipelined":
+        launches_per_layer = 2 + 5 * len(st.groups)
+    elif st.host and st.path == "staged":
+        launches_per_layer = 7
+    else:
+        launches_per_layer = 6
     if st.host:
         link = link_gbs
         achieved = scanned / kern_avg / 1e9
+        what = {"staged": ("gather_kernel", "gather launch"),
+                "pipelined": ("gather_kernel", "layer's gather launches (one per unit group, back to back on "
+                                               "their own stream, overlapped with the scans)"),
+                "fused": ("scan_kernel", "fused scan_topk call (its scan kernel loads the runs from pinned "
+                                         "host memory)")}[st.path]
         roof = {"bound": "link", "achieved": achieved, "peak": link, "unit": "GB/s", "frac": achieved / link,
-                "traffic": None, "kernel": "gather_kernel",
+                "traffic": None, "kernel": what[0],
                 "peak_source": "measured in this run: pinned host->device copy, 1 GiB, best of 10",
-                "note": "host-link bytes per gather launch (planned plane runs + active-channel scales) / launch time"}
+                "note": f"host-link bytes (planned plane runs + active-channel scales) per {what[1]} / its time"}
     else:
         hbm = peaks["hbm_gbs"]
         achieved = scanned / kern_avg / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-                "traffic": None, "kernel": "scan_kernel+merge_kernel",
-                "peak_source": f"{peak_src} HBM copy peak (MEASURED_PEAKS.json hbm_gbs)"}
+                "traffic": None, "kernel": "scan_kernel",
+                "peak_source": f"{peak_src} HBM copy peak (MEASURED_PEAKS.json hbm_gbs)",
+                "note": "scanned bytes per layer / the scan_topk call's time (scan + merge kernels)"}
     line = {
         "metric": METRIC, "value": us_layer, "unit": "µs/layer", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": elapsed / args.steps * 1e3, "higher_is_better": False,
@@ -457,6 +572,7 @@ def main():
         "config": {"workload": w.name, "n": w.n, "layers": L, "kv_heads": w.kv_heads, "sessions_per_gpu": w.seqs,
                    "G": w.G, "D": w.D, "k": w.k, "n_sink": w.n_sink, "n_recent": w.n_recent,
                    "budget": "fixed 32ch x 4 planes" if args.fixed else args.budget, "regime": w.regime,
+                   "path": st.path, "unit_groups": len(st.groups) if st.path == "pipelined" else 1,
                    "l2": "inputs larger than L2 (store and rows of all layers > 129 MB)"},
         "scan_gbs": scan_gbs,
         "scanned_bytes_per_layer": scanned,
@@ -466,6 +582,9 @@ def main():
                 "h2d_bytes_per_step": int(st.Q[0].numel() * 4), "d2h_bytes_per_step": int(st.out.numel() * 4)},
         "gpu_launches": launches_per_layer * L * args.steps,
         "stages_us_per_layer": stages,
+        "timing": "one CUDA graph replay per step" if use_graph else "eager launches",
+        "step_ms_min_median_max": [min(step_ms), statistics.median(step_ms), max(step_ms)],
+        "eager_issue_us_per_layer": issue_s * 1e6 / st.L,
         "clocks": clk,
     }
     if st.host:

@@ -51,18 +51,16 @@ bool smem_attr_needed(const void *func, size_t bytes) {
 
 ScanGrid scan_grid(int units, int n) {
     // About four resident CTAs per SM on a 152-SM part; at least one 32-block
-    // sub-chunk per CTA.
+    // sub-chunk per CTA (sub-chunks are dealt round-robin to a unit's CTAs).
     const int target_ctas = 4 * 152;
-    int nb = num_blocks(n);
-    int max_chunks = (nb + kSubBlocks - 1) / kSubBlocks;
+    const int nb = num_blocks(n);
+    const int n_sub = (nb + kSubBlocks - 1) / kSubBlocks;
     int chunks = (target_ctas + units - 1) / units;
-    if (chunks > max_chunks) chunks = max_chunks;
+    if (chunks > n_sub) chunks = n_sub;
     if (chunks < 1) chunks = 1;
-    int cb = (nb + chunks - 1) / chunks;
-    cb = (cb + kSubBlocks - 1) / kSubBlocks * kSubBlocks;
     ScanGrid g;
-    g.chunk_blocks = cb;
-    g.chunks = (nb + cb - 1) / cb;
+    g.chunks = chunks;
+    g.chunk_blocks = ((n_sub + chunks - 1) / chunks) * kSubBlocks;   // blocks per CTA, at most
     return g;
 }
 
@@ -82,8 +80,8 @@ int scan_m_sel(int chunks, int k_sel) {
 }
 
 int merge_parts(int chunks, int m_sel) {
-    // lists hold about 2m keys after the scan's final shrink
-    long long keys = (long long)chunks * 2 * (m_sel > 0 ? m_sel : 1);
+    // lists hold between m and 2m keys after the scan's final shrink (about 1.5 m)
+    long long keys = (long long)chunks * 3 * (m_sel > 0 ? m_sel : 1) / 2;
     int p = (int)((keys + 8191) / 8192);
     if (p > chunks) p = chunks;
     if (p > FATHOM_MERGE_MAX_LISTS) p = FATHOM_MERGE_MAX_LISTS;

@@ -34,8 +34,8 @@ __host__ __device__ inline Forced forced_range(int n, int n_sink, int n_recent) 
     return f;
 }
 
-// Scan decomposition: every unit's blocks are split into `chunks` CTAs of
-// `chunk_blocks` 64-token blocks (a multiple of the 32-block sub-chunk).
+// Scan decomposition: every unit's 32-block sub-chunks are dealt round-robin
+// to `chunks` CTAs; `chunk_blocks` is the most blocks one CTA gets.
 struct ScanGrid {
     int chunks;
     int chunk_blocks;

@@ -5,10 +5,11 @@
 // has a fixed slot per channel so no host synchronisation is needed).
 //
 // The destination of a unit is dense (runs are packed in channel order), so
-// the grid is laid over destination space: CTA x of unit u copies destination
-// words [x * W, (x + 1) * W), finding the runs that overlap that window from
-// the run list in shared memory.  Every thread keeps several 16-byte loads in
-// flight before storing, which is what a long-latency host link needs.
+// the work is laid over destination space in windows of W words: a CTA of
+// unit u copies windows x, x + gridDim.x, ..., finding the runs that overlap
+// each window from the run list in shared memory.  Every thread keeps several
+// 16-byte loads in flight before storing, which is what a long-latency host
+// link needs; about two CTAs per SM saturate the link.
 #include "fathom_internal.cuh"
 
 namespace fathom {
@@ -42,7 +43,7 @@ __device__ __forceinline__ void copy_span(const T *__restrict__ src, T *__restri
 }
 
 __global__ void __launch_bounds__(kGThreads)
-gather_kernel(int D, int nb, int x_planes, const uint64_t *__restrict__ store_planes,
+gather_kernel(int D, int nb, int x_planes, int x_total, const uint64_t *__restrict__ store_planes,
               const uint16_t *__restrict__ store_scales, const fathom_run *__restrict__ runs,
               uint64_t *__restrict__ stage_planes, uint16_t *__restrict__ stage_scales,
               size_t stage_words, size_t stage_scales_n, int vec_planes, int vec_scales) {
@@ -50,26 +51,29 @@ gather_kernel(int D, int nb, int x_planes, const uint64_t *__restrict__ store_pl
     const int u = blockIdx.y;
     for (int j = threadIdx.x; j < D; j += kGThreads) r[j] = runs[(size_t)u * D + j];
     __syncthreads();
-    const bool do_planes = (int)blockIdx.x < x_planes;
-    const size_t win = do_planes ? kGChunkWords : kGChunkScales;
-    const size_t cap = do_planes ? stage_words : stage_scales_n;
-    const size_t d0 = (size_t)(do_planes ? blockIdx.x : blockIdx.x - x_planes) * win;
-    if (d0 >= cap) return;
-    const size_t d1 = min(d0 + win, cap);
-    for (int j = 0; j < D; ++j) {
-        const size_t rs = do_planes ? r[j].dst_word : r[j].dst_scale;
-        const size_t rl = do_planes ? r[j].n_words : r[j].n_scales;
-        const size_t lo = max(rs, d0), hi = min(rs + rl, d1);
-        if (lo >= hi) continue;
-        const size_t src0 = (do_planes ? r[j].src_word : r[j].src_scale) + (lo - rs);
-        if (do_planes) {
-            copy_span<uint64_t, uint4>(store_planes + (size_t)u * D * FATHOM_PLANES * nb + src0,
-                                       stage_planes + (size_t)u * stage_words + lo,
-                                       (uint32_t)(hi - lo), vec_planes && ((src0 | lo) % 2 == 0));
-        } else {
-            copy_span<uint16_t, uint4>(store_scales + (size_t)u * D * nb + src0,
-                                       stage_scales + (size_t)u * stage_scales_n + lo,
-                                       (uint32_t)(hi - lo), vec_scales && ((src0 | lo) % 8 == 0));
+    // grid-stride over the unit's destination windows: plane windows, then scale windows
+    for (int x = blockIdx.x; x < x_total; x += gridDim.x) {
+        const bool do_planes = x < x_planes;
+        const size_t win = do_planes ? kGChunkWords : kGChunkScales;
+        const size_t cap = do_planes ? stage_words : stage_scales_n;
+        const size_t d0 = (size_t)(do_planes ? x : x - x_planes) * win;
+        if (d0 >= cap) continue;
+        const size_t d1 = min(d0 + win, cap);
+        for (int j = 0; j < D; ++j) {
+            const size_t rs = do_planes ? r[j].dst_word : r[j].dst_scale;
+            const size_t rl = do_planes ? r[j].n_words : r[j].n_scales;
+            const size_t lo = max(rs, d0), hi = min(rs + rl, d1);
+            if (lo >= hi) continue;
+            const size_t src0 = (do_planes ? r[j].src_word : r[j].src_scale) + (lo - rs);
+            if (do_planes) {
+                copy_span<uint64_t, uint4>(store_planes + (size_t)u * D * FATHOM_PLANES * nb + src0,
+                                           stage_planes + (size_t)u * stage_words + lo,
+                                           (uint32_t)(hi - lo), vec_planes && ((src0 | lo) % 2 == 0));
+            } else {
+                copy_span<uint16_t, uint4>(store_scales + (size_t)u * D * nb + src0,
+                                           stage_scales + (size_t)u * stage_scales_n + lo,
+                                           (uint32_t)(hi - lo), vec_scales && ((src0 | lo) % 8 == 0));
+            }
         }
     }
 }
@@ -89,8 +93,13 @@ int launch_gather(const fathom_shape &s, const uint64_t *sp, const uint16_t *ss,
     const int vec_planes = (a % 16 == 0) && (stage_words % 2 == 0) && (nb % 2 == 0);
     const uintptr_t b = (uintptr_t)ss | (uintptr_t)ds;
     const int vec_scales = (b % 16 == 0) && (stage_scales % 8 == 0) && (nb % 8 == 0);
-    dim3 grid(xp + xs, s.units);
-    gather_kernel<<<grid, kGThreads, 0, st>>>(s.D, nb, xp, sp, ss, runs, dp, ds, stage_words,
+    // a copy over the host link needs enough bytes in flight (each thread keeps
+    // 4 x 16 B outstanding) but not every SM: about two CTAs per SM in all, which
+    // leaves room for kernels that run beside the gather
+    int per_unit = (2 * 152 + s.units - 1) / s.units;
+    if (per_unit > xp + xs) per_unit = xp + xs;
+    dim3 grid(per_unit, s.units);
+    gather_kernel<<<grid, kGThreads, 0, st>>>(s.D, nb, xp, xp + xs, sp, ss, runs, dp, ds, stage_words,
                                               stage_scales, vec_planes, vec_scales);
     return launch_status("gather_kernel");
 }

@@ -3,8 +3,8 @@
 // by the G query heads, §2 forced sink/recent tokens, §7 one multiply-add per
 // active channel, token and head).
 //
-// Grid: (chunks, units).  A CTA streams its chunk of 64-token blocks in
-// sub-chunks of 32 blocks (2048 tokens).  For each sub-chunk the planned
+// Grid: (chunks, units).  A CTA streams sub-chunks of 32 blocks (2048 tokens)
+// of its unit, dealt round-robin over the unit's CTAs.  For each sub-chunk the planned
 // plane words of the active channels (grouped so that at most 64 planes are
 // staged at a time) and per-block weights are staged in shared memory, then
 // each thread scores 8 tokens of one block for all G heads:
@@ -42,7 +42,6 @@ namespace fathom {
 
 constexpr int kCHG = 32;                // channels per staged group (fixed runs of the sorted order)
 constexpr int kPG = kCHG * FATHOM_PLANES;   // plane words staged per group, at most
-constexpr int kPWStride = kPG + 2;      // padded row (uint2 units) -> distinct banks per block
 constexpr int NT = kScanThreads;
 
 template <int G>
@@ -67,7 +66,11 @@ struct SelScratch {
 
 template <int G>
 struct ScanSmem {
-    uint2 pw[kSubBlocks][kPWStride];
+    // plane words, slot-major: pw[slot][block].  The synchronous path stages up
+    // to kPG slots of one group; the pipelined path ping-pongs between the two
+    // halves [0, kPG/2) and [kPG/2, kPG).
+    uint2 pw[kPG][kSubBlocks];
+    uint16_t scb[2][kCHG][kSubBlocks];                  // prefetched fp16 scales (pipelined path)
     float w[kSubBlocks][ScanCfg<G>::WStride];
     uint64_t plane_src[FATHOM_PLANES * FATHOM_MAX_D];   // word offset of (active channel, plane)
     uint64_t ch_scale[FATHOM_MAX_D];                   // scale offset of active channel
@@ -82,20 +85,14 @@ struct ScanSmem {
     SelScratch<G> selg;   // first-sub-chunk selection, all heads at once
     SelScratch<1> sel1;   // list prunes
 };
-// After scoring, pw and w (adjacent, in that order) hold each thread's 8 * G
-// order words at a stride of 8 * G + 1 words (no bank conflicts).
-template <int G>
-constexpr bool order_words_fit() {
-    return sizeof(ScanSmem<G>::pw) + sizeof(ScanSmem<G>::w) >= (size_t)kScanThreads * (8 * G + 1) * 4 &&
-           offsetof(ScanSmem<G>, w) == sizeof(ScanSmem<G>::pw);
-}
-static_assert(order_words_fit<1>() && order_words_fit<2>() && order_words_fit<4>() && order_words_fit<8>(),
-              "staged order words must fit in the plane-word and weight staging areas");
+
 
 // ---------------------------------------------------------------------------
 // Inner loop: channels [a_lo, a_hi) of depth T of the current group.
+// pwcol points at this thread's block in slot 0 of the staged group: slot s of
+// the block is pwcol[s * kSubBlocks] (the lanes of a warp read 4 adjacent words).
 template <int G, int T>
-__device__ __forceinline__ void accum_depth(const uint2 *__restrict__ pwrow,
+__device__ __forceinline__ void accum_depth(const uint2 *__restrict__ pwcol,
                                             const float *__restrict__ wrow, int a_lo, int a_hi,
                                             int slot, uint32_t r, float (&acc)[8][G]) {
     constexpr float K = 8388608.0f + (float)(1 << T);
@@ -104,7 +101,7 @@ __device__ __forceinline__ void accum_depth(const uint2 *__restrict__ pwrow,
         uint32_t ylo = 0, yhi = 0;
 #pragma unroll
         for (int p = 0; p < T; ++p) {
-            const uint2 w = pwrow[slot + p];
+            const uint2 w = pwcol[(slot + p) * kSubBlocks];
             ylo = (ylo << 1) + ((w.x >> r) & 0x01010101u);
             yhi = (yhi << 1) + ((w.y >> r) & 0x01010101u);
         }
@@ -137,6 +134,17 @@ __device__ __forceinline__ void accum_depth(const uint2 *__restrict__ pwrow,
             for (int h = 0; h < G; ++h) acc[m][h] = fmaf(wv[h], f[m], acc[m][h]);
     }
 }
+
+// ---------------------------------------------------------------------------
+// 16-byte asynchronous global -> shared copies (zero-filled when bytes == 0).
+__device__ __forceinline__ void cp_async16(void *smem_dst, const void *gmem_src, int bytes) {
+    const unsigned d = (unsigned)__cvta_generic_to_shared(smem_dst);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(d), "l"(gmem_src), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory"); }
 
 // ---------------------------------------------------------------------------
 // CTA-wide threshold selection, S selections at once.
@@ -376,7 +384,7 @@ __global__ void __launch_bounds__(NT, (G <= 4) ? 3 : 1)
 scan_kernel(int n, int D, int chunk_blocks, int source, size_t stage_words, size_t stage_scales,
             const uint64_t *__restrict__ planes, const uint16_t *__restrict__ scales,
             const fathom_run *__restrict__ runs, const float *__restrict__ q, int k_sel, int m_sel,
-            int fixup, int ns, int r0, int nf, int cap, float *__restrict__ scores_opt,
+            int fixup, int ns, int r0, int nf, int cap, int vec, float *__restrict__ scores_opt,
             uint64_t *__restrict__ cand, int *__restrict__ cand_cnt, uint64_t *__restrict__ cand_tau,
             int *__restrict__ flags, float *__restrict__ forced_scores) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
@@ -385,8 +393,7 @@ scan_kernel(int n, int D, int chunk_blocks, int source, size_t stage_words, size
     const int u = blockIdx.y;
     const int chunk = blockIdx.x;
     const int nb = num_blocks(n);
-    const int b_begin = chunk * chunk_blocks;
-    const int b_end = min(nb, b_begin + chunk_blocks);
+    (void)chunk_blocks;
     const size_t cta = (size_t)u * gridDim.x + chunk;
     if (fixup) {
         // second pass: only chunks the merge flagged run again, keeping their exact top-k'
@@ -496,8 +503,38 @@ scan_kernel(int n, int D, int chunk_blocks, int source, size_t stage_words, size
     for (int h = 0; h < G; ++h) tau[h] = 0;
     bool first = true;
 
-    for (int sb = b_begin; sb < b_end; sb += kSubBlocks) {
-        const int nblk = min(kSubBlocks, b_end - sb);
+    // sub-chunks are dealt round-robin to the unit's CTAs (CTA c takes c, c + S,
+    // c + 2S, ...): all CTAs sweep the sequence together, so the addresses in use
+    // at any moment stay within a narrow band (few pages, few DRAM rows)
+    // The usual plan (one staging group of at most kPG / 2 planes, aligned runs)
+    // is double-buffered: while a sub-chunk is scored, cp.async already moves the
+    // next one's plane words and scales into the other half of the staging
+    // area, so loads stay in flight the whole time (this is what keeps a store
+    // across the host link busy).  Other plans stage synchronously.
+    const GroupDesc g0 = sm.grp[0];
+    const int nch0 = g0.n4 + g0.n3 + g0.n2 + g0.n1;
+    const int npl0 = 4 * g0.n4 + 3 * g0.n3 + 2 * g0.n2 + g0.n1;
+    const bool piped = vec && ng == 1 && npl0 <= kPG / 2;
+    auto stage_async = [&](int half, int sbx) {
+        for (int e = tid; e < npl0 * (kSubBlocks / 2); e += NT) {
+            const int sl = e / (kSubBlocks / 2), c = e % (kSubBlocks / 2);
+            const bool ok = sbx + 2 * c < nb;                 // nb even: both words in range or neither
+            const uint64_t *src = ok ? planes + sm.plane_src[sl] + sbx + 2 * c : planes;
+            cp_async16(&sm.pw[half * (kPG / 2) + sl][2 * c], src, ok ? 16 : 0);
+        }
+        for (int e = tid; e < nch0 * (kSubBlocks / 8); e += NT) {
+            const int al = e / (kSubBlocks / 8), c = e % (kSubBlocks / 8);
+            const bool ok = sbx + 8 * c < nb;                 // nb % 8 == 0 on this path
+            const uint16_t *src = ok ? scales + sm.ch_scale[al] + sbx + 8 * c : scales;
+            cp_async16(&sm.scb[half][al][8 * c], src, ok ? 16 : 0);
+        }
+    };
+    int half = 0;
+    if (piped && chunk * kSubBlocks < nb) stage_async(0, chunk * kSubBlocks);
+    if (piped) cp_async_commit();
+
+    for (int sb = chunk * kSubBlocks; sb < nb; sb += (int)gridDim.x * kSubBlocks) {
+        const int nblk = min(kSubBlocks, nb - sb);
         // make room in every head's candidate list before this sub-chunk
         if (k_sel > 0) {
 #pragma unroll 1
@@ -521,42 +558,78 @@ scan_kernel(int n, int D, int chunk_blocks, int source, size_t stage_words, size
 #pragma unroll
             for (int h = 0; h < G; ++h) acc[m][h] = 0.0f;
 
-        for (int gi = 0; gi < ng; ++gi) {
-            const GroupDesc g = sm.grp[gi];
-            const int nch = g.n4 + g.n3 + g.n2 + g.n1;
-            const int npl = 4 * g.n4 + 3 * g.n3 + 2 * g.n2 + g.n1;
+        if (piped) {
+            const int sbn = sb + (int)gridDim.x * kSubBlocks;
+            if (sbn < nb) stage_async(half ^ 1, sbn);
+            cp_async_commit();
+            cp_async_wait<1>();                 // this sub-chunk's copies have landed
             __syncthreads();
-            // stage plane words: slot-major, 32 consecutive blocks per slot
-            for (int e = tid; e < npl * kSubBlocks; e += NT) {
-                const int s = e / kSubBlocks, b = e % kSubBlocks;
-                uint2 v = make_uint2(0u, 0u);
-                if (b < nblk) {
-                    const uint64_t wd = __ldg(planes + sm.plane_src[g.p0 + s] + sb + b);
-                    v = make_uint2((uint32_t)wd, (uint32_t)(wd >> 32));
-                }
-                sm.pw[b][s] = v;
-            }
-            // stage block weights w_hj = q_hj * 2^-t_j * a_{beta,j}
-            for (int e = tid; e < nch * kSubBlocks; e += NT) {
+            // block weights w_hj = q_hj * 2^-t_j * a_{beta,j} from the prefetched scales
+            for (int e = tid; e < nch0 * kSubBlocks; e += NT) {
                 const int al = e / kSubBlocks, b = e % kSubBlocks;
-                const int a = g.a0 + al;
-                float a16 = 0.0f;
-                if (b < nblk) a16 = __half2float(__ushort_as_half(__ldg(scales + sm.ch_scale[a] + sb + b)));
+                const float a16 = __half2float(__ushort_as_half(sm.scb[half][al][b]));
 #pragma unroll
-                for (int h = 0; h < G; ++h) sm.w[b][al * G + h] = sm.qs[a][h] * a16;
+                for (int h = 0; h < G; ++h) sm.w[b][al * G + h] = sm.qs[al][h] * a16;
             }
             __syncthreads();
             if (bl < nblk) {
-                const uint2 *pwrow = sm.pw[bl];
+                const uint2 *pwcol = &sm.pw[half * (kPG / 2)][bl];
                 const float *wrow = sm.w[bl];
                 int a = 0, slot = 0;
-                accum_depth<G, 4>(pwrow, wrow, a, a + g.n4, slot, r, acc);
-                a += g.n4; slot += 4 * g.n4;
-                accum_depth<G, 3>(pwrow, wrow, a, a + g.n3, slot, r, acc);
-                a += g.n3; slot += 3 * g.n3;
-                accum_depth<G, 2>(pwrow, wrow, a, a + g.n2, slot, r, acc);
-                a += g.n2; slot += 2 * g.n2;
-                accum_depth<G, 1>(pwrow, wrow, a, a + g.n1, slot, r, acc);
+                accum_depth<G, 4>(pwcol, wrow, a, a + g0.n4, slot, r, acc);
+                a += g0.n4; slot += 4 * g0.n4;
+                accum_depth<G, 3>(pwcol, wrow, a, a + g0.n3, slot, r, acc);
+                a += g0.n3; slot += 3 * g0.n3;
+                accum_depth<G, 2>(pwcol, wrow, a, a + g0.n2, slot, r, acc);
+                a += g0.n2; slot += 2 * g0.n2;
+                accum_depth<G, 1>(pwcol, wrow, a, a + g0.n1, slot, r, acc);
+            }
+        } else {
+            for (int gi = 0; gi < ng; ++gi) {
+                const GroupDesc g = sm.grp[gi];
+                const int nch = g.n4 + g.n3 + g.n2 + g.n1;
+                const int npl = 4 * g.n4 + 3 * g.n3 + 2 * g.n2 + g.n1;
+                __syncthreads();
+                // stage plane words (slot-major) and block weights; with aligned runs
+                // and a full sub-chunk every load is 16 bytes
+                if (vec && nblk == kSubBlocks) {
+                    for (int e = tid; e < npl * (kSubBlocks / 2); e += NT) {
+                        const int sl = e / (kSubBlocks / 2), c = e % (kSubBlocks / 2);
+                        *reinterpret_cast<uint4 *>(&sm.pw[sl][2 * c]) =
+                            __ldg(reinterpret_cast<const uint4 *>(planes + sm.plane_src[g.p0 + sl] + sb) + c);
+                    }
+                } else {
+                    for (int e = tid; e < npl * kSubBlocks; e += NT) {
+                        const int sl = e / kSubBlocks, b = e % kSubBlocks;
+                        uint2 v = make_uint2(0u, 0u);
+                        if (b < nblk) {
+                            const uint64_t wd = __ldg(planes + sm.plane_src[g.p0 + sl] + sb + b);
+                            v = make_uint2((uint32_t)wd, (uint32_t)(wd >> 32));
+                        }
+                        sm.pw[sl][b] = v;
+                    }
+                }
+                for (int e = tid; e < nch * kSubBlocks; e += NT) {
+                    const int al = e / kSubBlocks, b = e % kSubBlocks;
+                    const int a = g.a0 + al;
+                    float a16 = 0.0f;
+                    if (b < nblk) a16 = __half2float(__ushort_as_half(__ldg(scales + sm.ch_scale[a] + sb + b)));
+#pragma unroll
+                    for (int h = 0; h < G; ++h) sm.w[b][al * G + h] = sm.qs[a][h] * a16;
+                }
+                __syncthreads();
+                if (bl < nblk) {
+                    const uint2 *pwcol = &sm.pw[0][bl];
+                    const float *wrow = sm.w[bl];
+                    int a = 0, slot = 0;
+                    accum_depth<G, 4>(pwcol, wrow, a, a + g.n4, slot, r, acc);
+                    a += g.n4; slot += 4 * g.n4;
+                    accum_depth<G, 3>(pwcol, wrow, a, a + g.n3, slot, r, acc);
+                    a += g.n3; slot += 3 * g.n3;
+                    accum_depth<G, 2>(pwcol, wrow, a, a + g.n2, slot, r, acc);
+                    a += g.n2; slot += 2 * g.n2;
+                    accum_depth<G, 1>(pwcol, wrow, a, a + g.n1, slot, r, acc);
+                }
             }
         }
 
@@ -603,40 +676,38 @@ scan_kernel(int n, int D, int chunk_blocks, int source, size_t stage_words, size
                 first = false;
             }
             // append every key >= tau (few once tau is set): a mask of the passing
-            // (token, head) pairs from the high words alone; the thread's order words
-            // go to shared memory (the plane-word staging area is free now), so the
-            // loop over set bits reads them by index instead of selecting registers
+            // (token, head) pairs from the high words alone, then per token a short
+            // loop over its passing heads
             uint32_t thi[G];
 #pragma unroll
             for (int h = 0; h < G; ++h) thi[h] = (uint32_t)(tau[h] >> 32);
-            uint64_t pm = 0;   // bit m * G + h
 #pragma unroll
-            for (int m = 0; m < 8; ++m)
+            for (int m = 0; m < 8; ++m) {
+                unsigned hm = 0;
 #pragma unroll
                 for (int h = 0; h < G; ++h)
-                    if (((cvm >> m) & 1u) && okey[m][h] >= thi[h]) pm |= 1ull << (m * G + h);
-            __syncthreads();   // every warp is done reading the staged plane words
-            uint32_t *ok_s = reinterpret_cast<uint32_t *>(&sm.pw[0][0]) + (size_t)tid * (8 * G + 1);
-            if (pm) {
-#pragma unroll
-                for (int m = 0; m < 8; ++m)
-#pragma unroll
-                    for (int h = 0; h < G; ++h) ok_s[m * G + h] = okey[m][h];
-            }
-            while (pm) {
-                const int b = __ffsll((long long)pm) - 1;
-                pm &= pm - 1;
-                const int m = b / G, h = b % G;
-                const uint32_t i = (uint32_t)(beta * 64 + (int)r + 8 * (m & 3) + 32 * (m >> 2));
-                const uint64_t kk = ((uint64_t)ok_s[b] << 32) | (uint64_t)(0xffffffffu - i);
-                if (kk >= sm.tau[h]) {
-                    const int pos = atomicAdd(&sm.cnt[h], 1);
-                    if (pos < cap) cand[(cta * G + h) * (size_t)cap + pos] = kk;
+                    if (((cvm >> m) & 1u) && okey[m][h] >= thi[h]) hm |= 1u << h;
+                while (hm) {
+                    const int h = __ffs(hm) - 1;
+                    hm &= hm - 1;
+                    uint32_t ok = okey[m][0];
+                    uint64_t th = tau[0];
+                    static_for<1, G>([&](auto hh) {
+                        if (h == hh) { ok = okey[m][hh]; th = tau[hh]; }
+                    });
+                    const uint32_t i = (uint32_t)(beta * 64 + (int)r + 8 * (m & 3) + 32 * (m >> 2));
+                    const uint64_t kk = ((uint64_t)ok << 32) | (uint64_t)(0xffffffffu - i);
+                    if (kk >= th) {
+                        const int pos = atomicAdd(&sm.cnt[h], 1);
+                        if (pos < cap) cand[(cta * G + h) * (size_t)cap + pos] = kk;
+                    }
                 }
             }
         }
-        __syncthreads();
+        __syncthreads();   // staging buffers and counters are reused by the next sub-chunk
+        half ^= 1;
     }
+    if (piped) cp_async_wait<0>();
 
     // ---- shrink long lists to about m keys (exactly k' in the second pass), then
     // publish counts and thresholds: every key this CTA dropped is < its threshold
@@ -866,6 +937,11 @@ static int launch_g(const fathom_shape &s, const uint64_t *planes, const uint16_
     uint64_t *ctau = (uint64_t *)(w + wl.tau_off);
     int *flags = (int *)(w + wl.flags_off);
     int *dirty = (int *)(w + wl.dirty_off);
+    // 16-byte staging loads need every plane-row and scale-row start 16-byte aligned:
+    // nb a multiple of 8 (n a multiple of 512), aligned strides and bases
+    const int nb = num_blocks(s.n);
+    const bool aligned_src = (source == FATHOM_SRC_STORE) || (stage_words % 2 == 0 && stage_scales % 8 == 0);
+    const int vec = (nb % 8 == 0) && aligned_src && ((uintptr_t)planes % 16 == 0) && ((uintptr_t)scales % 16 == 0);
     const size_t smem = sizeof(ScanSmem<G>);
     if (s.units > 65535) { set_error("scan: too many units for one launch"); return FATHOM_EINVAL; }
     ensure_smem(scan_kernel<G>, smem);
@@ -876,7 +952,7 @@ static int launch_g(const fathom_shape &s, const uint64_t *planes, const uint16_
     for (int pass = 0; pass < 2; ++pass) {
         scan_kernel<G><<<grid, NT, smem, st>>>(s.n, s.D, sg.chunk_blocks, source, stage_words,
                                                stage_scales, planes, scales, runs, q, k_sel, m_sel, pass,
-                                               f.ns, f.r0, nf, cap, pass ? nullptr : scores_opt, cand,
+                                               f.ns, f.r0, nf, cap, vec, pass ? nullptr : scores_opt, cand,
                                                cnt, ctau, flags, forced);
         int rc = launch_status("scan_kernel");
         if (rc) return rc;
