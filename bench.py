@@ -129,7 +129,7 @@ class Setup:
     """Builds the store and rows of one session on this rank (untimed)."""
 
     def __init__(self, w: synth.Workload, budget: int, rank: int, steps_total: int, fixed: bool,
-                 path: str = "pipelined", groups: int = 4):
+                 path: str = "fused", groups: int = 4):
         from bit_plane_kv_gb300 import binding as B
         self.B = B
         self.w, self.budget, self.fixed = w, budget, fixed
@@ -410,9 +410,9 @@ def main():
     ap.add_argument("--workload", default="host_1m", choices=sorted(synth.WORKLOADS))
     ap.add_argument("--budget", type=int, default=48)
     ap.add_argument("--fixed", action="store_true", help="the 136-bit fixed-depth comparison plan")
-    ap.add_argument("--path", default="pipelined", choices=["pipelined", "staged", "fused"],
-                    help="host regime: gathers overlapped with scans (default), gather then scan, "
-                         "or the scan reading the pinned store directly")
+    ap.add_argument("--path", default="fused", choices=["fused", "staged", "pipelined"],
+                    help="host regime: the scan reads the pinned store directly (default), gather then "
+                         "scan, or gathers overlapped with scans")
     ap.add_argument("--groups", type=int, default=4, help="unit groups of the pipelined path")
     ap.add_argument("--eager", action="store_true", help="time eager launches instead of a CUDA graph per step")
     ap.add_argument("--impl", default="fathom", choices=["fathom", "reference"])

@@ -97,6 +97,82 @@ __device__ __forceinline__ void write_plan(int u, int lane, int D, int nb, const
     }
 }
 
+// The (B+1)-th largest breakpoint b_{j,m} = g_j * 2^-(2m+1) over the warp's
+// channels (with multiplicity), by an MSD radix select on the bit patterns
+// (positive doubles order like their bit patterns).  `bp` holds the lane's 16
+// patterns (0 for channels past D or g_j <= 0); hist is the warp's 256 bins.
+// Requires more than B positive breakpoints.
+__device__ unsigned long long critical_breakpoint(const unsigned long long (&bp)[4 * kCh], int B,
+                                                  unsigned *hist) {
+    const int lane = threadIdx.x & 31;
+    unsigned long long mn = ~0ull, mx = 0ull;
+#pragma unroll
+    for (int e = 0; e < 4 * kCh; ++e)
+        if (bp[e]) { mn = min(mn, bp[e]); mx = max(mx, bp[e]); }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+        mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+        mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    }
+    if (mn == mx) return mn;
+    int hi_bit = 63 - __clzll((long long)(mn ^ mx));
+    unsigned long long pmask = (hi_bit == 63) ? 0ull : ~((2ull << hi_bit) - 1ull);
+    unsigned long long prefix = mn & pmask;
+    int need = B + 1;   // rank (from the top) still to find within the current bucket
+    while (true) {
+        const int lo = hi_bit >= 7 ? hi_bit - 7 : 0;
+        const unsigned long long dmask = (2ull << (hi_bit - lo)) - 1ull;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) hist[lane * 8 + i] = 0;
+        __syncwarp();
+#pragma unroll
+        for (int e = 0; e < 4 * kCh; ++e)
+            if (bp[e] && (bp[e] & pmask) == prefix) atomicAdd(&hist[(bp[e] >> lo) & dmask], 1u);
+        __syncwarp();
+        // lane l owns bins 255-8l .. 248-8l (descending)
+        unsigned loc = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) loc += hist[255 - 8 * lane - i];
+        unsigned incl = loc;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const unsigned y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
+        }
+        const unsigned excl = incl - loc;
+        int digit = -1, above = 0, bucket = 0;
+        if (excl < (unsigned)need && (unsigned)need <= incl) {
+            unsigned c = excl;
+            for (int i = 0; i < 8; ++i) {
+                const int bin = 255 - 8 * lane - i;
+                const unsigned hb = hist[bin];
+                if (c + hb >= (unsigned)need) { digit = bin; above = (int)c; bucket = (int)hb; break; }
+                c += hb;
+            }
+        }
+        const unsigned owner = __ballot_sync(0xffffffffu, digit >= 0);
+        const int src = __ffs(owner) - 1;
+        digit = __shfl_sync(0xffffffffu, digit, src);
+        above = __shfl_sync(0xffffffffu, above, src);
+        bucket = __shfl_sync(0xffffffffu, bucket, src);
+        __syncwarp();
+        prefix |= (unsigned long long)digit << lo;
+        pmask |= dmask << lo;
+        need -= above;
+        if (lo == 0) return prefix;              // every bit decided: this value
+        if (bucket == 1) {                        // one candidate left: find it exactly
+            unsigned long long v = ~0ull;
+#pragma unroll
+            for (int e = 0; e < 4 * kCh; ++e)
+                if (bp[e] && (bp[e] & pmask) == prefix) v = min(v, bp[e]);
+#pragma unroll
+            for (int o = 16; o; o >>= 1) v = min(v, __shfl_xor_sync(0xffffffffu, v, o));
+            return v;
+        }
+        hi_bit = lo - 1;
+    }
+}
+
 __global__ void __launch_bounds__(32 * kPlanWarps)
 plan_kernel(int units, int n, int D, int G, const float *__restrict__ q,
             const float *__restrict__ var, const int32_t *__restrict__ budget,
@@ -145,9 +221,36 @@ plan_kernel(int units, int n, int D, int G, const float *__restrict__ q,
         if (total(lo) <= B) { hi = lo; bisect = false; }   // budget not binding
     }
     if (bisect) {
-        for (int it = 0; it < 30; ++it) {
-            const double mid = __dsqrt_rn(__dmul_rn(lo, hi));
-            if (total(mid) <= B) hi = mid; else lo = mid;
+        // total(theta) = #{breakpoints b_{j,m} = g_j 2^-(2m+1) >= theta}, so theta
+        // fits the budget iff theta > b*, the (B+1)-th largest breakpoint: each
+        // step is then one exact compare instead of a count over the channels.
+        // The breakpoints are exact (power-of-two scaling) unless g is within
+        // 2^7 of the subnormal range; then, and with an explicit bracket, count.
+        bool exact_bp = !bracket && B >= 0;
+        unsigned long long bp[4 * kCh];
+#pragma unroll
+        for (int c = 0; c < kCh; ++c) {
+            const long long gb = __double_as_longlong(g[c]);
+            const bool pos = g[c] > 0.0;
+            exact_bp = exact_bp && (!pos || (gb >> 52) > 16);
+#pragma unroll
+            for (int m = 0; m < 4; ++m)
+                bp[4 * c + m] = pos ? (unsigned long long)(gb - ((long long)(2 * m + 1) << 52)) : 0ull;
+        }
+        exact_bp = __all_sync(0xffffffffu, exact_bp);
+        if (exact_bp) {
+            __shared__ unsigned hist_s[kPlanWarps][256];
+            const double bstar = __longlong_as_double(
+                (long long)critical_breakpoint(bp, B, hist_s[threadIdx.x / 32]));
+            for (int it = 0; it < 30; ++it) {
+                const double mid = __dsqrt_rn(__dmul_rn(lo, hi));
+                if (mid > bstar) hi = mid; else lo = mid;
+            }
+        } else {
+            for (int it = 0; it < 30; ++it) {
+                const double mid = __dsqrt_rn(__dmul_rn(lo, hi));
+                if (total(mid) <= B) hi = mid; else lo = mid;
+            }
         }
     }
     int t[kCh];

@@ -30,14 +30,18 @@ struct AttnHeader {
 };
 
 struct AttnLayout {
-    size_t wo, lists, total;
+    size_t wo, lists, merge, total;
 };
 
+// wo[warps][G][D] floats, lists[G * k] ints, merge[splits][D + 2] floats (one head
+// of the final combine at a time)
 __host__ __device__ inline AttnLayout attn_smem_layout(int G, int k, int D) {
     AttnLayout L;
+    const int splits = G * ((k + kAttnRows - 1) / kAttnRows);
     L.wo = (sizeof(AttnHeader) + 15) & ~(size_t)15;
     L.lists = L.wo + (size_t)kWarps * G * D * sizeof(float);
-    L.total = (L.lists + (size_t)G * k * sizeof(int) + 15) & ~(size_t)15;
+    L.merge = (L.lists + (size_t)G * k * sizeof(int) + 15) & ~(size_t)15;
+    L.total = (L.merge + (size_t)splits * (D + 2) * sizeof(float) + 15) & ~(size_t)15;
     return L;
 }
 
@@ -53,7 +57,7 @@ __device__ __forceinline__ bool contains(const int *lst, int k, int x) {
 __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
-constexpr int kRowsInFlight = 4;   // rows a warp loads before using them
+constexpr int kRowsInFlight = 8;   // rows a warp loads before using them
 
 // Grid: (G * chunks_per_head, units).  CTA (h, c) takes entries [c R, c R + R)
 // of head h's sorted list and handles the rows that h owns, i.e. that no lower
@@ -62,9 +66,9 @@ constexpr int kRowsInFlight = 4;   // rows a warp loads before using them
 // heads' lists.  Lane l holds channels 4l .. 4l+3 (D = 128: one 8-byte load of
 // K and one of V per row); other D take the general path with channel
 // j = l + 32 e.
-template <bool kVec>
-__global__ void __launch_bounds__(NA)
-attn_kernel(int n, int D, int G, int k, int cph, int splits, const uint16_t *__restrict__ krows,
+template <int G, bool kVec>
+__global__ void __launch_bounds__(NA, 2)
+attn_kernel(int n, int D, int k, int cph, int splits, const uint16_t *__restrict__ krows,
             const uint16_t *__restrict__ vrows, const float *__restrict__ q,
             const int32_t *__restrict__ topk, float *__restrict__ out, float *__restrict__ part,
             unsigned *__restrict__ ticket) {
@@ -84,23 +88,23 @@ attn_kernel(int n, int D, int G, int k, int cph, int splits, const uint16_t *__r
     __syncthreads();
 
     const float scale = 1.0f / sqrtf((float)D);   // 1/sqrt(D), correctly rounded
-    float m_h[FATHOM_MAX_G], l_h[FATHOM_MAX_G], o_h[FATHOM_MAX_G][4], qv[FATHOM_MAX_G][4];
+    float m_h[G], l_h[G], o_h[G][4], qv[G][4];
 #pragma unroll
-    for (int h = 0; h < FATHOM_MAX_G; ++h) {
+    for (int h = 0; h < G; ++h) {
         m_h[h] = -CUDART_INF_F;
         l_h[h] = 0.0f;
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
             o_h[h][e] = 0.0f;
             const int j = kVec ? 4 * lane + e : lane + 32 * e;
-            qv[h][e] = (h < G && j < D) ? q[((size_t)u * G + h) * D + j] : 0.0f;
+            qv[h][e] = (j < D) ? q[((size_t)u * G + h) * D + j] : 0.0f;
         }
     }
     const int *own = lists + (size_t)hown * k;
     for (int e0 = e_begin + warp * kRowsInFlight; e0 < e_end; e0 += kWarps * kRowsInFlight) {
-        int row[kRowsInFlight];
         unsigned mask[kRowsInFlight];
-        float kv[kRowsInFlight][4], vv[kRowsInFlight][4];
+        uint2 kp[kRowsInFlight], vp[kRowsInFlight];        // bf16 pairs, unpacked at use
+        float kv[kRowsInFlight][4], vv[kRowsInFlight][4];  // general path only
 #pragma unroll
         for (int r = 0; r < kRowsInFlight; ++r) {
             const int e = e0 + r;
@@ -118,18 +122,12 @@ attn_kernel(int n, int D, int G, int k, int cph, int splits, const uint16_t *__r
                 }
                 if (i < 0 || i >= n) m = 0;                 // not a token of this unit
             }
-            row[r] = i;
             mask[r] = m;
             const uint16_t *kr = krows + ((size_t)u * n + (m ? i : 0)) * D;
             const uint16_t *vr = vrows + ((size_t)u * n + (m ? i : 0)) * D;
             if (kVec) {
-                uint2 a = make_uint2(0u, 0u), b = make_uint2(0u, 0u);
-                if (m) {
-                    a = __ldg(reinterpret_cast<const uint2 *>(kr) + lane);
-                    b = __ldg(reinterpret_cast<const uint2 *>(vr) + lane);
-                }
-                kv[r][0] = bf16lo(a.x); kv[r][1] = bf16hi(a.x); kv[r][2] = bf16lo(a.y); kv[r][3] = bf16hi(a.y);
-                vv[r][0] = bf16lo(b.x); vv[r][1] = bf16hi(b.x); vv[r][2] = bf16lo(b.y); vv[r][3] = bf16hi(b.y);
+                kp[r] = m ? __ldg(reinterpret_cast<const uint2 *>(kr) + lane) : make_uint2(0u, 0u);
+                vp[r] = m ? __ldg(reinterpret_cast<const uint2 *>(vr) + lane) : make_uint2(0u, 0u);
             } else {
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
@@ -143,12 +141,20 @@ attn_kernel(int n, int D, int G, int k, int cph, int splits, const uint16_t *__r
 #pragma unroll
         for (int r = 0; r < kRowsInFlight; ++r) {
             if (!mask[r]) continue;                         // warp-uniform
+            float kk[4], vx[4];
+            if (kVec) {
+                kk[0] = bf16lo(kp[r].x); kk[1] = bf16hi(kp[r].x); kk[2] = bf16lo(kp[r].y); kk[3] = bf16hi(kp[r].y);
+                vx[0] = bf16lo(vp[r].x); vx[1] = bf16hi(vp[r].x); vx[2] = bf16lo(vp[r].y); vx[3] = bf16hi(vp[r].y);
+            } else {
 #pragma unroll
-            for (int h = 0; h < FATHOM_MAX_G; ++h) {
-                if (h >= G || !((mask[r] >> h) & 1u)) continue;
+                for (int c = 0; c < 4; ++c) { kk[c] = kv[r][c]; vx[c] = vv[r][c]; }
+            }
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+                if (!((mask[r] >> h) & 1u)) continue;
                 float d = 0.0f;
 #pragma unroll
-                for (int c = 0; c < 4; ++c) d = fmaf(qv[h][c], kv[r][c], d);
+                for (int c = 0; c < 4; ++c) d = fmaf(qv[h][c], kk[c], d);
 #pragma unroll
                 for (int o = 16; o; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
                 const float logit = d * scale;
@@ -157,16 +163,14 @@ attn_kernel(int n, int D, int G, int k, int cph, int splits, const uint16_t *__r
                 const float p = expf(logit - mn);
                 l_h[h] = l_h[h] * corr + p;
 #pragma unroll
-                for (int c = 0; c < 4; ++c) o_h[h][c] = o_h[h][c] * corr + p * vv[r][c];
+                for (int c = 0; c < 4; ++c) o_h[h][c] = o_h[h][c] * corr + p * vx[c];
                 m_h[h] = mn;
             }
         }
-        (void)row;
     }
     // ---- merge warps
 #pragma unroll
-    for (int h = 0; h < FATHOM_MAX_G; ++h) {
-        if (h >= G) continue;
+    for (int h = 0; h < G; ++h) {
         if (lane == 0) { sm.wm[warp][h] = m_h[h]; sm.wl[warp][h] = l_h[h]; }
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
@@ -201,20 +205,28 @@ attn_kernel(int n, int D, int G, int k, int cph, int splits, const uint16_t *__r
     if (!sm.is_last) return;
     __threadfence();
     const float *p0 = part + (size_t)u * splits * G * (D + 2);
-    for (int e = tid; e < G * D; e += NA) {
-        const int h = e / D, j = e % D;
-        float M = -CUDART_INF_F;
-        for (int sp = 0; sp < splits; ++sp) M = fmaxf(M, __ldcg(p0 + ((size_t)sp * G + h) * (D + 2)));
-        float L = 0.0f, O = 0.0f;
-        for (int sp = 0; sp < splits; ++sp) {
-            const float *ph = p0 + ((size_t)sp * G + h) * (D + 2);
-            const float ms = __ldcg(ph);
-            if (ms == -CUDART_INF_F) continue;
-            const float f = expf(ms - M);
-            L += f * __ldcg(ph + 1);
-            O += f * __ldcg(ph + 2 + j);
+    float *mg = reinterpret_cast<float *>(asmem_raw + lay.merge);   // [splits][D + 2], one head
+    for (int h = 0; h < G; ++h) {
+        // all of the head's partial states in one round of independent loads
+        for (int e = tid; e < splits * (D + 2); e += NA) {
+            const int sp = e / (D + 2), c = e % (D + 2);
+            mg[e] = __ldcg(p0 + ((size_t)sp * G + h) * (D + 2) + c);
         }
-        out[((size_t)u * G + h) * D + j] = O / L;
+        __syncthreads();
+        for (int j = tid; j < D; j += NA) {
+            float M = -CUDART_INF_F;
+            for (int sp = 0; sp < splits; ++sp) M = fmaxf(M, mg[sp * (D + 2)]);
+            float L = 0.0f, O = 0.0f;
+            for (int sp = 0; sp < splits; ++sp) {
+                const float ms = mg[sp * (D + 2)];
+                if (ms == -CUDART_INF_F) continue;
+                const float f = expf(ms - M);
+                L += f * mg[sp * (D + 2) + 1];
+                O += f * mg[sp * (D + 2) + 2 + j];
+            }
+            out[((size_t)u * G + h) * D + j] = O / L;
+        }
+        __syncthreads();
     }
     if (tid == 0) ticket[u] = 0u;   // ready for the next call
 }
@@ -229,15 +241,25 @@ int launch_sparse_attn(const fathom_shape &s, const uint16_t *krows, const uint1
     const size_t smem = attn_smem_layout(s.G, s.k, s.D).total;
     const int cph = (s.k + kAttnRows - 1) / kAttnRows;   // CTAs per head
     const bool vec = s.D == 128 && ((uintptr_t)krows % 8 == 0) && ((uintptr_t)vrows % 8 == 0);
-    if (vec) {
-        ensure_smem(attn_kernel<true>, smem);
-        attn_kernel<true><<<dim3(wl.splits, s.units), NA, smem, st>>>(
-            s.n, s.D, s.G, s.k, cph, wl.splits, krows, vrows, q, idx, out, part, ticket);
-    } else {
-        ensure_smem(attn_kernel<false>, smem);
-        attn_kernel<false><<<dim3(wl.splits, s.units), NA, smem, st>>>(
-            s.n, s.D, s.G, s.k, cph, wl.splits, krows, vrows, q, idx, out, part, ticket);
+    const dim3 grid(wl.splits, s.units);
+#define FATHOM_ATTN_LAUNCH(GG, VV)                                                               \
+    do {                                                                                         \
+        ensure_smem(attn_kernel<GG, VV>, smem);                                                  \
+        attn_kernel<GG, VV><<<grid, NA, smem, st>>>(s.n, s.D, s.k, cph, wl.splits, krows, vrows, \
+                                                    q, idx, out, part, ticket);                  \
+    } while (0)
+    switch (s.G * 2 + (vec ? 1 : 0)) {
+        case 2: FATHOM_ATTN_LAUNCH(1, false); break;
+        case 3: FATHOM_ATTN_LAUNCH(1, true); break;
+        case 4: FATHOM_ATTN_LAUNCH(2, false); break;
+        case 5: FATHOM_ATTN_LAUNCH(2, true); break;
+        case 8: FATHOM_ATTN_LAUNCH(4, false); break;
+        case 9: FATHOM_ATTN_LAUNCH(4, true); break;
+        case 16: FATHOM_ATTN_LAUNCH(8, false); break;
+        case 17: FATHOM_ATTN_LAUNCH(8, true); break;
+        default: set_error("sparse_attn: unsupported G=%d", s.G); return FATHOM_EINVAL;
     }
+#undef FATHOM_ATTN_LAUNCH
     return launch_status("attn_kernel");
 }
 
