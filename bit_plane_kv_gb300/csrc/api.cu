@@ -49,13 +49,40 @@ bool smem_attr_needed(const void *func, size_t bytes) {
     return true;
 }
 
-ScanGrid scan_grid(int units, int n) {
-    // About four resident CTAs per SM on a 152-SM part; at least one 32-block
-    // sub-chunk per CTA (sub-chunks are dealt round-robin to a unit's CTAs).
-    const int target_ctas = 4 * 152;
-    const int nb = num_blocks(n);
+// Streaming multiprocessors of the current device (0 if no device answers).
+int device_sm_count() {
+    static std::mutex mu;
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+        cudaGetLastError();
+        return 0;
+    }
+    std::lock_guard<std::mutex> lock(mu);
+    if (!cache[dev]) {
+        int v = 0;
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+            cudaGetLastError();
+            return 0;
+        }
+        cache[dev] = v;
+    }
+    return cache[dev];
+}
+
+ScanGrid scan_grid(const fathom_shape &s) {
+    // One full wave: as many CTAs as the device holds at once (SMs x resident
+    // scan CTAs per SM; 152 x 3 on GB300 when no device answers), at least one
+    // 32-block sub-chunk per CTA (sub-chunks are dealt round-robin to a unit's
+    // CTAs, so every CTA of a unit has the same work to within one sub-chunk).
+    int sms = device_sm_count();
+    if (sms <= 0) sms = 152;
+    int res = scan_resident_ctas(s.G);
+    if (res <= 0) res = (s.G <= 4) ? 3 : 1;
+    const int target_ctas = sms * res;
+    const int nb = num_blocks(s.n);
     const int n_sub = (nb + kSubBlocks - 1) / kSubBlocks;
-    int chunks = (target_ctas + units - 1) / units;
+    int chunks = (target_ctas + s.units - 1) / s.units;
     if (chunks > n_sub) chunks = n_sub;
     if (chunks < 1) chunks = 1;
     ScanGrid g;
@@ -73,10 +100,21 @@ int scan_cand_cap(const fathom_shape &s) {
 }
 
 int scan_m_sel(int chunks, int k_sel) {
+    // keys each CTA hands to the merge (between m and 2m): four times its
+    // expected share of the unit's k' winners, at least 32
     if (k_sel <= 0) return 0;
     int m = (4 * k_sel + chunks - 1) / chunks;
-    m = m < 64 ? 64 : m;
+    m = m < 32 ? 32 : m;
     return m > k_sel ? k_sel : m;
+}
+
+int scan_m_first(int n_sub, int k_sel, int m_sel) {
+    // rank of the threshold taken from a CTA's first sub-chunk: four times the
+    // expected winners of one sub-chunk, at least 16, at most m
+    if (k_sel <= 0) return 0;
+    int m = (4 * k_sel + n_sub - 1) / n_sub;
+    m = m < 16 ? 16 : m;
+    return m > m_sel ? m_sel : m;
 }
 
 int merge_parts(int chunks, int m_sel) {
@@ -89,7 +127,7 @@ int merge_parts(int chunks, int m_sel) {
 }
 
 ScanWorkspace scan_workspace_layout(const fathom_shape &s) {
-    ScanGrid g = scan_grid(s.units, s.n);
+    ScanGrid g = scan_grid(s);
     Forced f = forced_range(s.n, s.n_sink, s.n_recent);
     int k_sel = s.k - f.nf;
     if (k_sel < 1) k_sel = 1;

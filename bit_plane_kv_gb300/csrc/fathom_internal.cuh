@@ -40,7 +40,9 @@ struct ScanGrid {
     int chunks;
     int chunk_blocks;
 };
-ScanGrid scan_grid(int units, int n);
+ScanGrid scan_grid(const fathom_shape &s);
+int device_sm_count();
+int scan_resident_ctas(int G);   // resident scan CTAs per SM (0: no device)
 
 constexpr int kScanThreads = 256;
 constexpr int kSubBlocks = 32;               // blocks per sub-chunk (8 threads per block)
@@ -57,6 +59,7 @@ int scan_cand_cap(const fathom_shape &s);
 // Per-CTA candidate target m: about four times a chunk's share of k', at
 // least 64, at most k'.  Each chunk keeps its top-m per head in the first pass.
 int scan_m_sel(int chunks, int k_sel);
+int scan_m_first(int n_sub, int k_sel, int m_sel);
 // Merge parts per (unit, head): about 8192 expected candidate keys per part.
 int merge_parts(int chunks, int m_sel);
 

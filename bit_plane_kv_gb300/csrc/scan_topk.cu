@@ -23,17 +23,20 @@
 // Selection never materialises all scores.  Tokens are ordered by a 64-bit
 // key (score, ~index).  Each CTA keeps, per head, a candidate list of keys in
 // the workspace and a threshold key tau; a token is appended only if its key
-// >= tau.  tau starts as the exact k'-th key of the CTA's first sub-chunk
-// (selected straight from registers for all heads at once); when a list could
-// overflow it is pruned (loaded into registers once, radix-selected, written
-// back) to at least k' and at most k' + slack keys and tau rises to the new
-// bound; at the end every list is cut to its exact top-k'.  A token of the
-// CTA's top-k' is never dropped, so the union of the CTAs' lists holds the
-// unit's top-k'.  The merge kernel streams those lists through shared memory
-// (P CTAs per (unit, head), the last of which, by an atomic ticket, merges
-// the P partial results), selects the exact top-k', adds the forced tokens
-// and writes the kept set in ascending index order.
+// >= tau.  tau starts as a key of the CTA's first sub-chunk (selected straight
+// from registers for all heads at once) with between m1 and 2 m1 of that
+// sub-chunk's keys above it, m1 being four times the winners a sub-chunk
+// holds on average; at the end every list is cut back to m .. 2m keys, m
+// being four times the CTA's expected share of the k' winners (a list about
+// to overflow is cut the same way on the way).  The merge kernel streams
+// the lists through shared memory (P CTAs per (unit, head), the last of
+// which, by an atomic ticket, merges the P partial results), selects the
+// exact top-k', adds the forced tokens and writes the kept set in ascending
+// index order.  Any CTA whose tau lies above the k'-th key may have dropped
+// a winner: the merge flags it, and a second pass rescans exactly the
+// flagged chunks (keeping their exact top-k') before a second merge.
 #include <cstddef>
+#include <mutex>
 #include <type_traits>
 
 #include "fathom_internal.cuh"
@@ -364,12 +367,18 @@ __device__ void prune_lists_multi(SelScratch<G> &sm, uint64_t *lists, size_t cap
     }, target, slack, T, kept);
     if (tid < G) cnt_out[tid] = 0;
     __syncthreads();   // all keys are in registers: the lists may be overwritten
+    const int lane = tid & 31;
 #pragma unroll
     for (int i = 0; i < KPT; ++i)
         static_for<0, G>([&](auto h) {
-            if (i * nt + tid < count[h] && r[h][i] >= T[h]) {
-                const int pos = atomicAdd(&cnt_out[h], 1);
-                lists[h * cap + pos] = r[h][i];
+            const bool keep = i * nt + tid < count[h] && r[h][i] >= T[h];
+            const unsigned bal = __ballot_sync(0xffffffffu, keep);
+            if (bal) {   // one shared counter update per warp
+                const int leader = __ffs(bal) - 1;
+                int base = 0;
+                if (lane == leader) base = atomicAdd(&cnt_out[h], __popc(bal));
+                base = __shfl_sync(0xffffffffu, base, leader);
+                if (keep) lists[h * cap + base + __popc(bal & ((1u << lane) - 1u))] = r[h][i];
             }
         });
     __syncthreads();
@@ -384,7 +393,7 @@ __global__ void __launch_bounds__(NT, (G <= 4) ? 3 : 1)
 scan_kernel(int n, int D, int chunk_blocks, int source, size_t stage_words, size_t stage_scales,
             const uint64_t *__restrict__ planes, const uint16_t *__restrict__ scales,
             const fathom_run *__restrict__ runs, const float *__restrict__ q, int k_sel, int m_sel,
-            int fixup, int ns, int r0, int nf, int cap, int vec, float *__restrict__ scores_opt,
+            int m_first, int fixup, int ns, int r0, int nf, int cap, int vec, float *__restrict__ scores_opt,
             uint64_t *__restrict__ cand, int *__restrict__ cand_cnt, uint64_t *__restrict__ cand_tau,
             int *__restrict__ flags, float *__restrict__ forced_scores) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
@@ -400,7 +409,7 @@ scan_kernel(int n, int D, int chunk_blocks, int source, size_t stage_words, size
         bool any = false;
         for (int h = 0; h < G; ++h) any |= flags[cta * G + h] != 0;
         if (!any) return;
-        m_sel = k_sel;
+        m_sel = m_first = k_sel;
     }
 
     // ---- prologue: active channels sorted by depth (desc), ties by channel:
@@ -544,7 +553,7 @@ scan_kernel(int n, int D, int chunk_blocks, int source, size_t stage_words, size
                     uint64_t *lst = cand + (cta * G + h) * (size_t)cap;
                     uint64_t T;
                     const int nc = prune_list<kListKPT>(sm.sel1, lst, min(c, cap), m_sel, kPruneSlack, &T);
-                    if (tid == 0) { sm.cnt[h] = nc; sm.tau[h] = T; }
+                    if (tid == 0) { sm.cnt[h] = nc; sm.tau[h] = max((unsigned long long)sm.tau[h], (unsigned long long)T); }
                     __syncthreads();
                 }
             }
@@ -659,25 +668,26 @@ scan_kernel(int n, int D, int chunk_blocks, int source, size_t stage_words, size
             const uint32_t i = (uint32_t)(beta * 64 + (int)r + 8 * (m & 3) + 32 * (m >> 2));
             return ((uint64_t)okey[m][h] << 32) | (uint64_t)(0xffffffffu - i);
         };
+        if (k_sel > 0 && first) {
+            // a threshold from this first sub-chunk, all heads at once, from registers:
+            // between m1 and 2 m1 of its keys are >= it (m1: four times the winners
+            // one sub-chunk holds on average)
+            uint64_t T[G];
+            int kept[G];
+            select_thresholds<G>(sm.selg, [&](auto f) {
+#pragma unroll
+                for (int m = 0; m < 8; ++m)
+                    static_for<0, G>([&](auto h) { f(h, (cvm >> m) & 1u, key_of(m, h)); });
+            }, m_first, m_first, T, kept);
+#pragma unroll
+            for (int h = 0; h < G; ++h) tau[h] = T[h];
+            if (tid < G) sm.tau[tid] = T[tid];
+            first = false;
+        }
         if (k_sel > 0) {
-            if (first) {
-                // a threshold from this first sub-chunk, all heads at once, from registers:
-                // between m and 2m of its keys are >= it
-                uint64_t T[G];
-                int kept[G];
-                select_thresholds<G>(sm.selg, [&](auto f) {
-#pragma unroll
-                    for (int m = 0; m < 8; ++m)
-                        static_for<0, G>([&](auto h) { f(h, (cvm >> m) & 1u, key_of(m, h)); });
-                }, m_sel, m_sel, T, kept);
-#pragma unroll
-                for (int h = 0; h < G; ++h) tau[h] = T[h];
-                if (tid < G) sm.tau[tid] = T[tid];
-                first = false;
-            }
-            // append every key >= tau (few once tau is set): a mask of the passing
-            // (token, head) pairs from the high words alone, then per token a short
-            // loop over its passing heads
+            // append every key >= tau (few, about m1 .. 2 m1 per sub-chunk and head):
+            // a mask of the passing heads from the high words alone, then per token
+            // a short loop over them
             uint32_t thi[G];
 #pragma unroll
             for (int h = 0; h < G; ++h) thi[h] = (uint32_t)(tau[h] >> 32);
@@ -720,7 +730,7 @@ scan_kernel(int n, int D, int chunk_blocks, int source, size_t stage_words, size
         for (int h = 0; h < G; ++h) {
             cs[h] = min(sm.cnt[h], cap);
             fits = fits && cs[h] <= kMultiKPT * NT;
-            any_long = any_long || cs[h] > 4 * m_sel;
+            any_long = any_long || cs[h] > 2 * m_sel;
         }
         if (fits && any_long) {
             uint64_t T[G];
@@ -736,7 +746,7 @@ scan_kernel(int n, int D, int chunk_blocks, int source, size_t stage_words, size
 #pragma unroll 1
         for (int h = 0; h < G; ++h) {
             const int c = min(sm.cnt[h], cap);
-            const bool cut = fixup ? (c > k_sel) : (c > 4 * m_sel);
+            const bool cut = fixup ? (c > k_sel) : (c > 2 * m_sel);
             if (cut) {
                 uint64_t *lst = cand + (cta * G + h) * (size_t)cap;
                 uint64_t T;
@@ -779,11 +789,28 @@ struct MergeSmem {
 template <typename Base, typename Count>
 __device__ void stream_select(MergeSmem &sm, int nl, Base base, Count count, int k_sel) {
     const int tid = threadIdx.x;
-    if (tid == 0) {
-        int o = 0;
-        for (int l = 0; l < nl; ++l) { sm.off[l] = o; o += count(l); }
-        sm.off[nl] = o;
-        sm.count = 0;
+    // all list counts in one round of loads, then an exclusive scan by warp 0
+    // (lane l sums a run of ceil(nl / 32) consecutive counts)
+    for (int l = tid; l < nl; l += blockDim.x) sm.off[l + 1] = count(l);
+    __syncthreads();
+    if (tid < 32) {
+        const int per = (nl + 31) / 32;
+        const int l0 = min(nl, tid * per), l1 = min(nl, l0 + per);
+        int run = 0;
+        for (int l = l0; l < l1; ++l) run += sm.off[l + 1];
+        int incl = run;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (tid >= o) incl += y;
+        }
+        int acc = incl - run;
+        for (int l = l0; l < l1; ++l) {
+            const int c = sm.off[l + 1];
+            sm.off[l] = acc;
+            acc += c;
+        }
+        if (tid == 31) { sm.off[nl] = incl; sm.count = 0; }
     }
     __syncthreads();
     const int total = sm.off[nl];
@@ -892,19 +919,47 @@ merge_kernel(int n, int G, int k, int k_sel, int ns, int r0, int nf, int chunks,
     // bitonic sort of the k' winners by token index; padding keys 0 (index 0xffffffff) sort last
     int P2 = 1;
     while (P2 < k_sel) P2 <<= 1;
-    for (int e = sm.count + tid; e < P2; e += blockDim.x) sm.buf[e] = 0;
-    __syncthreads();
-    for (int size = 2; size <= P2; size <<= 1) {
-        for (int stride = size >> 1; stride > 0; stride >>= 1) {
-            for (int e = tid; e < P2 / 2; e += blockDim.x) {
-                const int lo = 2 * stride * (e / stride) + (e % stride);
-                const int hi = lo + stride;
-                const bool up = ((lo & size) == 0);
-                const uint64_t a = sm.buf[lo], b = sm.buf[hi];
-                const bool swap = up ? (key_index(a) > key_index(b)) : (key_index(a) < key_index(b));
-                if (swap) { sm.buf[lo] = b; sm.buf[hi] = a; }
+    if (P2 <= kMThreads) {
+        // one key per thread: compare-exchange partners within a warp by shuffles,
+        // farther ones through two alternating shared-memory buffers
+        uint64_t x = (tid < sm.count) ? sm.buf[tid] : 0ull;
+        __syncthreads();
+        uint64_t *xb[2] = {sm.buf, sm.buf + kMThreads};
+        int pb = 0;
+        for (int size = 2; size <= P2; size <<= 1) {
+            for (int stride = size >> 1; stride > 0; stride >>= 1) {
+                uint64_t y;
+                if (stride >= 32) {
+                    xb[pb][tid] = x;
+                    __syncthreads();
+                    y = xb[pb][tid ^ stride];
+                    pb ^= 1;
+                } else {
+                    y = __shfl_xor_sync(0xffffffffu, x, stride);
+                }
+                const bool take_min = ((tid & stride) == 0) == ((tid & size) == 0);
+                const bool x_first = key_index(x) < key_index(y);
+                x = (take_min == x_first) ? x : y;
             }
-            __syncthreads();
+        }
+        __syncthreads();
+        sm.buf[tid] = x;
+        __syncthreads();
+    } else {
+        for (int e = sm.count + tid; e < P2; e += blockDim.x) sm.buf[e] = 0;
+        __syncthreads();
+        for (int size = 2; size <= P2; size <<= 1) {
+            for (int stride = size >> 1; stride > 0; stride >>= 1) {
+                for (int e = tid; e < P2 / 2; e += blockDim.x) {
+                    const int lo = 2 * stride * (e / stride) + (e % stride);
+                    const int hi = lo + stride;
+                    const bool up = ((lo & size) == 0);
+                    const uint64_t a = sm.buf[lo], b = sm.buf[hi];
+                    const bool swap = up ? (key_index(a) > key_index(b)) : (key_index(a) < key_index(b));
+                    if (swap) { sm.buf[lo] = b; sm.buf[hi] = a; }
+                }
+                __syncthreads();
+            }
         }
     }
     for (int e = tid; e < k_sel; e += blockDim.x) {
@@ -920,7 +975,7 @@ static int launch_g(const fathom_shape &s, const uint64_t *planes, const uint16_
                     int source, size_t stage_words, size_t stage_scales, const fathom_run *runs,
                     const float *q, int32_t *idx, float *score, float *scores_opt, void *ws,
                     cudaStream_t st) {
-    const ScanGrid sg = scan_grid(s.units, s.n);
+    const ScanGrid sg = scan_grid(s);
     const Forced f = forced_range(s.n, s.n_sink, s.n_recent);
     const ScanWorkspace wl = scan_workspace_layout(s);
     const int k_sel = s.k - f.nf;
@@ -934,6 +989,7 @@ static int launch_g(const fathom_shape &s, const uint64_t *planes, const uint16_
     int *pcnt = (int *)(w + wl.part_cnt_off);
     unsigned *ticket = (unsigned *)(w + wl.ticket_off);
     const int m_sel = scan_m_sel(sg.chunks, k_sel);
+    const int m_first = scan_m_first((num_blocks(s.n) + kSubBlocks - 1) / kSubBlocks, k_sel, m_sel);
     uint64_t *ctau = (uint64_t *)(w + wl.tau_off);
     int *flags = (int *)(w + wl.flags_off);
     int *dirty = (int *)(w + wl.dirty_off);
@@ -951,7 +1007,7 @@ static int launch_g(const fathom_shape &s, const uint64_t *planes, const uint16_
     dim3 grid(sg.chunks, s.units);
     for (int pass = 0; pass < 2; ++pass) {
         scan_kernel<G><<<grid, NT, smem, st>>>(s.n, s.D, sg.chunk_blocks, source, stage_words,
-                                               stage_scales, planes, scales, runs, q, k_sel, m_sel, pass,
+                                               stage_scales, planes, scales, runs, q, k_sel, m_sel, m_first, pass,
                                                f.ns, f.r0, nf, cap, vec, pass ? nullptr : scores_opt, cand,
                                                cnt, ctau, flags, forced);
         int rc = launch_status("scan_kernel");
@@ -964,6 +1020,41 @@ static int launch_g(const fathom_shape &s, const uint64_t *planes, const uint16_
         if (k_sel == 0) break;   // nothing selected: no second pass needed
     }
     return FATHOM_OK;
+}
+
+// Resident CTAs of scan_kernel<G> per SM on the current device, with its
+// shared memory (0 when no device answers); cached per device.
+template <int G>
+static int resident_g() {
+    static std::mutex mu;
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+        cudaGetLastError();
+        return 0;
+    }
+    std::lock_guard<std::mutex> lock(mu);
+    if (!cache[dev]) {
+        const size_t smem = sizeof(ScanSmem<G>);
+        ensure_smem(scan_kernel<G>, smem);
+        int nbk = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nbk, scan_kernel<G>, NT, smem) != cudaSuccess) {
+            cudaGetLastError();
+            return 0;
+        }
+        cache[dev] = nbk;
+    }
+    return cache[dev];
+}
+
+int scan_resident_ctas(int G) {
+    switch (G) {
+        case 1: return resident_g<1>();
+        case 2: return resident_g<2>();
+        case 4: return resident_g<4>();
+        case 8: return resident_g<8>();
+        default: return 0;
+    }
 }
 
 int launch_scan_topk(const fathom_shape &s, const uint64_t *planes, const uint16_t *scales,

@@ -3,15 +3,17 @@
 // precision; §2: each head attends exactly over its own selected set, with no
 // mass redistribution for the rest).
 //
-// Grid: (G * ceil(k / kAttnRows), units).  A CTA takes a slice of one head's
-// sorted kept list and handles the rows that head owns (the first head, in
-// order, that lists the token), so the union of the heads' winners is fetched
-// exactly once; a row's head mask comes from binary searches in the other
-// lists.  Each warp keeps several rows in flight (K and V, bf16), computes
-// q_h . k / sqrt(D) for the heads in the row's mask and keeps an online
-// softmax state (running max, sum, weighted V) per head.  Warp states are
-// merged per CTA and written to the workspace; the last CTA of the unit (an
-// atomic ticket, no waiting) merges the splits and writes o_h.
+// Grid: (G * ceil(k / kAttnRows), units).  CTA (h, c) takes entries
+// [c R, c R + R) of head h's sorted kept list and handles the rows that h
+// owns -- the rows no lower head lists -- so every row of the union is
+// fetched exactly once.  The CTA first finds, for its R rows, which other
+// heads list them (one binary search per (row, head) pair, all threads at
+// once).  Each warp then loads a batch of rows (K and V, bf16) and computes
+// the G dot products of every row in the batch with one transpose reduction
+// across the warp, updates an online softmax state (running max, sum,
+// weighted V) per head, and the CTA merges its warps into one partial state
+// per head.  The last CTA of the unit (an atomic ticket, no waiting) merges
+// the partial states of all CTAs of the unit and writes o_h.
 #include <mutex>
 
 #include "fathom_internal.cuh"
@@ -21,27 +23,47 @@ namespace fathom {
 constexpr int NA = kAttnThreads;
 constexpr int kWarps = NA / 32;
 
-// Shared memory: a fixed header, then wo[warps][G][D] floats and the G
-// index lists (G * k ints), laid out by attn_smem_layout.
+// Rows per warp batch: RB rows x G heads = S dot products, reduced together.
+template <int G>
+struct AttnBatch {
+    static constexpr int RB = (32 / G) < 8 ? (32 / G) : 8;
+    static constexpr int S = RB * G;   // <= 32, a power of two
+};
+
 struct AttnHeader {
     int is_last;
+    int rows[kAttnRows];
+    unsigned rmask[kAttnRows];
     float wm[kWarps][FATHOM_MAX_G];
     float wl[kWarps][FATHOM_MAX_G];
+    float wf[kWarps][FATHOM_MAX_G];
+    float cl[FATHOM_MAX_G];
+    float pbuf[kWarps][32];
 };
+
+// Heads merged per round by the last CTA: all of them when their partial
+// states fit in about 96 KiB of shared memory, else one at a time.
+__host__ __device__ inline int attn_merge_heads(int G, int splits, int D) {
+    const size_t per_head = (size_t)splits * (D + 2) * sizeof(float);
+    return (size_t)G * per_head <= ((size_t)96 << 10) ? G : 1;
+}
 
 struct AttnLayout {
-    size_t wo, lists, merge, total;
+    size_t lists, wo, merge, total;
 };
 
-// wo[warps][G][D] floats, lists[G * k] ints, merge[splits][D + 2] floats (one head
-// of the final combine at a time)
-__host__ __device__ inline AttnLayout attn_smem_layout(int G, int k, int D) {
+// header, then the G index lists and the warps' weighted-V states; the last
+// CTA's merge buffer ([splits][heads of the round][D + 2] floats) reuses the
+// same bytes once they are no longer read
+__host__ __device__ inline AttnLayout attn_smem_layout(int G, int k, int D, int splits) {
     AttnLayout L;
-    const int splits = G * ((k + kAttnRows - 1) / kAttnRows);
-    L.wo = (sizeof(AttnHeader) + 15) & ~(size_t)15;
-    L.lists = L.wo + (size_t)kWarps * G * D * sizeof(float);
-    L.merge = (L.lists + (size_t)G * k * sizeof(int) + 15) & ~(size_t)15;
-    L.total = (L.merge + (size_t)splits * (D + 2) * sizeof(float) + 15) & ~(size_t)15;
+    L.lists = (sizeof(AttnHeader) + 15) & ~(size_t)15;
+    L.wo = (L.lists + (size_t)G * k * sizeof(int) + 15) & ~(size_t)15;
+    const size_t end_main = L.wo + (size_t)kWarps * G * D * sizeof(float);
+    L.merge = L.lists;
+    const size_t end_merge =
+        L.merge + (size_t)attn_merge_heads(G, splits, D) * splits * (D + 2) * sizeof(float);
+    L.total = ((end_main > end_merge ? end_main : end_merge) + 15) & ~(size_t)15;
     return L;
 }
 
@@ -57,34 +79,56 @@ __device__ __forceinline__ bool contains(const int *lst, int k, int x) {
 __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
-constexpr int kRowsInFlight = 8;   // rows a warp loads before using them
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
 
-// Grid: (G * chunks_per_head, units).  CTA (h, c) takes entries [c R, c R + R)
-// of head h's sorted list and handles the rows that h owns, i.e. that no lower
-// head lists: every row of the union is fetched exactly once.  The row's head
-// mask (which heads attend to it) comes from binary searches in the other
-// heads' lists.  Lane l holds channels 4l .. 4l+3 (D = 128: one 8-byte load of
-// K and one of V per row); other D take the general path with channel
-// j = l + 32 e.
+// Lane l holds channels 4l .. 4l+3 (kVec: D = 128, one 8-byte load of K and one
+// of V per row) or channels l + 32 e (any D <= 128).
 template <int G, bool kVec>
-__global__ void __launch_bounds__(NA, 2)
+__global__ void __launch_bounds__(NA, G >= 8 ? 1 : 2)
 attn_kernel(int n, int D, int k, int cph, int splits, const uint16_t *__restrict__ krows,
             const uint16_t *__restrict__ vrows, const float *__restrict__ q,
             const int32_t *__restrict__ topk, float *__restrict__ out, float *__restrict__ part,
             unsigned *__restrict__ ticket) {
+    constexpr int RB = AttnBatch<G>::RB, S = AttnBatch<G>::S;
     extern __shared__ __align__(16) unsigned char asmem_raw[];
     AttnHeader &sm = *reinterpret_cast<AttnHeader *>(asmem_raw);
-    const AttnLayout lay = attn_smem_layout(G, k, D);
-    float *wo = reinterpret_cast<float *>(asmem_raw + lay.wo);          // [warp][h][D]
+    const AttnLayout lay = attn_smem_layout(G, k, D, splits);
     int *lists = reinterpret_cast<int *>(asmem_raw + lay.lists);
+    float *wo = reinterpret_cast<float *>(asmem_raw + lay.wo);          // [warp][h][D]
     const int s = blockIdx.x, u = blockIdx.y;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int GK = G * k;
     const int hown = s / cph;
     const int e_begin = (s % cph) * kAttnRows;
-    const int e_end = min(k, e_begin + kAttnRows);
+    const int R = min(k, e_begin + kAttnRows) - e_begin;
 
-    for (int e = tid; e < GK; e += NA) lists[e] = topk[(size_t)u * GK + e];
+    // ---- the G sorted lists, then this CTA's rows and their head masks
+    const int32_t *src = topk + (size_t)u * G * k;
+    if ((k & 3) == 0 && ((uintptr_t)src & 15) == 0) {
+        for (int e = tid; e < G * k / 4; e += NA)
+            reinterpret_cast<int4 *>(lists)[e] = __ldg(reinterpret_cast<const int4 *>(src) + e);
+    } else {
+        for (int e = tid; e < G * k; e += NA) lists[e] = __ldg(src + e);
+    }
+    __syncthreads();
+    for (int r = tid; r < kAttnRows; r += NA) {
+        const int i = r < R ? lists[hown * k + e_begin + r] : -1;
+        sm.rows[r] = i;
+        sm.rmask[r] = (r < R && i >= 0 && i < n) ? (1u << hown) : 0u;
+    }
+    __syncthreads();
+    for (int p = tid; p < kAttnRows * G; p += NA) {
+        const int r = p % kAttnRows, h2 = p / kAttnRows;
+        if (h2 != hown && r < R && contains(lists + h2 * k, k, sm.rows[r])) atomicOr(&sm.rmask[r], 1u << h2);
+    }
     __syncthreads();
 
     const float scale = 1.0f / sqrtf((float)D);   // 1/sqrt(D), correctly rounded
@@ -100,101 +144,155 @@ attn_kernel(int n, int D, int k, int cph, int splits, const uint16_t *__restrict
             qv[h][e] = (j < D) ? q[((size_t)u * G + h) * D + j] : 0.0f;
         }
     }
-    const int *own = lists + (size_t)hown * k;
-    for (int e0 = e_begin + warp * kRowsInFlight; e0 < e_end; e0 += kWarps * kRowsInFlight) {
-        unsigned mask[kRowsInFlight];
-        uint2 kp[kRowsInFlight], vp[kRowsInFlight];        // bf16 pairs, unpacked at use
-        float kv[kRowsInFlight][4], vv[kRowsInFlight][4];  // general path only
+    float *pb = sm.pbuf[warp];
+    const int v = lane & (S - 1), vr = v / G, vh = v % G;   // this lane's (row, head) slot
+    const unsigned below = (1u << hown) - 1u;
+    for (int r0 = warp * RB; r0 < R; r0 += kWarps * RB) {
+        unsigned mask[RB];
+        uint2 kp[RB], vp[RB];                      // bf16 pairs (kVec)
+        float kv[RB][4], vv[RB][4];                // general path
 #pragma unroll
-        for (int r = 0; r < kRowsInFlight; ++r) {
-            const int e = e0 + r;
-            int i = -1;
+        for (int r = 0; r < RB; ++r) {
+            const int rr = r0 + r;
             unsigned m = 0;
-            if (e < e_end) {
-                i = own[e];
-                m = 1u << hown;
-                for (int h2 = 0; h2 < G; ++h2) {
-                    if (h2 == hown) continue;
-                    if (contains(lists + (size_t)h2 * k, k, i)) {
-                        if (h2 < hown) { m = 0; break; }   // a lower head owns this row
-                        m |= 1u << h2;
-                    }
-                }
-                if (i < 0 || i >= n) m = 0;                 // not a token of this unit
+            int i = 0;
+            if (rr < R) {
+                m = sm.rmask[rr];
+                i = sm.rows[rr];
+                if (!((m >> hown) & 1u) || (m & below)) m = 0;   // invalid, or a lower head owns it
             }
             mask[r] = m;
             const uint16_t *kr = krows + ((size_t)u * n + (m ? i : 0)) * D;
-            const uint16_t *vr = vrows + ((size_t)u * n + (m ? i : 0)) * D;
+            const uint16_t *vr_ = vrows + ((size_t)u * n + (m ? i : 0)) * D;
             if (kVec) {
                 kp[r] = m ? __ldg(reinterpret_cast<const uint2 *>(kr) + lane) : make_uint2(0u, 0u);
-                vp[r] = m ? __ldg(reinterpret_cast<const uint2 *>(vr) + lane) : make_uint2(0u, 0u);
+                vp[r] = m ? __ldg(reinterpret_cast<const uint2 *>(vr_) + lane) : make_uint2(0u, 0u);
             } else {
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
                     const int j = lane + 32 * c;
                     const bool ok = m && j < D;
                     kv[r][c] = ok ? __uint_as_float(((uint32_t)__ldg(kr + j)) << 16) : 0.0f;
-                    vv[r][c] = ok ? __uint_as_float(((uint32_t)__ldg(vr + j)) << 16) : 0.0f;
+                    vv[r][c] = ok ? __uint_as_float(((uint32_t)__ldg(vr_ + j)) << 16) : 0.0f;
                 }
             }
         }
+        // partial dots of every (row, head) slot, then one transpose reduction:
+        // afterwards lane l holds the full dot of slot l mod S
+        float a[S];
 #pragma unroll
-        for (int r = 0; r < kRowsInFlight; ++r) {
-            if (!mask[r]) continue;                         // warp-uniform
-            float kk[4], vx[4];
+        for (int r = 0; r < RB; ++r) {
+            float kk[4];
             if (kVec) {
                 kk[0] = bf16lo(kp[r].x); kk[1] = bf16hi(kp[r].x); kk[2] = bf16lo(kp[r].y); kk[3] = bf16hi(kp[r].y);
-                vx[0] = bf16lo(vp[r].x); vx[1] = bf16hi(vp[r].x); vx[2] = bf16lo(vp[r].y); vx[3] = bf16hi(vp[r].y);
             } else {
 #pragma unroll
-                for (int c = 0; c < 4; ++c) { kk[c] = kv[r][c]; vx[c] = vv[r][c]; }
+                for (int c = 0; c < 4; ++c) kk[c] = kv[r][c];
             }
 #pragma unroll
             for (int h = 0; h < G; ++h) {
-                if (!((mask[r] >> h) & 1u)) continue;
                 float d = 0.0f;
 #pragma unroll
                 for (int c = 0; c < 4; ++c) d = fmaf(qv[h][c], kk[c], d);
-#pragma unroll
-                for (int o = 16; o; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
-                const float logit = d * scale;
-                const float mn = fmaxf(m_h[h], logit);
-                const float corr = expf(m_h[h] - mn);
-                const float p = expf(logit - mn);
-                l_h[h] = l_h[h] * corr + p;
-#pragma unroll
-                for (int c = 0; c < 4; ++c) o_h[h][c] = o_h[h][c] * corr + p * vx[c];
-                m_h[h] = mn;
+                a[r * G + h] = d;
             }
         }
+#pragma unroll
+        for (int w = S / 2; w >= 1; w >>= 1) {
+            const bool up = (lane & w) != 0;
+#pragma unroll
+            for (int i = 0; i < w; ++i) {
+                const float send = up ? a[i] : a[i + w];
+                const float keep = up ? a[i + w] : a[i];
+                a[i] = keep + __shfl_xor_sync(0xffffffffu, send, w);
+            }
+        }
+#pragma unroll
+        for (int o = S; o < 32; o <<= 1) a[0] += __shfl_xor_sync(0xffffffffu, a[0], o);
+        // online softmax for slot (vr, vh), then per head across the batch's rows
+        unsigned mv = 0;
+        float mo = -CUDART_INF_F;
+#pragma unroll
+        for (int r = 0; r < RB; ++r) mv = (r == vr) ? mask[r] : mv;
+#pragma unroll
+        for (int h = 0; h < G; ++h) mo = (h == vh) ? m_h[h] : mo;
+        const bool live = (mv >> vh) & 1u;
+        const float logit = live ? a[0] * scale : -CUDART_INF_F;
+        float mn = logit;
+#pragma unroll
+        for (int o = G; o < S; o <<= 1) mn = fmaxf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+        mn = fmaxf(mn, mo);
+        float p = 0.0f, corr = 1.0f;
+        if (mn != -CUDART_INF_F) {
+            p = live ? expf(logit - mn) : 0.0f;
+            corr = expf(mo - mn);
+        }
+        float ps = p;
+#pragma unroll
+        for (int o = G; o < S; o <<= 1) ps += __shfl_xor_sync(0xffffffffu, ps, o);
+        if (lane < S) pb[lane] = p;
+        __syncwarp();
+#pragma unroll
+        for (int h = 0; h < G; ++h) {   // lane h holds slot (row 0, head h)
+            const float c = __shfl_sync(0xffffffffu, corr, h);
+            l_h[h] = l_h[h] * c + __shfl_sync(0xffffffffu, ps, h);
+            m_h[h] = __shfl_sync(0xffffffffu, mn, h);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) o_h[h][e] *= c;
+        }
+#pragma unroll
+        for (int r = 0; r < RB; ++r) {
+            float vx[4];
+            if (kVec) {
+                vx[0] = bf16lo(vp[r].x); vx[1] = bf16hi(vp[r].x); vx[2] = bf16lo(vp[r].y); vx[3] = bf16hi(vp[r].y);
+            } else {
+#pragma unroll
+                for (int c = 0; c < 4; ++c) vx[c] = vv[r][c];
+            }
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+                const float pr = pb[r * G + h];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) o_h[h][e] = fmaf(pr, vx[e], o_h[h][e]);
+            }
+        }
+        __syncwarp();
     }
-    // ---- merge warps
+    // ---- merge the warps: rescale each warp's state to the CTA maximum
+    if (lane == 0) {
+#pragma unroll
+        for (int h = 0; h < G; ++h) { sm.wm[warp][h] = m_h[h]; sm.wl[warp][h] = l_h[h]; }
+    }
+    __syncthreads();
 #pragma unroll
     for (int h = 0; h < G; ++h) {
-        if (lane == 0) { sm.wm[warp][h] = m_h[h]; sm.wl[warp][h] = l_h[h]; }
+        float M = -CUDART_INF_F;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) M = fmaxf(M, sm.wm[w][h]);
+        const float f = (m_h[h] == -CUDART_INF_F) ? 0.0f : expf(m_h[h] - M);
+        if (lane == 0) sm.wf[warp][h] = f;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
             const int j = kVec ? 4 * lane + c : lane + 32 * c;
-            if (j < D) wo[((size_t)warp * G + h) * D + j] = o_h[h][c];
+            if (j < D) wo[((size_t)warp * G + h) * D + j] = o_h[h][c] * f;
         }
     }
     __syncthreads();
     float *pp = part + ((size_t)u * splits + s) * G * (D + 2);
     for (int e = tid; e < G * (D + 2); e += NA) {
         const int h = e / (D + 2), c = e % (D + 2);
-        float M = -CUDART_INF_F;
-        for (int w = 0; w < kWarps; ++w) M = fmaxf(M, sm.wm[w][h]);
         float acc = 0.0f;
-        if (c == 0) acc = M;
-        else {
-            for (int w = 0; w < kWarps; ++w) {
-                const float f = (sm.wm[w][h] == -CUDART_INF_F) ? 0.0f : expf(sm.wm[w][h] - M);
-                acc += f * (c == 1 ? sm.wl[w][h] : wo[((size_t)w * G + h) * D + (c - 2)]);
-            }
+        if (c == 0) {
+            acc = -CUDART_INF_F;
+            for (int w = 0; w < kWarps; ++w) acc = fmaxf(acc, sm.wm[w][h]);
+        } else if (c == 1) {
+            for (int w = 0; w < kWarps; ++w) acc = fmaf(sm.wf[w][h], sm.wl[w][h], acc);
+        } else {
+            for (int w = 0; w < kWarps; ++w) acc += wo[((size_t)w * G + h) * D + (c - 2)];
         }
         pp[e] = acc;
     }
-    // ---- last CTA of the unit merges the splits
+    // ---- the last CTA of the unit merges the partial states
     __threadfence();
     __syncthreads();
     if (tid == 0) {
@@ -205,26 +303,38 @@ attn_kernel(int n, int D, int k, int cph, int splits, const uint16_t *__restrict
     if (!sm.is_last) return;
     __threadfence();
     const float *p0 = part + (size_t)u * splits * G * (D + 2);
-    float *mg = reinterpret_cast<float *>(asmem_raw + lay.merge);   // [splits][D + 2], one head
-    for (int h = 0; h < G; ++h) {
-        // all of the head's partial states in one round of independent loads
-        for (int e = tid; e < splits * (D + 2); e += NA) {
-            const int sp = e / (D + 2), c = e % (D + 2);
-            mg[e] = __ldcg(p0 + ((size_t)sp * G + h) * (D + 2) + c);
+    float *mg = reinterpret_cast<float *>(asmem_raw + lay.merge);   // [splits][nh][D + 2]
+    const int hc = attn_merge_heads(G, splits, D);
+    for (int h0 = 0; h0 < G; h0 += hc) {
+        const int nh = min(hc, G - h0), row = nh * (D + 2);
+        for (int e = tid; e < splits * row; e += NA) {
+            const int sp = e / row, c = e % row;
+            mg[e] = __ldcg(p0 + ((size_t)sp * G + h0) * (D + 2) + c);
         }
         __syncthreads();
-        for (int j = tid; j < D; j += NA) {
+        if (warp < nh) {   // warp hh: the head's maximum, split weights (in place of m) and sum
             float M = -CUDART_INF_F;
-            for (int sp = 0; sp < splits; ++sp) M = fmaxf(M, mg[sp * (D + 2)]);
-            float L = 0.0f, O = 0.0f;
-            for (int sp = 0; sp < splits; ++sp) {
-                const float ms = mg[sp * (D + 2)];
-                if (ms == -CUDART_INF_F) continue;
-                const float f = expf(ms - M);
-                L += f * mg[sp * (D + 2) + 1];
-                O += f * mg[sp * (D + 2) + 2 + j];
+            for (int sp = lane; sp < splits; sp += 32) M = fmaxf(M, mg[(size_t)sp * row + warp * (D + 2)]);
+            M = warp_max(M);
+            float L = 0.0f;
+            for (int sp = lane; sp < splits; sp += 32) {
+                float *b = mg + (size_t)sp * row + warp * (D + 2);
+                const float f = (b[0] == -CUDART_INF_F) ? 0.0f : expf(b[0] - M);
+                b[0] = f;
+                L = fmaf(f, b[1], L);
             }
-            out[((size_t)u * G + h) * D + j] = O / L;
+            L = warp_sum(L);
+            if (lane == 0) sm.cl[warp] = L;
+        }
+        __syncthreads();
+        for (int e = tid; e < nh * D; e += NA) {
+            const int hh = e / D, j = e % D;
+            float O = 0.0f;
+            for (int sp = 0; sp < splits; ++sp) {
+                const float *b = mg + (size_t)sp * row + hh * (D + 2);
+                O = fmaf(b[0], b[2 + j], O);
+            }
+            out[((size_t)u * G + h0 + hh) * D + j] = O / sm.cl[hh];
         }
         __syncthreads();
     }
@@ -238,7 +348,7 @@ int launch_sparse_attn(const fathom_shape &s, const uint16_t *krows, const uint1
     float *part = (float *)(w + wl.part_off);
     unsigned *ticket = (unsigned *)(w + wl.ticket_off);
     if (s.units > 65535) { set_error("sparse_attn: too many units for one launch"); return FATHOM_EINVAL; }
-    const size_t smem = attn_smem_layout(s.G, s.k, s.D).total;
+    const size_t smem = attn_smem_layout(s.G, s.k, s.D, wl.splits).total;
     const int cph = (s.k + kAttnRows - 1) / kAttnRows;   // CTAs per head
     const bool vec = s.D == 128 && ((uintptr_t)krows % 8 == 0) && ((uintptr_t)vrows % 8 == 0);
     const dim3 grid(wl.splits, s.units);

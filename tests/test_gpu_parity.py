@@ -185,7 +185,8 @@ def test_ragged_multi_tile_multi_unit():
 
 
 def test_long_chunks_exercise_pruning():
-    # 152 units x 64k tokens: 4 chunks per unit of 8 sub-chunks -> in-CTA prunes
+    # 152 units x 64k tokens: a few chunks per unit (one full wave of CTAs over
+    # 152 units), each of 8 or more sub-chunks -> in-CTA prunes
     w = W("qwen3_32k", n=65536)
     U = 152
     inp = Inputs(w, range(U), 65536)
@@ -268,8 +269,8 @@ def test_workspace_reuse_across_calls():
 
 
 def test_concentrated_winners_force_the_exact_second_pass():
-    # one unit of 64k tokens is split into 32 chunks that each keep only their
-    # top-64 in the first pass; amplifying the keys of one 2048-token stretch
+    # one unit of 64k tokens is split into 32 chunks that each keep only about
+    # their top-60 in the first pass; amplifying the keys of one 2048-token stretch
     # puts all k' = 476 winners in one chunk, which the merge must flag and the
     # second pass must rescan exactly
     w = W("qwen3_32k", n=65536)
