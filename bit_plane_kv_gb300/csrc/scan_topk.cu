@@ -293,6 +293,118 @@ __device__ void select_thresholds(SelScratch<S> &sm, Visit visit, int target, in
     }
 }
 
+// Bin of a score among 256 equal-width bins from smin (explicitly rounded
+// operations, so both passes below compute the same bin; monotone in s).
+__device__ __forceinline__ int score_bin(float s, float smin, float inv) {
+    const int b = (int)__fmul_rn(__fsub_rn(s, smin), inv);
+    return b < 0 ? 0 : (b > 255 ? 255 : b);
+}
+
+// For every selection h (S at once), a threshold key T[h] with at least m of
+// the visited keys at or above it and, unless the scores bunch into one bin,
+// at most 2m (T[h] = 0: fewer than m keys, keep them all).  One histogram of
+// the scores over 256 equal-width bins between their minimum and maximum
+// (value space, so the sparse upper tail gets fine bins), the boundary bin
+// found from the top, and T the smallest key in the bins at or above it.
+// Bins are monotone in the score, so exactly the keys in those bins are >= T.
+// visit(f) calls f(s, valid, score, key) for every item of every thread, in
+// lock step.  Three passes over registers and four barriers, no refinement
+// rounds: the callers only need a bound, not an exact rank.
+template <int S, typename Visit>
+__device__ void hist_thresholds(SelScratch<S> &sm, Visit visit, int m, uint64_t (&T)[S]) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
+    for (int i = tid; i < S * 256; i += blockDim.x) (&sm.hist[0][0])[i] = 0;
+    float lo[S], hi[S];
+    int cnt[S];
+#pragma unroll
+    for (int h = 0; h < S; ++h) { lo[h] = CUDART_INF_F; hi[h] = -CUDART_INF_F; cnt[h] = 0; }
+    visit([&](auto h, bool valid, float sc, uint64_t) {
+        if (valid) { lo[h] = fminf(lo[h], sc); hi[h] = fmaxf(hi[h], sc); ++cnt[h]; }
+    });
+#pragma unroll
+    for (int h = 0; h < S; ++h) {
+#pragma unroll
+        for (int o = 16; o; o >>= 1) {
+            lo[h] = fminf(lo[h], __shfl_xor_sync(0xffffffffu, lo[h], o));
+            hi[h] = fmaxf(hi[h], __shfl_xor_sync(0xffffffffu, hi[h], o));
+            cnt[h] += __shfl_xor_sync(0xffffffffu, cnt[h], o);
+        }
+        if (lane == 0) {
+            sm.red[0][h][warp] = __float_as_uint(lo[h]);
+            sm.red[1][h][warp] = __float_as_uint(hi[h]);
+            sm.red_n[h][warp] = cnt[h];
+        }
+    }
+    __syncthreads();
+    float smin[S], inv[S];
+    bool use[S];
+#pragma unroll
+    for (int h = 0; h < S; ++h) {
+        float a = CUDART_INF_F, z = -CUDART_INF_F;
+        int c = 0;
+        for (int w = 0; w < nw; ++w) {
+            a = fminf(a, __uint_as_float((uint32_t)sm.red[0][h][w]));
+            z = fmaxf(z, __uint_as_float((uint32_t)sm.red[1][h][w]));
+            c += sm.red_n[h][w];
+        }
+        use[h] = c >= m && c > 0;
+        const float span = __fsub_rn(z, a);
+        smin[h] = a;
+        inv[h] = (span > 0.0f && span < CUDART_INF_F) ? __fdiv_rn(256.0f, span) : 0.0f;
+    }
+    visit([&](auto h, bool valid, float sc, uint64_t) {
+        if (valid && use[h]) atomicAdd(&sm.hist[h][score_bin(sc, smin[h], inv[h])], 1u);
+    });
+    __syncthreads();
+    if (warp < S) {   // warp h finds selection h's boundary: lane l owns bins 255-8l .. 248-8l
+        const int h = warp;
+        unsigned loc = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) loc += sm.hist[h][255 - 8 * lane - i];
+        unsigned incl = loc;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const unsigned y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
+        }
+        const unsigned excl = incl - loc, need = (unsigned)m;
+        bool uh = false;
+        static_for<0, S>([&](auto hh) { if (h == hh) uh = use[hh]; });
+        if (lane == 0 && !uh) sm.digit[h] = -1;
+        if (uh && excl < need && need <= incl) {
+            unsigned c = excl;
+            for (int i = 0; i < 8; ++i) {
+                const int bin = 255 - 8 * lane - i;
+                c += sm.hist[h][bin];
+                if (c >= need) { sm.digit[h] = bin; break; }
+            }
+        }
+    }
+    __syncthreads();
+    int bnd[S];
+    unsigned long long kmin[S];
+#pragma unroll
+    for (int h = 0; h < S; ++h) { bnd[h] = sm.digit[h]; kmin[h] = ~0ull; }
+    visit([&](auto h, bool valid, float sc, uint64_t key) {
+        if (valid && bnd[h] >= 0 && score_bin(sc, smin[h], inv[h]) >= bnd[h])
+            kmin[h] = min(kmin[h], (unsigned long long)key);
+    });
+#pragma unroll
+    for (int h = 0; h < S; ++h) {
+#pragma unroll
+        for (int o = 16; o; o >>= 1) kmin[h] = min(kmin[h], __shfl_xor_sync(0xffffffffu, kmin[h], o));
+        if (lane == 0) sm.red[0][h][warp] = kmin[h];
+    }
+    __syncthreads();
+#pragma unroll
+    for (int h = 0; h < S; ++h) {
+        unsigned long long k = ~0ull;
+        for (int w = 0; w < nw; ++w) k = min(k, sm.red[0][h][w]);
+        T[h] = bnd[h] >= 0 ? k : 0ull;
+    }
+    __syncthreads();   // sm.red and sm.digit are reused by the next selection
+}
+
 // Appends the valid keys >= T (one per thread) to dst at a shared counter.
 template <int S>
 __device__ __forceinline__ void append_if(SelScratch<S> &sm, bool keep, uint64_t key, uint64_t *dst,
@@ -345,55 +457,19 @@ __device__ int prune_list(SelScratch<1> &sm, uint64_t *lst, int count, int targe
     return min(sm.new_cnt, count);
 }
 
-// Prunes the G lists of one CTA at once (keys in registers, KPT per head per
-// thread; every count <= KPT * blockDim.x): one selection for all heads
-// instead of G in a row.  lists: head h's list at lists + h * cap.
-template <int G, int KPT>
-__device__ void prune_lists_multi(SelScratch<G> &sm, uint64_t *lists, size_t cap, const int (&count)[G],
-                                  int target, int slack, uint64_t (&T)[G], int *cnt_out) {
-    const int tid = threadIdx.x, nt = blockDim.x;
-    uint64_t r[G][KPT];
-#pragma unroll
-    for (int i = 0; i < KPT; ++i)
-        static_for<0, G>([&](auto h) {
-            const int e = i * nt + tid;
-            r[h][i] = e < count[h] ? lists[h * cap + e] : 0ull;
-        });
-    int kept[G];
-    select_thresholds<G>(sm, [&](auto f) {
-#pragma unroll
-        for (int i = 0; i < KPT; ++i)
-            static_for<0, G>([&](auto h) { f(h, i * nt + tid < count[h], r[h][i]); });
-    }, target, slack, T, kept);
-    if (tid < G) cnt_out[tid] = 0;
-    __syncthreads();   // all keys are in registers: the lists may be overwritten
-    const int lane = tid & 31;
-#pragma unroll
-    for (int i = 0; i < KPT; ++i)
-        static_for<0, G>([&](auto h) {
-            const bool keep = i * nt + tid < count[h] && r[h][i] >= T[h];
-            const unsigned bal = __ballot_sync(0xffffffffu, keep);
-            if (bal) {   // one shared counter update per warp
-                const int leader = __ffs(bal) - 1;
-                int base = 0;
-                if (lane == leader) base = atomicAdd(&cnt_out[h], __popc(bal));
-                base = __shfl_sync(0xffffffffu, base, leader);
-                if (keep) lists[h * cap + base + __popc(bal & ((1u << lane) - 1u))] = r[h][i];
-            }
-        });
-    __syncthreads();
-}
-
 // ---------------------------------------------------------------------------
 constexpr int kListKPT = 26;   // register keys per thread for list prunes (cap <= 26 * 256)
-constexpr int kMultiKPT = 4;   // register keys per thread and head for the joint final shrink
+constexpr int kMultiKPT = 4;   // register keys per thread and head for the final shrink
 
-template <int G>
+// kFix = false: the first pass (histogram thresholds, no exact selection; a
+// list that would overflow publishes tau = max so that the merge flags it).
+// kFix = true: the exact second pass over the chunks the merge flagged.
+template <int G, bool kFix>
 __global__ void __launch_bounds__(NT, (G <= 4) ? 3 : 1)
 scan_kernel(int n, int D, int chunk_blocks, int source, size_t stage_words, size_t stage_scales,
             const uint64_t *__restrict__ planes, const uint16_t *__restrict__ scales,
             const fathom_run *__restrict__ runs, const float *__restrict__ q, int k_sel, int m_sel,
-            int m_first, int fixup, int ns, int r0, int nf, int cap, int vec, float *__restrict__ scores_opt,
+            int m_first, int ns, int r0, int nf, int cap, int vec, float *__restrict__ scores_opt,
             uint64_t *__restrict__ cand, int *__restrict__ cand_cnt, uint64_t *__restrict__ cand_tau,
             int *__restrict__ flags, float *__restrict__ forced_scores) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
@@ -404,7 +480,7 @@ scan_kernel(int n, int D, int chunk_blocks, int source, size_t stage_words, size
     const int nb = num_blocks(n);
     (void)chunk_blocks;
     const size_t cta = (size_t)u * gridDim.x + chunk;
-    if (fixup) {
+    if (kFix) {
         // second pass: only chunks the merge flagged run again, keeping their exact top-k'
         bool any = false;
         for (int h = 0; h < G; ++h) any |= flags[cta * G + h] != 0;
@@ -544,8 +620,8 @@ scan_kernel(int n, int D, int chunk_blocks, int source, size_t stage_words, size
 
     for (int sb = chunk * kSubBlocks; sb < nb; sb += (int)gridDim.x * kSubBlocks) {
         const int nblk = min(kSubBlocks, nb - sb);
-        // make room in every head's candidate list before this sub-chunk
-        if (k_sel > 0) {
+        // (second pass) make room in every head's candidate list before this sub-chunk
+        if (kFix && k_sel > 0) {
 #pragma unroll 1
             for (int h = 0; h < G; ++h) {
                 const int c = sm.cnt[h];
@@ -642,9 +718,8 @@ scan_kernel(int n, int D, int chunk_blocks, int source, size_t stage_words, size
             }
         }
 
-        // ---- epilogue: debug scores, forced tokens, then order words of the scores
+        // ---- epilogue: debug scores, forced tokens, then the candidates' keys
         const int beta = sb + bl;
-        uint32_t okey[8][G];                     // order_f32(score): the high word of a key
         unsigned cvm = 0;                        // bit m: a candidate (valid, not forced)
 #pragma unroll
         for (int m = 0; m < 8; ++m) {
@@ -661,24 +736,29 @@ scan_kernel(int n, int D, int chunk_blocks, int source, size_t stage_words, size
 #pragma unroll
                 for (int h = 0; h < G; ++h) forced_scores[((size_t)u * G + h) * nf + slot] = acc[m][h];
             }
-#pragma unroll
-            for (int h = 0; h < G; ++h) okey[m][h] = order_f32(acc[m][h]);
         }
         auto key_of = [&](int m, int h) -> uint64_t {
             const uint32_t i = (uint32_t)(beta * 64 + (int)r + 8 * (m & 3) + 32 * (m >> 2));
-            return ((uint64_t)okey[m][h] << 32) | (uint64_t)(0xffffffffu - i);
+            return ((uint64_t)order_f32(acc[m][h]) << 32) | (uint64_t)(0xffffffffu - i);
         };
         if (k_sel > 0 && first) {
             // a threshold from this first sub-chunk, all heads at once, from registers:
-            // between m1 and 2 m1 of its keys are >= it (m1: four times the winners
-            // one sub-chunk holds on average)
+            // at least m1 of its keys are >= it (m1: four times the winners one
+            // sub-chunk holds on average; the second pass: exactly k' .. 2k')
             uint64_t T[G];
-            int kept[G];
-            select_thresholds<G>(sm.selg, [&](auto f) {
+            auto visit = [&](auto f) {
 #pragma unroll
                 for (int m = 0; m < 8; ++m)
-                    static_for<0, G>([&](auto h) { f(h, (cvm >> m) & 1u, key_of(m, h)); });
-            }, m_first, m_first, T, kept);
+                    static_for<0, G>([&](auto h) { f(h, (cvm >> m) & 1u, acc[m][h], key_of(m, h)); });
+            };
+            if constexpr (kFix) {
+                int kept[G];
+                select_thresholds<G>(sm.selg, [&](auto f) {
+                    visit([&](auto h, bool v, float, uint64_t key) { f(h, v, key); });
+                }, m_first, m_first, T, kept);
+            } else {
+                hist_thresholds<G>(sm.selg, visit, m_first, T);
+            }
 #pragma unroll
             for (int h = 0; h < G; ++h) tau[h] = T[h];
             if (tid < G) sm.tau[tid] = T[tid];
@@ -686,27 +766,29 @@ scan_kernel(int n, int D, int chunk_blocks, int source, size_t stage_words, size
         }
         if (k_sel > 0) {
             // append every key >= tau (few, about m1 .. 2 m1 per sub-chunk and head):
-            // a mask of the passing heads from the high words alone, then per token
-            // a short loop over them
-            uint32_t thi[G];
+            // a mask of the heads whose score reaches tau's score (one float compare
+            // each; tau = 0 keeps everything), then per token a short loop over them
+            float tf[G];
 #pragma unroll
-            for (int h = 0; h < G; ++h) thi[h] = (uint32_t)(tau[h] >> 32);
+            for (int h = 0; h < G; ++h) {
+                const uint32_t thi = (uint32_t)(tau[h] >> 32);
+                tf[h] = (thi <= order_f32(-CUDART_INF_F)) ? -CUDART_INF_F : unorder_f32(thi);
+            }
 #pragma unroll
             for (int m = 0; m < 8; ++m) {
                 unsigned hm = 0;
 #pragma unroll
                 for (int h = 0; h < G; ++h)
-                    if (((cvm >> m) & 1u) && okey[m][h] >= thi[h]) hm |= 1u << h;
+                    if (((cvm >> m) & 1u) && acc[m][h] >= tf[h]) hm |= 1u << h;
                 while (hm) {
                     const int h = __ffs(hm) - 1;
                     hm &= hm - 1;
-                    uint32_t ok = okey[m][0];
+                    float sc = acc[m][0];
                     uint64_t th = tau[0];
                     static_for<1, G>([&](auto hh) {
-                        if (h == hh) { ok = okey[m][hh]; th = tau[hh]; }
+                        if (h == hh) { sc = acc[m][hh]; th = tau[hh]; }
                     });
-                    const uint32_t i = (uint32_t)(beta * 64 + (int)r + 8 * (m & 3) + 32 * (m >> 2));
-                    const uint64_t kk = ((uint64_t)ok << 32) | (uint64_t)(0xffffffffu - i);
+                    const uint64_t kk = make_key(sc, (uint32_t)(beta * 64 + (int)r + 8 * (m & 3) + 32 * (m >> 2)));
                     if (kk >= th) {
                         const int pos = atomicAdd(&sm.cnt[h], 1);
                         if (pos < cap) cand[(cta * G + h) * (size_t)cap + pos] = kk;
@@ -719,47 +801,81 @@ scan_kernel(int n, int D, int chunk_blocks, int source, size_t stage_words, size
     }
     if (piped) cp_async_wait<0>();
 
-    // ---- shrink long lists to about m keys (exactly k' in the second pass), then
-    // publish counts and thresholds: every key this CTA dropped is < its threshold
-    bool joint = false;
-    if (k_sel > 0 && !fixup) {
-        // usually every list is short: shrink all heads in one selection
-        int cs[G];
-        bool fits = true, any_long = false;
+    // ---- shrink long lists (first pass: to about m .. 2m keys by one histogram
+    // pass; second pass: exactly k'), then publish counts and thresholds: every
+    // key this CTA dropped is < its threshold
+    if constexpr (!kFix) {
+        if (k_sel > 0) {
+            int cs[G];
+            bool fits = true, any_long = false;
 #pragma unroll
-        for (int h = 0; h < G; ++h) {
-            cs[h] = min(sm.cnt[h], cap);
-            fits = fits && cs[h] <= kMultiKPT * NT;
-            any_long = any_long || cs[h] > 2 * m_sel;
-        }
-        if (fits && any_long) {
-            uint64_t T[G];
-            prune_lists_multi<G, kMultiKPT>(sm.selg, cand + cta * G * (size_t)cap, (size_t)cap, cs,
-                                           m_sel, m_sel, T, sm.cnt);
-            // a list that kept everything (T = 0) keeps its earlier threshold
-            if (tid < G) sm.tau[tid] = max((unsigned long long)sm.tau[tid], (unsigned long long)T[tid]);
-            __syncthreads();
-        }
-        joint = fits;
-    }
-    if (k_sel > 0 && !joint) {
-#pragma unroll 1
-        for (int h = 0; h < G; ++h) {
-            const int c = min(sm.cnt[h], cap);
-            const bool cut = fixup ? (c > k_sel) : (c > 2 * m_sel);
-            if (cut) {
-                uint64_t *lst = cand + (cta * G + h) * (size_t)cap;
-                uint64_t T;
-                const int nc = prune_list<kListKPT>(sm.sel1, lst, c, m_sel, fixup ? 0 : m_sel, &T);
-                if (tid == 0) { sm.cnt[h] = nc; sm.tau[h] = T; }
+            for (int h = 0; h < G; ++h) {
+                cs[h] = min(sm.cnt[h], cap);
+                fits = fits && cs[h] <= kMultiKPT * NT;
+                any_long = any_long || cs[h] > 2 * m_sel;
+            }
+            if (fits && any_long) {
+                uint64_t *lists = cand + cta * G * (size_t)cap;
+                uint64_t rk[G][kMultiKPT];
+#pragma unroll
+                for (int i = 0; i < kMultiKPT; ++i)
+                    static_for<0, G>([&](auto h) {
+                        const int e = i * NT + tid;
+                        rk[h][i] = e < cs[h] ? lists[h * (size_t)cap + e] : 0ull;
+                    });
+                uint64_t T[G];
+                hist_thresholds<G>(sm.selg, [&](auto f) {
+#pragma unroll
+                    for (int i = 0; i < kMultiKPT; ++i)
+                        static_for<0, G>([&](auto h) { f(h, i * NT + tid < cs[h], key_score(rk[h][i]), rk[h][i]); });
+                }, m_sel, T);
+                if (tid < G) sm.cnt[tid] = 0;
+                __syncthreads();   // every key is in registers: the lists may be overwritten
+                const int lane_ = tid & 31;
+#pragma unroll
+                for (int i = 0; i < kMultiKPT; ++i)
+                    static_for<0, G>([&](auto h) {
+                        const bool keep = i * NT + tid < cs[h] && rk[h][i] >= T[h];
+                        const unsigned bal = __ballot_sync(0xffffffffu, keep);
+                        if (bal) {
+                            const int leader = __ffs(bal) - 1;
+                            int base = 0;
+                            if (lane_ == leader) base = atomicAdd(&sm.cnt[h], __popc(bal));
+                            base = __shfl_sync(0xffffffffu, base, leader);
+                            if (keep) lists[h * (size_t)cap + base + __popc(bal & ((1u << lane_) - 1u))] = rk[h][i];
+                        }
+                    });
+                // a list that kept everything (T = 0) keeps its earlier threshold
+                if (tid < G) sm.tau[tid] = max((unsigned long long)sm.tau[tid], (unsigned long long)T[tid]);
                 __syncthreads();
             }
         }
-    }
-    if (tid < G) {
-        cand_cnt[cta * G + tid] = min(sm.cnt[tid], cap);
-        cand_tau[cta * G + tid] = sm.tau[tid];
-        if (fixup) flags[cta * G + tid] = 0;   // handled
+        if (tid < G) {
+            const int c = sm.cnt[tid];
+            cand_cnt[cta * G + tid] = min(c, cap);
+            // an overflowed list lost keys >= tau: the largest threshold makes the merge
+            // flag this chunk for the exact second pass
+            cand_tau[cta * G + tid] = c > cap ? ~0ull : sm.tau[tid];
+        }
+    } else {
+        if (k_sel > 0) {
+#pragma unroll 1
+            for (int h = 0; h < G; ++h) {
+                const int c = min(sm.cnt[h], cap);
+                if (c > k_sel) {
+                    uint64_t *lst = cand + (cta * G + h) * (size_t)cap;
+                    uint64_t T;
+                    const int nc = prune_list<kListKPT>(sm.sel1, lst, c, k_sel, 0, &T);
+                    if (tid == 0) { sm.cnt[h] = nc; sm.tau[h] = T; }
+                    __syncthreads();
+                }
+            }
+        }
+        if (tid < G) {
+            cand_cnt[cta * G + tid] = min(sm.cnt[tid], cap);
+            cand_tau[cta * G + tid] = sm.tau[tid];
+            flags[cta * G + tid] = 0;   // handled
+        }
     }
 }
 
@@ -1000,16 +1116,23 @@ static int launch_g(const fathom_shape &s, const uint64_t *planes, const uint16_
     const int vec = (nb % 8 == 0) && aligned_src && ((uintptr_t)planes % 16 == 0) && ((uintptr_t)scales % 16 == 0);
     const size_t smem = sizeof(ScanSmem<G>);
     if (s.units > 65535) { set_error("scan: too many units for one launch"); return FATHOM_EINVAL; }
-    ensure_smem(scan_kernel<G>, smem);
+    ensure_smem(scan_kernel<G, false>, smem);
+    ensure_smem(scan_kernel<G, true>, smem);
     const size_t msmem = sizeof(MergeSmem);
     ensure_smem(merge_kernel, msmem);
     const int nf = f.nf > 0 ? f.nf : 1;
     dim3 grid(sg.chunks, s.units);
     for (int pass = 0; pass < 2; ++pass) {
-        scan_kernel<G><<<grid, NT, smem, st>>>(s.n, s.D, sg.chunk_blocks, source, stage_words,
-                                               stage_scales, planes, scales, runs, q, k_sel, m_sel, m_first, pass,
-                                               f.ns, f.r0, nf, cap, vec, pass ? nullptr : scores_opt, cand,
-                                               cnt, ctau, flags, forced);
+        if (pass == 0)
+            scan_kernel<G, false><<<grid, NT, smem, st>>>(s.n, s.D, sg.chunk_blocks, source, stage_words,
+                                                          stage_scales, planes, scales, runs, q, k_sel, m_sel,
+                                                          m_first, f.ns, f.r0, nf, cap, vec, scores_opt, cand,
+                                                          cnt, ctau, flags, forced);
+        else
+            scan_kernel<G, true><<<grid, NT, smem, st>>>(s.n, s.D, sg.chunk_blocks, source, stage_words,
+                                                         stage_scales, planes, scales, runs, q, k_sel, m_sel,
+                                                         m_first, f.ns, f.r0, nf, cap, vec, nullptr, cand,
+                                                         cnt, ctau, flags, forced);
         int rc = launch_status("scan_kernel");
         if (rc) return rc;
         merge_kernel<<<dim3(wl.parts, s.G, s.units), kMThreads, msmem, st>>>(
@@ -1036,9 +1159,9 @@ static int resident_g() {
     std::lock_guard<std::mutex> lock(mu);
     if (!cache[dev]) {
         const size_t smem = sizeof(ScanSmem<G>);
-        ensure_smem(scan_kernel<G>, smem);
+        ensure_smem(scan_kernel<G, false>, smem);
         int nbk = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nbk, scan_kernel<G>, NT, smem) != cudaSuccess) {
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nbk, scan_kernel<G, false>, NT, smem) != cudaSuccess) {
             cudaGetLastError();
             return 0;
         }

@@ -145,6 +145,33 @@ def test_plan_bit_exact_over_budgets(G):
         assert od.sum() <= max(budgets[u], 0)
 
 
+def test_plan_bit_exact_across_magnitudes():
+    # queries and variances scaled by powers of ten from 1e-30 to 1e30: the
+    # bisection's geometric midpoints then cover most of the double exponent
+    # range (including the ends, where the plan falls back to fp64 operations)
+    # and must still give the oracle's theta bit for bit
+    w = W("qwen3_32k")
+    U = 512
+    gen = torch.Generator(device="cpu").manual_seed(20260123)
+    q = torch.stack([synth.unit_query(w, u % 64, "cuda") for u in range(U)])
+    _, var = B.fathom_calibrate(torch.stack([synth.unit_calib(w, u % 64, "cuda") for u in range(U)]))
+    sq = 10.0 ** torch.randint(-15, 16, (U, 1, 1), generator=gen).double()
+    sv = 10.0 ** torch.randint(-30, 31, (U, 1), generator=gen).double()
+    q = (q.double().cpu() * sq).float().cuda().contiguous()
+    var = (var.double().cpu() * sv).float().cuda().contiguous()
+    budgets = np.array([8, 24, 48, 64, 100, 200, 400], np.int32)[np.arange(U) % 7]
+    shape = B.make_shape(U, 65536, 128, 4, 1, 0, 0)
+    depth, theta, runs = B.fathom_plan(shape, q, var, torch.tensor(budgets, device="cuda"))
+    torch.cuda.synchronize()
+    qn, vn = q.cpu().numpy(), var.cpu().numpy()
+    th = theta.cpu().numpy()
+    dn = depth.cpu().numpy()
+    for u in range(U):
+        od, oth, _ = O.plan(qn[u], vn[u], int(budgets[u]))
+        np.testing.assert_array_equal(dn[u], od)
+        assert th[u] == oth, (u, th[u], oth)
+
+
 def test_plan_explicit_bracket_and_fixed():
     w = W("qwen3_32k")
     U = 16
