@@ -40,6 +40,9 @@ RUN_BYTES = 24
 
 SIGNATURES = {
     "fathom_calibrate": (ctypes.c_int, [_i32, _i32, _i32, _vp, _vp, _vp, _vp]),
+    "fathom_calibrate_klt": (ctypes.c_int, [_i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp]),
+    "fathom_rotate_keys": (ctypes.c_int, [ctypes.POINTER(Shape), _vp, ctypes.c_int, _i32, _vp, _vp, _vp, _vp]),
+    "fathom_rotate_query": (ctypes.c_int, [ctypes.POINTER(Shape), _vp, _i32, _vp, _vp, _vp]),
     "fathom_quantize_pack": (ctypes.c_int, [ctypes.POINTER(Shape), _vp, ctypes.c_int, _vp, _vp, _vp]),
     "fathom_plan": (ctypes.c_int, [ctypes.POINTER(Shape), _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
     "fathom_plan_fixed": (ctypes.c_int, [ctypes.POINTER(Shape), _vp, _vp, _i32, _i32, _vp, _vp, _vp]),
@@ -146,6 +149,45 @@ def fathom_calibrate(calib, mean=None, var=None, stream=None):
         mean = torch.empty(U, D, dtype=torch.float32, device=calib.device)
     _call("fathom_calibrate", U, m, D, _p(calib), _p(mean), _p(var), _stream(stream))
     return mean, var
+
+
+def fathom_calibrate_klt(calib, mean=None, V=None, lam=None, stream=None):
+    """calib [groups][m][D] fp32 -> (mean [groups][D] fp64, V [groups][D][D] fp64 (eigenvectors
+    as columns, eigenvalues descending), lambda [groups][D] fp32)."""
+    _check(calib, "calib", (torch.float32,))
+    Gr, m, D = calib.shape
+    dev = calib.device
+    if mean is None:
+        mean = torch.empty(Gr, D, dtype=torch.float64, device=dev)
+    if V is None:
+        V = torch.empty(Gr, D, D, dtype=torch.float64, device=dev)
+    if lam is None:
+        lam = torch.empty(Gr, D, dtype=torch.float32, device=dev)
+    _call("fathom_calibrate_klt", Gr, m, D, _p(calib), _p(mean), _p(V), _p(lam), _stream(stream))
+    return mean, V, lam
+
+
+def fathom_rotate_keys(shape: Shape, keys, groups, mean, V, out=None, stream=None):
+    """keys [U][n][D] fp32 or bf16 -> (k - mu_g) V_g [U][n][D] fp32, g = u % groups."""
+    _check(keys, "keys", (torch.float32, torch.bfloat16, torch.int16))
+    _check(mean, "mean", (torch.float64,), (groups, shape.D))
+    _check(V, "V", (torch.float64,), (groups, shape.D, shape.D))
+    dt = F32 if keys.dtype == torch.float32 else BF16
+    if out is None:
+        out = torch.empty(shape.units, shape.n, shape.D, dtype=torch.float32, device=keys.device)
+    _call("fathom_rotate_keys", ctypes.byref(shape), _p(keys), dt, int(groups), _p(mean), _p(V), _p(out),
+          _stream(stream))
+    return out
+
+
+def fathom_rotate_query(shape: Shape, q, groups, V, out=None, stream=None):
+    """q [U][G][D] fp32 -> q V_g [U][G][D] fp32, g = u % groups."""
+    _check(q, "q", (torch.float32,), (shape.units, shape.G, shape.D))
+    _check(V, "V", (torch.float64,), (groups, shape.D, shape.D))
+    if out is None:
+        out = torch.empty_like(q)
+    _call("fathom_rotate_query", ctypes.byref(shape), _p(q), int(groups), _p(V), _p(out), _stream(stream))
+    return out
 
 
 def fathom_quantize_pack(shape: Shape, keys, planes=None, scales=None, stream=None):

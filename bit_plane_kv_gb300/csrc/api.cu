@@ -209,6 +209,49 @@ int fathom_calibrate(int32_t units, int32_t m, int32_t D, const float *calib, fl
     return launch_calibrate(units, m, D, calib, mean_out, var_out, (cudaStream_t)stream);
 }
 
+int fathom_calibrate_klt(int32_t groups, int32_t m, int32_t D, const float *calib, double *mean,
+                         double *V, float *lambda, void *stream) {
+    g_err[0] = 0;
+    if (groups < 1 || m < 2 || D < 1 || D > FATHOM_MAX_D) {
+        set_error("calibrate_klt: need groups >= 1, m >= 2, 1 <= D <= %d", FATHOM_MAX_D);
+        return FATHOM_EINVAL;
+    }
+    NONNULL(calib);
+    NONNULL(mean);
+    NONNULL(V);
+    NONNULL(lambda);
+    return launch_calibrate_klt(groups, m, D, calib, mean, V, lambda, (cudaStream_t)stream);
+}
+
+int fathom_rotate_keys(const fathom_shape *shape, const void *keys, int keys_dtype, int32_t groups,
+                       const double *mean, const double *V, float *out, void *stream) {
+    g_err[0] = 0;
+    int rc = check_shape(shape, false);
+    if (rc) return rc;
+    if (keys_dtype != FATHOM_F32 && keys_dtype != FATHOM_BF16) {
+        set_error("keys_dtype must be FATHOM_F32 or FATHOM_BF16"); return FATHOM_EINVAL;
+    }
+    if (groups < 1) { set_error("groups must be >= 1 (got %d)", groups); return FATHOM_EINVAL; }
+    NONNULL(keys);
+    NONNULL(mean);
+    NONNULL(V);
+    NONNULL(out);
+    return launch_rotate_keys(*shape, keys, keys_dtype, groups, mean, V, out, (cudaStream_t)stream);
+}
+
+int fathom_rotate_query(const fathom_shape *shape, const float *q, int32_t groups, const double *V,
+                        float *q_rot, void *stream) {
+    g_err[0] = 0;
+    int rc = check_shape(shape, false);
+    if (rc) return rc;
+    if (groups < 1) { set_error("groups must be >= 1 (got %d)", groups); return FATHOM_EINVAL; }
+    if (shape->units > 65535 * 32) { set_error("rotate_query: too many units"); return FATHOM_EINVAL; }
+    NONNULL(q);
+    NONNULL(V);
+    NONNULL(q_rot);
+    return launch_rotate_query(*shape, q, groups, V, q_rot, (cudaStream_t)stream);
+}
+
 int fathom_quantize_pack(const fathom_shape *shape, const void *keys, int keys_dtype,
                          uint64_t *planes, uint16_t *scales, void *stream) {
     g_err[0] = 0;

@@ -111,6 +111,12 @@ inline void ensure_smem(F *func, size_t bytes) {
 // ---------------------------------------------------------------- launchers
 int launch_calibrate(int units, int m, int D, const float *calib, float *mean, float *var,
                      cudaStream_t st);
+int launch_calibrate_klt(int groups, int m, int D, const float *calib, double *mean, double *vec,
+                         float *lambda, cudaStream_t st);
+int launch_rotate_keys(const fathom_shape &s, const void *keys, int dtype, int groups, const double *mean,
+                       const double *vec, float *out, cudaStream_t st);
+int launch_rotate_query(const fathom_shape &s, const float *q, int groups, const double *vec, float *out,
+                        cudaStream_t st);
 int launch_quantize(const fathom_shape &s, const void *keys, int dtype, uint64_t *planes,
                     uint16_t *scales, cudaStream_t st);
 int launch_plan(const fathom_shape &s, const float *q, const float *var, const int32_t *budget,

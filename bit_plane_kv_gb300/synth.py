@@ -19,6 +19,9 @@ heads, 4 query heads per KV head, 128 channels; §1) with synthetic content:
 * value rows ~ N(0, 1).
 * rotated-basis workloads: keys R diag(sigma) z with a seeded random
   orthogonal R per unit (QR of a Gaussian matrix); queries R (N(0,1) sigma^0.5).
+* sigma, R and the calibration keys belong to a unit's (layer, KV head): in a
+  multi-session batch every sequence shares them (one calibration per layer
+  and head); keys, queries and values are the unit's own.
 * bf16 rows are the round-to-nearest-even of the fp32 draws.
 """
 from __future__ import annotations
@@ -67,6 +70,11 @@ class Workload:
     def layer_units(self, layer: int) -> list:
         return [self.unit_index(s, layer, h) for s in range(self.seqs) for h in range(self.kv_heads)]
 
+    def dist_unit(self, unit: int) -> int:
+        """The (layer, KV head) a unit belongs to: the index of its key distribution
+        and calibration set, shared by every sequence of a multi-session batch."""
+        return unit % (self.layers * self.kv_heads)
+
 
 # The five workloads: shapes, budgets and regimes as the Fathom measurements
 # describe them (single layer n=4096; Qwen3-8B decode at 32k; host-resident
@@ -102,7 +110,7 @@ def _gen(w, unit, kind, device, extra=0):
 
 
 def unit_sigma(w: Workload, unit: int, device="cpu") -> torch.Tensor:
-    g = _gen(w, unit, "sigma", device)
+    g = _gen(w, w.dist_unit(unit), "sigma", device)
     sigma = torch.exp(torch.randn(w.D, generator=g, device=device))
     if w.outliers:
         pick = torch.randperm(w.D, generator=g, device=device)[: w.outliers]
@@ -111,7 +119,7 @@ def unit_sigma(w: Workload, unit: int, device="cpu") -> torch.Tensor:
 
 
 def unit_rotation(w: Workload, unit: int, device="cpu") -> torch.Tensor:
-    g = _gen(w, unit, "rot", "cpu")
+    g = _gen(w, w.dist_unit(unit), "rot", "cpu")
     a = torch.randn(w.D, w.D, generator=g, dtype=torch.float64)
     qm, r = torch.linalg.qr(a)
     qm = qm * torch.sign(torch.diagonal(r))[None, :]
@@ -134,8 +142,9 @@ def unit_keys(w: Workload, unit: int, device="cpu", n: int | None = None) -> tor
 
 
 def unit_calib(w: Workload, unit: int, device="cpu") -> torch.Tensor:
+    """[1024][D] calibration keys of the unit's (layer, KV head)."""
     sigma = unit_sigma(w, unit, device)
-    g = _gen(w, unit, "calib", device)
+    g = _gen(w, w.dist_unit(unit), "calib", device)
     return _correlate(w, unit, torch.randn(CALIB_ROWS, w.D, generator=g, device=device), sigma, device)
 
 

@@ -97,6 +97,43 @@ typedef struct {
 int fathom_calibrate(int32_t units, int32_t m, int32_t D, const float *calib,
                      float *mean_out, float *var_out, void *stream);
 
+/* Rotated basis (§3.5), calibration.  For each calibration group g (one
+ * layer and KV head) from m calibration rows: the mean mu_g (fp64, rows in
+ * order), the covariance (fp64, ddof = 1) and its eigen-decomposition by
+ * cyclic Jacobi rotations in fp64 (sweeps until the off-diagonal square sum
+ * is <= 1e-30 of the total, at most 100): eigenvalues lambda_g in descending
+ * order, eigenvectors as the columns of V_g, each with its largest-magnitude
+ * component positive.  lambda_g takes the place of the variances in
+ * fathom_plan for a rotated store.
+ *   calib  [groups][m][D] fp32 (device), m >= 2
+ *   mean   [groups][D] fp64 (out, device)
+ *   V      [groups][D][D] fp64 (out, device): V[g][j][c] = component j of
+ *          eigenvector c
+ *   lambda [groups][D] fp32 (out, device)
+ * An offline step (store build); fp64 throughout. */
+int fathom_calibrate_klt(int32_t groups, int32_t m, int32_t D, const float *calib, double *mean,
+                         double *V, float *lambda, void *stream);
+
+/* Rotated keys (§3.5): out[u][i][c] = sum_j (k[u][i][j] - mu_g[j]) V_g[j][c]
+ * for unit u in group g = u % groups (units packed sequence, layer, KV head:
+ * groups = layers x KV heads shares a layer's and head's basis across the
+ * sequences).  k - mu is formed in fp64 and rounded to fp32, V_g is rounded
+ * to fp32, the sum is accumulated in fp32.  The result is the input of
+ * fathom_quantize_pack (keys_dtype FATHOM_F32) for a rotated store.
+ *   keys [units][n][D] fp32 or bf16 (keys_dtype), mean [groups][D] fp64,
+ *   V [groups][D][D] fp64, out [units][n][D] fp32; all device.
+ * Uses shape->units, n, D. */
+int fathom_rotate_keys(const fathom_shape *shape, const void *keys, int keys_dtype, int32_t groups,
+                       const double *mean, const double *V, float *out, void *stream);
+
+/* Rotated queries (§3.5): q_rot[u][h][c] = sum_j q[u][h][j] V_g[j][c], g =
+ * u % groups, fp32 accumulation.  The plan and the scan of a rotated store
+ * take q_rot; the exact attention takes the original q.
+ *   q [units][G][D] fp32, V [groups][D][D] fp64, q_rot [units][G][D] fp32
+ *   (out); all device.  Uses shape->units, D, G. */
+int fathom_rotate_query(const fathom_shape *shape, const float *q, int32_t groups, const double *V,
+                        float *q_rot, void *stream);
+
 /* Quantise and pack the K store (§3.2).  Per unit, channel j and 64-token
  * block beta: a = max_{i in beta} |k_ij| stored as fp16 (round to nearest
  * even, saturating at 65504); s = a / 8; code c = clip(floor(k / s), -8, 7) + 8

@@ -92,3 +92,18 @@ def test_workspace_sizes_scale_with_shape(lib):
     assert 0 < B.workspace_size(small, 0) < B.workspace_size(big, 0)
     assert 0 < B.workspace_size(small, 1) <= B.workspace_size(big, 1)
     assert B.workspace_size(big, 2) == 0
+
+
+def test_rotated_basis_calls_validate_arguments(lib):
+    d = ctypes.c_void_p(256)
+    rc = lib.fathom_calibrate_klt(1, 1, 128, d, d, d, d, None)
+    assert rc_msg(lib, rc)[0] == 1 and "m >= 2" in lib.fathom_last_error().decode()
+    rc = lib.fathom_calibrate_klt(1, 16, 128, d, None, d, d, None)
+    assert rc_msg(lib, rc) == (1, "mean is NULL")
+    s = B.make_shape(2, 4096, 128, 4, 64)
+    rc = lib.fathom_rotate_keys(ctypes.byref(s), d, 0, 0, d, d, d, None)
+    assert rc_msg(lib, rc)[0] == 1 and "groups" in lib.fathom_last_error().decode()
+    rc = lib.fathom_rotate_keys(ctypes.byref(s), d, 7, 1, d, d, d, None)
+    assert rc_msg(lib, rc)[0] == 1
+    rc = lib.fathom_rotate_query(ctypes.byref(s), d, 1, d, None, None)
+    assert rc_msg(lib, rc) == (1, "q_rot is NULL")

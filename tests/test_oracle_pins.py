@@ -418,3 +418,28 @@ def test_eigh_matches_numpy():
     np.testing.assert_allclose(V.T @ V, np.eye(D), atol=1e-12)
     for c in range(D):
         assert V[np.argmax(np.abs(V[:, c])), c] > 0
+
+
+def test_rotation_preserves_dot_products_and_norms():
+    # V from the oracle's own eigh is orthogonal, so the rotated keys keep the
+    # norms of the centred keys and q' . k' = q . (k - mu): the ranking of the
+    # tokens by the rotated scores is their ranking by q . k
+    rng = np.random.default_rng(29)
+    D, n = 16, 200
+    R, _ = np.linalg.qr(rng.normal(size=(D, D)))
+    sig = np.exp(rng.normal(size=D))
+    calib = ((rng.normal(size=(512, D)) * sig) @ R.T + 0.5).astype(np.float32)
+    keys = ((rng.normal(size=(n, D)) * sig) @ R.T + 0.5).astype(np.float32)
+    q = rng.normal(size=(3, D)).astype(np.float32)
+    mean, _, cov = O.calibrate(calib, with_cov=True)
+    lam, V = O.eigh(cov)
+    kr = O.rotate(keys, mean, V).astype(np.float64)
+    qr = O.rotate_query(q, V)
+    kc = keys.astype(np.float64) - mean
+    np.testing.assert_allclose(np.linalg.norm(kr, axis=1), np.linalg.norm(kc, axis=1), rtol=1e-6)
+    np.testing.assert_allclose(qr @ kr.T, q.astype(np.float64) @ kc.T, rtol=1e-5, atol=1e-5 * np.abs(q).sum())
+    # the rotated channels are uncorrelated on the calibration keys, with variances lambda
+    cr = O.rotate(calib, mean, V).astype(np.float64)
+    np.testing.assert_allclose(np.cov(cr, rowvar=False), np.diag(lam), atol=1e-5 * lam[0])
+    # identity basis: rotation is centring only
+    np.testing.assert_allclose(O.rotate(keys, mean, np.eye(D)), (keys - mean).astype(np.float32), rtol=1e-6)
