@@ -149,12 +149,27 @@ class Setup:
         self.krows = alloc(L, H, n, D, dtype=torch.bfloat16)
         self.vrows = alloc(L, H, n, D, dtype=torch.bfloat16)
         self.var = torch.empty(L, H, D, dtype=torch.float32, device=dev)
+        self.rotated = w.rotated
+        if self.rotated:
+            # rotated basis (one per layer and KV head, shared by the sequences):
+            # calibration once, then every layer's store holds the planes of (k - mu) V
+            nh = w.kv_heads
+            calib = torch.stack([synth.unit_calib(w, g, dev) for g in range(w.layers * nh)]).contiguous()
+            self.kmean, self.kV, lam = B.fathom_calibrate_klt(calib)
+            del calib
         for l in range(L):
             units = w.layer_units(l)
             keys = torch.stack([synth.unit_keys(w, u, dev) for u in units]).to(torch.bfloat16)
-            p, s = B.fathom_quantize_pack(self.shape, keys)
-            calib = torch.stack([synth.unit_calib(w, u, dev) for u in units])
-            _, self.var[l] = B.fathom_calibrate(calib)
+            if self.rotated:
+                g0 = l * nh
+                rk = B.fathom_rotate_keys(self.shape, keys, nh, self.kmean[g0:g0 + nh], self.kV[g0:g0 + nh])
+                p, s = B.fathom_quantize_pack(self.shape, rk)
+                del rk
+                self.var[l] = lam[g0:g0 + nh].repeat(H // nh, 1)    # unit i of the layer: head i % nh
+            else:
+                p, s = B.fathom_quantize_pack(self.shape, keys)
+                calib = torch.stack([synth.unit_calib(w, u, dev) for u in units])
+                _, self.var[l] = B.fathom_calibrate(calib)
             self.planes[l].copy_(p)
             self.scales[l].copy_(s)
             self.krows[l].copy_(keys)
@@ -171,8 +186,13 @@ class Setup:
                                            for l in range(L)]) for s in range(steps_total)]).contiguous()
         self.Qh = torch.empty(self.Q.shape, dtype=self.Q.dtype, pin_memory=True)
         self.Qh.copy_(self.Q)
-        self.budget_t = torch.full((H,), budget, dtype=torch.int32, device=dev)
-        bmax = 128 if fixed else budget
+        # per-layer budgets B_l when the workload has them (and no flat override), else flat
+        self.per_layer = w.per_layer and budget <= 0
+        lb = [w.budgets[l % len(w.budgets)] if self.per_layer else budget for l in range(L)]
+        self.budgets = lb
+        self.budget_t = torch.tensor([[b] * H for b in lb], dtype=torch.int32, device=dev)
+        self.qrot = torch.empty(L, H, self.G, D, dtype=torch.float32, device=dev) if self.rotated else None
+        bmax = 128 if fixed else max(lb)
         self.stage_w = max(2, min(bmax, 4 * D) * nb + (min(bmax, 4 * D) * nb) % 2)
         self.stage_s = max(8, (min(bmax, D) * nb + 7) // 8 * 8)
         self.stage_p = torch.zeros(H, self.stage_w, dtype=torch.int64, device=dev)
@@ -200,12 +220,18 @@ class Setup:
 
     def layer(self, l, q, ev=None):
         """One layer of the decode step; ev = optional (start, end) events around the
-        dominant stage (host regime: the gather, or the fused scan; HBM regime: the scan)."""
+        dominant stage (host regime: the gather, or the fused scan; HBM regime: the scan).
+        A rotated store is planned and scanned with the rotated queries q V; the exact
+        attention takes the original q."""
         B = self.B
+        qa = q
+        if self.rotated:
+            nh = self.w.kv_heads
+            q = B.fathom_rotate_query(self.shape, qa, nh, self.kV[l * nh:(l + 1) * nh], out=self.qrot[l])
         if self.fixed:
             B.fathom_plan_fixed(self.shape, q, self.var[l], 32, 4, depth=self.depth, runs=self.runs)
         else:
-            B.fathom_plan(self.shape, q, self.var[l], self.budget_t, depth=self.depth, theta=self.theta,
+            B.fathom_plan(self.shape, q, self.var[l], self.budget_t[l], depth=self.depth, theta=self.theta,
                           runs=self.runs)
         if self.host and self.path == "pipelined":
             self._gather_scan_pipelined(l, q, ev)
@@ -226,7 +252,7 @@ class Setup:
                                topk_idx=self.idx, topk_score=self.sel)
             if ev:
                 ev[1].record()
-        B.fathom_sparse_attn(self.shape, self.krows[l], self.vrows[l], q, self.idx, self.aws, out=self.out[l])
+        B.fathom_sparse_attn(self.shape, self.krows[l], self.vrows[l], qa, self.idx, self.aws, out=self.out[l])
 
     def _gather_scan_pipelined(self, l, q, ev=None):
         """Gathers of unit groups on a second stream, each group's scan on the main stream
@@ -256,8 +282,12 @@ class Setup:
         pipelined path reports its overlapped gather + scan as one stage)."""
         B = self.B
         ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+        qa = q
         ev[0].record()
-        B.fathom_plan(self.shape, q, self.var[l], self.budget_t, depth=self.depth, theta=self.theta,
+        if self.rotated:
+            nh = self.w.kv_heads
+            q = B.fathom_rotate_query(self.shape, qa, nh, self.kV[l * nh:(l + 1) * nh], out=self.qrot[l])
+        B.fathom_plan(self.shape, q, self.var[l], self.budget_t[l], depth=self.depth, theta=self.theta,
                       runs=self.runs)
         ev[1].record()
         if self.host and self.path == "staged":
@@ -273,7 +303,7 @@ class Setup:
             B.fathom_scan_topk(self.shape, self.planes[l], self.scales[l], self.runs, q, self.ws,
                                topk_idx=self.idx, topk_score=self.sel)
         ev[3].record()
-        B.fathom_sparse_attn(self.shape, self.krows[l], self.vrows[l], q, self.idx, self.aws, out=self.out[l])
+        B.fathom_sparse_attn(self.shape, self.krows[l], self.vrows[l], qa, self.idx, self.aws, out=self.out[l])
         ev[4].record()
         return ev
 
@@ -341,9 +371,17 @@ def measured_peaks():
 
 
 # ---------------------------------------------------------------- CPU oracle baseline
+def unit_budget(w: synth.Workload, budget: int, unit: int) -> int:
+    """The unit's code-bit budget: the flat budget, or its layer's B_l (budget <= 0)."""
+    if w.per_layer and budget <= 0:
+        return w.budgets[((unit // w.kv_heads) % w.layers) % len(w.budgets)]
+    return budget
+
+
 def oracle_layer_sample(w: synth.Workload, budget: int, unit: int):
     """Time the CPU oracle on one unit of the workload (the whole per-unit step:
-    plan, gather, scores, selection, attention); returns seconds."""
+    query rotation for a rotated store, plan, gather, scores, selection,
+    attention); returns seconds."""
     from oracle import oracle as O
     O.build()
     n = w.n
@@ -352,17 +390,28 @@ def oracle_layer_sample(w: synth.Workload, budget: int, unit: int):
     kb = keys.view(torch.int16).numpy().view(np.uint16)
     vb = synth.unit_values(w, unit, "cpu").to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
     q = synth.unit_query(w, unit, "cpu", step=1).numpy()
-    _, var = O.calibrate(synth.unit_calib(w, unit, "cpu").numpy())
+    calib = synth.unit_calib(w, unit, "cpu").numpy()
+    V = None
+    if w.rotated:                              # store build, not part of the step
+        mean, _, cov = O.calibrate(calib, with_cov=True)
+        lam, V = O.eigh(cov)
+        var = lam.astype(np.float32)
+        k32 = O.rotate(k32, mean, V)
+    else:
+        _, var = O.calibrate(calib)
+        var = var.astype(np.float32)
     P, S, _ = O.quantize_pack(k32)            # store build: not part of the step
+    b = unit_budget(w, budget, unit)
     t0 = time.perf_counter()
-    depth, theta, _ = O.plan(q, var.astype(np.float32), budget)
+    qs = O.rotate_query(q, V).astype(np.float32) if w.rotated else q
+    depth, theta, _ = O.plan(qs, var, b)
     runs = O.runs(depth, n)
     if w.regime == "host":
         nb = (n + 63) // 64
         sp, ss = O.gather(runs, P, S, int(depth.sum()) * nb, int((depth > 0).sum()) * nb)
-        s = O.scores_staged(runs, sp, ss, depth, q, n)
+        s = O.scores_staged(runs, sp, ss, depth, qs, n)
     else:
-        s = O.scores(P[None], S[None], depth[None], q[None], n)[0]
+        s = O.scores(P[None], S[None], depth[None], qs[None], n)[0]
     idx, _ = O.select(s, w.k, w.n_sink, w.n_recent)
     O.attention(kb, vb, q, idx)
     return time.perf_counter() - t0
@@ -378,6 +427,21 @@ def cpu_baseline(w, budget, reps=1):
 
 
 # ---------------------------------------------------------------- main
+def workload_config(w: synth.Workload, args) -> dict:
+    """The JSON line's config (the same for both arms)."""
+    per_layer = w.per_layer and args.budget <= 0
+    budgets = [w.budgets[l % len(w.budgets)] if per_layer else args.budget for l in range(w.layers)]
+    path = args.path if w.regime == "host" else "hbm"
+    return {"workload": w.name, "n": w.n, "layers": w.layers, "kv_heads": w.kv_heads, "sessions_per_gpu": w.seqs,
+            "G": w.G, "D": w.D, "k": w.k, "n_sink": w.n_sink, "n_recent": w.n_recent,
+            "budget": ("fixed 32ch x 4 planes" if args.fixed else
+                       f"per layer {budgets}" if per_layer else args.budget),
+            "basis": "rotated (KLT per layer and KV head)" if w.rotated else "channels",
+            "regime": w.regime, "path": path,
+            "unit_groups": args.groups if path == "pipelined" else 1,
+            "l2": "inputs larger than L2 (store and rows of all layers > 129 MB)"}
+
+
 def run_reference(args, w, rank, world):
     """The CPU oracle on the same workload, as the reference arm."""
     if rank != 0:
@@ -394,8 +458,7 @@ def run_reference(args, w, rank, world):
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": us_layer * w.layers / 1e3,
             "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded Qwen3-8B-shaped keys/queries/values)",
-            "config": {"workload": w.name, "n": w.n, "layers": w.layers, "kv_heads": w.kv_heads, "G": w.G,
-                       "D": w.D, "k": w.k, "budget": args.budget, "regime": w.regime},
+            "config": workload_config(w, args),
             "cpu_baseline": {"value": us_layer, "unit": "µs/layer", "cores": 1, "kind": "oracle",
                              "sample": f"one unit per step at n={w.n}, scaled x{w.units_per_layer()} units per layer"},
             "e2e": {"value": us_layer, "unit": "µs/layer", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -408,7 +471,8 @@ def main():
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--workload", default="host_1m", choices=sorted(synth.WORKLOADS))
-    ap.add_argument("--budget", type=int, default=48)
+    ap.add_argument("--budget", type=int, default=None,
+                    help="flat code-bit budget (default: 48, or the per-layer budgets of a workload that has them)")
     ap.add_argument("--fixed", action="store_true", help="the 136-bit fixed-depth comparison plan")
     ap.add_argument("--path", default="fused", choices=["fused", "staged", "pipelined"],
                     help="host regime: the scan reads the pinned store directly (default), gather then "
@@ -424,6 +488,8 @@ def main():
     args.warmup = max(args.warmup, 3)
     rank, world = dist_setup(args.gpus)
     w = synth.WORKLOADS[args.workload]
+    if args.budget is None:
+        args.budget = 0 if w.per_layer else 48
     if args.layers:
         w = synth.shrink(w, layers=args.layers)
     if args.regime:
@@ -545,6 +611,7 @@ def main():
         launches_per_layer = 7
     else:
         launches_per_layer = 6
+    launches_per_layer += 1 if st.rotated else 0     # the query rotation
     if st.host:
         link = link_gbs
         achieved = scanned / kern_avg / 1e9
@@ -569,11 +636,7 @@ def main():
         "warmup": args.warmup, "ms_per_step": elapsed / args.steps * 1e3, "higher_is_better": False,
         "scaling": "weak", "vs_baseline": None, "dtype": "fp32 (u64 bit planes, fp16 scales, bf16 rows)",
         "data": "synthetic (seeded Qwen3-8B-shaped keys/queries/values, no trained weights)",
-        "config": {"workload": w.name, "n": w.n, "layers": L, "kv_heads": w.kv_heads, "sessions_per_gpu": w.seqs,
-                   "G": w.G, "D": w.D, "k": w.k, "n_sink": w.n_sink, "n_recent": w.n_recent,
-                   "budget": "fixed 32ch x 4 planes" if args.fixed else args.budget, "regime": w.regime,
-                   "path": st.path, "unit_groups": len(st.groups) if st.path == "pipelined" else 1,
-                   "l2": "inputs larger than L2 (store and rows of all layers > 129 MB)"},
+        "config": workload_config(w, args),
         "scan_gbs": scan_gbs,
         "scanned_bytes_per_layer": scanned,
         "scanned_bits_per_token": bits_per_token,

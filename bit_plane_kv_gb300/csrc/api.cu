@@ -71,23 +71,31 @@ int device_sm_count() {
 }
 
 ScanGrid scan_grid(const fathom_shape &s) {
-    // One full wave: as many CTAs as the device holds at once (SMs x resident
-    // scan CTAs per SM; 152 x 3 on GB300 when no device answers), at least one
-    // 32-block sub-chunk per CTA (sub-chunks are dealt round-robin to a unit's
-    // CTAs, so every CTA of a unit has the same work to within one sub-chunk).
+    // Sub-chunks (32 blocks) of a unit are dealt round-robin to its `chunks`
+    // CTAs, so every CTA of a unit has ceil(n_sub / chunks) of them at most.
+    // With `slots` CTAs resident at once (SMs x resident scan CTAs per SM;
+    // 152 x 3 on GB300 when no device answers) the scan takes about
+    // waves x (sub-chunks per CTA + 1) sub-chunk times, the 1 standing for a
+    // CTA's fixed work (plan prologue, first threshold, final shrink).  Take
+    // the chunk count that minimises it (ties: fewer CTAs).
     int sms = device_sm_count();
     if (sms <= 0) sms = 152;
     int res = scan_resident_ctas(s.G);
     if (res <= 0) res = (s.G <= 4) ? 3 : 1;
-    const int target_ctas = sms * res;
+    const long long slots = (long long)sms * res;
     const int nb = num_blocks(s.n);
     const int n_sub = (nb + kSubBlocks - 1) / kSubBlocks;
-    int chunks = (target_ctas + s.units - 1) / s.units;
-    if (chunks > n_sub) chunks = n_sub;
-    if (chunks < 1) chunks = 1;
+    int best = 1;
+    long long best_cost = -1;
+    for (int c = 1; c <= n_sub; ++c) {
+        const long long waves = ((long long)s.units * c + slots - 1) / slots;
+        const long long cost = waves * ((n_sub + c - 1) / c + 1);
+        if (best_cost < 0 || cost < best_cost) { best_cost = cost; best = c; }
+        if ((long long)s.units * c >= 8 * slots) break;   // more CTAs than this never pay
+    }
     ScanGrid g;
-    g.chunks = chunks;
-    g.chunk_blocks = ((n_sub + chunks - 1) / chunks) * kSubBlocks;   // blocks per CTA, at most
+    g.chunks = best;
+    g.chunk_blocks = ((n_sub + best - 1) / best) * kSubBlocks;   // blocks per CTA, at most
     return g;
 }
 
@@ -150,7 +158,13 @@ ScanWorkspace scan_workspace_layout(const fathom_shape &s) {
 
 AttnWorkspace attn_workspace_layout(const fathom_shape &s) {
     AttnWorkspace w;
-    w.splits = s.G * ((s.k + kAttnRows - 1) / kAttnRows);
+    // 128 entries of a head's kept list per CTA; 256 (fewer CTAs, each list
+    // loaded and searched fewer times) once 128 would need more than two waves
+    int sms = device_sm_count();
+    if (sms <= 0) sms = 152;
+    const long long ctas128 = (long long)s.units * s.G * ((s.k + 127) / 128);
+    w.rows = ctas128 > 2LL * 2 * sms ? 256 : 128;
+    w.splits = s.G * ((s.k + w.rows - 1) / w.rows);
     if (w.splits < 1) w.splits = 1;
     w.part_off = 0;
     w.ticket_off = align256((size_t)s.units * w.splits * s.G * (s.D + 2) * sizeof(float));

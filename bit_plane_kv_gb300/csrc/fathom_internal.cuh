@@ -71,8 +71,9 @@ struct ScanWorkspace {
 ScanWorkspace scan_workspace_layout(const fathom_shape &s);
 
 constexpr int kAttnThreads = 256;
-constexpr int kAttnRows = 64;   // union rows per CTA
+constexpr int kAttnRowsMax = 512;   // kept-list entries per CTA, at most
 struct AttnWorkspace {
+    int rows;     // kept-list entries per CTA
     int splits;
     size_t part_off, ticket_off, total;
 };

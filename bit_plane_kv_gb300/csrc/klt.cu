@@ -17,7 +17,7 @@
 //                      shared memory; then eigenvalues in descending order and
 //                      each eigenvector's largest-magnitude component positive
 //   klt_rotate_keys    (k - mu) V per token, fp32 tiles of 64 tokens
-//   klt_rotate_query   q V per head
+//   klt_rotate_query   q V per head, V_g staged once for several units
 #include "fathom_internal.cuh"
 
 namespace fathom {
@@ -231,26 +231,61 @@ klt_rotate_keys_kernel(int n, int D, int groups, const T *__restrict__ keys, con
     }
 }
 
-// One CTA per unit, thread c computes output channel c for every head.
-__global__ void __launch_bounds__(FATHOM_MAX_D)
-klt_rotate_query_kernel(int G, int D, int groups, const float *__restrict__ q, const double *__restrict__ vec,
-                        float *__restrict__ out) {
-    __shared__ float qs[FATHOM_MAX_G][FATHOM_MAX_D];
-    const int u = blockIdx.x, g = u % groups, c = threadIdx.x;
-    for (int e = c; e < G * D; e += blockDim.x) qs[e / D][e % D] = q[(size_t)u * G * D + e];
-    __syncthreads();
-    if (c >= D) return;
-    float acc[FATHOM_MAX_G];
-#pragma unroll
-    for (int h = 0; h < FATHOM_MAX_G; ++h) acc[h] = 0.0f;
+// Grid (groups, ceil(units_per_group / kQUnits)): a CTA stages V_g once in fp32
+// (every thread keeps 32 independent 16-byte loads in flight) and rotates the
+// queries of up to kQUnits units of group g (units g, g + groups, ...);
+// thread t computes output channel t % 128 of half of the (unit, head) rows.
+constexpr int kQUnits = 1;
+constexpr int kQThreads = 256;
+__global__ void __launch_bounds__(kQThreads)
+klt_rotate_query_kernel(int units, int G, int D, int groups, const float *__restrict__ q,
+                        const double *__restrict__ vec, float *__restrict__ out) {
+    extern __shared__ __align__(16) float qsm[];
+    float *Vs = qsm;                                        // [D][D] (row stride FATHOM_MAX_D)
+    float *qs = qsm + FATHOM_MAX_D * FATHOM_MAX_D;          // [kQUnits * G][FATHOM_MAX_D]
+    const int g = blockIdx.x, tid = threadIdx.x;
+    const int t0 = blockIdx.y * kQUnits;
     const double *Vg = vec + (size_t)g * D * D;
-    for (int j = 0; j < D; ++j) {
-        const float v = __double2float_rn(Vg[(size_t)j * D + c]);
+    if (D == FATHOM_MAX_D && ((uintptr_t)Vg & 15) == 0) {
+        constexpr int kPer = FATHOM_MAX_D * FATHOM_MAX_D / 2 / kQThreads;   // double2 per thread
+        double2 r[kPer];
 #pragma unroll
-        for (int h = 0; h < FATHOM_MAX_G; ++h)
-            if (h < G) acc[h] = fmaf(qs[h][j], v, acc[h]);
+        for (int i = 0; i < kPer; ++i) r[i] = __ldg(reinterpret_cast<const double2 *>(Vg) + tid + i * kQThreads);
+#pragma unroll
+        for (int i = 0; i < kPer; ++i)
+            reinterpret_cast<float2 *>(Vs)[tid + i * kQThreads] = make_float2(__double2float_rn(r[i].x),
+                                                                              __double2float_rn(r[i].y));
+    } else {
+        for (int e = tid; e < D * D; e += kQThreads) Vs[(e / D) * FATHOM_MAX_D + e % D] = __double2float_rn(Vg[e]);
     }
-    for (int h = 0; h < G; ++h) out[((size_t)u * G + h) * D + c] = acc[h];
+    int nu = 0;
+    for (int t = 0; t < kQUnits; ++t) {
+        const long long u = (long long)g + (long long)groups * (t0 + t);
+        if (u >= units) break;
+        for (int e = tid; e < G * D; e += kQThreads) qs[(t * G + e / D) * FATHOM_MAX_D + e % D] = q[u * G * D + e];
+        ++nu;
+    }
+    __syncthreads();
+    const int c = tid % FATHOM_MAX_D, part = tid / FATHOM_MAX_D;
+    if (c >= D) return;
+    constexpr int kRows = kQUnits * FATHOM_MAX_G / 2;      // (unit, head) rows per thread
+    const int rows = nu * G, r0 = part * kRows;
+    float acc[kRows];
+#pragma unroll
+    for (int i = 0; i < kRows; ++i) acc[i] = 0.0f;
+    for (int j = 0; j < D; ++j) {
+        const float v = Vs[j * FATHOM_MAX_D + c];
+#pragma unroll
+        for (int i = 0; i < kRows; ++i)
+            if (r0 + i < rows) acc[i] = fmaf(qs[(r0 + i) * FATHOM_MAX_D + j], v, acc[i]);
+    }
+#pragma unroll
+    for (int i = 0; i < kRows; ++i) {
+        if (r0 + i < rows) {
+            const long long u = (long long)g + (long long)groups * (t0 + (r0 + i) / G);
+            out[(u * G + (r0 + i) % G) * D + c] = acc[i];
+        }
+    }
 }
 
 int launch_calibrate_klt(int groups, int m, int D, const float *calib, double *mean, double *vec,
@@ -288,7 +323,12 @@ int launch_rotate_keys(const fathom_shape &s, const void *keys, int dtype, int g
 
 int launch_rotate_query(const fathom_shape &s, const float *q, int groups, const double *vec, float *out,
                         cudaStream_t st) {
-    klt_rotate_query_kernel<<<s.units, FATHOM_MAX_D, 0, st>>>(s.G, s.D, groups, q, vec, out);
+    const int per_group = (s.units + groups - 1) / groups;   // units of the most populous group
+    const dim3 grid(groups < s.units ? groups : s.units, (per_group + kQUnits - 1) / kQUnits);
+    if (grid.x > 65535 * 32 || grid.y > 65535) { set_error("rotate_query: too many units"); return FATHOM_EINVAL; }
+    const size_t smem = ((size_t)FATHOM_MAX_D * FATHOM_MAX_D + (size_t)kQUnits * FATHOM_MAX_G * FATHOM_MAX_D) * sizeof(float);
+    ensure_smem(klt_rotate_query_kernel, smem);
+    klt_rotate_query_kernel<<<grid, kQThreads, smem, st>>>(s.units, s.G, s.D, groups, q, vec, out);
     return launch_status("klt_rotate_query_kernel");
 }
 

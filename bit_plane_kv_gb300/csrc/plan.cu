@@ -17,7 +17,7 @@
 
 namespace fathom {
 
-constexpr int kPlanWarps = 4;
+constexpr int kPlanWarps = 1;   // one unit per CTA: the fp64 chains of many units spread over the SMs
 constexpr int kCh = FATHOM_MAX_D / 32;   // channels per lane
 
 // t(g, theta) = #{m in 0..3 : g >= theta * 2^(2m+1)}.  For a normal positive

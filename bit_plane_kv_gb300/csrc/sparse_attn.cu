@@ -3,7 +3,7 @@
 // precision; §2: each head attends exactly over its own selected set, with no
 // mass redistribution for the rest).
 //
-// Grid: (G * ceil(k / kAttnRows), units).  CTA (h, c) takes entries
+// Grid: (G * ceil(k / R), units).  CTA (h, c) takes entries
 // [c R, c R + R) of head h's sorted kept list and handles the rows that h
 // owns -- the rows no lower head lists -- so every row of the union is
 // fetched exactly once.  The CTA first finds, for its R rows, which other
@@ -32,8 +32,8 @@ struct AttnBatch {
 
 struct AttnHeader {
     int is_last;
-    int rows[kAttnRows];
-    unsigned rmask[kAttnRows];
+    int rows[kAttnRowsMax];
+    unsigned rmask[kAttnRowsMax];
     float wm[kWarps][FATHOM_MAX_G];
     float wl[kWarps][FATHOM_MAX_G];
     float wf[kWarps][FATHOM_MAX_G];
@@ -94,7 +94,7 @@ __device__ __forceinline__ float warp_sum(float v) {
 // of V per row) or channels l + 32 e (any D <= 128).
 template <int G, bool kVec>
 __global__ void __launch_bounds__(NA, G >= 8 ? 1 : 2)
-attn_kernel(int n, int D, int k, int cph, int splits, const uint16_t *__restrict__ krows,
+attn_kernel(int n, int D, int k, int rows_cta, int cph, int splits, const uint16_t *__restrict__ krows,
             const uint16_t *__restrict__ vrows, const float *__restrict__ q,
             const int32_t *__restrict__ topk, float *__restrict__ out, float *__restrict__ part,
             unsigned *__restrict__ ticket) {
@@ -107,8 +107,8 @@ attn_kernel(int n, int D, int k, int cph, int splits, const uint16_t *__restrict
     const int s = blockIdx.x, u = blockIdx.y;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int hown = s / cph;
-    const int e_begin = (s % cph) * kAttnRows;
-    const int R = min(k, e_begin + kAttnRows) - e_begin;
+    const int e_begin = (s % cph) * rows_cta;
+    const int R = min(k, e_begin + rows_cta) - e_begin;
 
     // ---- the G sorted lists, then this CTA's rows and their head masks
     const int32_t *src = topk + (size_t)u * G * k;
@@ -119,14 +119,14 @@ attn_kernel(int n, int D, int k, int cph, int splits, const uint16_t *__restrict
         for (int e = tid; e < G * k; e += NA) lists[e] = __ldg(src + e);
     }
     __syncthreads();
-    for (int r = tid; r < kAttnRows; r += NA) {
+    for (int r = tid; r < R; r += NA) {
         const int i = r < R ? lists[hown * k + e_begin + r] : -1;
         sm.rows[r] = i;
         sm.rmask[r] = (r < R && i >= 0 && i < n) ? (1u << hown) : 0u;
     }
     __syncthreads();
-    for (int p = tid; p < kAttnRows * G; p += NA) {
-        const int r = p % kAttnRows, h2 = p / kAttnRows;
+    for (int p = tid; p < R * G; p += NA) {
+        const int r = p % R, h2 = p / R;
         if (h2 != hown && r < R && contains(lists + h2 * k, k, sm.rows[r])) atomicOr(&sm.rmask[r], 1u << h2);
     }
     __syncthreads();
@@ -349,13 +349,13 @@ int launch_sparse_attn(const fathom_shape &s, const uint16_t *krows, const uint1
     unsigned *ticket = (unsigned *)(w + wl.ticket_off);
     if (s.units > 65535) { set_error("sparse_attn: too many units for one launch"); return FATHOM_EINVAL; }
     const size_t smem = attn_smem_layout(s.G, s.k, s.D, wl.splits).total;
-    const int cph = (s.k + kAttnRows - 1) / kAttnRows;   // CTAs per head
+    const int cph = (s.k + wl.rows - 1) / wl.rows;   // CTAs per head
     const bool vec = s.D == 128 && ((uintptr_t)krows % 8 == 0) && ((uintptr_t)vrows % 8 == 0);
     const dim3 grid(wl.splits, s.units);
 #define FATHOM_ATTN_LAUNCH(GG, VV)                                                               \
     do {                                                                                         \
         ensure_smem(attn_kernel<GG, VV>, smem);                                                  \
-        attn_kernel<GG, VV><<<grid, NA, smem, st>>>(s.n, s.D, s.k, cph, wl.splits, krows, vrows, \
+        attn_kernel<GG, VV><<<grid, NA, smem, st>>>(s.n, s.D, s.k, wl.rows, cph, wl.splits, krows, vrows, \
                                                     q, idx, out, part, ticket);                  \
     } while (0)
     switch (s.G * 2 + (vec ? 1 : 0)) {
