@@ -891,14 +891,112 @@ constexpr int kMThreads = 512;
 constexpr int kMBuf = 8192;                  // keys in the shared-memory buffer
 constexpr int kMKPT = kMBuf / kMThreads;     // register keys per thread for a buffer prune
 
+constexpr int kMSmall = 1024;              // keys of the boundary bin ranked directly, at most
 struct MergeSmem {
     SelScratch<1> sel;
     uint64_t buf[kMBuf];
+    uint64_t small[kMSmall];                 // the boundary bin's keys (exact selection)
+    float fred[2][kMThreads / 32];
+    int bin_sel, bin_above, n_small;
     int off[FATHOM_MERGE_MAX_LISTS + 1];     // prefix sums of the streamed lists' counts
     int count;
     int is_last;
     uint64_t thresh;                         // the k'-th key of what was streamed (0: fewer keys)
 };
+
+// Cuts sm.buf[0 .. count) to its exact top-k keys (keys are unique) and
+// returns the k-th key.  One histogram of the scores over 256 equal-width
+// bins between their minimum and maximum finds the bin b holding the k-th
+// key; every key in the bins above b is kept, and the keys of bin b (few: the
+// bins are fine where the k-th key falls) are ranked against each other to
+// find the k-th exactly.  A bin of more than kMSmall keys (scores bunched
+// together) takes the radix select instead.  Requires count > k.
+__device__ uint64_t merge_exact_top(MergeSmem &sm, int count, int k) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
+    float lo = CUDART_INF_F, hi = -CUDART_INF_F;
+    for (int e = tid; e < count; e += blockDim.x) {
+        const float sc = key_score(sm.buf[e]);
+        lo = fminf(lo, sc);
+        hi = fmaxf(hi, sc);
+    }
+    for (int i = tid; i < 256; i += blockDim.x) sm.sel.hist[0][i] = 0;
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+        lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+        hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+    }
+    if (lane == 0) { sm.fred[0][warp] = lo; sm.fred[1][warp] = hi; }
+    if (tid == 0) sm.n_small = 0;
+    __syncthreads();
+    lo = CUDART_INF_F; hi = -CUDART_INF_F;
+    for (int w = 0; w < nw; ++w) { lo = fminf(lo, sm.fred[0][w]); hi = fmaxf(hi, sm.fred[1][w]); }
+    const float span = __fsub_rn(hi, lo);
+    const float inv = (span > 0.0f && span < CUDART_INF_F) ? __fdiv_rn(256.0f, span) : 0.0f;
+    for (int e = tid; e < count; e += blockDim.x) atomicAdd(&sm.sel.hist[0][score_bin(key_score(sm.buf[e]), lo, inv)], 1u);
+    __syncthreads();
+    if (warp == 0) {   // lane l owns bins 255-8l .. 248-8l; find the bin of the k-th key from the top
+        unsigned loc = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) loc += sm.sel.hist[0][255 - 8 * lane - i];
+        unsigned incl = loc;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const unsigned y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
+        }
+        const unsigned excl = incl - loc;
+        if (excl < (unsigned)k && (unsigned)k <= incl) {
+            unsigned c = excl;
+            for (int i = 0; i < 8; ++i) {
+                const int bin = 255 - 8 * lane - i;
+                const unsigned hb = sm.sel.hist[0][bin];
+                if (c + hb >= (unsigned)k) { sm.bin_sel = bin; sm.bin_above = (int)c; break; }
+                c += hb;
+            }
+        }
+    }
+    __syncthreads();
+    const int b = sm.bin_sel, above = sm.bin_above;
+    if ((int)sm.sel.hist[0][b] > kMSmall) {   // bunched scores: radix select
+        uint64_t T;
+        const int nc = prune_list<kMKPT>(sm.sel, sm.buf, count, k, 0, &T);
+        __syncthreads();
+        if (tid == 0) { sm.count = nc; sm.thresh = T; }
+        __syncthreads();
+        return T;
+    }
+    for (int e = tid; e < count; e += blockDim.x) {
+        const uint64_t key = sm.buf[e];
+        if (score_bin(key_score(key), lo, inv) == b) sm.small[atomicAdd(&sm.n_small, 1)] = key;
+    }
+    __syncthreads();
+    const int ns = sm.n_small, need = k - above;     // the need-th largest key of bin b is the k-th overall
+    for (int e = tid; e < ns; e += blockDim.x) {
+        const uint64_t x = sm.small[e];
+        int rank = 0;
+        for (int j = 0; j < ns; ++j) rank += sm.small[j] > x ? 1 : 0;
+        if (rank == need - 1) sm.thresh = x;
+    }
+    __syncthreads();
+    const uint64_t T = sm.thresh;
+    // every key is >= T or not: keep the k keys >= T, compacted in place through registers
+    uint64_t r[kMKPT];
+    const int used = (count + (int)blockDim.x - 1) / (int)blockDim.x;
+#pragma unroll
+    for (int i = 0; i < kMKPT; ++i) {
+        const int e = i * (int)blockDim.x + tid;
+        r[i] = (i < used && e < count) ? sm.buf[e] : 0ull;
+    }
+    if (tid == 0) sm.sel.new_cnt = 0;
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < kMKPT; ++i)
+        if (i < used) append_if<1>(sm.sel, (i * (int)blockDim.x + tid < count) && r[i] >= T, r[i], sm.buf, count);
+    __syncthreads();
+    if (tid == 0) sm.count = sm.sel.new_cnt;
+    __syncthreads();
+    return T;
+}
 
 // Streams `nl` lists (list l: base(l), count(l)) into sm.buf and leaves the
 // exact top-k' (or everything, if fewer) in sm.buf[0 .. sm.count).
@@ -934,12 +1032,8 @@ __device__ void stream_select(MergeSmem &sm, int nl, Base base, Count count, int
     while (done < total) {
         int room = kMBuf - sm.count;
         if (room < kMThreads) {              // make room: cut the buffer to its exact top-k'
-            uint64_t T;
-            const int nc = prune_list<kMKPT>(sm.sel, sm.buf, sm.count, k_sel, 0, &T);
-            __syncthreads();
-            if (tid == 0) sm.count = nc;
-            __syncthreads();
-            room = kMBuf - nc;
+            merge_exact_top(sm, sm.count, k_sel);
+            room = kMBuf - sm.count;
         }
         const int take = min(room, total - done);
         const int c0 = sm.count;
@@ -958,15 +1052,20 @@ __device__ void stream_select(MergeSmem &sm, int nl, Base base, Count count, int
         done += take;
     }
     if (sm.count > k_sel) {
-        uint64_t T;
-        const int nc = prune_list<kMKPT>(sm.sel, sm.buf, sm.count, k_sel, 0, &T);
-        __syncthreads();
-        if (tid == 0) { sm.count = nc; sm.thresh = T; }
-    } else if (tid == 0) {
-        // k' keys or fewer: the threshold is the smallest of them
+        merge_exact_top(sm, sm.count, k_sel);    // leaves the k'-th key in sm.thresh
+    } else {
+        // k' keys or fewer: the threshold is the smallest of them (0: fewer than k')
+        const int c = sm.count;
         unsigned long long mn = ~0ull;
-        for (int e = 0; e < sm.count; ++e) mn = min(mn, (unsigned long long)sm.buf[e]);
-        sm.thresh = (sm.count == k_sel) ? mn : 0ull;
+        for (int e = tid; e < c; e += blockDim.x) mn = min(mn, (unsigned long long)sm.buf[e]);
+#pragma unroll
+        for (int o = 16; o; o >>= 1) mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+        if ((tid & 31) == 0) sm.sel.red[0][0][tid >> 5] = mn;
+        __syncthreads();
+        if (tid == 0) {
+            for (int w = 1; w < (int)(blockDim.x >> 5); ++w) mn = min(mn, sm.sel.red[0][0][w]);
+            sm.thresh = (c == k_sel) ? mn : 0ull;
+        }
     }
     __syncthreads();
 }
