@@ -36,9 +36,13 @@ if ROOT not in sys.path:
 from bit_plane_kv_gb300 import synth  # noqa: E402
 
 METRIC = "decode-step µs/layer and scan GB/s (% of PCIe/HBM roofline) at 1M tokens"
-CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+CLOCK_FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
                 "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
                 "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+# Measured DRAM traffic of the first-pass scan over its algorithmic bytes (planned plane
+# runs + active-channel scales), from a full ncu capture of one HBM-resident layer of
+# host_256k: 14.42 MB read for 14.7 MB planned.
+SCAN_DRAM_PER_ALGO_BYTE = 14.42 / 14.70
 
 
 def log(*a):
@@ -84,23 +88,39 @@ def rank_workload(w: synth.Workload, rank: int) -> synth.Workload:
 
 # ---------------------------------------------------------------- clocks
 class ClockSampler:
+    """nvidia-smi sampling every 10 ms with timestamps; stop() keeps the samples that fall
+    inside the timed region (host wall-clock window), or, when the region is shorter than
+    the sampling period, the samples nearest to it."""
+
     def __init__(self):
         self.proc = None
         self.path = None
 
-    def start(self):
+    def start(self, wait_s=3.0):
         try:
             fd, self.path = tempfile.mkstemp(suffix=".csv")
             os.close(fd)
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={CLOCK_FIELDS}", "--format=csv,noheader,nounits",
-                                          "-lms", "50"], stdout=self.fh, stderr=subprocess.DEVNULL)
+                                          "-lms", "10"], stdout=self.fh, stderr=subprocess.DEVNULL)
+            t0 = time.time()
+            while time.time() - t0 < wait_s and os.path.getsize(self.path) == 0:
+                time.sleep(0.02)
         except Exception:
             self.proc = None
 
-    def stop(self, device_index=0):
+    @staticmethod
+    def _epoch(ts):
+        import datetime
+        try:
+            return datetime.datetime.strptime(ts.strip(), "%Y/%m/%d %H:%M:%S.%f").timestamp()
+        except ValueError:
+            return None
+
+    def stop(self, device_index=0, window=None):
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        time.sleep(0.03)
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
@@ -110,18 +130,28 @@ class ClockSampler:
         rows = []
         for line in open(self.path):
             f = [x.strip() for x in line.split(",")]
-            if len(f) < 9 or not f[0].isdigit() or int(f[0]) != device_index:
+            if len(f) < 10 or not f[1].isdigit() or int(f[1]) != device_index:
                 continue
-            rows.append(f)
+            rows.append((self._epoch(f[0]), f[1:]))
         os.unlink(self.path)
-        if not rows:
+        inside = rows
+        how = "all samples"
+        if window and rows and all(t is not None for t, _ in rows):
+            a, b = window
+            inside = [r for r in rows if a <= r[0] <= b]
+            how = "inside the timed region"
+            if not inside:   # region shorter than the sampling period: the nearest samples
+                rows.sort(key=lambda r: min(abs(r[0] - a), abs(r[0] - b)))
+                inside = rows[:2]
+                how = "nearest to the timed region (shorter than the 10 ms period)"
+        if not inside:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
-        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
-        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        sm = [float(r[1]) for _, r in inside if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for _, r in inside if r[2].replace(".", "").isdigit()]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        reasons = sorted({names[i] for _, r in inside for i in range(4) if r[5 + i].lower() == "active"})
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": reasons, "samples": len(rows)}
+                "reasons": reasons, "samples": len(inside), "window": how}
 
 
 # ---------------------------------------------------------------- workload
@@ -534,6 +564,8 @@ def main():
     except Exception as exc:               # no graph capture: time the eager step
         log(f"[bench] CUDA graph capture unavailable ({exc}); timing eager launches")
         use_graph, graph = False, None
+    clocks = ClockSampler()
+    clocks.start()                              # running (first sample taken) before the timed region
     if use_graph:
         for s in range(args.warmup):            # the first replays upload the graph
             st.qcur.copy_(st.Q[s], non_blocking=True)
@@ -542,10 +574,9 @@ def main():
     evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(st.L)]
            for _ in range(args.steps)]
     step_ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
-    clocks = ClockSampler()
-    clocks.start()
     barrier(world)
     torch.cuda.synchronize()
+    wall0 = time.time()
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     kern = []
     t_start.record()
@@ -559,8 +590,9 @@ def main():
         step_ev[s + 1].record()
     t_end.record()
     torch.cuda.synchronize()
+    wall1 = time.time()
     barrier(world)
-    clk = clocks.stop(torch.cuda.current_device())
+    clk = clocks.stop(torch.cuda.current_device(), window=(wall0, wall1))
     elapsed = t_start.elapsed_time(t_end) / 1e3
     step_ms = [step_ev[i].elapsed_time(step_ev[i + 1]) for i in range(args.steps)]
     elapsed = max_over_ranks(elapsed, world)
@@ -622,13 +654,16 @@ def main():
                                          "host memory)")}[st.path]
         roof = {"bound": "link", "achieved": achieved, "peak": link, "unit": "GB/s", "frac": achieved / link,
                 "traffic": None, "kernel": what[0],
+                "traffic_note": "the runs cross the host link, not HBM: no DRAM counter measures them",
                 "peak_source": "measured in this run: pinned host->device copy, 1 GiB, best of 10",
                 "note": f"host-link bytes (planned plane runs + active-channel scales) per {what[1]} / its time"}
     else:
         hbm = peaks["hbm_gbs"]
         achieved = scanned / kern_avg / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-                "traffic": None, "kernel": "scan_kernel",
+                "traffic": scanned * SCAN_DRAM_PER_ALGO_BYTE, "kernel": "scan_kernel",
+                "traffic_note": "DRAM bytes per layer's first-pass scan launch: the measured DRAM/algorithmic "
+                                "ratio of a one-layer host_256k ncu capture times this run's planned bytes",
                 "peak_source": f"{peak_src} HBM copy peak (MEASURED_PEAKS.json hbm_gbs)",
                 "note": "scanned bytes per layer / the scan_topk call's time (scan + merge kernels)"}
     line = {

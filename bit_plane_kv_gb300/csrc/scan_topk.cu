@@ -99,7 +99,7 @@ __device__ __forceinline__ void accum_depth(const uint2 *__restrict__ pwcol,
                                             const float *__restrict__ wrow, int a_lo, int a_hi,
                                             int slot, uint32_t r, float (&acc)[8][G]) {
     constexpr float K = 8388608.0f + (float)(1 << T);
-#pragma unroll 2
+#pragma unroll 1
     for (int a = a_lo; a < a_hi; ++a, slot += T) {
         uint32_t ylo = 0, yhi = 0;
 #pragma unroll
@@ -464,7 +464,9 @@ constexpr int kMultiKPT = 4;   // register keys per thread and head for the fina
 // kFix = false: the first pass (histogram thresholds, no exact selection; a
 // list that would overflow publishes tau = max so that the merge flags it).
 // kFix = true: the exact second pass over the chunks the merge flagged.
-template <int G, bool kFix>
+// kScores: also write every token's score (a diagnostic output; kept out of
+// the other instantiations so that their loop stays small).
+template <int G, bool kFix, bool kScores>
 __global__ void __launch_bounds__(NT, (G <= 4) ? 3 : 1)
 scan_kernel(int n, int D, int chunk_blocks, int source, size_t stage_words, size_t stage_scales,
             const uint64_t *__restrict__ planes, const uint16_t *__restrict__ scales,
@@ -727,7 +729,7 @@ scan_kernel(int n, int D, int chunk_blocks, int source, size_t stage_words, size
             const bool valid = (bl < nblk) && (i < n);
             const bool forced = (i < ns || i >= r0);
             if (valid && !forced) cvm |= 1u << m;
-            if (valid && scores_opt) {
+            if (kScores && valid) {
 #pragma unroll
                 for (int h = 0; h < G; ++h) scores_opt[((size_t)u * G + h) * n + i] = acc[m][h];
             }
@@ -1215,23 +1217,23 @@ static int launch_g(const fathom_shape &s, const uint64_t *planes, const uint16_
     const int vec = (nb % 8 == 0) && aligned_src && ((uintptr_t)planes % 16 == 0) && ((uintptr_t)scales % 16 == 0);
     const size_t smem = sizeof(ScanSmem<G>);
     if (s.units > 65535) { set_error("scan: too many units for one launch"); return FATHOM_EINVAL; }
-    ensure_smem(scan_kernel<G, false>, smem);
-    ensure_smem(scan_kernel<G, true>, smem);
+    ensure_smem(scan_kernel<G, false, false>, smem);
+    ensure_smem(scan_kernel<G, false, true>, smem);
+    ensure_smem(scan_kernel<G, true, false>, smem);
     const size_t msmem = sizeof(MergeSmem);
     ensure_smem(merge_kernel, msmem);
     const int nf = f.nf > 0 ? f.nf : 1;
     dim3 grid(sg.chunks, s.units);
     for (int pass = 0; pass < 2; ++pass) {
-        if (pass == 0)
-            scan_kernel<G, false><<<grid, NT, smem, st>>>(s.n, s.D, sg.chunk_blocks, source, stage_words,
-                                                          stage_scales, planes, scales, runs, q, k_sel, m_sel,
-                                                          m_first, f.ns, f.r0, nf, cap, vec, scores_opt, cand,
-                                                          cnt, ctau, flags, forced);
-        else
-            scan_kernel<G, true><<<grid, NT, smem, st>>>(s.n, s.D, sg.chunk_blocks, source, stage_words,
-                                                         stage_scales, planes, scales, runs, q, k_sel, m_sel,
-                                                         m_first, f.ns, f.r0, nf, cap, vec, nullptr, cand,
-                                                         cnt, ctau, flags, forced);
+#define FATHOM_SCAN_LAUNCH(FIX, SC)                                                                       \
+    scan_kernel<G, FIX, SC><<<grid, NT, smem, st>>>(s.n, s.D, sg.chunk_blocks, source, stage_words,         \
+                                                    stage_scales, planes, scales, runs, q, k_sel, m_sel,      \
+                                                    m_first, f.ns, f.r0, nf, cap, vec,                        \
+                                                    SC ? scores_opt : nullptr, cand, cnt, ctau, flags, forced)
+        if (pass == 1) FATHOM_SCAN_LAUNCH(true, false);
+        else if (scores_opt) FATHOM_SCAN_LAUNCH(false, true);
+        else FATHOM_SCAN_LAUNCH(false, false);
+#undef FATHOM_SCAN_LAUNCH
         int rc = launch_status("scan_kernel");
         if (rc) return rc;
         merge_kernel<<<dim3(wl.parts, s.G, s.units), kMThreads, msmem, st>>>(
@@ -1258,9 +1260,9 @@ static int resident_g() {
     std::lock_guard<std::mutex> lock(mu);
     if (!cache[dev]) {
         const size_t smem = sizeof(ScanSmem<G>);
-        ensure_smem(scan_kernel<G, false>, smem);
+        ensure_smem(scan_kernel<G, false, false>, smem);
         int nbk = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nbk, scan_kernel<G, false>, NT, smem) != cudaSuccess) {
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nbk, scan_kernel<G, false, false>, NT, smem) != cudaSuccess) {
             cudaGetLastError();
             return 0;
         }
