@@ -76,7 +76,12 @@ def run_gpu(inp: Inputs, k, budget, n_sink=4, n_recent=32, regime="hbm", bracket
     ws = B.alloc_workspace(shape, B.WS_SCAN_TOPK)
     scores = torch.full((U, w.G, inp.n), float("nan"), device="cuda") if want_scores else None
     nb = B.nblocks(inp.n)
-    if regime == "host":
+    if regime == "fused":
+        # host-resident store read by the scan straight from pinned memory (the bench's default path)
+        hp = r["planes"].cpu().pin_memory()
+        hs = r["scales"].cpu().pin_memory()
+        src_p, src_s, source = hp, hs, B.SRC_STORE
+    elif regime == "host":
         hp = r["planes"].cpu().pin_memory()
         hs = r["scales"].cpu().pin_memory()
         bmax = int(np.max(budget)) if fixed is None else fixed[0] * fixed[1]
@@ -95,7 +100,7 @@ def run_gpu(inp: Inputs, k, budget, n_sink=4, n_recent=32, regime="hbm", bracket
     r["scores"] = scores
     aws = B.alloc_workspace(shape, B.WS_SPARSE_ATTN)
     kr, vr = inp.krows, inp.vrows
-    if regime == "host":
+    if regime in ("host", "fused"):
         kr, vr = kr.cpu().pin_memory(), vr.cpu().pin_memory()
     r["out"] = B.fathom_sparse_attn(shape, kr, vr, inp.q, r["idx"], aws)
     torch.cuda.synchronize()
