@@ -194,6 +194,8 @@ class Setup:
                 g0 = l * nh
                 rk = B.fathom_rotate_keys(self.shape, keys, nh, self.kmean[g0:g0 + nh], self.kV[g0:g0 + nh])
                 p, s = B.fathom_quantize_pack(self.shape, rk)
+                if l == 0:
+                    self.rkeys = rk                    # the rotated keys layer 0's store was coded from
                 del rk
                 self.var[l] = lam[g0:g0 + nh].repeat(H // nh, 1)    # unit i of the layer: head i % nh
             else:
@@ -531,7 +533,7 @@ def main():
     from bit_plane_kv_gb300 import binding as B
     import __graft_entry__
     __graft_entry__.build()
-    total_steps = args.warmup + 2 * args.steps
+    total_steps = args.warmup + 2 * args.steps + max(args.warmup, 10)   # + distinct graph warm-up queries
     st = Setup(w, args.budget, rank, total_steps, args.fixed, args.path, args.groups)
     link_gbs = measure_link_peak() if st.host else None
     peaks, peak_src = measured_peaks()
@@ -566,9 +568,15 @@ def main():
         use_graph, graph = False, None
     clocks = ClockSampler()
     clocks.start()                              # running (first sample taken) before the timed region
+    # graph warm-up: the first replays upload the graph, and a host-resident store needs
+    # several steps with different queries (different planned channels) before its reads
+    # reach their steady rate, as in a decode loop: at least 10 replays, each with its own
+    # queries (none of them used by the timed steps)
+    graph_warmup = max(args.warmup, 10) if use_graph else 0
+    q_gw = args.warmup + 2 * args.steps         # first query index reserved for the graph warm-up
     if use_graph:
-        for s in range(args.warmup):            # the first replays upload the graph
-            st.qcur.copy_(st.Q[s], non_blocking=True)
+        for s in range(graph_warmup):
+            st.qcur.copy_(st.Q[q_gw + s], non_blocking=True)
             graph.replay()
         torch.cuda.synchronize()
     evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(st.L)]
@@ -595,6 +603,7 @@ def main():
     clk = clocks.stop(torch.cuda.current_device(), window=(wall0, wall1))
     elapsed = t_start.elapsed_time(t_end) / 1e3
     step_ms = [step_ev[i].elapsed_time(step_ev[i + 1]) for i in range(args.steps)]
+    log("[bench] step ms: " + " ".join(f"{x:.3f}" for x in step_ms))
     elapsed = max_over_ranks(elapsed, world)
     if use_graph:
         # the captured events hold the last replay's stage times; one more replay per step for the average
@@ -617,6 +626,35 @@ def main():
     e1.record()
     torch.cuda.synchronize()
     e2e_elapsed = max_over_ranks(e0.elapsed_time(e1) / 1e3, world)
+
+    # decode-time append: coding the block of a new token into the store (the step before
+    # the scan in a decode loop); timed on layer 0's store for its last block, which codes
+    # the same values again, as a graph of `steps` appends
+    append_us = None
+    try:
+        B = st.B
+        blk, cnt = (st.n - 1) // 64, (st.n - 1) % 64 + 1
+        keys_l0 = st.rkeys if st.rotated else st.krows[0]
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            B.fathom_append_block(st.shape, keys_l0, blk, cnt, st.planes[0], st.scales[0])
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        ag = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(ag):
+            for _ in range(args.steps):
+                B.fathom_append_block(st.shape, keys_l0, blk, cnt, st.planes[0], st.scales[0])
+        ag.replay()
+        torch.cuda.synchronize()
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a0.record()
+        ag.replay()
+        a1.record()
+        torch.cuda.synchronize()
+        append_us = a0.elapsed_time(a1) * 1e3 / args.steps
+    except Exception as exc:   # reported as missing, never as a number
+        log(f"[bench] append timing unavailable: {exc}")
 
     # per-stage breakdown (separate pass, events between the calls)
     stage_ev = []
@@ -680,7 +718,9 @@ def main():
                 "h2d_bytes_per_step": int(st.Q[0].numel() * 4), "d2h_bytes_per_step": int(st.out.numel() * 4)},
         "gpu_launches": launches_per_layer * L * args.steps,
         "stages_us_per_layer": stages,
+        "append_us_per_layer": append_us,
         "timing": "one CUDA graph replay per step" if use_graph else "eager launches",
+        "graph_warmup_replays": graph_warmup,
         "step_ms_min_median_max": [min(step_ms), statistics.median(step_ms), max(step_ms)],
         "eager_issue_us_per_layer": issue_s * 1e6 / st.L,
         "clocks": clk,

@@ -28,11 +28,16 @@ _vp, _i32, _sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
 class Shape(ctypes.Structure):
     _fields_ = [("units", ctypes.c_int32), ("n", ctypes.c_int32), ("D", ctypes.c_int32),
                 ("G", ctypes.c_int32), ("k", ctypes.c_int32), ("n_sink", ctypes.c_int32),
-                ("n_recent", ctypes.c_int32)]
+                ("n_recent", ctypes.c_int32), ("n_cap", ctypes.c_int32)]
 
     def __repr__(self):
         return (f"Shape(units={self.units}, n={self.n}, D={self.D}, G={self.G}, k={self.k}, "
-                f"n_sink={self.n_sink}, n_recent={self.n_recent})")
+                f"n_sink={self.n_sink}, n_recent={self.n_recent}, n_cap={self.n_cap})")
+
+    @property
+    def cap(self) -> int:
+        """Tokens the per-unit arrays are laid out for."""
+        return self.n_cap if self.n_cap > 0 else self.n
 
 
 RUN_FIELDS = ("src_word", "n_words", "dst_word", "src_scale", "n_scales", "dst_scale")
@@ -44,6 +49,7 @@ SIGNATURES = {
     "fathom_rotate_keys": (ctypes.c_int, [ctypes.POINTER(Shape), _vp, ctypes.c_int, _i32, _vp, _vp, _vp, _vp]),
     "fathom_rotate_query": (ctypes.c_int, [ctypes.POINTER(Shape), _vp, _i32, _vp, _vp, _vp]),
     "fathom_quantize_pack": (ctypes.c_int, [ctypes.POINTER(Shape), _vp, ctypes.c_int, _vp, _vp, _vp]),
+    "fathom_append_block": (ctypes.c_int, [ctypes.POINTER(Shape), _vp, ctypes.c_int, _i32, _i32, _vp, _vp, _vp]),
     "fathom_plan": (ctypes.c_int, [ctypes.POINTER(Shape), _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
     "fathom_plan_fixed": (ctypes.c_int, [ctypes.POINTER(Shape), _vp, _vp, _i32, _i32, _vp, _vp, _vp]),
     "fathom_gather": (ctypes.c_int, [ctypes.POINTER(Shape), _vp, _vp, _vp, _vp, _vp, _sz, _sz, _vp]),
@@ -115,8 +121,8 @@ def _check(t, name, dtypes, shape=None, dev=True):
     return t
 
 
-def make_shape(units, n, D=128, G=4, k=1, n_sink=4, n_recent=32) -> Shape:
-    return Shape(units, n, D, G, k, n_sink, n_recent)
+def make_shape(units, n, D=128, G=4, k=1, n_sink=4, n_recent=32, n_cap=0) -> Shape:
+    return Shape(units, n, D, G, k, n_sink, n_recent, n_cap)
 
 
 def nblocks(n: int) -> int:
@@ -174,7 +180,7 @@ def fathom_rotate_keys(shape: Shape, keys, groups, mean, V, out=None, stream=Non
     _check(V, "V", (torch.float64,), (groups, shape.D, shape.D))
     dt = F32 if keys.dtype == torch.float32 else BF16
     if out is None:
-        out = torch.empty(shape.units, shape.n, shape.D, dtype=torch.float32, device=keys.device)
+        out = torch.empty(shape.units, shape.cap, shape.D, dtype=torch.float32, device=keys.device)
     _call("fathom_rotate_keys", ctypes.byref(shape), _p(keys), dt, int(groups), _p(mean), _p(V), _p(out),
           _stream(stream))
     return out
@@ -195,13 +201,26 @@ def fathom_quantize_pack(shape: Shape, keys, planes=None, scales=None, stream=No
     scales [U][D][nb] (int16 storage of fp16 bits)."""
     _check(keys, "keys", (torch.float32, torch.bfloat16, torch.int16))
     dt = F32 if keys.dtype == torch.float32 else BF16
-    nb = nblocks(shape.n)
+    nb = nblocks(shape.cap)
     dev = keys.device
     if planes is None:
         planes = torch.empty(shape.units, shape.D, 4, nb, dtype=torch.int64, device=dev)
     if scales is None:
         scales = torch.empty(shape.units, shape.D, nb, dtype=torch.int16, device=dev)
     _call("fathom_quantize_pack", ctypes.byref(shape), _p(keys), dt, _p(planes), _p(scales),
+          _stream(stream))
+    return planes, scales
+
+
+def fathom_append_block(shape: Shape, keys, block, count, planes, scales, stream=None):
+    """Quantise block `block` (its first `count` tokens) of every unit of the key rows
+    keys [U][cap][D] (fp32 or bf16) into the store planes [U][D][4][cap blocks],
+    scales [U][D][cap blocks], in place."""
+    _check(keys, "keys", (torch.float32, torch.bfloat16, torch.int16), (shape.units, shape.cap, shape.D))
+    _check(planes, "planes", (torch.int64,), (shape.units, shape.D, 4, nblocks(shape.cap)))
+    _check(scales, "scales", (torch.int16,), (shape.units, shape.D, nblocks(shape.cap)))
+    dt = F32 if keys.dtype == torch.float32 else BF16
+    _call("fathom_append_block", ctypes.byref(shape), _p(keys), dt, int(block), int(count), _p(planes), _p(scales),
           _stream(stream))
     return planes, scales
 
@@ -283,8 +302,8 @@ def fathom_sparse_attn_noalloc(shape: Shape, k_rows, v_rows, q, topk_idx, out, s
     """fathom_sparse_attn with the library's own fixed scratch (no workspace, no
     allocation inside the call): for callers that may not allocate device memory.
     `out` [U][G][D] fp32 must be provided by the caller."""
-    _check(k_rows, "k_rows", (torch.bfloat16, torch.int16), (shape.units, shape.n, shape.D))
-    _check(v_rows, "v_rows", (torch.bfloat16, torch.int16), (shape.units, shape.n, shape.D))
+    _check(k_rows, "k_rows", (torch.bfloat16, torch.int16), (shape.units, shape.cap, shape.D))
+    _check(v_rows, "v_rows", (torch.bfloat16, torch.int16), (shape.units, shape.cap, shape.D))
     _check(q, "q", (torch.float32,), (shape.units, shape.G, shape.D))
     _check(topk_idx, "topk_idx", (torch.int32,), (shape.units, shape.G, shape.k))
     _check(out, "out", (torch.float32,), (shape.units, shape.G, shape.D))
@@ -295,8 +314,8 @@ def fathom_sparse_attn_noalloc(shape: Shape, k_rows, v_rows, q, topk_idx, out, s
 
 def fathom_sparse_attn(shape: Shape, k_rows, v_rows, q, topk_idx, workspace, out=None, stream=None):
     """k_rows, v_rows [U][n][D] bf16 (device or pinned host) -> out [U][G][D] fp32."""
-    _check(k_rows, "k_rows", (torch.bfloat16, torch.int16), (shape.units, shape.n, shape.D))
-    _check(v_rows, "v_rows", (torch.bfloat16, torch.int16), (shape.units, shape.n, shape.D))
+    _check(k_rows, "k_rows", (torch.bfloat16, torch.int16), (shape.units, shape.cap, shape.D))
+    _check(v_rows, "v_rows", (torch.bfloat16, torch.int16), (shape.units, shape.cap, shape.D))
     _check(q, "q", (torch.float32,), (shape.units, shape.G, shape.D))
     _check(topk_idx, "topk_idx", (torch.int32,), (shape.units, shape.G, shape.k))
     _check(workspace, "workspace", (torch.uint8,))

@@ -182,7 +182,11 @@ static int check_shape(const fathom_shape *s, bool need_select) {
     if (s->n < 1 || s->n > (1 << 28)) { set_error("n must be in [1, 2^28] (got %d)", s->n); return FATHOM_EINVAL; }
     if (s->D < 1 || s->D > FATHOM_MAX_D) { set_error("D must be in [1, %d] (got %d)", FATHOM_MAX_D, s->D); return FATHOM_EINVAL; }
     if (!(s->G == 1 || s->G == 2 || s->G == 4 || s->G == 8)) { set_error("G must be 1, 2, 4 or 8 (got %d)", s->G); return FATHOM_EINVAL; }
-    if ((size_t)s->units * s->D * FATHOM_PLANES * (size_t)num_blocks(s->n) >= ((size_t)1 << 40)) {
+    if (s->n_cap != 0 && (s->n_cap < s->n || s->n_cap > (1 << 28))) {
+        set_error("n_cap must be 0 or in [n, 2^28] (got n_cap=%d, n=%d)", s->n_cap, s->n); return FATHOM_EINVAL;
+    }
+    if ((size_t)s->units * s->D * FATHOM_PLANES * (size_t)cap_blocks(*s) >= ((size_t)1 << 40) ||
+        (size_t)s->D * FATHOM_PLANES * (size_t)cap_blocks(*s) >= ((size_t)1 << 32)) {
         set_error("store too large"); return FATHOM_EINVAL;
     }
     if (need_select) {
@@ -209,7 +213,7 @@ extern "C" {
 
 const char *fathom_last_error(void) { return g_err; }
 
-const char *fathom_version(void) { return "fathom-gb300 0.1 (sm_103a)"; }
+const char *fathom_version(void) { return "fathom-gb300 0.2 (sm_103a)"; }
 
 int fathom_calibrate(int32_t units, int32_t m, int32_t D, const float *calib, float *mean_out,
                      float *var_out, void *stream) {
@@ -264,6 +268,25 @@ int fathom_rotate_query(const fathom_shape *shape, const float *q, int32_t group
     NONNULL(V);
     NONNULL(q_rot);
     return launch_rotate_query(*shape, q, groups, V, q_rot, (cudaStream_t)stream);
+}
+
+int fathom_append_block(const fathom_shape *shape, const void *keys, int keys_dtype, int32_t block,
+                        int32_t count, uint64_t *planes, uint16_t *scales, void *stream) {
+    g_err[0] = 0;
+    int rc = check_shape(shape, false);
+    if (rc) return rc;
+    if (keys_dtype != FATHOM_F32 && keys_dtype != FATHOM_BF16) {
+        set_error("keys_dtype must be FATHOM_F32 or FATHOM_BF16"); return FATHOM_EINVAL;
+    }
+    if (block < 0 || count < 1 || count > FATHOM_BLOCK || (long long)FATHOM_BLOCK * block + count > cap_tokens(*shape)) {
+        set_error("append_block: need block >= 0, 1 <= count <= 64 and 64 * block + count <= capacity %d "
+                  "(got block=%d, count=%d)", cap_tokens(*shape), block, count);
+        return FATHOM_EINVAL;
+    }
+    NONNULL(keys);
+    NONNULL(planes);
+    NONNULL(scales);
+    return launch_append(*shape, keys, keys_dtype, block, count, planes, scales, (cudaStream_t)stream);
 }
 
 int fathom_quantize_pack(const fathom_shape *shape, const void *keys, int keys_dtype,

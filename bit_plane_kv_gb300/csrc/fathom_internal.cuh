@@ -22,6 +22,11 @@ __host__ __device__ inline int num_blocks(int n) { return (n + FATHOM_BLOCK - 1)
 // Forced tokens (§2): the first n_sink and the last n_recent tokens.  With
 // ns = min(n_sink, n) and r0 = max(ns, n - n_recent), token i is forced iff
 // i < ns or i >= r0, and |forced| = ns + n - r0.
+// Tokens and 64-token blocks the per-unit arrays are laid out for (the
+// shape's capacity; n when no capacity is given).
+inline int cap_tokens(const fathom_shape &s) { return s.n_cap > 0 ? s.n_cap : s.n; }
+inline int cap_blocks(const fathom_shape &s) { return num_blocks(cap_tokens(s)); }
+
 struct Forced {
     int ns, r0, nf;
 };
@@ -118,6 +123,8 @@ int launch_rotate_keys(const fathom_shape &s, const void *keys, int dtype, int g
                        const double *vec, float *out, cudaStream_t st);
 int launch_rotate_query(const fathom_shape &s, const float *q, int groups, const double *vec, float *out,
                         cudaStream_t st);
+int launch_append(const fathom_shape &s, const void *keys, int dtype, int block, int count, uint64_t *planes,
+                  uint16_t *scales, cudaStream_t st);
 int launch_quantize(const fathom_shape &s, const void *keys, int dtype, uint64_t *planes,
                     uint16_t *scales, cudaStream_t st);
 int launch_plan(const fathom_shape &s, const float *q, const float *var, const int32_t *budget,

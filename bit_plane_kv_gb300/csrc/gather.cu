@@ -43,7 +43,7 @@ __device__ __forceinline__ void copy_span(const T *__restrict__ src, T *__restri
 }
 
 __global__ void __launch_bounds__(kGThreads)
-gather_kernel(int D, int nb, int x_planes, int x_total, const uint64_t *__restrict__ store_planes,
+gather_kernel(int D, int nb, int cb, int x_planes, int x_total, const uint64_t *__restrict__ store_planes,
               const uint16_t *__restrict__ store_scales, const fathom_run *__restrict__ runs,
               uint64_t *__restrict__ stage_planes, uint16_t *__restrict__ stage_scales,
               size_t stage_words, size_t stage_scales_n, int vec_planes, int vec_scales) {
@@ -64,13 +64,23 @@ gather_kernel(int D, int nb, int x_planes, int x_total, const uint64_t *__restri
             const size_t rl = do_planes ? r[j].n_words : r[j].n_scales;
             const size_t lo = max(rs, d0), hi = min(rs + rl, d1);
             if (lo >= hi) continue;
-            const size_t src0 = (do_planes ? r[j].src_word : r[j].src_scale) + (lo - rs);
             if (do_planes) {
-                copy_span<uint64_t, uint4>(store_planes + (size_t)u * D * FATHOM_PLANES * nb + src0,
-                                           stage_planes + (size_t)u * stage_words + lo,
-                                           (uint32_t)(hi - lo), vec_planes && ((src0 | lo) % 2 == 0));
+                // the run is the first nb words of t planes that lie cb words apart in the
+                // store (one contiguous span when cb = nb); copy it plane by plane
+                const uint64_t *sbase = store_planes + (size_t)u * D * FATHOM_PLANES * cb + r[j].src_word;
+                size_t d = lo;
+                while (d < hi) {
+                    const size_t p = (d - rs) / nb, o = (d - rs) - p * nb;
+                    const size_t seg = (cb == nb) ? hi - d : min(hi - d, nb - o);
+                    const size_t src0 = p * cb + o;
+                    copy_span<uint64_t, uint4>(sbase + src0, stage_planes + (size_t)u * stage_words + d,
+                                               (uint32_t)seg,
+                                               vec_planes && (((r[j].src_word + src0) | d) % 2 == 0));
+                    d += seg;
+                }
             } else {
-                copy_span<uint16_t, uint4>(store_scales + (size_t)u * D * nb + src0,
+                const size_t src0 = r[j].src_scale + (lo - rs);
+                copy_span<uint16_t, uint4>(store_scales + (size_t)u * D * cb + src0,
                                            stage_scales + (size_t)u * stage_scales_n + lo,
                                            (uint32_t)(hi - lo), vec_scales && ((src0 | lo) % 8 == 0));
             }
@@ -81,7 +91,7 @@ gather_kernel(int D, int nb, int x_planes, int x_total, const uint64_t *__restri
 int launch_gather(const fathom_shape &s, const uint64_t *sp, const uint16_t *ss,
                   const fathom_run *runs, uint64_t *dp, uint16_t *ds, size_t stage_words,
                   size_t stage_scales, cudaStream_t st) {
-    const int nb = num_blocks(s.n);
+    const int nb = num_blocks(s.n), cb = cap_blocks(s);
     // windows past the largest possible destination (every plane, every scale) never copy
     const size_t max_w = (size_t)s.D * FATHOM_PLANES * nb, max_s = (size_t)s.D * nb;
     const size_t wcap = stage_words < max_w ? stage_words : max_w;
@@ -90,16 +100,16 @@ int launch_gather(const fathom_shape &s, const uint64_t *sp, const uint16_t *ss,
     const int xs = (int)((scap + kGChunkScales - 1) / kGChunkScales);
     if (s.units > 65535) { set_error("gather: too many units for one launch"); return FATHOM_EINVAL; }
     const uintptr_t a = (uintptr_t)sp | (uintptr_t)dp;
-    const int vec_planes = (a % 16 == 0) && (stage_words % 2 == 0) && (nb % 2 == 0);
+    const int vec_planes = (a % 16 == 0) && (stage_words % 2 == 0) && (nb % 2 == 0) && (cb % 2 == 0);
     const uintptr_t b = (uintptr_t)ss | (uintptr_t)ds;
-    const int vec_scales = (b % 16 == 0) && (stage_scales % 8 == 0) && (nb % 8 == 0);
+    const int vec_scales = (b % 16 == 0) && (stage_scales % 8 == 0) && (nb % 8 == 0) && (cb % 8 == 0);
     // a copy over the host link needs enough bytes in flight (each thread keeps
     // 4 x 16 B outstanding) but not every SM: about two CTAs per SM in all, which
     // leaves room for kernels that run beside the gather
     int per_unit = (2 * 152 + s.units - 1) / s.units;
     if (per_unit > xp + xs) per_unit = xp + xs;
     dim3 grid(per_unit, s.units);
-    gather_kernel<<<grid, kGThreads, 0, st>>>(s.D, nb, xp, xp + xs, sp, ss, runs, dp, ds, stage_words,
+    gather_kernel<<<grid, kGThreads, 0, st>>>(s.D, nb, cb, xp, xp + xs, sp, ss, runs, dp, ds, stage_words,
                                               stage_scales, vec_planes, vec_scales);
     return launch_status("gather_kernel");
 }

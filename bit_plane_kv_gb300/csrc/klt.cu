@@ -174,7 +174,7 @@ klt_eigh_kernel(int D, double *__restrict__ vec, float *__restrict__ lambda) {
 // the centred tile is fp32 ((k - mu) rounded once from fp64).
 template <typename T>
 __global__ void __launch_bounds__(kRotThreads)
-klt_rotate_keys_kernel(int n, int D, int groups, const T *__restrict__ keys, const double *__restrict__ mean,
+klt_rotate_keys_kernel(int n, int ctok, int D, int groups, const T *__restrict__ keys, const double *__restrict__ mean,
                        const double *__restrict__ vec, float *__restrict__ out) {
     extern __shared__ __align__(16) float rsm[];
     float *Vs = rsm;                                   // [128][128]
@@ -189,7 +189,7 @@ klt_rotate_keys_kernel(int n, int D, int groups, const T *__restrict__ keys, con
     const int tr = tid / 32, tc = tid % 32;
     for (int i0 = blockIdx.x * kRotTokens; i0 < n; i0 += gridDim.x * kRotTokens) {
         __syncthreads();   // the previous tile's reads of xs are done
-        const T *kb = keys + ((size_t)u * n + i0) * D;
+        const T *kb = keys + ((size_t)u * ctok + i0) * D;
         for (int e = tid; e < kRotTokens * FATHOM_MAX_D; e += kRotThreads) {
             const int i = e / FATHOM_MAX_D, j = e % FATHOM_MAX_D;
             float v = 0.0f;
@@ -225,7 +225,7 @@ klt_rotate_keys_kernel(int n, int D, int groups, const T *__restrict__ keys, con
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
                 const int col = tc + 32 * c;
-                if (col < D) out[((size_t)u * n + i) * D + col] = acc[a][c];
+                if (col < D) out[((size_t)u * ctok + i) * D + col] = acc[a][c];
             }
         }
     }
@@ -311,11 +311,11 @@ int launch_rotate_keys(const fathom_shape &s, const void *keys, int dtype, int g
     const dim3 grid(tiles < 16 ? tiles : 16, s.units);   // each CTA stages V_g once for several tiles
     if (dtype == FATHOM_F32) {
         ensure_smem(klt_rotate_keys_kernel<float>, smem);
-        klt_rotate_keys_kernel<float><<<grid, kRotThreads, smem, st>>>(s.n, s.D, groups, (const float *)keys, mean,
+        klt_rotate_keys_kernel<float><<<grid, kRotThreads, smem, st>>>(s.n, cap_tokens(s), s.D, groups, (const float *)keys, mean,
                                                                        vec, out);
     } else {
         ensure_smem(klt_rotate_keys_kernel<uint16_t>, smem);
-        klt_rotate_keys_kernel<uint16_t><<<grid, kRotThreads, smem, st>>>(s.n, s.D, groups, (const uint16_t *)keys,
+        klt_rotate_keys_kernel<uint16_t><<<grid, kRotThreads, smem, st>>>(s.n, cap_tokens(s), s.D, groups, (const uint16_t *)keys,
                                                                           mean, vec, out);
     }
     return launch_status("klt_rotate_keys_kernel");

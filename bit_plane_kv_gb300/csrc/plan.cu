@@ -65,7 +65,7 @@ __device__ __forceinline__ void importance(int u, int lane, int D, int G, const 
 }
 
 // Writes depth and the run list of one unit from per-lane depths t[c].
-__device__ __forceinline__ void write_plan(int u, int lane, int D, int nb, const int (&t)[kCh],
+__device__ __forceinline__ void write_plan(int u, int lane, int D, int nb, int cb, const int (&t)[kCh],
                                            uint8_t *depth, fathom_run *runs) {
     uint32_t carry_w = 0, carry_s = 0;
 #pragma unroll
@@ -84,10 +84,10 @@ __device__ __forceinline__ void write_plan(int u, int lane, int D, int nb, const
         if (j < D) {
             depth[(size_t)u * D + j] = (uint8_t)tj;
             fathom_run r;
-            r.src_word = (uint32_t)j * FATHOM_PLANES * nb;
+            r.src_word = (uint32_t)j * FATHOM_PLANES * cb;
             r.n_words = (uint32_t)tj * nb;
             r.dst_word = (carry_w + (uint32_t)(st - tj)) * nb;
-            r.src_scale = (uint32_t)j * nb;
+            r.src_scale = (uint32_t)j * cb;
             r.n_scales = act ? (uint32_t)nb : 0u;
             r.dst_scale = (carry_s + (uint32_t)(sa - act)) * nb;
             runs[(size_t)u * D + j] = r;
@@ -174,7 +174,7 @@ __device__ unsigned long long critical_breakpoint(const unsigned long long (&bp)
 }
 
 __global__ void __launch_bounds__(32 * kPlanWarps)
-plan_kernel(int units, int n, int D, int G, const float *__restrict__ q,
+plan_kernel(int units, int n, int cb, int D, int G, const float *__restrict__ q,
             const float *__restrict__ var, const int32_t *__restrict__ budget,
             const double *__restrict__ bracket, uint8_t *__restrict__ depth,
             double *__restrict__ theta_out, fathom_run *__restrict__ runs) {
@@ -212,7 +212,7 @@ plan_kernel(int units, int n, int D, int G, const float *__restrict__ q,
         }
         if (gmax == 0.0) {                       // nothing worth reading
             int t0[kCh] = {0};
-            write_plan(u, lane, D, nb, t0, depth, runs);
+            write_plan(u, lane, D, nb, cb, t0, depth, runs);
             if (lane == 0) theta_out[u] = 0.0;
             return;
         }
@@ -256,14 +256,14 @@ plan_kernel(int units, int n, int D, int G, const float *__restrict__ q,
     int t[kCh];
 #pragma unroll
     for (int c = 0; c < kCh; ++c) t[c] = depth_of(g[c], hi);
-    write_plan(u, lane, D, nb, t, depth, runs);
+    write_plan(u, lane, D, nb, cb, t, depth, runs);
     if (lane == 0) theta_out[u] = hi;
 }
 
 // Fixed-depth comparison plan: the n_sel channels of largest g (ties: lower
 // index) at depth t_fixed.
 __global__ void __launch_bounds__(32 * kPlanWarps)
-plan_fixed_kernel(int units, int n, int D, int G, const float *__restrict__ q,
+plan_fixed_kernel(int units, int n, int cb, int D, int G, const float *__restrict__ q,
                   const float *__restrict__ var, int n_sel, int t_fixed,
                   uint8_t *__restrict__ depth, fathom_run *__restrict__ runs) {
     __shared__ double gs[kPlanWarps][FATHOM_MAX_D];
@@ -288,14 +288,14 @@ plan_fixed_kernel(int units, int n, int D, int G, const float *__restrict__ q,
         }
         t[c] = (j < D && better < n_sel) ? t_fixed : 0;
     }
-    write_plan(u, lane, D, nb, t, depth, runs);
+    write_plan(u, lane, D, nb, cb, t, depth, runs);
 }
 
 int launch_plan(const fathom_shape &s, const float *q, const float *var, const int32_t *budget,
                 const double *bracket, uint8_t *depth, double *theta, fathom_run *runs,
                 cudaStream_t st) {
     const int grid = (s.units + kPlanWarps - 1) / kPlanWarps;
-    plan_kernel<<<grid, 32 * kPlanWarps, 0, st>>>(s.units, s.n, s.D, s.G, q, var, budget, bracket,
+    plan_kernel<<<grid, 32 * kPlanWarps, 0, st>>>(s.units, s.n, cap_blocks(s), s.D, s.G, q, var, budget, bracket,
                                                   depth, theta, runs);
     return launch_status("plan_kernel");
 }
@@ -303,7 +303,7 @@ int launch_plan(const fathom_shape &s, const float *q, const float *var, const i
 int launch_plan_fixed(const fathom_shape &s, const float *q, const float *var, int n_sel,
                       int t_fixed, uint8_t *depth, fathom_run *runs, cudaStream_t st) {
     const int grid = (s.units + kPlanWarps - 1) / kPlanWarps;
-    plan_fixed_kernel<<<grid, 32 * kPlanWarps, 0, st>>>(s.units, s.n, s.D, s.G, q, var, n_sel,
+    plan_fixed_kernel<<<grid, 32 * kPlanWarps, 0, st>>>(s.units, s.n, cap_blocks(s), s.D, s.G, q, var, n_sel,
                                                         t_fixed, depth, runs);
     return launch_status("plan_fixed_kernel");
 }

@@ -1,7 +1,8 @@
 // quantize.cu -- 4-bit symmetric per-channel quantiser and channel-major
 // bit-plane packing (Fathom §3.2, bit-plane K cache).
 //
-// One CTA takes four consecutive 64-token blocks of one unit.  Each block is
+// One CTA takes four consecutive 64-token blocks of one unit (decode-time
+// appends launch the same kernel over one block).  Each block is
 // staged row-major in shared memory (coalesced loads of whole key rows), then
 // thread (channel j, half h) reduces its 32 tokens' |k|, combines the two
 // halves into the block maximum a, rounds a to fp16 and codes its 32 tokens:
@@ -49,10 +50,13 @@ struct QSmem {
     uint16_t sc[FATHOM_MAX_D][kQBlocks];
 };
 
+// Blocks [block0, block1) of every unit of a sequence of n tokens; keys rows
+// `ctok` tokens apart per unit, planes and scales `cb` blocks apart per
+// (channel, plane).
 template <typename T>
 __global__ void __launch_bounds__(kQThreads)
-quantize_kernel(int n, int D, const T *__restrict__ keys, uint64_t *__restrict__ planes,
-                uint16_t *__restrict__ scales) {
+quantize_kernel(int n, int D, int ctok, int cb, int block0, int block1, const T *__restrict__ keys,
+                uint64_t *__restrict__ planes, uint16_t *__restrict__ scales) {
     extern __shared__ __align__(16) unsigned char qsmem[];
     QSmem &sm = *reinterpret_cast<QSmem *>(qsmem);
     auto &tile = sm.tile;
@@ -61,11 +65,10 @@ quantize_kernel(int n, int D, const T *__restrict__ keys, uint64_t *__restrict__
     auto &sc = sm.sc;
 
     const int u = blockIdx.y;
-    const int nb = num_blocks(n);
-    const int beta0 = blockIdx.x * kQBlocks;
-    const int nbl = min(kQBlocks, nb - beta0);
+    const int beta0 = block0 + blockIdx.x * kQBlocks;
+    const int nbl = min(kQBlocks, block1 - beta0);
     const int tid = threadIdx.x;
-    const T *K = keys + (size_t)u * n * D;
+    const T *K = keys + (size_t)u * ctok * D;
 
     for (int bl = 0; bl < nbl; ++bl) {
         const int i0 = (beta0 + bl) * 64;
@@ -107,35 +110,47 @@ quantize_kernel(int n, int D, const T *__restrict__ keys, uint64_t *__restrict__
     }
     __syncthreads();
     // plane words: planes[u][j][p][beta0 + bl]
-    uint64_t *P = planes + (size_t)u * D * FATHOM_PLANES * nb;
+    uint64_t *P = planes + (size_t)u * D * FATHOM_PLANES * cb;
     for (int e = tid; e < D * FATHOM_PLANES * nbl; e += kQThreads) {
         const int bl = e % nbl;
         const int jp = e / nbl;
         const int j = jp / FATHOM_PLANES, p = jp % FATHOM_PLANES;
         const uint64_t w = (uint64_t)words[j][p][bl][0] | ((uint64_t)words[j][p][bl][1] << 32);
-        P[(size_t)jp * nb + beta0 + bl] = w;
+        P[(size_t)jp * cb + beta0 + bl] = w;
     }
-    uint16_t *S = scales + (size_t)u * D * nb;
+    uint16_t *S = scales + (size_t)u * D * cb;
     for (int e = tid; e < D * nbl; e += kQThreads) {
         const int bl = e % nbl, j = e / nbl;
-        S[(size_t)j * nb + beta0 + bl] = sc[j][bl];
+        S[(size_t)j * cb + beta0 + bl] = sc[j][bl];
     }
+}
+
+static int launch_blocks(const fathom_shape &s, int n, int block0, int block1, const void *keys, int dtype,
+                         uint64_t *planes, uint16_t *scales, cudaStream_t st, const char *what) {
+    dim3 grid((block1 - block0 + kQBlocks - 1) / kQBlocks, s.units);
+    if (grid.y > 65535) { set_error("%s: too many units for one launch", what); return FATHOM_EINVAL; }
+    const size_t smem = sizeof(QSmem);
+    const int ctok = cap_tokens(s), cb = cap_blocks(s);
+    if (dtype == FATHOM_F32) {
+        ensure_smem(quantize_kernel<float>, smem);
+        quantize_kernel<float><<<grid, kQThreads, smem, st>>>(n, s.D, ctok, cb, block0, block1,
+                                                              (const float *)keys, planes, scales);
+    } else {
+        ensure_smem(quantize_kernel<uint16_t>, smem);
+        quantize_kernel<uint16_t><<<grid, kQThreads, smem, st>>>(n, s.D, ctok, cb, block0, block1,
+                                                                 (const uint16_t *)keys, planes, scales);
+    }
+    return launch_status("quantize_kernel");
 }
 
 int launch_quantize(const fathom_shape &s, const void *keys, int dtype, uint64_t *planes,
                     uint16_t *scales, cudaStream_t st) {
-    const int nb = num_blocks(s.n);
-    dim3 grid((nb + kQBlocks - 1) / kQBlocks, s.units);
-    if (grid.y > 65535) { set_error("quantize: too many units for one launch"); return FATHOM_EINVAL; }
-    const size_t smem = sizeof(QSmem);
-    if (dtype == FATHOM_F32) {
-        ensure_smem(quantize_kernel<float>, smem);
-        quantize_kernel<float><<<grid, kQThreads, smem, st>>>(s.n, s.D, (const float *)keys, planes, scales);
-    } else {
-        ensure_smem(quantize_kernel<uint16_t>, smem);
-        quantize_kernel<uint16_t><<<grid, kQThreads, smem, st>>>(s.n, s.D, (const uint16_t *)keys, planes, scales);
-    }
-    return launch_status("quantize_kernel");
+    return launch_blocks(s, s.n, 0, num_blocks(s.n), keys, dtype, planes, scales, st, "quantize");
+}
+
+int launch_append(const fathom_shape &s, const void *keys, int dtype, int block, int count, uint64_t *planes,
+                  uint16_t *scales, cudaStream_t st) {
+    return launch_blocks(s, 64 * block + count, block, block + 1, keys, dtype, planes, scales, st, "append_block");
 }
 
 }  // namespace fathom

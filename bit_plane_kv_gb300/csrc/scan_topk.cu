@@ -468,7 +468,7 @@ constexpr int kMultiKPT = 4;   // register keys per thread and head for the fina
 // the other instantiations so that their loop stays small).
 template <int G, bool kFix, bool kScores>
 __global__ void __launch_bounds__(NT, (G <= 4) ? 3 : 1)
-scan_kernel(int n, int D, int chunk_blocks, int source, size_t stage_words, size_t stage_scales,
+scan_kernel(int n, int cb, int D, int chunk_blocks, int source, size_t stage_words, size_t stage_scales,
             const uint64_t *__restrict__ planes, const uint16_t *__restrict__ scales,
             const fathom_run *__restrict__ runs, const float *__restrict__ q, int k_sel, int m_sel,
             int m_first, int ns, int r0, int nf, int cap, int vec, float *__restrict__ scores_opt,
@@ -507,7 +507,7 @@ scan_kernel(int n, int D, int chunk_blocks, int source, size_t stage_words, size
             ((uint64_t)rr.dst_word + (uint64_t)t * nb > stage_words ||
              (uint64_t)rr.dst_scale + (t > 0 ? (uint64_t)nb : 0) > stage_scales))
             t = 0;
-        if (source == FATHOM_SRC_STORE && rr.src_word != (uint32_t)tid * FATHOM_PLANES * nb) t = 0;
+        if (source == FATHOM_SRC_STORE && rr.src_word != (uint32_t)tid * FATHOM_PLANES * cb) t = 0;
     }
     unsigned my_mask = 0;   // lanes of this warp with the same depth as this thread
     if (tid < FATHOM_MAX_D) {
@@ -553,17 +553,19 @@ scan_kernel(int n, int D, int chunk_blocks, int source, size_t stage_words, size
         int pos = start[t] + __popc(my_mask & ((1u << lane) - 1u));
         for (int w2 = 0; w2 < wid; ++w2) pos += sm.wcnt[t][w2];
         const uint64_t wbase = (source == FATHOM_SRC_STORE)
-                                   ? ((uint64_t)u * D + tid) * FATHOM_PLANES * nb
+                                   ? ((uint64_t)u * D + tid) * FATHOM_PLANES * cb
                                    : (uint64_t)u * stage_words + rr.dst_word;
         const uint64_t sbase = (source == FATHOM_SRC_STORE)
-                                   ? ((uint64_t)u * D + tid) * nb
+                                   ? ((uint64_t)u * D + tid) * cb
                                    : (uint64_t)u * stage_scales + rr.dst_scale;
         sm.ch_t[pos] = t;
         sm.ch_scale[pos] = sbase;
         const float sc = ldexpf(1.0f, -t);
         for (int h = 0; h < G; ++h) sm.qs[pos][h] = q[((size_t)u * G + h) * D + tid] * sc;
         const int sl = slot_of(pos);
-        for (int p = 0; p < t; ++p) sm.plane_src[sl + p] = wbase + (uint64_t)p * nb;
+        // the store keeps a channel's planes cb words apart, staging packs them nb apart
+        const uint64_t pstride = (source == FATHOM_SRC_STORE) ? (uint64_t)cb : (uint64_t)nb;
+        for (int p = 0; p < t; ++p) sm.plane_src[sl + p] = wbase + (uint64_t)p * pstride;
     }
     const int n_groups = (A + kCHG - 1) / kCHG;
     if (tid < n_groups) {
@@ -1214,7 +1216,9 @@ static int launch_g(const fathom_shape &s, const uint64_t *planes, const uint16_
     // nb a multiple of 8 (n a multiple of 512), aligned strides and bases
     const int nb = num_blocks(s.n);
     const bool aligned_src = (source == FATHOM_SRC_STORE) || (stage_words % 2 == 0 && stage_scales % 8 == 0);
-    const int vec = (nb % 8 == 0) && aligned_src && ((uintptr_t)planes % 16 == 0) && ((uintptr_t)scales % 16 == 0);
+    const int cb = cap_blocks(s);
+    const int vec = (nb % 8 == 0) && (source != FATHOM_SRC_STORE || cb % 8 == 0) && aligned_src &&
+                    ((uintptr_t)planes % 16 == 0) && ((uintptr_t)scales % 16 == 0);
     const size_t smem = sizeof(ScanSmem<G>);
     if (s.units > 65535) { set_error("scan: too many units for one launch"); return FATHOM_EINVAL; }
     ensure_smem(scan_kernel<G, false, false>, smem);
@@ -1226,7 +1230,7 @@ static int launch_g(const fathom_shape &s, const uint64_t *planes, const uint16_
     dim3 grid(sg.chunks, s.units);
     for (int pass = 0; pass < 2; ++pass) {
 #define FATHOM_SCAN_LAUNCH(FIX, SC)                                                                       \
-    scan_kernel<G, FIX, SC><<<grid, NT, smem, st>>>(s.n, s.D, sg.chunk_blocks, source, stage_words,         \
+    scan_kernel<G, FIX, SC><<<grid, NT, smem, st>>>(s.n, cb, s.D, sg.chunk_blocks, source, stage_words,     \
                                                     stage_scales, planes, scales, runs, q, k_sel, m_sel,      \
                                                     m_first, f.ns, f.r0, nf, cap, vec,                        \
                                                     SC ? scores_opt : nullptr, cand, cnt, ctau, flags, forced)

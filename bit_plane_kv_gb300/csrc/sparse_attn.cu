@@ -94,7 +94,7 @@ __device__ __forceinline__ float warp_sum(float v) {
 // of V per row) or channels l + 32 e (any D <= 128).
 template <int G, bool kVec>
 __global__ void __launch_bounds__(NA, G >= 8 ? 1 : 2)
-attn_kernel(int n, int D, int k, int rows_cta, int cph, int splits, const uint16_t *__restrict__ krows,
+attn_kernel(int n, int ctok, int D, int k, int rows_cta, int cph, int splits, const uint16_t *__restrict__ krows,
             const uint16_t *__restrict__ vrows, const float *__restrict__ q,
             const int32_t *__restrict__ topk, float *__restrict__ out, float *__restrict__ part,
             unsigned *__restrict__ ticket) {
@@ -162,8 +162,8 @@ attn_kernel(int n, int D, int k, int rows_cta, int cph, int splits, const uint16
                 if (!((m >> hown) & 1u) || (m & below)) m = 0;   // invalid, or a lower head owns it
             }
             mask[r] = m;
-            const uint16_t *kr = krows + ((size_t)u * n + (m ? i : 0)) * D;
-            const uint16_t *vr_ = vrows + ((size_t)u * n + (m ? i : 0)) * D;
+            const uint16_t *kr = krows + ((size_t)u * ctok + (m ? i : 0)) * D;
+            const uint16_t *vr_ = vrows + ((size_t)u * ctok + (m ? i : 0)) * D;
             if (kVec) {
                 kp[r] = m ? __ldg(reinterpret_cast<const uint2 *>(kr) + lane) : make_uint2(0u, 0u);
                 vp[r] = m ? __ldg(reinterpret_cast<const uint2 *>(vr_) + lane) : make_uint2(0u, 0u);
@@ -355,7 +355,7 @@ int launch_sparse_attn(const fathom_shape &s, const uint16_t *krows, const uint1
 #define FATHOM_ATTN_LAUNCH(GG, VV)                                                               \
     do {                                                                                         \
         ensure_smem(attn_kernel<GG, VV>, smem);                                                  \
-        attn_kernel<GG, VV><<<grid, NA, smem, st>>>(s.n, s.D, s.k, wl.rows, cph, wl.splits, krows, vrows, \
+        attn_kernel<GG, VV><<<grid, NA, smem, st>>>(s.n, cap_tokens(s), s.D, s.k, wl.rows, cph, wl.splits, krows, vrows, \
                                                     q, idx, out, part, ticket);                  \
     } while (0)
     switch (s.G * 2 + (vec ? 1 : 0)) {

@@ -28,6 +28,16 @@
  *   fathom_last_error() returns the calling thread's last message.  Nothing
  *   throws across this ABI and nothing aborts the process.
  * - Inputs are never modified.  Outputs may not alias inputs.
+ *
+ * Capacity
+ * --------
+ * The per-unit arrays (key and value rows, the bit-plane store) are laid out
+ * for C = (n_cap ? n_cap : n) tokens, cb = ceil(C / 64) blocks: rows
+ * [units][C][D], planes [units][D][4][cb], scales [units][D][cb].  Every call
+ * reads and writes only the first n tokens (nb blocks) of each unit, so a store
+ * allocated once for C tokens grows block by block during decoding
+ * (fathom_append_block) and is scanned at its current length n.  With n_cap = 0
+ * the layouts are exactly [units][n][D], [units][D][4][nb], [units][D][nb].
  */
 #ifndef FATHOM_H
 #define FATHOM_H
@@ -59,7 +69,7 @@ typedef enum { FATHOM_WS_SCAN_TOPK = 0, FATHOM_WS_SPARSE_ATTN = 1 } fathom_works
 
 /* Which copy of the bit-plane store a scan reads. */
 typedef enum {
-    FATHOM_SRC_STORE = 0,   /* the store in place, layout [U][D][4][nb] (HBM-resident regime) */
+    FATHOM_SRC_STORE = 0,   /* the store in place, layout [U][D][4][cb] (HBM or pinned host memory) */
     FATHOM_SRC_STAGING = 1  /* the staging area written by fathom_gather (host-resident regime) */
 } fathom_source;
 
@@ -68,10 +78,11 @@ typedef enum {
  * scales, relative to the unit's store (src) and the unit's staging area
  * (dst).  Destinations are contiguous in ascending channel order. */
 typedef struct {
-    uint32_t src_word;   /* = j * 4 * nb: first plane word of channel j in the store */
-    uint32_t n_words;    /* = t_j * nb: channel j's first t_j planes, one contiguous run */
+    uint32_t src_word;   /* = j * 4 * cb: first plane word of channel j in the store */
+    uint32_t n_words;    /* = t_j * nb: channel j's first t_j planes (one contiguous run when
+                            cb = nb; planes cb words apart otherwise) */
     uint32_t dst_word;   /* = sum_{j' < j} t_j' * nb */
-    uint32_t src_scale;  /* = j * nb */
+    uint32_t src_scale;  /* = j * cb */
     uint32_t n_scales;   /* = nb if t_j > 0 else 0 */
     uint32_t dst_scale;  /* = nb * #{j' < j : t_j' > 0} */
 } fathom_run;
@@ -84,6 +95,8 @@ typedef struct {
     int32_t k;        /* tokens kept per query head, |forced| <= k <= min(n, 2048) */
     int32_t n_sink;   /* first tokens always kept (the pages use 4) */
     int32_t n_recent; /* last tokens always kept (the pages use 32) */
+    int32_t n_cap;    /* tokens the per-unit arrays are laid out for: 0 means n, else n <= n_cap
+                         (a store that grows during decoding; see "Capacity" above) */
 } fathom_shape;
 
 /* ---------------------------------------------------------------------- */
@@ -120,8 +133,8 @@ int fathom_calibrate_klt(int32_t groups, int32_t m, int32_t D, const float *cali
  * sequences).  k - mu is formed in fp64 and rounded to fp32, V_g is rounded
  * to fp32, the sum is accumulated in fp32.  The result is the input of
  * fathom_quantize_pack (keys_dtype FATHOM_F32) for a rotated store.
- *   keys [units][n][D] fp32 or bf16 (keys_dtype), mean [groups][D] fp64,
- *   V [groups][D][D] fp64, out [units][n][D] fp32; all device.
+ *   keys [units][C][D] fp32 or bf16 (keys_dtype), mean [groups][D] fp64,
+ *   V [groups][D][D] fp64, out [units][C][D] fp32 (first n tokens written); all device.
  * Uses shape->units, n, D. */
 int fathom_rotate_keys(const fathom_shape *shape, const void *keys, int keys_dtype, int32_t groups,
                        const double *mean, const double *V, float *out, void *stream);
@@ -142,13 +155,26 @@ int fathom_rotate_query(const fathom_shape *shape, const float *q, int32_t group
  * token 64*beta + i at bit i.  Tail tokens past n have all-zero bits and do
  * not enter a.  Reading the first t planes of a channel then gives the t-bit
  * mid-rise code c >> (4 - t).
- *   keys   [units][n][D], fp32 or bf16 (keys_dtype), device
- *   planes [units][D][4][nb] uint64 (out, device): channel j's planes 0..3
+ *   keys   [units][C][D], fp32 or bf16 (keys_dtype), device (first n tokens read)
+ *   planes [units][D][4][cb] uint64 (out, device; first nb blocks written): channel j's planes 0..3
  *          each contiguous over the sequence (§3.6)
- *   scales [units][D][nb] fp16 bit patterns (out, device)
+ *   scales [units][D][cb] fp16 bit patterns (out, device)
  * Uses shape->units, n, D. */
 int fathom_quantize_pack(const fathom_shape *shape, const void *keys, int keys_dtype,
                          uint64_t *planes, uint16_t *scales, void *stream);
+
+/* Decode-time append (the step before the scan in a decode loop, §2, §3.2):
+ * quantise block `block` (tokens 64*block .. 64*block + count - 1, 1 <= count
+ * <= 64) of every unit into the store, exactly as fathom_quantize_pack would
+ * code a sequence of 64*block + count tokens: a block that is still filling
+ * is coded again as its tokens arrive (its maximum, and so its codes, can
+ * change); tokens past `count` have all-zero bits and do not enter the
+ * maximum.  Reads keys [units][C][D] (the rows buffer, fp32 or bf16) at that
+ * block, writes its 4 plane words and its scale per channel; other blocks are
+ * untouched.  Requires 64*block + count <= C (the shape's capacity); shape->n
+ * is not used. */
+int fathom_append_block(const fathom_shape *shape, const void *keys, int keys_dtype, int32_t block,
+                        int32_t count, uint64_t *planes, uint16_t *scales, void *stream);
 
 /* Per-query-group read plan (§3.3, §3.6).  Per unit:
  *   g_j = (sum_h q_hj^2) * var_j  (fp64, h ascending);
@@ -180,7 +206,8 @@ int fathom_plan_fixed(const fathom_shape *shape, const float *q, const float *va
                       fathom_run *runs, void *stream);
 
 /* Gather (§3.6): for every unit and every channel, copy run[j].n_words plane
- * words from store_planes + src_word to stage_planes + dst_word and
+ * words from store_planes + src_word to stage_planes + dst_word (the first nb
+ * words of each of the channel's t_j planes, which lie cb words apart) and
  * run[j].n_scales scales likewise; zero-length runs copy nothing, so the run
  * list needs no host synchronisation.  The store is typically pinned host
  * memory read over the host link; staging is device memory.
@@ -204,8 +231,8 @@ int fathom_gather(const fathom_shape *shape, const uint64_t *store_planes,
  * the last n_recent tokens plus the k - |forced| other tokens of largest
  * s_h (ties: lower index), written in ascending token order with their
  * scores.
- *   planes/scales: source (FATHOM_SRC_STORE: the store [U][D][4][nb] /
- *   [U][D][nb]; FATHOM_SRC_STAGING: staging [U][stage_words] /
+ *   planes/scales: source (FATHOM_SRC_STORE: the store [U][D][4][cb] /
+ *   [U][D][cb]; FATHOM_SRC_STAGING: staging [U][stage_words] /
  *   [U][stage_nscales] laid out by the run list; the strides are ignored
  *   for FATHOM_SRC_STORE)
  *   runs [units][D], q [units][G][D] fp32
@@ -226,7 +253,7 @@ int fathom_scan_topk(const fathom_shape *shape, const uint64_t *planes,
  * and V rows; at most G * k rows), and per head
  *   o_h = sum_{i in S_h} softmax_i(q_h . k_i / sqrt(D)) v_i
  * with fp32 accumulation and no mass for unselected tokens.
- *   k_rows, v_rows [units][n][D] bf16 bit patterns (device or pinned host)
+ *   k_rows, v_rows [units][C][D] bf16 bit patterns (device or pinned host)
  *   q [units][G][D] fp32, topk_idx [units][G][k] int32, each row ascending
  *   out [units][G][D] fp32 (out)
  *   workspace: at least fathom_workspace_size(shape, FATHOM_WS_SPARSE_ATTN)

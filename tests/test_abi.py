@@ -35,7 +35,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 def test_version_and_struct_sizes(lib):
     assert "sm_103a" in B.version()
-    assert ctypes.sizeof(B.Shape) == 7 * 4
+    assert ctypes.sizeof(B.Shape) == 8 * 4
     assert B.RUN_BYTES == 24
 
 
@@ -46,6 +46,7 @@ def rc_msg(lib, rc):
 @pytest.mark.parametrize("field,value,frag", [
     ("units", 0, "units"), ("n", 0, "n must"), ("D", 0, "D must"), ("D", 129, "D must"),
     ("G", 3, "G must"), ("k", 0, "k must"), ("k", 5000, "k must"), ("n_sink", -1, "n_sink"),
+    ("n_cap", 100, "n_cap"),
 ])
 def test_shape_validation(lib, field, value, frag):
     s = B.make_shape(2, 4096, 128, 4, 64)
@@ -107,3 +108,13 @@ def test_rotated_basis_calls_validate_arguments(lib):
     assert rc_msg(lib, rc)[0] == 1
     rc = lib.fathom_rotate_query(ctypes.byref(s), d, 1, d, None, None)
     assert rc_msg(lib, rc) == (1, "q_rot is NULL")
+
+
+def test_append_block_validates_its_block(lib):
+    d = ctypes.c_void_p(256)
+    s = B.make_shape(2, 4096, 128, 4, 64, n_cap=4160)
+    for block, count in ((-1, 64), (0, 0), (0, 65), (65, 1), (64, 65)):
+        rc = lib.fathom_append_block(ctypes.byref(s), d, 1, block, count, d, d, None)
+        assert rc_msg(lib, rc)[0] == 1 and "append_block" in lib.fathom_last_error().decode()
+    rc = lib.fathom_append_block(ctypes.byref(s), d, 1, 65, 0, d, d, None)
+    assert rc_msg(lib, rc)[0] == 1
