@@ -516,6 +516,7 @@ def main():
     ap.add_argument("--regime", default="", choices=["", "hbm", "host"],
                     help="override where the store and rows live (default: the workload's)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-fidelity", action="store_true", help="skip the (untimed) fidelity measurement")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     rank, world = dist_setup(args.gpus)
@@ -666,6 +667,31 @@ def main():
     stages = {nm: statistics.mean(e[i].elapsed_time(e[i + 1]) * 1e3 for e in stage_ev) for i, nm in enumerate(names)}
     log("[bench] per-layer stages (µs): " + ", ".join(f"{k} {v:.1f}" for k, v in stages.items()))
 
+    # fidelity of the timed path (untimed): layer 0 at the last timed step's query,
+    # against dense attention and against attention over the exact top-k
+    fidelity = None
+    if not args.no_fidelity:
+        try:
+            from bit_plane_kv_gb300 import fidelity as FID
+            q0 = st.Q[args.warmup + args.steps - 1, 0].contiguous()
+            st.layer(0, q0)
+            res = FID.compare(st.shape, st.krows[0], st.vrows[0], q0, st.idx, st.out[0],
+                              workspaces={"scan": st.ws, "attn": st.aws})
+            fidelity = {
+                "layer": 0, "budget": st.budgets[0] if not st.fixed else "fixed 136-bit",
+                "rel_l2_vs_dense_mean": float(res["rel_dense"].mean()),
+                "rel_l2_vs_dense_max": float(res["rel_dense"].max()),
+                "rel_l2_vs_exact_topk_mean": float(res["rel_exact"].mean()),
+                "exact_topk_rel_l2_vs_dense_mean": float(res["exact_vs_dense"].mean()),
+                "exact_topk_overlap_mean": float(res["overlap"].mean()),
+                "note": "relative L2 error of the attention output per (unit, head), averaged; overlap = "
+                        "fraction of the exact top-k (q . k over the bf16 rows) the scan kept",
+            }
+            log(f"[bench] fidelity: {fidelity}")
+        except Exception as exc:   # reported as missing, never as a number
+            log(f"[bench] fidelity unavailable: {exc}")
+            fidelity = {"error": str(exc)[:200]}
+
     L, H = st.L, st.H
     layer_steps = args.steps * L * world
     us_layer = elapsed * 1e6 / layer_steps         # whole job: all ranks' layer-steps
@@ -719,6 +745,7 @@ def main():
         "gpu_launches": launches_per_layer * L * args.steps,
         "stages_us_per_layer": stages,
         "append_us_per_layer": append_us,
+        "fidelity": fidelity,
         "timing": "one CUDA graph replay per step" if use_graph else "eager launches",
         "graph_warmup_replays": graph_warmup,
         "step_ms_min_median_max": [min(step_ms), statistics.median(step_ms), max(step_ms)],

@@ -17,7 +17,7 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "_build", "libfathom.so")
 
 F32, BF16 = 0, 1
-WS_SCAN_TOPK, WS_SPARSE_ATTN = 0, 1
+WS_SCAN_TOPK, WS_SPARSE_ATTN, WS_DENSE_ATTN = 0, 1, 2
 SRC_STORE, SRC_STAGING = 0, 1
 MAX_D, MAX_G, MAX_K = 128, 8, 2048
 
@@ -55,8 +55,13 @@ SIGNATURES = {
     "fathom_gather": (ctypes.c_int, [ctypes.POINTER(Shape), _vp, _vp, _vp, _vp, _vp, _sz, _sz, _vp]),
     "fathom_scan_topk": (ctypes.c_int, [ctypes.POINTER(Shape), _vp, _vp, ctypes.c_int, _sz, _sz, _vp,
                                         _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "fathom_exact_topk": (ctypes.c_int, [ctypes.POINTER(Shape), _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "fathom_sparse_attn": (ctypes.c_int, [ctypes.POINTER(Shape), _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "fathom_dense_attn": (ctypes.c_int, [ctypes.POINTER(Shape), _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "fathom_sparse_attn_noalloc": (ctypes.c_int, [ctypes.POINTER(Shape), _vp, _vp, _vp, _vp, _vp, _vp]),
+    "fathom_rel_err": (ctypes.c_int, [_i32, _i32, _vp, _vp, _vp, _vp]),
+    "fathom_set_overlap": (ctypes.c_int, [_i32, _i32, _vp, _vp, _vp, _vp]),
+    "fathom_greedy_budgets": (ctypes.c_int, [_i32, _i32, _vp, _i32, _i32, _i32, _vp]),
     "fathom_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(Shape), ctypes.c_int]),
     "fathom_last_error": (ctypes.c_char_p, []),
     "fathom_version": (ctypes.c_char_p, []),
@@ -296,6 +301,80 @@ def fathom_scan_topk(shape: Shape, planes, scales, runs, q, workspace, source=SR
           _p(runs), _p(q), _p(topk_idx), _p(topk_score), _p(scores), _p(workspace),
           workspace.numel(), _stream(stream))
     return topk_idx, topk_score
+
+
+def fathom_exact_topk(shape: Shape, k_rows, q, workspace, topk_idx=None, topk_score=None, scores=None,
+                      stream=None):
+    """Fidelity reference: the kept set with every token scored exactly, q . k
+    over all D channels of its bf16 row.  k_rows [U][cap][D] bf16 -> topk_idx
+    [U][G][k] int32 ascending, topk_score [U][G][k] fp32 (workspace of kind
+    WS_SCAN_TOPK)."""
+    _check(k_rows, "k_rows", (torch.bfloat16, torch.int16), (shape.units, shape.cap, shape.D))
+    _check(q, "q", (torch.float32,), (shape.units, shape.G, shape.D))
+    _check(workspace, "workspace", (torch.uint8,))
+    dev = q.device
+    if topk_idx is None:
+        topk_idx = torch.empty(shape.units, shape.G, shape.k, dtype=torch.int32, device=dev)
+    if topk_score is None:
+        topk_score = torch.empty(shape.units, shape.G, shape.k, dtype=torch.float32, device=dev)
+    if scores is not None:
+        _check(scores, "scores", (torch.float32,), (shape.units, shape.G, shape.n))
+    _call("fathom_exact_topk", ctypes.byref(shape), _p(k_rows), _p(q), _p(topk_idx), _p(topk_score),
+          _p(scores), _p(workspace), workspace.numel(), _stream(stream))
+    return topk_idx, topk_score
+
+
+def fathom_dense_attn(shape: Shape, k_rows, v_rows, q, workspace, out=None, stream=None):
+    """Fidelity reference: attention of every head over all n tokens.
+    k_rows, v_rows [U][cap][D] bf16 -> out [U][G][D] fp32 (workspace of kind
+    WS_DENSE_ATTN)."""
+    _check(k_rows, "k_rows", (torch.bfloat16, torch.int16), (shape.units, shape.cap, shape.D))
+    _check(v_rows, "v_rows", (torch.bfloat16, torch.int16), (shape.units, shape.cap, shape.D))
+    _check(q, "q", (torch.float32,), (shape.units, shape.G, shape.D))
+    _check(workspace, "workspace", (torch.uint8,))
+    if out is None:
+        out = torch.empty(shape.units, shape.G, shape.D, dtype=torch.float32, device=q.device)
+    _call("fathom_dense_attn", ctypes.byref(shape), _p(k_rows), _p(v_rows), _p(q), _p(out),
+          _p(workspace), workspace.numel(), _stream(stream))
+    return out
+
+
+def fathom_rel_err(a, ref, err=None, stream=None):
+    """a, ref [..., D] fp32 (device) -> err [...] fp64: ||a - ref|| / ||ref|| per row."""
+    _check(a, "a", (torch.float32,))
+    _check(ref, "ref", (torch.float32,), tuple(a.shape))
+    D = a.shape[-1]
+    rows = a.numel() // D if D else 0
+    if err is None:
+        err = torch.empty(a.shape[:-1], dtype=torch.float64, device=a.device)
+    _check(err, "err", (torch.float64,), tuple(a.shape[:-1]))
+    _call("fathom_rel_err", rows, D, _p(a), _p(ref), _p(err), _stream(stream))
+    return err
+
+
+def fathom_set_overlap(a, b, count=None, stream=None):
+    """a, b [..., k] int32 ascending (device) -> count [...] int32: shared indices per row."""
+    _check(a, "a", (torch.int32,))
+    _check(b, "b", (torch.int32,), tuple(a.shape))
+    k = a.shape[-1]
+    rows = a.numel() // k if k else 0
+    if count is None:
+        count = torch.empty(a.shape[:-1], dtype=torch.int32, device=a.device)
+    _check(count, "count", (torch.int32,), tuple(a.shape[:-1]))
+    _call("fathom_set_overlap", rows, k, _p(a), _p(b), _p(count), _stream(stream))
+    return count
+
+
+def fathom_greedy_budgets(err, b_min, step, b_mean):
+    """err [layers][levels] (host array-like, fp64) -> budgets [layers] (numpy int32)."""
+    import numpy as np
+    e = np.ascontiguousarray(np.asarray(err, dtype=np.float64))
+    if e.ndim != 2:
+        raise ValueError("err must be [layers][levels]")
+    out = np.zeros(e.shape[0], dtype=np.int32)
+    _call("fathom_greedy_budgets", e.shape[0], e.shape[1], e.ctypes.data, int(b_min), int(step), int(b_mean),
+          out.ctypes.data)
+    return out
 
 
 def fathom_sparse_attn_noalloc(shape: Shape, k_rows, v_rows, q, topk_idx, out, stream=None):

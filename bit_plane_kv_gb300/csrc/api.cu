@@ -6,6 +6,8 @@
 
 #include <mutex>
 
+#include <cmath>
+
 #include "fathom_internal.cuh"
 
 namespace fathom {
@@ -166,6 +168,24 @@ AttnWorkspace attn_workspace_layout(const fathom_shape &s) {
     w.rows = ctas128 > 2LL * 2 * sms ? 256 : 128;
     w.splits = s.G * ((s.k + w.rows - 1) / w.rows);
     if (w.splits < 1) w.splits = 1;
+    w.part_off = 0;
+    w.ticket_off = align256((size_t)s.units * w.splits * s.G * (s.D + 2) * sizeof(float));
+    w.total = align256(w.ticket_off + (size_t)s.units * sizeof(uint32_t));
+    return w;
+}
+
+AttnWorkspace dense_workspace_layout(const fathom_shape &s) {
+    // about four waves of 2 CTAs per SM over the units, at most 64 splits, at
+    // least 1024 tokens per split (a multiple of the 64-token block)
+    int sms = device_sm_count();
+    if (sms <= 0) sms = 152;
+    AttnWorkspace w;
+    int splits = (4 * 2 * sms + s.units - 1) / s.units;
+    const int max_splits = (s.n + 1023) / 1024;
+    splits = splits < 1 ? 1 : (splits > 64 ? 64 : splits);
+    splits = splits > max_splits ? max_splits : splits;
+    w.rows = ((s.n + splits - 1) / splits + 63) / 64 * 64;
+    w.splits = (s.n + w.rows - 1) / w.rows;
     w.part_off = 0;
     w.ticket_off = align256((size_t)s.units * w.splits * s.G * (s.D + 2) * sizeof(float));
     w.total = align256(w.ticket_off + (size_t)s.units * sizeof(uint32_t));
@@ -356,6 +376,7 @@ size_t fathom_workspace_size(const fathom_shape *shape, int which) {
     if (check_shape(shape, true)) return 0;
     if (which == FATHOM_WS_SCAN_TOPK) return scan_workspace_layout(*shape).total;
     if (which == FATHOM_WS_SPARSE_ATTN) return attn_workspace_layout(*shape).total;
+    if (which == FATHOM_WS_DENSE_ATTN) return dense_workspace_layout(*shape).total;
     return 0;
 }
 
@@ -387,6 +408,87 @@ int fathom_scan_topk(const fathom_shape *shape, const uint64_t *planes, const ui
     if (((uintptr_t)workspace & 255) != 0) { set_error("workspace must be 256-byte aligned"); return FATHOM_EINVAL; }
     return launch_scan_topk(*shape, planes, scales, source, stage_words, stage_scales_n, runs, q,
                             topk_idx, topk_score, scores_opt, workspace, (cudaStream_t)stream);
+}
+
+int fathom_exact_topk(const fathom_shape *shape, const uint16_t *k_rows, const float *q,
+                      int32_t *topk_idx, float *topk_score, float *scores_opt,
+                      void *workspace, size_t workspace_bytes, void *stream) {
+    g_err[0] = 0;
+    int rc = check_shape(shape, true);
+    if (rc) return rc;
+    NONNULL(k_rows);
+    NONNULL(q);
+    NONNULL(topk_idx);
+    NONNULL(topk_score);
+    NONNULL(workspace);
+    size_t need = scan_workspace_layout(*shape).total;
+    if (workspace_bytes < need) {
+        set_error("exact_topk workspace too small: %zu < %zu bytes", workspace_bytes, need);
+        return FATHOM_ENOMEM;
+    }
+    if (((uintptr_t)workspace & 255) != 0) { set_error("workspace must be 256-byte aligned"); return FATHOM_EINVAL; }
+    return launch_scan_topk(*shape, (const uint64_t *)k_rows, nullptr, FATHOM_SRC_ROWS, 0, 0, nullptr, q,
+                            topk_idx, topk_score, scores_opt, workspace, (cudaStream_t)stream);
+}
+
+int fathom_dense_attn(const fathom_shape *shape, const uint16_t *k_rows, const uint16_t *v_rows,
+                      const float *q, float *out, void *workspace, size_t workspace_bytes, void *stream) {
+    g_err[0] = 0;
+    int rc = check_shape(shape, false);
+    if (rc) return rc;
+    NONNULL(k_rows);
+    NONNULL(v_rows);
+    NONNULL(q);
+    NONNULL(out);
+    NONNULL(workspace);
+    const size_t need = dense_workspace_layout(*shape).total;
+    if (workspace_bytes < need) {
+        set_error("dense_attn workspace too small: %zu < %zu bytes", workspace_bytes, need);
+        return FATHOM_ENOMEM;
+    }
+    if (((uintptr_t)workspace & 255) != 0) { set_error("workspace must be 256-byte aligned"); return FATHOM_EINVAL; }
+    return launch_dense_attn(*shape, k_rows, v_rows, q, out, workspace, (cudaStream_t)stream);
+}
+
+int fathom_rel_err(int32_t rows, int32_t D, const float *a, const float *ref, double *err, void *stream) {
+    g_err[0] = 0;
+    if (rows < 0 || D < 1) { set_error("rel_err: need rows >= 0 and D >= 1 (rows=%d, D=%d)", rows, D); return FATHOM_EINVAL; }
+    if (rows == 0) return FATHOM_OK;
+    NONNULL(a);
+    NONNULL(ref);
+    NONNULL(err);
+    return launch_rel_err(rows, D, a, ref, err, (cudaStream_t)stream);
+}
+
+int fathom_set_overlap(int32_t rows, int32_t k, const int32_t *a, const int32_t *b, int32_t *count,
+                       void *stream) {
+    g_err[0] = 0;
+    if (rows < 0 || k < 1) { set_error("set_overlap: need rows >= 0 and k >= 1 (rows=%d, k=%d)", rows, k); return FATHOM_EINVAL; }
+    if (rows == 0) return FATHOM_OK;
+    NONNULL(a);
+    NONNULL(b);
+    NONNULL(count);
+    return launch_set_overlap(rows, k, a, b, count, (cudaStream_t)stream);
+}
+
+int fathom_greedy_budgets(int32_t layers, int32_t levels, const double *err, int32_t b_min, int32_t step,
+                          int32_t b_mean, int32_t *budgets) {
+    g_err[0] = 0;
+    if (layers < 1 || levels < 1 || step < 1 || b_min < 0) {
+        set_error("greedy_budgets: need layers, levels, step >= 1 and b_min >= 0");
+        return FATHOM_EINVAL;
+    }
+    const long long b_max = (long long)b_min + (long long)step * (levels - 1);
+    if (b_mean < b_min || b_mean > b_max || (b_mean - b_min) % step != 0) {
+        set_error("greedy_budgets: b_mean=%d must be one of the levels %d, %d, ..., %lld", b_mean, b_min,
+                  b_min + step, b_max);
+        return FATHOM_EINVAL;
+    }
+    NONNULL(err);
+    NONNULL(budgets);
+    for (long long i = 0; i < (long long)layers * levels; ++i)
+        if (!std::isfinite(err[i])) { set_error("greedy_budgets: err[%lld] is not finite", i); return FATHOM_EINVAL; }
+    return greedy_budgets(layers, levels, err, b_min, step, b_mean, budgets);
 }
 
 int fathom_sparse_attn(const fathom_shape *shape, const uint16_t *k_rows, const uint16_t *v_rows,

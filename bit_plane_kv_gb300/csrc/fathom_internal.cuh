@@ -83,6 +83,7 @@ struct AttnWorkspace {
     size_t part_off, ticket_off, total;
 };
 AttnWorkspace attn_workspace_layout(const fathom_shape &s);
+AttnWorkspace dense_workspace_layout(const fathom_shape &s);   // dense attention (fidelity reference)
 
 // ---------------------------------------------------------------- selection keys
 // A 64-bit key orders (score descending, token index ascending): the high
@@ -141,7 +142,13 @@ int launch_scan_topk(const fathom_shape &s, const uint64_t *planes, const uint16
                      cudaStream_t st);
 int launch_sparse_attn(const fathom_shape &s, const uint16_t *krows, const uint16_t *vrows,
                        const float *q, const int32_t *idx, float *out, void *ws, cudaStream_t st);
+int launch_dense_attn(const fathom_shape &s, const uint16_t *krows, const uint16_t *vrows, const float *q,
+                      float *out, void *ws, cudaStream_t st);
 int launch_sparse_attn_noalloc(const fathom_shape &s, const uint16_t *krows, const uint16_t *vrows,
                                const float *q, const int32_t *idx, float *out, cudaStream_t st);
+
+int launch_rel_err(int rows, int D, const float *a, const float *ref, double *err, cudaStream_t st);
+int launch_set_overlap(int rows, int k, const int32_t *a, const int32_t *b, int32_t *count, cudaStream_t st);
+int greedy_budgets(int layers, int levels, const double *err, int b_min, int step, int b_mean, int32_t *budgets);
 
 }  // namespace fathom

@@ -466,9 +466,12 @@ constexpr int kMultiKPT = 4;   // register keys per thread and head for the fina
 // kFix = true: the exact second pass over the chunks the merge flagged.
 // kScores: also write every token's score (a diagnostic output; kept out of
 // the other instantiations so that their loop stays small).
-template <int G, bool kFix, bool kScores>
+// kRows: score every token exactly from its bf16 key row (q . k in fp32, all
+// channels; `planes` holds the rows [units][ctok][D]) instead of the planned
+// planes; the selection is the same.  The exact top-k of a fidelity check.
+template <int G, bool kFix, bool kScores, bool kRows>
 __global__ void __launch_bounds__(NT, (G <= 4) ? 3 : 1)
-scan_kernel(int n, int cb, int D, int chunk_blocks, int source, size_t stage_words, size_t stage_scales,
+scan_kernel(int n, int cb, int ctok, int D, int chunk_blocks, int source, size_t stage_words, size_t stage_scales,
             const uint64_t *__restrict__ planes, const uint16_t *__restrict__ scales,
             const fathom_run *__restrict__ runs, const float *__restrict__ q, int k_sel, int m_sel,
             int m_first, int ns, int r0, int nf, int cap, int vec, float *__restrict__ scores_opt,
@@ -497,7 +500,7 @@ scan_kernel(int n, int cb, int D, int chunk_blocks, int source, size_t stage_wor
     const int lane = tid & 31, wid = tid >> 5;
     int t = 0;
     fathom_run rr = {0, 0, 0, 0, 0, 0};
-    if (tid < D) {
+    if (!kRows && tid < D) {
         rr = runs[(size_t)u * D + tid];
         t = (int)(rr.n_words / (uint32_t)nb);
         t = t > FATHOM_PLANES ? FATHOM_PLANES : t;
@@ -581,6 +584,9 @@ scan_kernel(int n, int cb, int D, int chunk_blocks, int source, size_t stage_wor
         sm.grp[tid] = g;
     }
     if (tid == 0) sm.n_groups = n_groups;
+    if constexpr (kRows) {   // every channel, unscaled queries
+        for (int e = tid; e < D * G; e += NT) sm.qs[e / G][e % G] = q[((size_t)u * G + e % G) * D + e / G];
+    }
     __syncthreads();
 
     const int ng = sm.n_groups;
@@ -647,7 +653,40 @@ scan_kernel(int n, int cb, int D, int chunk_blocks, int source, size_t stage_wor
 #pragma unroll
             for (int h = 0; h < G; ++h) acc[m][h] = 0.0f;
 
-        if (piped) {
+        if constexpr (kRows) {
+            // exact scores: 4 channels of q (all heads) at a time from shared memory,
+            // then the 8 tokens' key rows (8-byte loads of 4 bf16 channels)
+            const uint16_t *rows = reinterpret_cast<const uint16_t *>(planes);
+            const int beta = sb + bl;
+            for (int j0 = 0; j0 < D; j0 += 4) {
+                float qv[4][G];
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+#pragma unroll
+                    for (int h = 0; h < G; ++h) qv[c][h] = (j0 + c < D) ? sm.qs[j0 + c][h] : 0.0f;
+#pragma unroll
+                for (int m = 0; m < 8; ++m) {
+                    const int i = beta * 64 + (int)r + 8 * m;
+                    if (bl < nblk && i < n) {
+                        const uint16_t *kr = rows + ((size_t)u * ctok + i) * D + j0;
+                        float kf[4];
+                        if (vec) {
+                            const uint2 v = __ldg(reinterpret_cast<const uint2 *>(kr));
+                            kf[0] = __uint_as_float(v.x << 16); kf[1] = __uint_as_float(v.x & 0xffff0000u);
+                            kf[2] = __uint_as_float(v.y << 16); kf[3] = __uint_as_float(v.y & 0xffff0000u);
+                        } else {
+#pragma unroll
+                            for (int c = 0; c < 4; ++c)
+                                kf[c] = (j0 + c < D) ? __uint_as_float(((uint32_t)__ldg(kr + c)) << 16) : 0.0f;
+                        }
+#pragma unroll
+                        for (int c = 0; c < 4; ++c)
+#pragma unroll
+                            for (int h = 0; h < G; ++h) acc[m][h] = fmaf(qv[c][h], kf[c], acc[m][h]);
+                    }
+                }
+            }
+        } else if (piped) {
             const int sbn = sb + (int)gridDim.x * kSubBlocks;
             if (sbn < nb) stage_async(half ^ 1, sbn);
             cp_async_commit();
@@ -1217,26 +1256,39 @@ static int launch_g(const fathom_shape &s, const uint64_t *planes, const uint16_
     const int nb = num_blocks(s.n);
     const bool aligned_src = (source == FATHOM_SRC_STORE) || (stage_words % 2 == 0 && stage_scales % 8 == 0);
     const int cb = cap_blocks(s);
-    const int vec = (nb % 8 == 0) && (source != FATHOM_SRC_STORE || cb % 8 == 0) && aligned_src &&
-                    ((uintptr_t)planes % 16 == 0) && ((uintptr_t)scales % 16 == 0);
+    const bool rows_src = source == FATHOM_SRC_ROWS;
+    // rows: 8-byte loads of 4 bf16 channels need D % 4 == 0 and an aligned base
+    const int vec = rows_src ? (s.D % 4 == 0 && (uintptr_t)planes % 8 == 0)
+                             : (nb % 8 == 0) && (source != FATHOM_SRC_STORE || cb % 8 == 0) && aligned_src &&
+                                   ((uintptr_t)planes % 16 == 0) && ((uintptr_t)scales % 16 == 0);
     const size_t smem = sizeof(ScanSmem<G>);
     if (s.units > 65535) { set_error("scan: too many units for one launch"); return FATHOM_EINVAL; }
-    ensure_smem(scan_kernel<G, false, false>, smem);
-    ensure_smem(scan_kernel<G, false, true>, smem);
-    ensure_smem(scan_kernel<G, true, false>, smem);
+    ensure_smem(scan_kernel<G, false, false, false>, smem);
+    ensure_smem(scan_kernel<G, false, true, false>, smem);
+    ensure_smem(scan_kernel<G, true, false, false>, smem);
+    ensure_smem(scan_kernel<G, false, false, true>, smem);
+    ensure_smem(scan_kernel<G, false, true, true>, smem);
+    ensure_smem(scan_kernel<G, true, false, true>, smem);
     const size_t msmem = sizeof(MergeSmem);
     ensure_smem(merge_kernel, msmem);
     const int nf = f.nf > 0 ? f.nf : 1;
     dim3 grid(sg.chunks, s.units);
     for (int pass = 0; pass < 2; ++pass) {
-#define FATHOM_SCAN_LAUNCH(FIX, SC)                                                                       \
-    scan_kernel<G, FIX, SC><<<grid, NT, smem, st>>>(s.n, cb, s.D, sg.chunk_blocks, source, stage_words,     \
-                                                    stage_scales, planes, scales, runs, q, k_sel, m_sel,      \
-                                                    m_first, f.ns, f.r0, nf, cap, vec,                        \
-                                                    SC ? scores_opt : nullptr, cand, cnt, ctau, flags, forced)
-        if (pass == 1) FATHOM_SCAN_LAUNCH(true, false);
-        else if (scores_opt) FATHOM_SCAN_LAUNCH(false, true);
-        else FATHOM_SCAN_LAUNCH(false, false);
+#define FATHOM_SCAN_LAUNCH(FIX, SC, RW)                                                                    \
+    scan_kernel<G, FIX, SC, RW><<<grid, NT, smem, st>>>(s.n, cb, cap_tokens(s), s.D, sg.chunk_blocks, source, \
+                                                        stage_words, stage_scales, planes, scales, runs, q,   \
+                                                        k_sel, m_sel, m_first, f.ns, f.r0, nf, cap, vec,      \
+                                                        SC ? scores_opt : nullptr, cand, cnt, ctau, flags,    \
+                                                        forced)
+        if (rows_src) {
+            if (pass == 1) FATHOM_SCAN_LAUNCH(true, false, true);
+            else if (scores_opt) FATHOM_SCAN_LAUNCH(false, true, true);
+            else FATHOM_SCAN_LAUNCH(false, false, true);
+        } else {
+            if (pass == 1) FATHOM_SCAN_LAUNCH(true, false, false);
+            else if (scores_opt) FATHOM_SCAN_LAUNCH(false, true, false);
+            else FATHOM_SCAN_LAUNCH(false, false, false);
+        }
 #undef FATHOM_SCAN_LAUNCH
         int rc = launch_status("scan_kernel");
         if (rc) return rc;
@@ -1264,9 +1316,9 @@ static int resident_g() {
     std::lock_guard<std::mutex> lock(mu);
     if (!cache[dev]) {
         const size_t smem = sizeof(ScanSmem<G>);
-        ensure_smem(scan_kernel<G, false, false>, smem);
+        ensure_smem(scan_kernel<G, false, false, false>, smem);
         int nbk = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nbk, scan_kernel<G, false, false>, NT, smem) != cudaSuccess) {
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nbk, scan_kernel<G, false, false, false>, NT, smem) != cudaSuccess) {
             cudaGetLastError();
             return 0;
         }

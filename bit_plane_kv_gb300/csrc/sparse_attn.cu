@@ -90,174 +90,17 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
-// Lane l holds channels 4l .. 4l+3 (kVec: D = 128, one 8-byte load of K and one
-// of V per row) or channels l + 32 e (any D <= 128).
+// Warp merge, this CTA's partial state per head, and (last CTA of the unit, by
+// an atomic ticket) the merge of all partial states into o_h.  m_h, l_h, o_h:
+// this thread's online-softmax state (lane l holds channels 4l..4l+3, kVec, or
+// l + 32 e).  Shared by the sparse and the dense attention.
 template <int G, bool kVec>
-__global__ void __launch_bounds__(NA, G >= 8 ? 1 : 2)
-attn_kernel(int n, int ctok, int D, int k, int rows_cta, int cph, int splits, const uint16_t *__restrict__ krows,
-            const uint16_t *__restrict__ vrows, const float *__restrict__ q,
-            const int32_t *__restrict__ topk, float *__restrict__ out, float *__restrict__ part,
-            unsigned *__restrict__ ticket) {
-    constexpr int RB = AttnBatch<G>::RB, S = AttnBatch<G>::S;
-    extern __shared__ __align__(16) unsigned char asmem_raw[];
-    AttnHeader &sm = *reinterpret_cast<AttnHeader *>(asmem_raw);
-    const AttnLayout lay = attn_smem_layout(G, k, D, splits);
-    int *lists = reinterpret_cast<int *>(asmem_raw + lay.lists);
-    float *wo = reinterpret_cast<float *>(asmem_raw + lay.wo);          // [warp][h][D]
-    const int s = blockIdx.x, u = blockIdx.y;
+__device__ __forceinline__ void attn_finish(AttnHeader &sm, unsigned char *asmem_raw, const AttnLayout &lay,
+                                            int D, int s, int u, int splits, const float (&m_h)[G],
+                                            const float (&l_h)[G], float (&o_h)[G][4], float *__restrict__ out,
+                                            float *__restrict__ part, unsigned *__restrict__ ticket) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int hown = s / cph;
-    const int e_begin = (s % cph) * rows_cta;
-    const int R = min(k, e_begin + rows_cta) - e_begin;
-
-    // ---- the G sorted lists, then this CTA's rows and their head masks
-    const int32_t *src = topk + (size_t)u * G * k;
-    if ((k & 3) == 0 && ((uintptr_t)src & 15) == 0) {
-        for (int e = tid; e < G * k / 4; e += NA)
-            reinterpret_cast<int4 *>(lists)[e] = __ldg(reinterpret_cast<const int4 *>(src) + e);
-    } else {
-        for (int e = tid; e < G * k; e += NA) lists[e] = __ldg(src + e);
-    }
-    __syncthreads();
-    for (int r = tid; r < R; r += NA) {
-        const int i = r < R ? lists[hown * k + e_begin + r] : -1;
-        sm.rows[r] = i;
-        sm.rmask[r] = (r < R && i >= 0 && i < n) ? (1u << hown) : 0u;
-    }
-    __syncthreads();
-    for (int p = tid; p < R * G; p += NA) {
-        const int r = p % R, h2 = p / R;
-        if (h2 != hown && r < R && contains(lists + h2 * k, k, sm.rows[r])) atomicOr(&sm.rmask[r], 1u << h2);
-    }
-    __syncthreads();
-
-    const float scale = 1.0f / sqrtf((float)D);   // 1/sqrt(D), correctly rounded
-    float m_h[G], l_h[G], o_h[G][4], qv[G][4];
-#pragma unroll
-    for (int h = 0; h < G; ++h) {
-        m_h[h] = -CUDART_INF_F;
-        l_h[h] = 0.0f;
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            o_h[h][e] = 0.0f;
-            const int j = kVec ? 4 * lane + e : lane + 32 * e;
-            qv[h][e] = (j < D) ? q[((size_t)u * G + h) * D + j] : 0.0f;
-        }
-    }
-    float *pb = sm.pbuf[warp];
-    const int v = lane & (S - 1), vr = v / G, vh = v % G;   // this lane's (row, head) slot
-    const unsigned below = (1u << hown) - 1u;
-    for (int r0 = warp * RB; r0 < R; r0 += kWarps * RB) {
-        unsigned mask[RB];
-        uint2 kp[RB], vp[RB];                      // bf16 pairs (kVec)
-        float kv[RB][4], vv[RB][4];                // general path
-#pragma unroll
-        for (int r = 0; r < RB; ++r) {
-            const int rr = r0 + r;
-            unsigned m = 0;
-            int i = 0;
-            if (rr < R) {
-                m = sm.rmask[rr];
-                i = sm.rows[rr];
-                if (!((m >> hown) & 1u) || (m & below)) m = 0;   // invalid, or a lower head owns it
-            }
-            mask[r] = m;
-            const uint16_t *kr = krows + ((size_t)u * ctok + (m ? i : 0)) * D;
-            const uint16_t *vr_ = vrows + ((size_t)u * ctok + (m ? i : 0)) * D;
-            if (kVec) {
-                kp[r] = m ? __ldg(reinterpret_cast<const uint2 *>(kr) + lane) : make_uint2(0u, 0u);
-                vp[r] = m ? __ldg(reinterpret_cast<const uint2 *>(vr_) + lane) : make_uint2(0u, 0u);
-            } else {
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    const int j = lane + 32 * c;
-                    const bool ok = m && j < D;
-                    kv[r][c] = ok ? __uint_as_float(((uint32_t)__ldg(kr + j)) << 16) : 0.0f;
-                    vv[r][c] = ok ? __uint_as_float(((uint32_t)__ldg(vr_ + j)) << 16) : 0.0f;
-                }
-            }
-        }
-        // partial dots of every (row, head) slot, then one transpose reduction:
-        // afterwards lane l holds the full dot of slot l mod S
-        float a[S];
-#pragma unroll
-        for (int r = 0; r < RB; ++r) {
-            float kk[4];
-            if (kVec) {
-                kk[0] = bf16lo(kp[r].x); kk[1] = bf16hi(kp[r].x); kk[2] = bf16lo(kp[r].y); kk[3] = bf16hi(kp[r].y);
-            } else {
-#pragma unroll
-                for (int c = 0; c < 4; ++c) kk[c] = kv[r][c];
-            }
-#pragma unroll
-            for (int h = 0; h < G; ++h) {
-                float d = 0.0f;
-#pragma unroll
-                for (int c = 0; c < 4; ++c) d = fmaf(qv[h][c], kk[c], d);
-                a[r * G + h] = d;
-            }
-        }
-#pragma unroll
-        for (int w = S / 2; w >= 1; w >>= 1) {
-            const bool up = (lane & w) != 0;
-#pragma unroll
-            for (int i = 0; i < w; ++i) {
-                const float send = up ? a[i] : a[i + w];
-                const float keep = up ? a[i + w] : a[i];
-                a[i] = keep + __shfl_xor_sync(0xffffffffu, send, w);
-            }
-        }
-#pragma unroll
-        for (int o = S; o < 32; o <<= 1) a[0] += __shfl_xor_sync(0xffffffffu, a[0], o);
-        // online softmax for slot (vr, vh), then per head across the batch's rows
-        unsigned mv = 0;
-        float mo = -CUDART_INF_F;
-#pragma unroll
-        for (int r = 0; r < RB; ++r) mv = (r == vr) ? mask[r] : mv;
-#pragma unroll
-        for (int h = 0; h < G; ++h) mo = (h == vh) ? m_h[h] : mo;
-        const bool live = (mv >> vh) & 1u;
-        const float logit = live ? a[0] * scale : -CUDART_INF_F;
-        float mn = logit;
-#pragma unroll
-        for (int o = G; o < S; o <<= 1) mn = fmaxf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
-        mn = fmaxf(mn, mo);
-        float p = 0.0f, corr = 1.0f;
-        if (mn != -CUDART_INF_F) {
-            p = live ? expf(logit - mn) : 0.0f;
-            corr = expf(mo - mn);
-        }
-        float ps = p;
-#pragma unroll
-        for (int o = G; o < S; o <<= 1) ps += __shfl_xor_sync(0xffffffffu, ps, o);
-        if (lane < S) pb[lane] = p;
-        __syncwarp();
-#pragma unroll
-        for (int h = 0; h < G; ++h) {   // lane h holds slot (row 0, head h)
-            const float c = __shfl_sync(0xffffffffu, corr, h);
-            l_h[h] = l_h[h] * c + __shfl_sync(0xffffffffu, ps, h);
-            m_h[h] = __shfl_sync(0xffffffffu, mn, h);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) o_h[h][e] *= c;
-        }
-#pragma unroll
-        for (int r = 0; r < RB; ++r) {
-            float vx[4];
-            if (kVec) {
-                vx[0] = bf16lo(vp[r].x); vx[1] = bf16hi(vp[r].x); vx[2] = bf16lo(vp[r].y); vx[3] = bf16hi(vp[r].y);
-            } else {
-#pragma unroll
-                for (int c = 0; c < 4; ++c) vx[c] = vv[r][c];
-            }
-#pragma unroll
-            for (int h = 0; h < G; ++h) {
-                const float pr = pb[r * G + h];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) o_h[h][e] = fmaf(pr, vx[e], o_h[h][e]);
-            }
-        }
-        __syncwarp();
-    }
+    float *wo = reinterpret_cast<float *>(asmem_raw + lay.wo);          // [warp][h][D]
     // ---- merge the warps: rescale each warp's state to the CTA maximum
     if (lane == 0) {
 #pragma unroll
@@ -339,6 +182,270 @@ attn_kernel(int n, int ctok, int D, int k, int rows_cta, int cph, int splits, co
         __syncthreads();
     }
     if (tid == 0) ticket[u] = 0u;   // ready for the next call
+}
+
+// One batch of RB rows (token ti[r] of the unit, attended by the heads in
+// mask[r]; mask 0: no row): loads K and V (bf16), the G dot products of every
+// row with one transpose reduction across the warp, and the online-softmax
+// update of every head's state.
+template <int G, bool kVec>
+__device__ __forceinline__ void attn_batch(const unsigned (&mask)[AttnBatch<G>::RB], const int (&ti)[AttnBatch<G>::RB],
+                                           const uint16_t *__restrict__ krows, const uint16_t *__restrict__ vrows,
+                                           size_t ubase, int D, float scale, const float (&qv)[G][4],
+                                           float (&m_h)[G], float (&l_h)[G], float (&o_h)[G][4], float *pb) {
+    constexpr int RB = AttnBatch<G>::RB, S = AttnBatch<G>::S;
+    const int lane = threadIdx.x & 31;
+    const int v = lane & (S - 1), vr = v / G, vh = v % G;   // this lane's (row, head) slot
+    uint2 kp[RB], vp[RB];                      // bf16 pairs (kVec)
+    float kv[RB][4], vv[RB][4];                // general path
+#pragma unroll
+    for (int r = 0; r < RB; ++r) {
+        const unsigned m = mask[r];
+        const uint16_t *kr = krows + (ubase + (m ? ti[r] : 0)) * D;
+        const uint16_t *vr_ = vrows + (ubase + (m ? ti[r] : 0)) * D;
+        if (kVec) {
+            kp[r] = m ? __ldg(reinterpret_cast<const uint2 *>(kr) + lane) : make_uint2(0u, 0u);
+            vp[r] = m ? __ldg(reinterpret_cast<const uint2 *>(vr_) + lane) : make_uint2(0u, 0u);
+        } else {
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const int j = lane + 32 * c;
+                const bool ok = m && j < D;
+                kv[r][c] = ok ? __uint_as_float(((uint32_t)__ldg(kr + j)) << 16) : 0.0f;
+                vv[r][c] = ok ? __uint_as_float(((uint32_t)__ldg(vr_ + j)) << 16) : 0.0f;
+            }
+        }
+    }
+        // partial dots of every (row, head) slot, then one transpose reduction:
+        // afterwards lane l holds the full dot of slot l mod S
+        float a[S];
+#pragma unroll
+        for (int r = 0; r < RB; ++r) {
+            float kk[4];
+            if (kVec) {
+                kk[0] = bf16lo(kp[r].x); kk[1] = bf16hi(kp[r].x); kk[2] = bf16lo(kp[r].y); kk[3] = bf16hi(kp[r].y);
+            } else {
+#pragma unroll
+                for (int c = 0; c < 4; ++c) kk[c] = kv[r][c];
+            }
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+                float d = 0.0f;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) d = fmaf(qv[h][c], kk[c], d);
+                a[r * G + h] = d;
+            }
+        }
+#pragma unroll
+        for (int w = S / 2; w >= 1; w >>= 1) {
+            const bool up = (lane & w) != 0;
+#pragma unroll
+            for (int i = 0; i < w; ++i) {
+                const float send = up ? a[i] : a[i + w];
+                const float keep = up ? a[i + w] : a[i];
+                a[i] = keep + __shfl_xor_sync(0xffffffffu, send, w);
+            }
+        }
+#pragma unroll
+        for (int o = S; o < 32; o <<= 1) a[0] += __shfl_xor_sync(0xffffffffu, a[0], o);
+        // online softmax for slot (vr, vh), then per head across the batch's rows
+        unsigned mv = 0;
+        float mo = -CUDART_INF_F;
+#pragma unroll
+        for (int r = 0; r < RB; ++r) mv = (r == vr) ? mask[r] : mv;
+#pragma unroll
+        for (int h = 0; h < G; ++h) mo = (h == vh) ? m_h[h] : mo;
+        const bool live = (mv >> vh) & 1u;
+        const float logit = live ? a[0] * scale : -CUDART_INF_F;
+        float mn = logit;
+#pragma unroll
+        for (int o = G; o < S; o <<= 1) mn = fmaxf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+        mn = fmaxf(mn, mo);
+        float p = 0.0f, corr = 1.0f;
+        if (mn != -CUDART_INF_F) {
+            p = live ? expf(logit - mn) : 0.0f;
+            corr = expf(mo - mn);
+        }
+        float ps = p;
+#pragma unroll
+        for (int o = G; o < S; o <<= 1) ps += __shfl_xor_sync(0xffffffffu, ps, o);
+        if (lane < S) pb[lane] = p;
+        __syncwarp();
+#pragma unroll
+        for (int h = 0; h < G; ++h) {   // lane h holds slot (row 0, head h)
+            const float c = __shfl_sync(0xffffffffu, corr, h);
+            l_h[h] = l_h[h] * c + __shfl_sync(0xffffffffu, ps, h);
+            m_h[h] = __shfl_sync(0xffffffffu, mn, h);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) o_h[h][e] *= c;
+        }
+#pragma unroll
+        for (int r = 0; r < RB; ++r) {
+            float vx[4];
+            if (kVec) {
+                vx[0] = bf16lo(vp[r].x); vx[1] = bf16hi(vp[r].x); vx[2] = bf16lo(vp[r].y); vx[3] = bf16hi(vp[r].y);
+            } else {
+#pragma unroll
+                for (int c = 0; c < 4; ++c) vx[c] = vv[r][c];
+            }
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+                const float pr = pb[r * G + h];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) o_h[h][e] = fmaf(pr, vx[e], o_h[h][e]);
+            }
+        }
+        __syncwarp();
+}
+
+// Lane l holds channels 4l .. 4l+3 (kVec: D = 128, one 8-byte load of K and one
+// of V per row) or channels l + 32 e (any D <= 128).
+template <int G, bool kVec>
+__global__ void __launch_bounds__(NA, G >= 8 ? 1 : 2)
+attn_kernel(int n, int ctok, int D, int k, int rows_cta, int cph, int splits, const uint16_t *__restrict__ krows,
+            const uint16_t *__restrict__ vrows, const float *__restrict__ q,
+            const int32_t *__restrict__ topk, float *__restrict__ out, float *__restrict__ part,
+            unsigned *__restrict__ ticket) {
+    constexpr int RB = AttnBatch<G>::RB;
+    extern __shared__ __align__(16) unsigned char asmem_raw[];
+    AttnHeader &sm = *reinterpret_cast<AttnHeader *>(asmem_raw);
+    const AttnLayout lay = attn_smem_layout(G, k, D, splits);
+    int *lists = reinterpret_cast<int *>(asmem_raw + lay.lists);
+    const int s = blockIdx.x, u = blockIdx.y;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int hown = s / cph;
+    const int e_begin = (s % cph) * rows_cta;
+    const int R = min(k, e_begin + rows_cta) - e_begin;
+
+    // ---- the G sorted lists, then this CTA's rows and their head masks
+    const int32_t *src = topk + (size_t)u * G * k;
+    if ((k & 3) == 0 && ((uintptr_t)src & 15) == 0) {
+        for (int e = tid; e < G * k / 4; e += NA)
+            reinterpret_cast<int4 *>(lists)[e] = __ldg(reinterpret_cast<const int4 *>(src) + e);
+    } else {
+        for (int e = tid; e < G * k; e += NA) lists[e] = __ldg(src + e);
+    }
+    __syncthreads();
+    for (int r = tid; r < R; r += NA) {
+        const int i = r < R ? lists[hown * k + e_begin + r] : -1;
+        sm.rows[r] = i;
+        sm.rmask[r] = (r < R && i >= 0 && i < n) ? (1u << hown) : 0u;
+    }
+    __syncthreads();
+    for (int p = tid; p < R * G; p += NA) {
+        const int r = p % R, h2 = p / R;
+        if (h2 != hown && r < R && contains(lists + h2 * k, k, sm.rows[r])) atomicOr(&sm.rmask[r], 1u << h2);
+    }
+    __syncthreads();
+
+    const float scale = 1.0f / sqrtf((float)D);   // 1/sqrt(D), correctly rounded
+    float m_h[G], l_h[G], o_h[G][4], qv[G][4];
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+        m_h[h] = -CUDART_INF_F;
+        l_h[h] = 0.0f;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            o_h[h][e] = 0.0f;
+            const int j = kVec ? 4 * lane + e : lane + 32 * e;
+            qv[h][e] = (j < D) ? q[((size_t)u * G + h) * D + j] : 0.0f;
+        }
+    }
+    float *pb = sm.pbuf[warp];
+    const unsigned below = (1u << hown) - 1u;
+    for (int r0 = warp * RB; r0 < R; r0 += kWarps * RB) {
+        unsigned mask[RB];
+        int ti[RB];
+#pragma unroll
+        for (int r = 0; r < RB; ++r) {
+            const int rr = r0 + r;
+            unsigned m = 0;
+            int i = 0;
+            if (rr < R) {
+                m = sm.rmask[rr];
+                i = sm.rows[rr];
+                if (!((m >> hown) & 1u) || (m & below)) m = 0;   // invalid, or a lower head owns it
+            }
+            mask[r] = m;
+            ti[r] = i;
+        }
+        attn_batch<G, kVec>(mask, ti, krows, vrows, (size_t)u * ctok, D, scale, qv, m_h, l_h, o_h, pb);
+    }
+    attn_finish<G, kVec>(sm, asmem_raw, lay, D, s, u, splits, m_h, l_h, o_h, out, part, ticket);
+}
+
+// Dense attention over every token (the fidelity reference): grid (splits, units),
+// CTA c attends all G heads over tokens [c R, c R + R) with the same batch step,
+// then the same partial states and last-CTA merge.
+template <int G, bool kVec>
+__global__ void __launch_bounds__(NA, G >= 8 ? 1 : 2)
+dense_attn_kernel(int n, int ctok, int D, int rows_cta, int splits, const uint16_t *__restrict__ krows,
+                  const uint16_t *__restrict__ vrows, const float *__restrict__ q, float *__restrict__ out,
+                  float *__restrict__ part, unsigned *__restrict__ ticket) {
+    constexpr int RB = AttnBatch<G>::RB;
+    extern __shared__ __align__(16) unsigned char asmem_raw[];
+    AttnHeader &sm = *reinterpret_cast<AttnHeader *>(asmem_raw);
+    const AttnLayout lay = attn_smem_layout(G, 0, D, splits);
+    const int s = blockIdx.x, u = blockIdx.y;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int i_begin = s * rows_cta;
+    const int R = max(0, min(n, i_begin + rows_cta) - i_begin);
+    const float scale = 1.0f / sqrtf((float)D);
+    float m_h[G], l_h[G], o_h[G][4], qv[G][4];
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+        m_h[h] = -CUDART_INF_F;
+        l_h[h] = 0.0f;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            o_h[h][e] = 0.0f;
+            const int j = kVec ? 4 * lane + e : lane + 32 * e;
+            qv[h][e] = (j < D) ? q[((size_t)u * G + h) * D + j] : 0.0f;
+        }
+    }
+    float *pb = sm.pbuf[warp];
+    for (int r0 = warp * RB; r0 < R; r0 += kWarps * RB) {
+        unsigned mask[RB];
+        int ti[RB];
+#pragma unroll
+        for (int r = 0; r < RB; ++r) {
+            mask[r] = (r0 + r < R) ? (1u << G) - 1u : 0u;
+            ti[r] = i_begin + r0 + r;
+        }
+        attn_batch<G, kVec>(mask, ti, krows, vrows, (size_t)u * ctok, D, scale, qv, m_h, l_h, o_h, pb);
+    }
+    attn_finish<G, kVec>(sm, asmem_raw, lay, D, s, u, splits, m_h, l_h, o_h, out, part, ticket);
+}
+
+int launch_dense_attn(const fathom_shape &s, const uint16_t *krows, const uint16_t *vrows, const float *q,
+                      float *out, void *ws, cudaStream_t st) {
+    const AttnWorkspace wl = dense_workspace_layout(s);
+    char *w = (char *)ws;
+    float *part = (float *)(w + wl.part_off);
+    unsigned *ticket = (unsigned *)(w + wl.ticket_off);
+    if (s.units > 65535) { set_error("dense_attn: too many units for one launch"); return FATHOM_EINVAL; }
+    const size_t smem = attn_smem_layout(s.G, 0, s.D, wl.splits).total;
+    const bool vec = s.D == 128 && ((uintptr_t)krows % 8 == 0) && ((uintptr_t)vrows % 8 == 0);
+    const dim3 grid(wl.splits, s.units);
+#define FATHOM_DENSE_LAUNCH(GG, VV)                                                                       \
+    do {                                                                                                  \
+        ensure_smem(dense_attn_kernel<GG, VV>, smem);                                                     \
+        dense_attn_kernel<GG, VV><<<grid, NA, smem, st>>>(s.n, cap_tokens(s), s.D, wl.rows, wl.splits, krows, \
+                                                          vrows, q, out, part, ticket);                   \
+    } while (0)
+    switch (s.G * 2 + (vec ? 1 : 0)) {
+        case 2: FATHOM_DENSE_LAUNCH(1, false); break;
+        case 3: FATHOM_DENSE_LAUNCH(1, true); break;
+        case 4: FATHOM_DENSE_LAUNCH(2, false); break;
+        case 5: FATHOM_DENSE_LAUNCH(2, true); break;
+        case 8: FATHOM_DENSE_LAUNCH(4, false); break;
+        case 9: FATHOM_DENSE_LAUNCH(4, true); break;
+        case 16: FATHOM_DENSE_LAUNCH(8, false); break;
+        case 17: FATHOM_DENSE_LAUNCH(8, true); break;
+        default: set_error("dense_attn: unsupported G=%d", s.G); return FATHOM_EINVAL;
+    }
+#undef FATHOM_DENSE_LAUNCH
+    return launch_status("dense_attn_kernel");
 }
 
 int launch_sparse_attn(const fathom_shape &s, const uint16_t *krows, const uint16_t *vrows,

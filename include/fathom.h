@@ -65,12 +65,13 @@ typedef enum {
 
 typedef enum { FATHOM_F32 = 0, FATHOM_BF16 = 1 } fathom_dtype;
 
-typedef enum { FATHOM_WS_SCAN_TOPK = 0, FATHOM_WS_SPARSE_ATTN = 1 } fathom_workspace_kind;
+typedef enum { FATHOM_WS_SCAN_TOPK = 0, FATHOM_WS_SPARSE_ATTN = 1, FATHOM_WS_DENSE_ATTN = 2 } fathom_workspace_kind;
 
 /* Which copy of the bit-plane store a scan reads. */
 typedef enum {
     FATHOM_SRC_STORE = 0,   /* the store in place, layout [U][D][4][cb] (HBM or pinned host memory) */
-    FATHOM_SRC_STAGING = 1  /* the staging area written by fathom_gather (host-resident regime) */
+    FATHOM_SRC_STAGING = 1, /* the staging area written by fathom_gather (host-resident regime) */
+    FATHOM_SRC_ROWS = 2     /* internal: the bf16 key rows (fathom_exact_topk) */
 } fathom_source;
 
 /* One slot of the fixed-size run list (§3.6): one per channel, zero length
@@ -247,6 +248,60 @@ int fathom_scan_topk(const fathom_shape *shape, const uint64_t *planes,
                      size_t stage_nscales, const fathom_run *runs, const float *q,
                      int32_t *topk_idx, float *topk_score, float *scores_opt,
                      void *workspace, size_t workspace_bytes, void *stream);
+
+/* Fidelity reference, exact top-k (§2 evaluation, the "exact top-k" the
+ * pages compare against): the same kept set as fathom_scan_topk (first n_sink
+ * and last n_recent tokens plus the k - |forced| others of largest score per
+ * head, ties to the lower index, ascending output) with every token scored
+ * exactly from its bf16 key row, s_h(i) = q_h . k_i in fp32, all D channels.
+ *   k_rows [units][C][D] bf16 (device or pinned host), q [units][G][D] fp32
+ *   topk_idx, topk_score, scores_opt, workspace: as fathom_scan_topk (the same
+ *   workspace size). */
+int fathom_exact_topk(const fathom_shape *shape, const uint16_t *k_rows, const float *q,
+                      int32_t *topk_idx, float *topk_score, float *scores_opt,
+                      void *workspace, size_t workspace_bytes, void *stream);
+
+/* Fidelity reference, dense attention (§2: the pages measure the relative
+ * L2 error of the sparse output against full attention): per unit and head,
+ * o_h = sum over all n tokens of softmax_i(q_h . k_i / sqrt(D)) v_i, bf16 rows,
+ * fp32 accumulation; the same arithmetic as fathom_sparse_attn over every token.
+ *   k_rows, v_rows [units][C][D] bf16 (device or pinned host), q [units][G][D]
+ *   fp32, out [units][G][D] fp32 (out)
+ *   workspace: at least fathom_workspace_size(shape, FATHOM_WS_DENSE_ATTN)
+ *   bytes, 256-byte aligned, zero-filled before its first use; left ready
+ *   for the next call. */
+int fathom_dense_attn(const fathom_shape *shape, const uint16_t *k_rows, const uint16_t *v_rows,
+                      const float *q, float *out, void *workspace, size_t workspace_bytes,
+                      void *stream);
+
+/* Fidelity diagnostic, relative L2 error per row (§4, §5: the attention
+ * output error the pages report): err[r] = ||a_r - ref_r||_2 / ||ref_r||_2
+ * with both sums in fp64; ||a_r||_2 when ref_r is all zeros.
+ *   a, ref [rows][D] fp32, err [rows] fp64 (out), all device memory.
+ *   rows == 0 enqueues nothing. */
+int fathom_rel_err(int32_t rows, int32_t D, const float *a, const float *ref, double *err,
+                   void *stream);
+
+/* Fidelity diagnostic, agreement of two kept sets (§5: agreement with the
+ * exact top-k): count[r] = number of indices row r of a shares with row r of
+ * b.  a, b [rows][k] int32, each row strictly ascending (as fathom_scan_topk
+ * and fathom_exact_topk write them); count [rows] int32 (out); device memory.
+ * Rows that are not ascending give an unspecified count. */
+int fathom_set_overlap(int32_t rows, int32_t k, const int32_t *a, const int32_t *b,
+                       int32_t *count, void *stream);
+
+/* Greedy per-layer budgets (§3.4: bits go to the layer whose error falls the
+ * most per bit, B_l in {24, ..., 128} around a target mean).  Host code, no
+ * GPU.  The budget levels are b_min + step * i, i = 0 .. levels - 1, and
+ * err [layers][levels] (host, fp64, finite) is each layer's measured error at
+ * each level.  Every layer starts at b_min; layers * (b_mean - b_min) / step
+ * times, `step` bits go to the layer with the largest err[l][i] - err[l][i+1]
+ * at its current level i (ties to the lower layer; layers at the top level
+ * take no more), so the budgets average exactly b_mean.
+ *   budgets [layers] int32 (host, out).
+ *   FATHOM_EINVAL when b_mean is not one of the levels. */
+int fathom_greedy_budgets(int32_t layers, int32_t levels, const double *err, int32_t b_min,
+                          int32_t step, int32_t b_mean, int32_t *budgets);
 
 /* Exact sparse attention over the winners (§1, §2, §3.1).  Per unit, the
  * union of the G heads' kept sets is fetched once at full precision (bf16 K

@@ -12,7 +12,9 @@
  *   §3.2 bit-plane K cache (quantiser, planes, prefix dequantisation)
  *   §3.3 per-query read depth (g_j, reverse water-filling, 30-step bisection)
  *   §3.5 KLT-rotated basis
+ *   §3.4 per-layer budgets (flat, greedy)
  *   §3.6 host-resident store as contiguous runs, fixed-size run list
+ *   §4/§5 fidelity: relative L2 error against dense and exact top-k attention
  *   Appx. A toy example (6 keys x 4 channels, 2 query heads)
  *
  * Arithmetic: fp64 for everything the pages leave open; the plan's decisions
@@ -37,6 +39,9 @@
  *      bisection is skipped and theta = lo.
  *   R9 selection ties: lower token index wins; output ascending by index.
  *   R10 attention scale 1/sqrt(D); no mass redistribution.
+ *   R21 the greedy per-layer plan starts every layer at the lowest budget and
+ *      adds one budget step at a time to the layer whose measured error falls
+ *      the most, until the budgets average the target.
  */
 #include <math.h>
 #include <stdint.h>
@@ -466,6 +471,49 @@ void oracle_attention(int n, int D, int G, const uint16_t *krows,
         for (int j = 0; j < D; ++j) out[(size_t)h * D + j] /= den;
     }
     free(logit);
+}
+
+/* ------------------------------------------------------------------------ */
+/* §4/§5 fidelity references and §3.4 greedy per-layer budgets               */
+/* ------------------------------------------------------------------------ */
+
+/* Exact score of every token, the quantity the exact top-k ranks:
+ * s_h(i) = sum_j q_hj k_ij over the key rows widened exactly, fp64.
+ *   keys [n][D] fp32, q [G][D] fp32, out [G][n]. */
+void oracle_exact_scores(int n, int D, int G, const float *keys, const float *q, double *out)
+{
+    for (int h = 0; h < G; ++h)
+        for (int i = 0; i < n; ++i) {
+            double d = 0.0;
+            for (int j = 0; j < D; ++j)
+                d += (double)q[(size_t)h * D + j] * (double)keys[(size_t)i * D + j];
+            out[(size_t)h * n + i] = d;
+        }
+}
+
+/* Greedy per-layer plan (§3.4, reading R21): budget levels b_min + step*i,
+ * i = 0 .. levels-1; err [layers][levels].  Every layer starts at level 0;
+ * layers*(b_mean-b_min)/step times, one level is added to the layer whose
+ * error drops the most on its next level (the lowest such layer on a tie),
+ * skipping layers already at the top level.  budgets [layers] (out). */
+void oracle_greedy_budgets(int layers, int levels, const double *err, int b_min, int step,
+                           int b_mean, int32_t *budgets)
+{
+    int *lev = (int *)calloc((size_t)layers, sizeof(int));
+    int incs = layers * (b_mean - b_min) / step;
+    for (int it = 0; it < incs; ++it) {
+        int best = -1;
+        double best_drop = 0.0;
+        for (int l = 0; l < layers; ++l) {
+            if (lev[l] == levels - 1) continue;
+            double drop = err[l * levels + lev[l]] - err[l * levels + lev[l] + 1];
+            if (best == -1 || drop > best_drop) { best = l; best_drop = drop; }
+        }
+        if (best == -1) break;
+        lev[best] += 1;
+    }
+    for (int l = 0; l < layers; ++l) budgets[l] = b_min + step * lev[l];
+    free(lev);
 }
 
 /* ------------------------------------------------------------------------ */

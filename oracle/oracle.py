@@ -61,6 +61,8 @@ _SIGS = {
     "oracle_scores_staged": (None, [_i, _i, _i, _P(_u32), _P(_u64), _P(_u16), _P(_u8), _P(_f), _P(_d)]),
     "oracle_select": (_i, [_i, _i, _P(_d), _i, _i, _i, _P(_i32), _P(_d)]),
     "oracle_attention": (None, [_i, _i, _i, _P(_u16), _P(_u16), _P(_f), _P(_i32), _i, _P(_d)]),
+    "oracle_exact_scores": (None, [_i, _i, _i, _P(_f), _P(_f), _P(_d)]),
+    "oracle_greedy_budgets": (None, [_i, _i, _P(_d), _i, _i, _i, _P(_i32)]),
     "oracle_calibrate": (None, [_i, _i, _P(_f), _P(_d), _P(_d), _P(_d)]),
     "oracle_eigh": (_i, [_i, _P(_d), _P(_d), _P(_d)]),
     "oracle_rotate": (None, [_i, _i, _P(_f), _P(_d), _P(_d), _P(_f)]),
@@ -255,6 +257,45 @@ def attention(krows, vrows, q, idx):
     out = np.zeros((G, D), np.float64)
     lib().oracle_attention(n, D, G, _ptr(K, np.uint16), _ptr(V, np.uint16), _ptr(qq, np.float32),
                            _ptr(ii, np.int32), int(k), _ptr(out, np.float64))
+    return out
+
+
+# ---------------------------------------------------------------- fidelity / budgets
+def exact_scores(keys, q):
+    """keys [n][D] fp32 (bf16 rows widened exactly), q [G][D] fp32 -> [G][n] fp64: q . k."""
+    k = _arr(keys, np.float32)
+    qq = _arr(q, np.float32)
+    n, D = k.shape
+    G = qq.shape[0]
+    out = np.zeros((G, n), np.float64)
+    lib().oracle_exact_scores(n, D, G, _ptr(k, np.float32), _ptr(qq, np.float32), _ptr(out, np.float64))
+    return out
+
+
+def dense_attention(krows, vrows, q):
+    """Attention of every head over all n rows (bf16 bits) -> [G][D] fp64."""
+    n = np.asarray(krows).shape[0]
+    G = np.asarray(q).shape[0]
+    idx = np.tile(np.arange(n, dtype=np.int32), (G, 1))
+    return attention(krows, vrows, q, idx)
+
+
+def rel_l2(a, ref):
+    """Relative L2 error per row, ||a - ref|| / ||ref|| (||a|| where ref is zero)."""
+    a = np.asarray(a, np.float64)
+    ref = np.asarray(ref, np.float64)
+    num = np.sqrt(np.sum((a - ref) ** 2, axis=-1))
+    den = np.sqrt(np.sum(ref ** 2, axis=-1))
+    return np.where(den > 0, num / np.where(den > 0, den, 1.0), num)
+
+
+def greedy_budgets(err, b_min, step, b_mean):
+    """err [layers][levels] -> budgets [layers] int32 (levels b_min + step*i)."""
+    e = _arr(err, np.float64)
+    L, levels = e.shape
+    out = np.zeros(L, np.int32)
+    lib().oracle_greedy_budgets(L, levels, _ptr(e, np.float64), int(b_min), int(step), int(b_mean),
+                                _ptr(out, np.int32))
     return out
 
 

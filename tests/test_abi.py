@@ -4,6 +4,7 @@ import ctypes
 import os
 import re
 
+import numpy as np
 import pytest
 
 from bit_plane_kv_gb300 import binding as B
@@ -92,7 +93,23 @@ def test_workspace_sizes_scale_with_shape(lib):
     big = B.make_shape(8, 1 << 20, 128, 4, 512)
     assert 0 < B.workspace_size(small, 0) < B.workspace_size(big, 0)
     assert 0 < B.workspace_size(small, 1) <= B.workspace_size(big, 1)
-    assert B.workspace_size(big, 2) == 0
+    assert 0 < B.workspace_size(small, 2) <= B.workspace_size(big, 2)
+    assert B.workspace_size(big, 3) == 0
+
+
+def test_fidelity_reference_calls_validate_arguments(lib):
+    d = ctypes.c_void_p(256)
+    s = B.make_shape(2, 4096, 128, 4, 64)
+    need = lib.fathom_workspace_size(ctypes.byref(s), B.WS_SCAN_TOPK)
+    rc = lib.fathom_exact_topk(ctypes.byref(s), None, d, d, d, None, d, need, None)
+    assert rc_msg(lib, rc)[0] == 1
+    rc = lib.fathom_exact_topk(ctypes.byref(s), d, d, d, d, None, d, need - 1, None)
+    assert rc_msg(lib, rc)[0] == 3
+    dn = lib.fathom_workspace_size(ctypes.byref(s), B.WS_DENSE_ATTN)
+    rc = lib.fathom_dense_attn(ctypes.byref(s), d, d, d, None, d, dn, None)
+    assert rc_msg(lib, rc) == (1, "out is NULL")
+    rc = lib.fathom_dense_attn(ctypes.byref(s), d, d, d, d, d, dn - 1, None)
+    assert rc_msg(lib, rc)[0] == 3
 
 
 def test_rotated_basis_calls_validate_arguments(lib):
@@ -118,3 +135,28 @@ def test_append_block_validates_its_block(lib):
         assert rc_msg(lib, rc)[0] == 1 and "append_block" in lib.fathom_last_error().decode()
     rc = lib.fathom_append_block(ctypes.byref(s), d, 1, 65, 0, d, d, None)
     assert rc_msg(lib, rc)[0] == 1
+
+
+def test_fidelity_helpers_validate_and_greedy_matches_oracle(lib):
+    # rows == 0 enqueues nothing; bad sizes are rejected before any launch
+    assert lib.fathom_rel_err(0, 128, None, None, None, None) == 0
+    assert rc_msg(lib, lib.fathom_rel_err(4, 0, None, None, None, None))[0] == 1
+    assert rc_msg(lib, lib.fathom_set_overlap(4, 0, None, None, None, None))[0] == 1
+    assert lib.fathom_set_overlap(0, 8, None, None, None, None) == 0
+    # the greedy allocation is host code: it runs here and must equal the oracle's
+    from oracle import oracle as O
+    rng = np.random.default_rng(41)
+    for trial in range(40):
+        L, levels = int(rng.integers(1, 9)), int(rng.integers(1, 15))
+        err = rng.uniform(0, 1, size=(L, levels))
+        if trial % 3 == 0:
+            err = np.round(err, 1)                        # many ties
+        for b_mean in sorted({24, 24 + 8 * (levels - 1), 24 + 8 * int(rng.integers(0, levels))}):
+            np.testing.assert_array_equal(B.fathom_greedy_budgets(err, 24, 8, b_mean),
+                                          O.greedy_budgets(err, 24, 8, b_mean))
+    with pytest.raises(B.FathomError):
+        B.fathom_greedy_budgets(np.zeros((2, 14)), 24, 8, 50)           # 50 is not a level
+    with pytest.raises(B.FathomError):
+        B.fathom_greedy_budgets(np.full((2, 14), np.nan), 24, 8, 48)
+    with pytest.raises(B.FathomError):
+        B.fathom_greedy_budgets(np.zeros((2, 3)), 24, 8, 48)            # above the top level (40)

@@ -443,3 +443,89 @@ def test_rotation_preserves_dot_products_and_norms():
     np.testing.assert_allclose(np.cov(cr, rowvar=False), np.diag(lam), atol=1e-5 * lam[0])
     # identity basis: rotation is centring only
     np.testing.assert_allclose(O.rotate(keys, mean, np.eye(D)), (keys - mean).astype(np.float32), rtol=1e-6)
+
+
+# ------------------------------------------------------------------ §4/§5 fidelity references
+def test_exact_scores_one_hot_keys_and_hand_example():
+    # key i is c_i times the unit vector of channel i mod D: its score for head h
+    # is q[h, i mod D] * c_i exactly, so a transposed operand, a wrong head or
+    # channel index, or a dropped sign fails
+    rng = np.random.default_rng(31)
+    D, n, G = 8, 40, 3
+    c = rng.choice([-2.0, -0.5, 0.25, 1.0, 3.0], size=n)
+    keys = np.zeros((n, D), np.float32)
+    keys[np.arange(n), np.arange(n) % D] = c
+    q = rng.normal(size=(G, D)).astype(np.float32)
+    s = O.exact_scores(keys, q)
+    assert s.shape == (G, n)
+    for h in range(G):
+        for i in range(n):
+            assert s[h, i] == float(q[h, i % D]) * c[i]
+    # a hand example: (2, 0.25, -4) . (1, -2, 0.5) = 2 - 0.5 - 2
+    assert O.exact_scores([[1.0, -2.0, 0.5]], [[2.0, 0.25, -4.0]])[0, 0] == -0.5
+
+
+def test_dense_attention_two_token_closed_form():
+    # keys 0 and a e_0, query x e_0: weights 1 / (1 + e^z) and e^z / (1 + e^z)
+    # with z = a x / sqrt(D)
+    D, a, x = 4, 1.5, 2.0
+    K = to_bf16_bits(np.array([[0, 0, 0, 0], [a, 0, 0, 0]], np.float32))
+    V = to_bf16_bits(np.array([[1, 2, 3, 4], [-1, 0.5, 0, 8]], np.float32))
+    q = np.array([[x, 0, 0, 0], [0, 1, 0, 0]], np.float32)
+    out = O.dense_attention(K, V, q)
+    z = a * x / math.sqrt(D)
+    w1 = math.exp(z) / (1 + math.exp(z))
+    v0, v1 = bf16_to_f64(V[0]), bf16_to_f64(V[1])
+    np.testing.assert_allclose(out[0], (1 - w1) * v0 + w1 * v1, rtol=1e-14)
+    np.testing.assert_allclose(out[1], 0.5 * (v0 + v1), rtol=1e-14)   # head 2 is orthogonal to both keys
+
+
+def test_rel_l2_definition():
+    assert O.rel_l2([3.0, 4.0, 0.0], [0.0, 0.0, 5.0]) == pytest.approx(math.sqrt(2.0), rel=1e-15)
+    assert O.rel_l2([3.0, 4.0], [0.0, 0.0]) == 5.0              # zero reference: the norm of a
+    np.testing.assert_array_equal(O.rel_l2(np.ones((2, 3)), np.ones((2, 3))), [0.0, 0.0])
+
+
+# ------------------------------------------------------------------ §3.4 greedy per-layer budgets
+def _convex_table(rng, layers, levels):
+    # strictly decreasing errors with strictly shrinking drops, distinct across layers
+    drops = np.sort(rng.uniform(0.01, 1.0, size=(layers, levels - 1)), axis=1)[:, ::-1]
+    err = np.zeros((layers, levels))
+    err[:, 0] = rng.uniform(5.0, 6.0, size=layers)
+    err[:, 1:] = err[:, :1] - np.cumsum(drops, axis=1)
+    return err
+
+
+@pytest.mark.parametrize("layers,levels", [(2, 4), (3, 5), (4, 4)])
+def test_greedy_budgets_are_brute_force_optimal_on_convex_errors(layers, levels):
+    # with decreasing drops, adding the largest next drop each time minimises the
+    # total error among all allocations of the same total
+    rng = np.random.default_rng(37 + layers)
+    b_min, step = 24, 8
+    for _ in range(5):
+        err = _convex_table(rng, layers, levels)
+        for m in range(levels):
+            b_mean = b_min + step * m
+            got = O.greedy_budgets(err, b_min, step, b_mean)
+            assert got.sum() == layers * b_mean
+            best, best_lev = None, None
+            for lev in itertools.product(range(levels), repeat=layers):
+                if sum(lev) != layers * m:
+                    continue
+                tot = sum(err[l, lev[l]] for l in range(layers))
+                if best is None or tot < best - 1e-12:
+                    best, best_lev = tot, lev
+            np.testing.assert_array_equal(got, b_min + step * np.array(best_lev))
+
+
+def test_greedy_budgets_hand_examples():
+    # non-convex layer 0: one step goes to layer 1 (drop 0.5 > 0.1), the next to
+    # layer 0 (0.1 > 0.05); the brute-force optimum (40, 24) is not what greedy picks
+    err = [[1.0, 0.9, 0.0], [1.0, 0.5, 0.45]]
+    np.testing.assert_array_equal(O.greedy_budgets(err, 24, 8, 32), [32, 32])
+    # equal drops: the lower layer first
+    np.testing.assert_array_equal(O.greedy_budgets([[2.0, 1.0], [2.0, 1.0]], 24, 8, 28), [32, 24])
+    # layers at the top level take no more: the target mean at the top puts all at the top
+    np.testing.assert_array_equal(O.greedy_budgets([[3.0, 2.0], [3.0, 0.0]], 24, 104, 128), [128, 128])
+    # flat target at the floor
+    np.testing.assert_array_equal(O.greedy_budgets([[3.0, 2.0], [3.0, 0.0]], 24, 8, 24), [24, 24])
