@@ -667,6 +667,43 @@ def main():
     stages = {nm: statistics.mean(e[i].elapsed_time(e[i + 1]) * 1e3 for e in stage_ev) for i, nm in enumerate(names)}
     log("[bench] per-layer stages (µs): " + ", ".join(f"{k} {v:.1f}" for k, v in stages.items()))
 
+    # rotated workloads: the calibration-free basis from the sessions' own keys
+    # (one layer of the workload, and one layer of 8 KV heads at 100k tokens)
+    klt_online = None
+    if st.rotated:
+        try:
+            B = st.B
+
+            def time_online(shape, rows, reps=3):
+                ws = B.alloc_workspace(shape, B.WS_KLT_ONLINE)
+                m = torch.empty(shape.units, shape.D, dtype=torch.float64, device="cuda")
+                V = torch.empty(shape.units, shape.D, shape.D, dtype=torch.float64, device="cuda")
+                lam = torch.empty(shape.units, shape.D, dtype=torch.float32, device="cuda")
+                for _ in range(2):
+                    B.fathom_klt_online(shape, rows, ws, m, V, lam)
+                torch.cuda.synchronize()
+                a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a0.record()
+                for _ in range(reps):
+                    B.fathom_klt_online(shape, rows, ws, m, V, lam)
+                a1.record()
+                torch.cuda.synchronize()
+                return a0.elapsed_time(a1) * 1e3 / reps
+
+            us_layer = time_online(st.shape, st.krows[0])
+            units8 = st.w.layer_units(0)[:8]
+            rows100k = torch.stack([synth.unit_keys(st.w, u, "cuda", n=100000) for u in units8]).to(torch.bfloat16)
+            us_100k = time_online(B.make_shape(8, 100000, st.D, st.G, 1, 0, 0), rows100k)
+            del rows100k
+            klt_online = {"us_per_layer": us_layer, "layer_units": st.H, "layer_tokens": st.n,
+                          "us_8_heads_100k_tokens": us_100k,
+                          "note": "fathom_klt_online (mean, covariance, fp32 Jacobi) on each unit's own keys, "
+                                  "CUDA events, mean of 3 calls after 2 warm-up calls"}
+            log(f"[bench] online basis: {klt_online}")
+        except Exception as exc:   # reported as missing, never as a number
+            log(f"[bench] online basis timing unavailable: {exc}")
+            klt_online = {"error": str(exc)[:200]}
+
     # fidelity of the timed path (untimed): layer 0 at the last timed step's query,
     # against dense attention and against attention over the exact top-k
     fidelity = None
@@ -677,15 +714,37 @@ def main():
             st.layer(0, q0)
             res = FID.compare(st.shape, st.krows[0], st.vrows[0], q0, st.idx, st.out[0],
                               workspaces={"scan": st.ws, "attn": st.aws})
+            # the same kept sets attended with keys rebuilt from the store's four planes
+            # (no bf16 K rows), timed over 3 calls
+            B = st.B
+            qk = st.qrot[0] if st.rotated else q0
+            pl_out = torch.empty_like(st.out[0])
+            B.fathom_sparse_attn_planes(st.shape, st.planes[0], st.scales[0], st.vrows[0], qk, st.idx, st.aws, out=pl_out)
+            torch.cuda.synchronize()
+            p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            p0.record()
+            for _ in range(3):
+                B.fathom_sparse_attn_planes(st.shape, st.planes[0], st.scales[0], st.vrows[0], qk, st.idx, st.aws,
+                                            out=pl_out)
+            p1.record()
+            torch.cuda.synchronize()
+            dense0 = B.fathom_dense_attn(st.shape, st.krows[0], st.vrows[0], q0,
+                                         B.alloc_workspace(st.shape, B.WS_DENSE_ATTN))
+            rel_pl = B.fathom_rel_err(pl_out, dense0).cpu().numpy()
+            rel_pl_rows = B.fathom_rel_err(pl_out, st.out[0]).cpu().numpy()
             fidelity = {
                 "layer": 0, "budget": st.budgets[0] if not st.fixed else "fixed 136-bit",
+                "planes_k_rel_l2_vs_dense_mean": float(rel_pl.mean()),
+                "planes_k_rel_l2_vs_bf16_k_mean": float(rel_pl_rows.mean()),
+                "planes_k_attn_us_per_layer": p0.elapsed_time(p1) * 1e3 / 3,
                 "rel_l2_vs_dense_mean": float(res["rel_dense"].mean()),
                 "rel_l2_vs_dense_max": float(res["rel_dense"].max()),
                 "rel_l2_vs_exact_topk_mean": float(res["rel_exact"].mean()),
                 "exact_topk_rel_l2_vs_dense_mean": float(res["exact_vs_dense"].mean()),
                 "exact_topk_overlap_mean": float(res["overlap"].mean()),
                 "note": "relative L2 error of the attention output per (unit, head), averaged; overlap = "
-                        "fraction of the exact top-k (q . k over the bf16 rows) the scan kept",
+                        "fraction of the exact top-k (q . k over the bf16 rows) the scan kept; planes_k: the "
+                        "kept sets attended with keys rebuilt from the store's four planes instead of bf16 K rows",
             }
             log(f"[bench] fidelity: {fidelity}")
         except Exception as exc:   # reported as missing, never as a number
@@ -746,6 +805,7 @@ def main():
         "stages_us_per_layer": stages,
         "append_us_per_layer": append_us,
         "fidelity": fidelity,
+        "klt_online": klt_online,
         "timing": "one CUDA graph replay per step" if use_graph else "eager launches",
         "graph_warmup_replays": graph_warmup,
         "step_ms_min_median_max": [min(step_ms), statistics.median(step_ms), max(step_ms)],

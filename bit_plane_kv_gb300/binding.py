@@ -17,7 +17,7 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "_build", "libfathom.so")
 
 F32, BF16 = 0, 1
-WS_SCAN_TOPK, WS_SPARSE_ATTN, WS_DENSE_ATTN = 0, 1, 2
+WS_SCAN_TOPK, WS_SPARSE_ATTN, WS_DENSE_ATTN, WS_KLT_ONLINE = 0, 1, 2, 3
 SRC_STORE, SRC_STAGING = 0, 1
 MAX_D, MAX_G, MAX_K = 128, 8, 2048
 
@@ -58,7 +58,10 @@ SIGNATURES = {
     "fathom_exact_topk": (ctypes.c_int, [ctypes.POINTER(Shape), _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "fathom_sparse_attn": (ctypes.c_int, [ctypes.POINTER(Shape), _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "fathom_dense_attn": (ctypes.c_int, [ctypes.POINTER(Shape), _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "fathom_sparse_attn_planes": (ctypes.c_int, [ctypes.POINTER(Shape), _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz,
+                                                 _vp]),
     "fathom_sparse_attn_noalloc": (ctypes.c_int, [ctypes.POINTER(Shape), _vp, _vp, _vp, _vp, _vp, _vp]),
+    "fathom_klt_online": (ctypes.c_int, [ctypes.POINTER(Shape), _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "fathom_rel_err": (ctypes.c_int, [_i32, _i32, _vp, _vp, _vp, _vp]),
     "fathom_set_overlap": (ctypes.c_int, [_i32, _i32, _vp, _vp, _vp, _vp]),
     "fathom_greedy_budgets": (ctypes.c_int, [_i32, _i32, _vp, _i32, _i32, _i32, _vp]),
@@ -339,6 +342,26 @@ def fathom_dense_attn(shape: Shape, k_rows, v_rows, q, workspace, out=None, stre
     return out
 
 
+def fathom_klt_online(shape: Shape, k_rows, workspace=None, mean=None, V=None, lam=None, stream=None):
+    """Per-unit rotated basis from the unit's own key rows [U][cap][D] bf16 ->
+    (mean [U][D] f64, V [U][D][D] f64, lambda [U][D] f32)."""
+    _check(k_rows, "k_rows", (torch.bfloat16, torch.int16), (shape.units, shape.cap, shape.D))
+    dev = "cuda"
+    if workspace is None:
+        workspace = alloc_workspace(shape, WS_KLT_ONLINE, device=dev)
+    _check(workspace, "workspace", (torch.uint8,))
+    U, D = shape.units, shape.D
+    if mean is None:
+        mean = torch.empty(U, D, dtype=torch.float64, device=dev)
+    if V is None:
+        V = torch.empty(U, D, D, dtype=torch.float64, device=dev)
+    if lam is None:
+        lam = torch.empty(U, D, dtype=torch.float32, device=dev)
+    _call("fathom_klt_online", ctypes.byref(shape), _p(k_rows), _p(mean), _p(V), _p(lam), _p(workspace),
+          workspace.numel(), _stream(stream))
+    return mean, V, lam
+
+
 def fathom_rel_err(a, ref, err=None, stream=None):
     """a, ref [..., D] fp32 (device) -> err [...] fp64: ||a - ref|| / ||ref|| per row."""
     _check(a, "a", (torch.float32,))
@@ -374,6 +397,24 @@ def fathom_greedy_budgets(err, b_min, step, b_mean):
     out = np.zeros(e.shape[0], dtype=np.int32)
     _call("fathom_greedy_budgets", e.shape[0], e.shape[1], e.ctypes.data, int(b_min), int(step), int(b_mean),
           out.ctypes.data)
+    return out
+
+
+def fathom_sparse_attn_planes(shape: Shape, planes, scales, v_rows, q, topk_idx, workspace, out=None,
+                              stream=None):
+    """Sparse attention with the winners' keys rebuilt from the store's four planes.
+    planes [U][D][4][cb], scales [U][D][cb], v_rows [U][cap][D] bf16 -> out [U][G][D] fp32."""
+    cb = nblocks(shape.cap)
+    _check(planes, "planes", (torch.int64,), (shape.units, shape.D, 4, cb))
+    _check(scales, "scales", (torch.int16,), (shape.units, shape.D, cb))
+    _check(v_rows, "v_rows", (torch.bfloat16, torch.int16), (shape.units, shape.cap, shape.D))
+    _check(q, "q", (torch.float32,), (shape.units, shape.G, shape.D))
+    _check(topk_idx, "topk_idx", (torch.int32,), (shape.units, shape.G, shape.k))
+    _check(workspace, "workspace", (torch.uint8,))
+    if out is None:
+        out = torch.empty(shape.units, shape.G, shape.D, dtype=torch.float32, device=q.device)
+    _call("fathom_sparse_attn_planes", ctypes.byref(shape), _p(planes), _p(scales), _p(v_rows), _p(q),
+          _p(topk_idx), _p(out), _p(workspace), workspace.numel(), _stream(stream))
     return out
 
 

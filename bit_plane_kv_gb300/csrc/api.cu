@@ -377,6 +377,10 @@ size_t fathom_workspace_size(const fathom_shape *shape, int which) {
     if (which == FATHOM_WS_SCAN_TOPK) return scan_workspace_layout(*shape).total;
     if (which == FATHOM_WS_SPARSE_ATTN) return attn_workspace_layout(*shape).total;
     if (which == FATHOM_WS_DENSE_ATTN) return dense_workspace_layout(*shape).total;
+    if (which == FATHOM_WS_KLT_ONLINE) {
+        if (shape->n < 2) { set_error("klt_online needs n >= 2 tokens"); return 0; }
+        return klt_online_layout(*shape).total;
+    }
     return 0;
 }
 
@@ -431,6 +435,29 @@ int fathom_exact_topk(const fathom_shape *shape, const uint16_t *k_rows, const f
                             topk_idx, topk_score, scores_opt, workspace, (cudaStream_t)stream);
 }
 
+int fathom_sparse_attn_planes(const fathom_shape *shape, const uint64_t *planes, const uint16_t *scales,
+                              const uint16_t *v_rows, const float *q, const int32_t *topk_idx, float *out,
+                              void *workspace, size_t workspace_bytes, void *stream) {
+    g_err[0] = 0;
+    int rc = check_shape(shape, true);
+    if (rc) return rc;
+    NONNULL(planes);
+    NONNULL(scales);
+    NONNULL(v_rows);
+    NONNULL(q);
+    NONNULL(topk_idx);
+    NONNULL(out);
+    NONNULL(workspace);
+    const size_t need = attn_workspace_layout(*shape).total;
+    if (workspace_bytes < need) {
+        set_error("sparse_attn_planes workspace too small: %zu < %zu bytes", workspace_bytes, need);
+        return FATHOM_ENOMEM;
+    }
+    if (((uintptr_t)workspace & 255) != 0) { set_error("workspace must be 256-byte aligned"); return FATHOM_EINVAL; }
+    return launch_sparse_attn_planes(*shape, planes, scales, v_rows, q, topk_idx, out, workspace,
+                                     (cudaStream_t)stream);
+}
+
 int fathom_dense_attn(const fathom_shape *shape, const uint16_t *k_rows, const uint16_t *v_rows,
                       const float *q, float *out, void *workspace, size_t workspace_bytes, void *stream) {
     g_err[0] = 0;
@@ -448,6 +475,26 @@ int fathom_dense_attn(const fathom_shape *shape, const uint16_t *k_rows, const u
     }
     if (((uintptr_t)workspace & 255) != 0) { set_error("workspace must be 256-byte aligned"); return FATHOM_EINVAL; }
     return launch_dense_attn(*shape, k_rows, v_rows, q, out, workspace, (cudaStream_t)stream);
+}
+
+int fathom_klt_online(const fathom_shape *shape, const uint16_t *k_rows, double *mean, double *V, float *lambda,
+                      void *workspace, size_t workspace_bytes, void *stream) {
+    g_err[0] = 0;
+    int rc = check_shape(shape, false);
+    if (rc) return rc;
+    if (shape->n < 2) { set_error("klt_online needs n >= 2 tokens (n=%d)", shape->n); return FATHOM_EINVAL; }
+    NONNULL(k_rows);
+    NONNULL(mean);
+    NONNULL(V);
+    NONNULL(lambda);
+    NONNULL(workspace);
+    const size_t need = klt_online_layout(*shape).total;
+    if (workspace_bytes < need) {
+        set_error("klt_online workspace too small: %zu < %zu bytes", workspace_bytes, need);
+        return FATHOM_ENOMEM;
+    }
+    if (((uintptr_t)workspace & 255) != 0) { set_error("workspace must be 256-byte aligned"); return FATHOM_EINVAL; }
+    return launch_klt_online(*shape, k_rows, mean, V, lambda, workspace, (cudaStream_t)stream);
 }
 
 int fathom_rel_err(int32_t rows, int32_t D, const float *a, const float *ref, double *err, void *stream) {

@@ -144,9 +144,20 @@ int launch_sparse_attn(const fathom_shape &s, const uint16_t *krows, const uint1
                        const float *q, const int32_t *idx, float *out, void *ws, cudaStream_t st);
 int launch_dense_attn(const fathom_shape &s, const uint16_t *krows, const uint16_t *vrows, const float *q,
                       float *out, void *ws, cudaStream_t st);
+int launch_sparse_attn_planes(const fathom_shape &s, const uint64_t *planes, const uint16_t *scales,
+                              const uint16_t *vrows, const float *q, const int32_t *idx, float *out, void *ws,
+                              cudaStream_t st);
 int launch_sparse_attn_noalloc(const fathom_shape &s, const uint16_t *krows, const uint16_t *vrows,
                                const float *q, const int32_t *idx, float *out, cudaStream_t st);
 
+// Online rotated basis: partial sums per (unit, slice of tps tokens).
+struct KltOnlineWs {
+    int slices = 1, tps = 0;
+    size_t mean_off = 0, cov_off = 0, total = 0;
+};
+KltOnlineWs klt_online_layout(const fathom_shape &s);
+int launch_klt_online(const fathom_shape &s, const uint16_t *rows, double *mean, double *vec, float *lambda,
+                      void *ws, cudaStream_t st);
 int launch_rel_err(int rows, int D, const float *a, const float *ref, double *err, cudaStream_t st);
 int launch_set_overlap(int rows, int k, const int32_t *a, const int32_t *b, int32_t *count, cudaStream_t st);
 int greedy_budgets(int layers, int levels, const double *err, int b_min, int step, int b_mean, int32_t *budgets);

@@ -332,4 +332,313 @@ int launch_rotate_query(const fathom_shape &s, const float *q, int groups, const
     return launch_status("klt_rotate_query_kernel");
 }
 
+
+// ---------------------------------------------------------------- online basis
+// A session's own keys give its basis (Fathom Appx. D: mean, eigenbasis and
+// eigenvalues without calibration data).  fp64 runs at a small fraction of
+// the fp32 rate on this part, so the per-token work is fp32 with fp64 only
+// where partial results are combined:
+//   klt_online_mean_kernel  fp32 sums over runs of 64 tokens, folded in fp64,
+//                           one partial per (unit, slice)
+//   klt_online_cov_kernel   the slices' partials summed in a fixed order give
+//                           mu; rows centred in fp32 and staged 32 tokens at a
+//                           time; each thread accumulates an 8 x 8 tile of the
+//                           upper triangle (a per-stage fp32 sum added into a
+//                           running fp32 total), one partial per slice
+//   klt_online_reduce_kernel  covariance = fixed-order fp64 sum of the
+//                           slices' partials / (n - 1), mirrored
+//   klt_eigh32_kernel       parallel cyclic Jacobi in fp32 (round-robin
+//                           ordering: D / 2 disjoint pairs rotated at once)
+constexpr int kOnThreads = 160;       // 136 upper-triangle tiles of 8 x 8 (+ staging helpers)
+constexpr int kOnTiles = 136;
+constexpr int kOnStage = 32;          // tokens staged per round
+constexpr int kOnMeanThreads = 256;
+constexpr int kEig32Threads = 256;
+constexpr int kEigPad = FATHOM_MAX_D + 1;
+
+__device__ __forceinline__ float bf16_to_f32(uint16_t b) { return __uint_as_float(((uint32_t)b) << 16); }
+
+// Grid (slices, units).  Thread t sums channel t % 128 over the slice's tokens
+// of parity t / 128, in fp32 runs of 64 tokens folded into fp64.
+__global__ void __launch_bounds__(kOnMeanThreads)
+klt_online_mean_kernel(int n, int ctok, int D, int tps, const uint16_t *__restrict__ rows,
+                       double *__restrict__ part) {
+    __shared__ double red[kOnMeanThreads];
+    const int s = blockIdx.x, u = blockIdx.y, tid = threadIdx.x;
+    const int j = tid % FATHOM_MAX_D, par = tid / FATHOM_MAX_D;
+    const int i0 = s * tps, i1 = min(n, i0 + tps);
+    double acc = 0.0;
+    if (j < D) {
+        const uint16_t *base = rows + (size_t)u * ctok * D + j;
+        for (int r0 = i0 + par; r0 < i1; r0 += 128) {
+            float run = 0.0f;
+            const int r1 = min(i1, r0 + 128);
+            for (int i = r0; i < r1; i += 2) run += bf16_to_f32(__ldg(base + (size_t)i * D));
+            acc += (double)run;
+        }
+    }
+    red[tid] = acc;
+    __syncthreads();
+    if (tid < FATHOM_MAX_D && tid < D)
+        part[((size_t)u * gridDim.x + s) * FATHOM_MAX_D + tid] = red[tid] + red[tid + FATHOM_MAX_D];
+}
+
+// Grid (slices, units), kOnThreads threads.
+__global__ void __launch_bounds__(kOnThreads)
+klt_online_cov_kernel(int n, int ctok, int D, int tps, const uint16_t *__restrict__ rows,
+                      const double *__restrict__ mean_part, double *__restrict__ mean_out,
+                      float *__restrict__ cov_part) {
+    __shared__ __align__(16) float xs[kOnStage][FATHOM_MAX_D];
+    __shared__ float mu[FATHOM_MAX_D];
+    const int s = blockIdx.x, u = blockIdx.y, tid = threadIdx.x;
+    const int S = gridDim.x;
+    if (tid < FATHOM_MAX_D) {
+        double m = 0.0;
+        if (tid < D) {
+            for (int q = 0; q < S; ++q) m += mean_part[((size_t)u * S + q) * FATHOM_MAX_D + tid];
+            m /= (double)n;
+            if (s == 0) mean_out[(size_t)u * D + tid] = m;
+        }
+        mu[tid] = __double2float_rn(m);
+    }
+    // this thread's tile (ti <= tj) of the upper triangle
+    int ti = 0, tj = 0;
+    {
+        int t = tid < kOnTiles ? tid : 0;
+        while (t >= 16 - ti) { t -= 16 - ti; ++ti; }
+        tj = ti + t;
+    }
+    float tot[8][8], stg[8][8];
+#pragma unroll
+    for (int a = 0; a < 8; ++a)
+#pragma unroll
+        for (int b = 0; b < 8; ++b) tot[a][b] = 0.0f;
+    const int i0 = s * tps, i1 = min(n, i0 + tps);
+    const uint16_t *base = rows + (size_t)u * ctok * D;
+    for (int r0 = i0; r0 < i1; r0 += kOnStage) {
+        __syncthreads();   // mu ready / the previous stage's reads are done
+        for (int e = tid; e < kOnStage * FATHOM_MAX_D; e += kOnThreads) {
+            const int i = e / FATHOM_MAX_D, j = e % FATHOM_MAX_D;
+            float v = 0.0f;
+            if (r0 + i < i1 && j < D) v = bf16_to_f32(__ldg(base + (size_t)(r0 + i) * D + j)) - mu[j];
+            xs[i][j] = v;
+        }
+        __syncthreads();
+        if (tid < kOnTiles) {
+#pragma unroll
+            for (int a = 0; a < 8; ++a)
+#pragma unroll
+                for (int b = 0; b < 8; ++b) stg[a][b] = 0.0f;
+            const int rn = min(kOnStage, i1 - r0);
+            for (int i = 0; i < rn; ++i) {
+                const float4 a0 = *reinterpret_cast<const float4 *>(&xs[i][8 * ti]);
+                const float4 a1 = *reinterpret_cast<const float4 *>(&xs[i][8 * ti + 4]);
+                const float4 b0 = *reinterpret_cast<const float4 *>(&xs[i][8 * tj]);
+                const float4 b1 = *reinterpret_cast<const float4 *>(&xs[i][8 * tj + 4]);
+                const float va[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+                const float vb[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+                for (int a = 0; a < 8; ++a)
+#pragma unroll
+                    for (int b = 0; b < 8; ++b) stg[a][b] = fmaf(va[a], vb[b], stg[a][b]);
+            }
+#pragma unroll
+            for (int a = 0; a < 8; ++a)
+#pragma unroll
+                for (int b = 0; b < 8; ++b) tot[a][b] += stg[a][b];
+        }
+    }
+    if (tid < kOnTiles) {
+        float *P = cov_part + ((size_t)u * S + s) * FATHOM_MAX_D * FATHOM_MAX_D;
+#pragma unroll
+        for (int a = 0; a < 8; ++a) {
+            float4 *dst = reinterpret_cast<float4 *>(P + (size_t)(8 * ti + a) * FATHOM_MAX_D + 8 * tj);
+            dst[0] = make_float4(tot[a][0], tot[a][1], tot[a][2], tot[a][3]);
+            dst[1] = make_float4(tot[a][4], tot[a][5], tot[a][6], tot[a][7]);
+        }
+    }
+}
+
+// Grid (D * D / 256 rounded up, units): one entry per thread, fp64 sum over the
+// slices in order, / (n - 1); entries below the diagonal read the mirror.
+__global__ void __launch_bounds__(256)
+klt_online_reduce_kernel(int n, int D, int S, const float *__restrict__ cov_part, double *__restrict__ cov) {
+    const int u = blockIdx.y;
+    const int e = blockIdx.x * 256 + threadIdx.x;
+    if (e >= D * D) return;
+    const int a = e / D, b = e % D;
+    const int lo = min(a, b), hi = max(a, b);
+    const float *P = cov_part + (size_t)u * S * FATHOM_MAX_D * FATHOM_MAX_D + (size_t)lo * FATHOM_MAX_D + hi;
+    double acc = 0.0;
+    for (int q = 0; q < S; ++q) acc += (double)P[(size_t)q * FATHOM_MAX_D * FATHOM_MAX_D];
+    cov[(size_t)u * D * D + e] = acc / (double)(n - 1);
+}
+
+// One CTA per unit.  On entry vec holds the covariance (fp64); on exit the
+// eigenvectors (unit-length columns, fp32 values widened), eigenvalues descending, each
+// vector's largest-magnitude component positive.  Round-robin ordering over
+// Dp = D rounded up to even indices: in step t, pair 0 is (0, 1 + t mod (Dp - 1))
+// and pair i > 0 is (1 + (t + i) mod (Dp - 1), 1 + (t - i) mod (Dp - 1)); every
+// pair meets once per sweep of Dp - 1 steps.  A pair rotates when
+// |a_pr| > 2^-23 sqrt(|a_pp a_rr|); sweeps stop when one rotates nothing, when
+// the off-diagonal square sum is <= 1e-12 of the total, or after 24 sweeps.
+__global__ void __launch_bounds__(kEig32Threads)
+klt_eigh32_kernel(int D, double *__restrict__ vec, float *__restrict__ lambda) {
+    extern __shared__ __align__(16) float esm[];
+    float *A = esm;                                  // [128][129]
+    float *V = esm + FATHOM_MAX_D * kEigPad;         // [128][129]
+    __shared__ int pp[FATHOM_MAX_D / 2], pr[FATHOM_MAX_D / 2];
+    __shared__ float pc[FATHOM_MAX_D / 2], ps[FATHOM_MAX_D / 2];
+    __shared__ float red[2][kEig32Threads / 32];
+    __shared__ float lam_s[FATHOM_MAX_D];
+    __shared__ int rank_s[FATHOM_MAX_D];
+    const int u = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int Dp = D + (D & 1), half = Dp / 2;
+    double *Vg = vec + (size_t)u * D * D;
+    for (int e = tid; e < Dp * Dp; e += kEig32Threads) {
+        const int x = e / Dp, y = e % Dp;
+        A[x * kEigPad + y] = (x < D && y < D) ? __double2float_rn(Vg[(size_t)x * D + y]) : 0.0f;
+        V[x * kEigPad + y] = (x == y) ? 1.0f : 0.0f;
+    }
+    __syncthreads();
+    for (int sweep = 0; sweep < 24; ++sweep) {
+        float off = 0.0f, tot = 0.0f;
+        for (int e = tid; e < Dp * Dp; e += kEig32Threads) {
+            const int x = e / Dp, y = e % Dp;
+            const float v = A[x * kEigPad + y] * A[x * kEigPad + y];
+            tot += v;
+            if (x != y) off += v;
+        }
+#pragma unroll
+        for (int o = 16; o; o >>= 1) {
+            off += __shfl_xor_sync(0xffffffffu, off, o);
+            tot += __shfl_xor_sync(0xffffffffu, tot, o);
+        }
+        if (lane == 0) { red[0][warp] = off; red[1][warp] = tot; }
+        __syncthreads();
+        off = 0.0f; tot = 0.0f;
+        for (int w = 0; w < kEig32Threads / 32; ++w) { off += red[0][w]; tot += red[1][w]; }
+        if (off <= 1e-12f * tot || off == 0.0f) break;          // the same decision in every thread
+        int rotated = 0;
+        for (int t = 0; t < Dp - 1; ++t) {
+            if (tid < half) {
+                int p, r;
+                if (tid == 0) { p = 0; r = 1 + t % (Dp - 1); }
+                else {
+                    p = 1 + (t + tid) % (Dp - 1);
+                    r = 1 + (t - tid + (Dp - 1)) % (Dp - 1);
+                }
+                if (p > r) { const int q = p; p = r; r = q; }
+                const float apr = A[p * kEigPad + r], app = A[p * kEigPad + p], arr = A[r * kEigPad + r];
+                float c = 1.0f, sn = 0.0f;
+                if (apr != 0.0f && fabsf(apr) > 1.1920929e-7f * sqrtf(fabsf(app * arr))) {
+                    const float th = (arr - app) / (2.0f * apr);
+                    const float tt = fabsf(th) > 1e18f ? 0.5f / th
+                                                       : (th >= 0.0f ? 1.0f : -1.0f) / (fabsf(th) + sqrtf(1.0f + th * th));
+                    c = 1.0f / sqrtf(1.0f + tt * tt);
+                    sn = tt * c;
+                    rotated = 1;
+                }
+                pp[tid] = p; pr[tid] = r; pc[tid] = c; ps[tid] = sn;
+            }
+            __syncthreads();
+            for (int e = tid; e < half * Dp; e += kEig32Threads) {   // columns p and r of A and V
+                const int x = e % Dp, i = e / Dp;
+                const int p = pp[i], r = pr[i];
+                const float c = pc[i], sn = ps[i];
+                const float axp = A[x * kEigPad + p], axr = A[x * kEigPad + r];
+                A[x * kEigPad + p] = c * axp - sn * axr;
+                A[x * kEigPad + r] = sn * axp + c * axr;
+                const float vxp = V[x * kEigPad + p], vxr = V[x * kEigPad + r];
+                V[x * kEigPad + p] = c * vxp - sn * vxr;
+                V[x * kEigPad + r] = sn * vxp + c * vxr;
+            }
+            __syncthreads();
+            for (int e = tid; e < half * Dp; e += kEig32Threads) {   // rows p and r of A
+                const int x = e % Dp, i = e / Dp;
+                const int p = pp[i], r = pr[i];
+                const float c = pc[i], sn = ps[i];
+                const float apx = A[p * kEigPad + x], arx = A[r * kEigPad + x];
+                A[p * kEigPad + x] = c * apx - sn * arx;
+                A[r * kEigPad + x] = sn * apx + c * arx;
+            }
+            __syncthreads();
+        }
+        if (!__syncthreads_or(rotated)) break;
+    }
+    // eigenvalues in descending order (ties: lower index first), vectors permuted alike
+    if (tid < D) lam_s[tid] = A[tid * kEigPad + tid];
+    __syncthreads();
+    if (tid < D) {
+        int rk = 0;
+        for (int y = 0; y < D; ++y) rk += (lam_s[y] > lam_s[tid] || (lam_s[y] == lam_s[tid] && y < tid)) ? 1 : 0;
+        rank_s[tid] = rk;
+        lambda[(size_t)u * D + rk] = lam_s[tid];
+    }
+    __syncthreads();
+    for (int e = tid; e < D * D; e += kEig32Threads) {   // A <- V with columns moved to their ranks
+        const int row = e / D, col = e % D;
+        A[row * kEigPad + rank_s[col]] = V[row * kEigPad + col];
+    }
+    __syncthreads();
+    if (tid < D) {
+        // column tid: unit length again (the fp32 rotations let c^2 + s^2 drift from
+        // 1 by an ulp each, which accumulates over the sweeps; norm in fp64) and its
+        // largest-magnitude component (first of equals) positive
+        int arg = 0;
+        double nn = 0.0;
+        for (int y = 0; y < D; ++y) {
+            const float a = A[y * kEigPad + tid];
+            nn += (double)a * (double)a;
+            if (fabsf(a) > fabsf(A[arg * kEigPad + tid])) arg = y;
+        }
+        const float sc = (float)((A[arg * kEigPad + tid] < 0.0f ? -1.0 : 1.0) / sqrt(nn));
+        for (int y = 0; y < D; ++y) A[y * kEigPad + tid] *= sc;
+    }
+    __syncthreads();
+    for (int e = tid; e < D * D; e += kEig32Threads) Vg[e] = (double)A[(e / D) * kEigPad + e % D];
+}
+
+static size_t klt_align(size_t x) { return (x + 255) & ~(size_t)255; }
+
+KltOnlineWs klt_online_layout(const fathom_shape &s) {
+    int sms = device_sm_count();
+    if (sms <= 0) sms = 152;
+    KltOnlineWs w;
+    // about four CTAs per SM over the units, at least 512 tokens per slice
+    int S = (4 * sms + s.units - 1) / s.units;
+    const int max_s = (s.n + 511) / 512;
+    S = S < 1 ? 1 : (S > max_s ? max_s : S);
+    w.tps = ((s.n + S - 1) / S + kOnStage - 1) / kOnStage * kOnStage;
+    w.slices = (s.n + w.tps - 1) / w.tps;
+    w.mean_off = 0;
+    w.cov_off = klt_align((size_t)s.units * w.slices * FATHOM_MAX_D * sizeof(double));
+    w.total = klt_align(w.cov_off + (size_t)s.units * w.slices * FATHOM_MAX_D * FATHOM_MAX_D * sizeof(float));
+    return w;
+}
+
+int launch_klt_online(const fathom_shape &s, const uint16_t *rows, double *mean, double *vec, float *lambda,
+                      void *ws, cudaStream_t st) {
+    if (s.units > 65535) { set_error("klt_online: too many units for one launch"); return FATHOM_EINVAL; }
+    const KltOnlineWs w = klt_online_layout(s);
+    char *base = (char *)ws;
+    double *mpart = (double *)(base + w.mean_off);
+    float *cpart = (float *)(base + w.cov_off);
+    const int ctok = cap_tokens(s);
+    klt_online_mean_kernel<<<dim3(w.slices, s.units), kOnMeanThreads, 0, st>>>(s.n, ctok, s.D, w.tps, rows, mpart);
+    int rc = launch_status("klt_online_mean_kernel");
+    if (rc) return rc;
+    klt_online_cov_kernel<<<dim3(w.slices, s.units), kOnThreads, 0, st>>>(s.n, ctok, s.D, w.tps, rows, mpart, mean,
+                                                                          cpart);
+    rc = launch_status("klt_online_cov_kernel");
+    if (rc) return rc;
+    klt_online_reduce_kernel<<<dim3((s.D * s.D + 255) / 256, s.units), 256, 0, st>>>(s.n, s.D, w.slices, cpart, vec);
+    rc = launch_status("klt_online_reduce_kernel");
+    if (rc) return rc;
+    const size_t smem = 2 * (size_t)FATHOM_MAX_D * kEigPad * sizeof(float);
+    ensure_smem(klt_eigh32_kernel, smem);
+    klt_eigh32_kernel<<<s.units, kEig32Threads, smem, st>>>(s.D, vec, lambda);
+    return launch_status("klt_eigh32_kernel");
+}
+
 }  // namespace fathom

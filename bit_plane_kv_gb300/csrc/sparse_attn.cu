@@ -23,6 +23,16 @@ namespace fathom {
 constexpr int NA = kAttnThreads;
 constexpr int kWarps = NA / 32;
 
+// Where the batch step reads K: bf16 rows [units][ctok][D], or the 4-bit store
+// ([units][D][4][cb] planes, [units][D][cb] fp16 scales) with every winner's key
+// rebuilt from all four planes.
+struct KSource {
+    const uint16_t *rows;
+    const uint64_t *planes;
+    const uint16_t *scales;
+    int cb;
+};
+
 // Rows per warp batch: RB rows x G heads = S dot products, reduced together.
 template <int G>
 struct AttnBatch {
@@ -185,25 +195,54 @@ __device__ __forceinline__ void attn_finish(AttnHeader &sm, unsigned char *asmem
 }
 
 // One batch of RB rows (token ti[r] of the unit, attended by the heads in
-// mask[r]; mask 0: no row): loads K and V (bf16), the G dot products of every
+// mask[r]; mask 0: no row): loads K (bf16 rows, or kPlanes: rebuilt from the
+// store's four planes) and V (bf16), the G dot products of every
 // row with one transpose reduction across the warp, and the online-softmax
 // update of every head's state.
-template <int G, bool kVec>
+template <int G, bool kVec, bool kPlanes>
 __device__ __forceinline__ void attn_batch(const unsigned (&mask)[AttnBatch<G>::RB], const int (&ti)[AttnBatch<G>::RB],
-                                           const uint16_t *__restrict__ krows, const uint16_t *__restrict__ vrows,
+                                           const KSource &ks, const uint16_t *__restrict__ vrows, int u,
                                            size_t ubase, int D, float scale, const float (&qv)[G][4],
                                            float (&m_h)[G], float (&l_h)[G], float (&o_h)[G][4], float *pb) {
     constexpr int RB = AttnBatch<G>::RB, S = AttnBatch<G>::S;
     const int lane = threadIdx.x & 31;
     const int v = lane & (S - 1), vr = v / G, vh = v % G;   // this lane's (row, head) slot
     uint2 kp[RB], vp[RB];                      // bf16 pairs (kVec)
-    float kv[RB][4], vv[RB][4];                // general path
+    float kv[RB][4], vv[RB][4];                // general path (and keys rebuilt from the planes)
 #pragma unroll
     for (int r = 0; r < RB; ++r) {
         const unsigned m = mask[r];
-        const uint16_t *kr = krows + (ubase + (m ? ti[r] : 0)) * D;
+        const uint16_t *kr = ks.rows + (ubase + (m ? ti[r] : 0)) * D;
         const uint16_t *vr_ = vrows + (ubase + (m ? ti[r] : 0)) * D;
-        if (kVec) {
+        if constexpr (kPlanes) {
+            // code c of token i, channel j: bit i % 64 of the block's four plane
+            // words (plane 0 = MSB); the key is (c - 7.5) a / 8, exact in fp32
+            const int beta = m ? (ti[r] >> 6) : 0, sh = m ? (ti[r] & 63) : 0;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const int j = kVec ? 4 * lane + c : lane + 32 * c;
+                float kx = 0.0f;
+                if (m && j < D) {
+                    const size_t ch = (size_t)u * D + j;
+                    const uint64_t *pw = ks.planes + ch * 4 * (size_t)ks.cb + beta;
+                    const uint32_t code = (uint32_t)((__ldg(pw) >> sh) & 1u) << 3 |
+                                          (uint32_t)((__ldg(pw + ks.cb) >> sh) & 1u) << 2 |
+                                          (uint32_t)((__ldg(pw + 2 * (size_t)ks.cb) >> sh) & 1u) << 1 |
+                                          (uint32_t)((__ldg(pw + 3 * (size_t)ks.cb) >> sh) & 1u);
+                    const float a = __half2float(__ushort_as_half(__ldg(ks.scales + ch * ks.cb + beta)));
+                    kx = ((float)code - 7.5f) * (a * 0.125f);
+                }
+                kv[r][c] = kx;
+            }
+            if (kVec) vp[r] = m ? __ldg(reinterpret_cast<const uint2 *>(vr_) + lane) : make_uint2(0u, 0u);
+            else {
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const int j = lane + 32 * c;
+                    vv[r][c] = (m && j < D) ? __uint_as_float(((uint32_t)__ldg(vr_ + j)) << 16) : 0.0f;
+                }
+            }
+        } else if (kVec) {
             kp[r] = m ? __ldg(reinterpret_cast<const uint2 *>(kr) + lane) : make_uint2(0u, 0u);
             vp[r] = m ? __ldg(reinterpret_cast<const uint2 *>(vr_) + lane) : make_uint2(0u, 0u);
         } else {
@@ -222,7 +261,7 @@ __device__ __forceinline__ void attn_batch(const unsigned (&mask)[AttnBatch<G>::
 #pragma unroll
         for (int r = 0; r < RB; ++r) {
             float kk[4];
-            if (kVec) {
+            if (kVec && !kPlanes) {
                 kk[0] = bf16lo(kp[r].x); kk[1] = bf16hi(kp[r].x); kk[2] = bf16lo(kp[r].y); kk[3] = bf16hi(kp[r].y);
             } else {
 #pragma unroll
@@ -300,9 +339,9 @@ __device__ __forceinline__ void attn_batch(const unsigned (&mask)[AttnBatch<G>::
 
 // Lane l holds channels 4l .. 4l+3 (kVec: D = 128, one 8-byte load of K and one
 // of V per row) or channels l + 32 e (any D <= 128).
-template <int G, bool kVec>
+template <int G, bool kVec, bool kPlanes>
 __global__ void __launch_bounds__(NA, G >= 8 ? 1 : 2)
-attn_kernel(int n, int ctok, int D, int k, int rows_cta, int cph, int splits, const uint16_t *__restrict__ krows,
+attn_kernel(int n, int ctok, int D, int k, int rows_cta, int cph, int splits, const KSource ks,
             const uint16_t *__restrict__ vrows, const float *__restrict__ q,
             const int32_t *__restrict__ topk, float *__restrict__ out, float *__restrict__ part,
             unsigned *__restrict__ ticket) {
@@ -369,7 +408,7 @@ attn_kernel(int n, int ctok, int D, int k, int rows_cta, int cph, int splits, co
             mask[r] = m;
             ti[r] = i;
         }
-        attn_batch<G, kVec>(mask, ti, krows, vrows, (size_t)u * ctok, D, scale, qv, m_h, l_h, o_h, pb);
+        attn_batch<G, kVec, kPlanes>(mask, ti, ks, vrows, u, (size_t)u * ctok, D, scale, qv, m_h, l_h, o_h, pb);
     }
     attn_finish<G, kVec>(sm, asmem_raw, lay, D, s, u, splits, m_h, l_h, o_h, out, part, ticket);
 }
@@ -379,7 +418,7 @@ attn_kernel(int n, int ctok, int D, int k, int rows_cta, int cph, int splits, co
 // then the same partial states and last-CTA merge.
 template <int G, bool kVec>
 __global__ void __launch_bounds__(NA, G >= 8 ? 1 : 2)
-dense_attn_kernel(int n, int ctok, int D, int rows_cta, int splits, const uint16_t *__restrict__ krows,
+dense_attn_kernel(int n, int ctok, int D, int rows_cta, int splits, const KSource ks,
                   const uint16_t *__restrict__ vrows, const float *__restrict__ q, float *__restrict__ out,
                   float *__restrict__ part, unsigned *__restrict__ ticket) {
     constexpr int RB = AttnBatch<G>::RB;
@@ -412,7 +451,7 @@ dense_attn_kernel(int n, int ctok, int D, int rows_cta, int splits, const uint16
             mask[r] = (r0 + r < R) ? (1u << G) - 1u : 0u;
             ti[r] = i_begin + r0 + r;
         }
-        attn_batch<G, kVec>(mask, ti, krows, vrows, (size_t)u * ctok, D, scale, qv, m_h, l_h, o_h, pb);
+        attn_batch<G, kVec, false>(mask, ti, ks, vrows, u, (size_t)u * ctok, D, scale, qv, m_h, l_h, o_h, pb);
     }
     attn_finish<G, kVec>(sm, asmem_raw, lay, D, s, u, splits, m_h, l_h, o_h, out, part, ticket);
 }
@@ -427,10 +466,11 @@ int launch_dense_attn(const fathom_shape &s, const uint16_t *krows, const uint16
     const size_t smem = attn_smem_layout(s.G, 0, s.D, wl.splits).total;
     const bool vec = s.D == 128 && ((uintptr_t)krows % 8 == 0) && ((uintptr_t)vrows % 8 == 0);
     const dim3 grid(wl.splits, s.units);
+    const KSource ks{krows, nullptr, nullptr, 0};
 #define FATHOM_DENSE_LAUNCH(GG, VV)                                                                       \
     do {                                                                                                  \
         ensure_smem(dense_attn_kernel<GG, VV>, smem);                                                     \
-        dense_attn_kernel<GG, VV><<<grid, NA, smem, st>>>(s.n, cap_tokens(s), s.D, wl.rows, wl.splits, krows, \
+        dense_attn_kernel<GG, VV><<<grid, NA, smem, st>>>(s.n, cap_tokens(s), s.D, wl.rows, wl.splits, ks, \
                                                           vrows, q, out, part, ticket);                   \
     } while (0)
     switch (s.G * 2 + (vec ? 1 : 0)) {
@@ -448,8 +488,23 @@ int launch_dense_attn(const fathom_shape &s, const uint16_t *krows, const uint16
     return launch_status("dense_attn_kernel");
 }
 
+static int launch_sparse_attn_src(const fathom_shape &s, const KSource &ks, const uint16_t *vrows,
+                                  const float *q, const int32_t *idx, float *out, void *ws, cudaStream_t st);
+
 int launch_sparse_attn(const fathom_shape &s, const uint16_t *krows, const uint16_t *vrows,
                        const float *q, const int32_t *idx, float *out, void *ws, cudaStream_t st) {
+    return launch_sparse_attn_src(s, KSource{krows, nullptr, nullptr, 0}, vrows, q, idx, out, ws, st);
+}
+
+int launch_sparse_attn_planes(const fathom_shape &s, const uint64_t *planes, const uint16_t *scales,
+                              const uint16_t *vrows, const float *q, const int32_t *idx, float *out, void *ws,
+                              cudaStream_t st) {
+    return launch_sparse_attn_src(s, KSource{nullptr, planes, scales, cap_blocks(s)}, vrows, q, idx, out, ws, st);
+}
+
+static int launch_sparse_attn_src(const fathom_shape &s, const KSource &ks, const uint16_t *vrows,
+                                  const float *q, const int32_t *idx, float *out, void *ws, cudaStream_t st) {
+    const bool planes = ks.planes != nullptr;
     const AttnWorkspace wl = attn_workspace_layout(s);
     char *w = (char *)ws;
     float *part = (float *)(w + wl.part_off);
@@ -457,13 +512,19 @@ int launch_sparse_attn(const fathom_shape &s, const uint16_t *krows, const uint1
     if (s.units > 65535) { set_error("sparse_attn: too many units for one launch"); return FATHOM_EINVAL; }
     const size_t smem = attn_smem_layout(s.G, s.k, s.D, wl.splits).total;
     const int cph = (s.k + wl.rows - 1) / wl.rows;   // CTAs per head
-    const bool vec = s.D == 128 && ((uintptr_t)krows % 8 == 0) && ((uintptr_t)vrows % 8 == 0);
+    const bool vec = s.D == 128 && (planes || (uintptr_t)ks.rows % 8 == 0) && ((uintptr_t)vrows % 8 == 0);
     const dim3 grid(wl.splits, s.units);
-#define FATHOM_ATTN_LAUNCH(GG, VV)                                                               \
-    do {                                                                                         \
-        ensure_smem(attn_kernel<GG, VV>, smem);                                                  \
-        attn_kernel<GG, VV><<<grid, NA, smem, st>>>(s.n, cap_tokens(s), s.D, s.k, wl.rows, cph, wl.splits, krows, vrows, \
-                                                    q, idx, out, part, ticket);                  \
+#define FATHOM_ATTN_LAUNCH(GG, VV)                                                                        \
+    do {                                                                                                  \
+        if (planes) {                                                                                     \
+            ensure_smem(attn_kernel<GG, VV, true>, smem);                                                 \
+            attn_kernel<GG, VV, true><<<grid, NA, smem, st>>>(s.n, cap_tokens(s), s.D, s.k, wl.rows, cph,  \
+                                                              wl.splits, ks, vrows, q, idx, out, part, ticket); \
+        } else {                                                                                          \
+            ensure_smem(attn_kernel<GG, VV, false>, smem);                                                \
+            attn_kernel<GG, VV, false><<<grid, NA, smem, st>>>(s.n, cap_tokens(s), s.D, s.k, wl.rows, cph, \
+                                                               wl.splits, ks, vrows, q, idx, out, part, ticket); \
+        }                                                                                                 \
     } while (0)
     switch (s.G * 2 + (vec ? 1 : 0)) {
         case 2: FATHOM_ATTN_LAUNCH(1, false); break;

@@ -65,7 +65,12 @@ typedef enum {
 
 typedef enum { FATHOM_F32 = 0, FATHOM_BF16 = 1 } fathom_dtype;
 
-typedef enum { FATHOM_WS_SCAN_TOPK = 0, FATHOM_WS_SPARSE_ATTN = 1, FATHOM_WS_DENSE_ATTN = 2 } fathom_workspace_kind;
+typedef enum {
+    FATHOM_WS_SCAN_TOPK = 0,
+    FATHOM_WS_SPARSE_ATTN = 1,
+    FATHOM_WS_DENSE_ATTN = 2,
+    FATHOM_WS_KLT_ONLINE = 3
+} fathom_workspace_kind;
 
 /* Which copy of the bit-plane store a scan reads. */
 typedef enum {
@@ -249,6 +254,25 @@ int fathom_scan_topk(const fathom_shape *shape, const uint64_t *planes,
                      int32_t *topk_idx, float *topk_score, float *scores_opt,
                      void *workspace, size_t workspace_bytes, void *stream);
 
+/* Rotated basis without calibration data (Appx. D: the mean, eigenbasis and
+ * eigenvalues of a session's own keys; the pages report this under 1 ms at
+ * 100k tokens).  Per unit, over its n live key rows: mean mu (fp32 runs of 64
+ * tokens folded in fp64), covariance (ddof = 1) of the rows centred on mu
+ * rounded to fp32 (fp32 products, per-slice fp32 sums combined in fp64 in a
+ * fixed order), eigen-decomposition by parallel cyclic Jacobi in fp32
+ * (eigenvalues descending, each eigenvector's largest-magnitude component
+ * positive).  Each unit is its own group: pass groups = units to
+ * fathom_rotate_keys and fathom_rotate_query, and lambda to fathom_plan.
+ *   k_rows [units][C][D] bf16 (device or pinned host), n >= 2 live tokens
+ *   mean   [units][D] fp64 (out, device)
+ *   V      [units][D][D] fp64 (out, device): V[u][j][c] = component j of
+ *          eigenvector c (fp32 values)
+ *   lambda [units][D] fp32 (out, device)
+ *   workspace: at least fathom_workspace_size(shape, FATHOM_WS_KLT_ONLINE)
+ *   bytes, 256-byte aligned (no zero-fill needed). */
+int fathom_klt_online(const fathom_shape *shape, const uint16_t *k_rows, double *mean, double *V,
+                      float *lambda, void *workspace, size_t workspace_bytes, void *stream);
+
 /* Fidelity reference, exact top-k (§2 evaluation, the "exact top-k" the
  * pages compare against): the same kept set as fathom_scan_topk (first n_sink
  * and last n_recent tokens plus the k - |forced| others of largest score per
@@ -316,6 +340,24 @@ int fathom_greedy_budgets(int32_t layers, int32_t levels, const double *err, int
 int fathom_sparse_attn(const fathom_shape *shape, const uint16_t *k_rows,
                        const uint16_t *v_rows, const float *q, const int32_t *topk_idx,
                        float *out, void *workspace, size_t workspace_bytes, void *stream);
+
+/* Sparse attention with the winners' keys rebuilt from the bit-plane store
+ * (§7 names this as the unbuilt next step: the 4-bit channel-major store as
+ * the K cache itself, no bf16 K rows).  As fathom_sparse_attn, except that
+ * the key of a winner i is read from all four planes of its block and
+ * channel, k_ij = (c_ij - 7.5) a_{i/64, j} / 8 (the 4-bit mid-rise value, exact
+ * in fp32).  Each winner reads 4 D plane words and D scales from separate
+ * 32-byte sectors, against one 2 D-byte row: this is the single-token
+ * reconstruction cost the pages name.
+ *   planes [units][D][4][cb], scales [units][D][cb] (the store, device or
+ *   pinned host), v_rows [units][C][D] bf16, q [units][G][D] fp32 (the scan's
+ *   queries: for a rotated store q' = q V, whose logits differ from q . k by
+ *   q . mu, the same for every token), topk_idx [units][G][k] ascending,
+ *   out [units][G][D] fp32 (out), workspace: as fathom_sparse_attn. */
+int fathom_sparse_attn_planes(const fathom_shape *shape, const uint64_t *planes,
+                              const uint16_t *scales, const uint16_t *v_rows, const float *q,
+                              const int32_t *topk_idx, float *out, void *workspace,
+                              size_t workspace_bytes, void *stream);
 
 /* fathom_sparse_attn without a workspace argument, for callers that cannot
  * allocate device memory for the library: a host framework that owns all

@@ -477,6 +477,57 @@ void oracle_attention(int n, int D, int G, const uint16_t *krows,
 /* §4/§5 fidelity references and §3.4 greedy per-layer budgets               */
 /* ------------------------------------------------------------------------ */
 
+/* §7 (the store as the K cache): every token's key rebuilt from all four
+ * planes of its block and channel, k_ij = dequant(c_ij, 4, a_{i/64, j}).
+ *   planes [D][4][cb], scales [D][cb] of one unit; keys [n][D] (out). */
+void oracle_reconstruct(int n, int D, int cb, const uint64_t *planes, const uint16_t *scales,
+                        double *keys)
+{
+    for (int i = 0; i < n; ++i) {
+        int beta = i / 64, bit = i % 64;
+        for (int j = 0; j < D; ++j) {
+            int c = 0;
+            for (int p = 0; p < ORACLE_PLANES; ++p) {
+                uint64_t w = planes[((size_t)j * ORACLE_PLANES + p) * cb + beta];
+                c = (c << 1) | (int)((w >> bit) & 1u);
+            }
+            keys[(size_t)i * D + j] = oracle_dequant(c, 4, oracle_fp16_value(scales[(size_t)j * cb + beta]));
+        }
+    }
+}
+
+/* Attention as oracle_attention with the keys given as fp64 values
+ * keys [n][D] (the rebuilt keys), values still bf16 rows. */
+void oracle_attention_keys(int n, int D, int G, const double *keys, const uint16_t *vrows,
+                           const float *q, const int32_t *idx, int k, double *out)
+{
+    (void)n;
+    double *logit = (double *)malloc(sizeof(double) * (size_t)(k > 0 ? k : 1));
+    double scale = 1.0 / sqrt((double)D);
+    for (int h = 0; h < G; ++h) {
+        double mx = -INFINITY;
+        for (int r = 0; r < k; ++r) {
+            int i = idx[(size_t)h * k + r];
+            double d = 0.0;
+            for (int j = 0; j < D; ++j)
+                d += (double)q[(size_t)h * D + j] * keys[(size_t)i * D + j];
+            logit[r] = d * scale;
+            if (logit[r] > mx) mx = logit[r];
+        }
+        double den = 0.0;
+        for (int j = 0; j < D; ++j) out[(size_t)h * D + j] = 0.0;
+        for (int r = 0; r < k; ++r) {
+            double p = exp(logit[r] - mx);
+            den += p;
+            int i = idx[(size_t)h * k + r];
+            for (int j = 0; j < D; ++j)
+                out[(size_t)h * D + j] += p * oracle_bf16_value(vrows[(size_t)i * D + j]);
+        }
+        for (int j = 0; j < D; ++j) out[(size_t)h * D + j] /= den;
+    }
+    free(logit);
+}
+
 /* Exact score of every token, the quantity the exact top-k ranks:
  * s_h(i) = sum_j q_hj k_ij over the key rows widened exactly, fp64.
  *   keys [n][D] fp32, q [G][D] fp32, out [G][n]. */

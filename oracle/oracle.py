@@ -61,6 +61,8 @@ _SIGS = {
     "oracle_scores_staged": (None, [_i, _i, _i, _P(_u32), _P(_u64), _P(_u16), _P(_u8), _P(_f), _P(_d)]),
     "oracle_select": (_i, [_i, _i, _P(_d), _i, _i, _i, _P(_i32), _P(_d)]),
     "oracle_attention": (None, [_i, _i, _i, _P(_u16), _P(_u16), _P(_f), _P(_i32), _i, _P(_d)]),
+    "oracle_reconstruct": (None, [_i, _i, _i, _P(_u64), _P(_u16), _P(_d)]),
+    "oracle_attention_keys": (None, [_i, _i, _i, _P(_d), _P(_u16), _P(_f), _P(_i32), _i, _P(_d)]),
     "oracle_exact_scores": (None, [_i, _i, _i, _P(_f), _P(_f), _P(_d)]),
     "oracle_greedy_budgets": (None, [_i, _i, _P(_d), _i, _i, _i, _P(_i32)]),
     "oracle_calibrate": (None, [_i, _i, _P(_f), _P(_d), _P(_d), _P(_d)]),
@@ -261,6 +263,30 @@ def attention(krows, vrows, q, idx):
 
 
 # ---------------------------------------------------------------- fidelity / budgets
+def reconstruct(planes_unit, scales_unit, n):
+    """One unit's store planes [D][4][cb], scales [D][cb] -> keys [n][D] fp64 at all four planes."""
+    P = _arr(planes_unit, np.uint64)
+    S = _arr(scales_unit, np.uint16)
+    D, _, cb = P.shape
+    out = np.zeros((n, D), np.float64)
+    lib().oracle_reconstruct(int(n), D, cb, _ptr(P, np.uint64), _ptr(S, np.uint16), _ptr(out, np.float64))
+    return out
+
+
+def attention_keys(keys, vrows, q, idx):
+    """Attention with fp64 keys [n][D] and bf16 value rows (u16 bits) -> [G][D] fp64."""
+    K = _arr(keys, np.float64)
+    V = _arr(vrows, np.uint16)
+    qq = _arr(q, np.float32)
+    ii = _arr(idx, np.int32)
+    n, D = K.shape
+    G, k = ii.shape
+    out = np.zeros((G, D), np.float64)
+    lib().oracle_attention_keys(n, D, G, _ptr(K, np.float64), _ptr(V, np.uint16), _ptr(qq, np.float32),
+                                _ptr(ii, np.int32), int(k), _ptr(out, np.float64))
+    return out
+
+
 def exact_scores(keys, q):
     """keys [n][D] fp32 (bf16 rows widened exactly), q [G][D] fp32 -> [G][n] fp64: q . k."""
     k = _arr(keys, np.float32)

@@ -94,7 +94,8 @@ def test_workspace_sizes_scale_with_shape(lib):
     assert 0 < B.workspace_size(small, 0) < B.workspace_size(big, 0)
     assert 0 < B.workspace_size(small, 1) <= B.workspace_size(big, 1)
     assert 0 < B.workspace_size(small, 2) <= B.workspace_size(big, 2)
-    assert B.workspace_size(big, 3) == 0
+    assert 0 < B.workspace_size(small, 3) <= B.workspace_size(big, 3)
+    assert B.workspace_size(big, 4) == 0
 
 
 def test_fidelity_reference_calls_validate_arguments(lib):
@@ -135,6 +136,30 @@ def test_append_block_validates_its_block(lib):
         assert rc_msg(lib, rc)[0] == 1 and "append_block" in lib.fathom_last_error().decode()
     rc = lib.fathom_append_block(ctypes.byref(s), d, 1, 65, 0, d, d, None)
     assert rc_msg(lib, rc)[0] == 1
+
+
+def test_online_basis_validates_arguments(lib):
+    d = ctypes.c_void_p(256)
+    s = B.make_shape(2, 4096, 128, 4, 64)
+    need = lib.fathom_workspace_size(ctypes.byref(s), B.WS_KLT_ONLINE)
+    assert need > 0
+    rc = lib.fathom_klt_online(ctypes.byref(s), d, None, d, d, d, need, None)
+    assert rc_msg(lib, rc) == (1, "mean is NULL")
+    rc = lib.fathom_klt_online(ctypes.byref(s), d, d, d, d, d, need - 1, None)
+    assert rc_msg(lib, rc)[0] == 3
+    one = B.make_shape(2, 1, 128, 4, 1, 0, 0)
+    rc = lib.fathom_klt_online(ctypes.byref(one), d, d, d, d, d, need, None)
+    assert rc_msg(lib, rc)[0] == 1 and "n >= 2" in lib.fathom_last_error().decode()
+
+
+def test_plane_key_attention_validates_arguments(lib):
+    d = ctypes.c_void_p(256)
+    s = B.make_shape(2, 4096, 128, 4, 64)
+    need = lib.fathom_workspace_size(ctypes.byref(s), B.WS_SPARSE_ATTN)
+    rc = lib.fathom_sparse_attn_planes(ctypes.byref(s), None, d, d, d, d, d, d, need, None)
+    assert rc_msg(lib, rc) == (1, "planes is NULL")
+    rc = lib.fathom_sparse_attn_planes(ctypes.byref(s), d, d, d, d, d, d, d, need - 1, None)
+    assert rc_msg(lib, rc)[0] == 3
 
 
 def test_fidelity_helpers_validate_and_greedy_matches_oracle(lib):

@@ -25,7 +25,7 @@ from bit_plane_kv_gb300 import fidelity as F
 from bit_plane_kv_gb300 import synth
 from oracle import oracle as O
 
-from fathom_cases import ATTN_RTOL, Inputs, u16
+from fathom_cases import ATTN_RTOL, Inputs, u16, u64
 
 pytestmark = pytest.mark.gpu
 EXACT_RTOL = 1e-5
@@ -175,3 +175,34 @@ def test_greedy_budgets_from_errors_measured_on_the_gpu():
     budgets = F.greedy_layer_budgets(table, 24, 8, 48)
     np.testing.assert_array_equal(budgets, O.greedy_budgets(table, 24, 8, 48))
     assert budgets.sum() == 48 * w.layers and np.all((budgets >= 24) & (budgets <= 128))
+
+
+# ------------------------------------------------------------------ keys rebuilt from the store
+@pytest.mark.parametrize("D,G,n,k,where,cap", [
+    (128, 4, 3000, 300, "hbm", 0),
+    (128, 4, 4096, 512, "host", 0),        # store in pinned host memory
+    (128, 4, 2000, 256, "hbm", 2560),      # capacity layout
+    (98, 2, 777, 60, "hbm", 0),            # D % 4 != 0
+    (128, 8, 1500, 100, "hbm", 0),
+])
+def test_attention_with_keys_rebuilt_from_planes_matches_oracle(D, G, n, k, where, cap):
+    w = _generic(D, G)
+    U = 2
+    inp = Inputs(w, range(U), n)
+    c = cap or n
+    keys = torch.zeros(U, c, D, dtype=torch.bfloat16, device="cuda")
+    vals = torch.zeros(U, c, D, dtype=torch.bfloat16, device="cuda")
+    keys[:, :n], vals[:, :n] = inp.krows, inp.vrows
+    shape = B.make_shape(U, n, D, G, k, 4, 32, n_cap=cap)
+    planes, scales = B.fathom_quantize_pack(shape, keys)
+    # any valid kept sets: the exact top-k
+    idx, _ = B.fathom_exact_topk(shape, keys, inp.q, B.alloc_workspace(shape, B.WS_SCAN_TOPK))
+    if where == "host":
+        planes, scales = planes.cpu().pin_memory(), scales.cpu().pin_memory()
+    out = B.fathom_sparse_attn_planes(shape, planes, scales, vals, inp.q, idx, B.alloc_workspace(shape, B.WS_SPARSE_ATTN))
+    torch.cuda.synchronize()
+    for ui in range(U):
+        kk = O.reconstruct(u64(planes[ui].cpu()), u16(scales[ui].cpu()), n)
+        o = O.attention_keys(kk, u16(inp.vrows[ui]), inp.q[ui].cpu().numpy(), idx[ui].cpu().numpy())
+        rel = O.rel_l2(out[ui].cpu().numpy(), o)
+        assert np.all(rel <= ATTN_RTOL), rel

@@ -142,3 +142,109 @@ def test_klt_full_path_with_per_layer_budgets():
         for h in range(w.G):
             inter = len(set(idx[ui, h].cpu().numpy().tolist()) & set(exact[ui, h].tolist()))
             assert inter >= 0.5 * k, inter
+
+
+# ---------------------------------------------------------------- online basis (Appx. D)
+# Tolerances of the fp32 online basis against the oracle's fp64 calibration of
+# the same bf16 rows:
+# * mean: fp32 sums of 64-token runs folded in fp64, |err| <= 64 u mean|k_j|
+#   (u = 2^-24), tested at 4e-6 mean|k_j|;
+# * covariance: per slice of T tokens fp32 sums of 32-token stages, each entry
+#   within (32 + T/32 + 1) u sum|x_a x_b| / (n - 1) <= 5e-6 lambda_max for T <= 2048,
+#   so ||dC||_2 <= 128 * 5e-6 lambda_max ~ 6.4e-4 lambda_max at worst; the fp32
+#   Jacobi adds a backward error of order sweeps * D * u ||C||.  Eigenvalues
+#   and eigen-residuals ||C v - lambda v|| are tested at 1e-3 lambda_max,
+#   orthonormality of V at 1e-5.
+ONLINE_TOL = 1e-3
+
+
+def _online_case(n, cap=0, units=None):
+    w = _klt_workload()
+    units = list(range(w.units)) if units is None else units
+    cap = cap or n
+    krows = torch.full((len(units), cap, w.D), 9e3, dtype=torch.bfloat16, device="cuda")   # never read past n
+    for i, u in enumerate(units):
+        krows[i, :n] = synth.unit_keys(w, u, "cuda", n=n).to(torch.bfloat16)
+    shape = B.make_shape(len(units), n, w.D, w.G, 1, 0, 0, n_cap=cap if cap != n else 0)   # k is not used
+    return w, units, shape, krows
+
+
+def _check_online_unit(keys_bf16, mean, V, lam):
+    kk = keys_bf16.float().cpu().numpy()
+    om, _, cov = O.calibrate(kk, with_cov=True)
+    ol, _ = O.eigh(cov)
+    m = mean.cpu().numpy()
+    assert np.all(np.abs(m - om) <= 4e-6 * np.abs(kk.astype(np.float64)).mean(0) + 1e-30)
+    gl = lam.cpu().numpy().astype(np.float64)
+    Vg = V.cpu().numpy()
+    lmax = ol[0]
+    assert np.all(np.diff(gl) <= 0)                                      # descending
+    np.testing.assert_allclose(gl, ol, rtol=0, atol=ONLINE_TOL * lmax)
+    res = np.linalg.norm(cov @ Vg - Vg * gl[None, :], axis=0)
+    assert np.all(res <= ONLINE_TOL * lmax), float(res.max() / lmax)
+    np.testing.assert_allclose(Vg.T @ Vg, np.eye(Vg.shape[0]), rtol=0, atol=1e-5)
+    arg = np.argmax(np.abs(Vg), axis=0)
+    assert np.all(Vg[arg, np.arange(Vg.shape[1])] > 0)
+
+
+@pytest.mark.parametrize("n,cap", [(5000, 0), (777, 1024), (64, 0), (2, 0)])
+def test_online_basis_matches_oracle(n, cap):
+    w, units, shape, krows = _online_case(n, cap)
+    mean, V, lam = B.fathom_klt_online(shape, krows)
+    torch.cuda.synchronize()
+    for ui in range(len(units)):
+        _check_online_unit(krows[ui, :n], mean[ui], V[ui], lam[ui])
+
+
+def test_online_basis_at_100k_tokens():
+    # the size the pages quote: 100k tokens of one layer's 8 KV heads, two units checked
+    w = synth.WORKLOADS["klt_32x64k"]
+    n = 100000
+    units = w.layer_units(0)[:8]
+    krows = torch.stack([synth.unit_keys(w, u, "cuda", n=n) for u in units]).to(torch.bfloat16)
+    shape = B.make_shape(len(units), n, w.D, w.G, 64, 4, 32)
+    mean, V, lam = B.fathom_klt_online(shape, krows)
+    torch.cuda.synchronize()
+    for ui in (0, 5):
+        _check_online_unit(krows[ui], mean[ui], V[ui], lam[ui])
+
+
+def test_online_basis_full_path():
+    # the whole path on a store built in each unit's own basis (groups = units)
+    w, units, shape0, krows = _online_case(6000)
+    U, n, k = len(units), 6000, 300
+    shape = B.make_shape(U, n, w.D, w.G, k, w.n_sink, w.n_recent)
+    vrows = torch.stack([synth.unit_values(w, u, "cuda", n=n) for u in units]).to(torch.bfloat16)
+    q = torch.stack([synth.unit_query(w, u, "cuda") for u in units]).contiguous()
+    mean, V, lam = B.fathom_klt_online(shape, krows)
+    kr = B.fathom_rotate_keys(shape, krows, U, mean, V)
+    qr = B.fathom_rotate_query(shape, q, U, V)
+    planes, scales = B.fathom_quantize_pack(shape, kr)
+    budget = torch.full((U,), 48, dtype=torch.int32, device="cuda")
+    depth, theta, runs = B.fathom_plan(shape, qr, lam, budget)
+    scores = torch.full((U, w.G, n), float("nan"), device="cuda")
+    idx, _ = B.fathom_scan_topk(shape, planes, scales, runs, qr, B.alloc_workspace(shape, B.WS_SCAN_TOPK),
+                                scores=scores)
+    out = B.fathom_sparse_attn(shape, krows, vrows, q, idx, B.alloc_workspace(shape, B.WS_SPARSE_ATTN))
+    torch.cuda.synchronize()
+    for ui in range(U):
+        Vg, mu = V[ui].cpu().numpy(), mean[ui].cpu().numpy()
+        kk = krows[ui].float().cpu().numpy()
+        ref = O.rotate(kk, mu, Vg).astype(np.float64)
+        err = np.abs(kr[ui].cpu().numpy().astype(np.float64) - ref)
+        assert np.all(err <= ROT_RTOL * _rotation_bound(kk.astype(np.float64) - mu, Vg) + 1e-30)
+        keys_r = kr[ui].cpu().numpy()
+        qq = qr[ui].cpu().numpy()
+        P, S, C = O.quantize_pack(keys_r)
+        np.testing.assert_array_equal(u64(planes[ui]), P)
+        od, oth, _ = O.plan(qq, lam[ui].cpu().numpy(), 48)
+        np.testing.assert_array_equal(depth[ui].cpu().numpy(), od)
+        assert theta[ui].item() == oth
+        ref_s = O.scores(P[None], S[None], od[None], qq[None], n)[0]
+        got = scores[ui].cpu().numpy().astype(np.float64)
+        assert np.all(np.abs(got - ref_s) <= SCORE_RTOL * khat_magnitude(C, S, od, qq, n) + 1e-30)
+        oi, _ = O.select(got, k, w.n_sink, w.n_recent)
+        np.testing.assert_array_equal(idx[ui].cpu().numpy(), oi)
+        o = O.attention(u16(krows[ui]), u16(vrows[ui]), q[ui].cpu().numpy(), oi)
+        rel = np.linalg.norm(out[ui].cpu().numpy().astype(np.float64) - o, axis=1) / np.linalg.norm(o, axis=1)
+        assert np.all(rel <= ATTN_RTOL), rel

@@ -529,3 +529,40 @@ def test_greedy_budgets_hand_examples():
     np.testing.assert_array_equal(O.greedy_budgets([[3.0, 2.0], [3.0, 0.0]], 24, 104, 128), [128, 128])
     # flat target at the floor
     np.testing.assert_array_equal(O.greedy_budgets([[3.0, 2.0], [3.0, 0.0]], 24, 8, 24), [24, 24])
+
+
+# ------------------------------------------------------------------ §7 keys rebuilt from the store
+def test_reconstruct_reads_the_codes_back_from_the_planes():
+    # the rebuilt key is the 4-bit mid-rise value of the code the quantiser chose:
+    # (c - 7.5) a16 / 8 with c from the codes array (not from the plane bits), and
+    # within half a step of the key; a16 may round a down by up to 2^-11 relative,
+    # and then the largest key (clipped to code 15) is off by a - 7.5 a16 / 8,
+    # at most (1 + 16 * 2^-11) half steps
+    rng = np.random.default_rng(43)
+    n, D = 200, 12                        # a ragged last block
+    keys = (rng.normal(size=(n, D)) * np.exp(rng.normal(size=D))).astype(np.float32)
+    P, S, C = O.quantize_pack(keys)
+    got = O.reconstruct(P, S, n)
+    a16 = S.view(np.float16).astype(np.float64)          # [D][nb]
+    blk = np.arange(n) // 64
+    expect = (C.astype(np.float64) - 7.5) * a16[:, blk].T / 8.0
+    np.testing.assert_array_equal(got, expect)
+    step = a16[:, blk].T / 8.0
+    assert np.all(np.abs(got - keys) <= 0.5 * step * (1 + 16 * 2.0 ** -11) + 1e-30)
+    # a capacity layout (cb > nb) reads the same words
+    Pc = np.zeros((D, 4, 7), np.uint64)
+    Sc = np.zeros((D, 7), np.uint16)
+    Pc[:, :, :P.shape[2]] = P
+    Sc[:, :S.shape[1]] = S
+    np.testing.assert_array_equal(O.reconstruct(Pc, Sc, n), got)
+
+
+def test_attention_with_fp64_keys_equals_bf16_row_attention():
+    # keys that are bf16 values give exactly the attention over the bf16 rows
+    rng = np.random.default_rng(47)
+    n, D, G = 50, 16, 2
+    K = to_bf16_bits(rng.normal(size=(n, D)))
+    V = to_bf16_bits(rng.normal(size=(n, D)))
+    q = rng.normal(size=(G, D)).astype(np.float32)
+    idx = np.sort(rng.choice(n, size=(G, 9), replace=False), axis=1).astype(np.int32)
+    np.testing.assert_array_equal(O.attention_keys(bf16_to_f64(K), V, q, idx), O.attention(K, V, q, idx))
