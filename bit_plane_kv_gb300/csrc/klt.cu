@@ -353,7 +353,7 @@ constexpr int kOnThreads = 160;       // 136 upper-triangle tiles of 8 x 8 (+ st
 constexpr int kOnTiles = 136;
 constexpr int kOnStage = 32;          // tokens staged per round
 constexpr int kOnMeanThreads = 256;
-constexpr int kEig32Threads = 256;
+constexpr int kEig32Threads = 512;
 constexpr int kEigPad = FATHOM_MAX_D + 1;
 
 __device__ __forceinline__ float bf16_to_f32(uint16_t b) { return __uint_as_float(((uint32_t)b) << 16); }
@@ -479,9 +479,11 @@ klt_online_reduce_kernel(int n, int D, int S, const float *__restrict__ cov_part
 // vector's largest-magnitude component positive.  Round-robin ordering over
 // Dp = D rounded up to even indices: in step t, pair 0 is (0, 1 + t mod (Dp - 1))
 // and pair i > 0 is (1 + (t + i) mod (Dp - 1), 1 + (t - i) mod (Dp - 1)); every
-// pair meets once per sweep of Dp - 1 steps.  A pair rotates when
-// |a_pr| > 2^-23 sqrt(|a_pp a_rr|); sweeps stop when one rotates nothing, when
-// the off-diagonal square sum is <= 1e-12 of the total, or after 24 sweeps.
+// pair meets once per sweep of Dp - 1 steps.  A pair rotates when |a_pr| exceeds
+// both 2^-23 sqrt(|a_pp a_rr|) and 2^-22 ||A||_F (fp32 rounding leaves
+// off-diagonal entries of about 2^-24 ||A|| that no rotation removes); sweeps
+// stop when one rotates nothing or after 24 sweeps.  Warp w applies the
+// rotations of pairs w, w + 16, ... with its lanes over the rows.
 __global__ void __launch_bounds__(kEig32Threads)
 klt_eigh32_kernel(int D, double *__restrict__ vec, float *__restrict__ lambda) {
     extern __shared__ __align__(16) float esm[];
@@ -489,36 +491,30 @@ klt_eigh32_kernel(int D, double *__restrict__ vec, float *__restrict__ lambda) {
     float *V = esm + FATHOM_MAX_D * kEigPad;         // [128][129]
     __shared__ int pp[FATHOM_MAX_D / 2], pr[FATHOM_MAX_D / 2];
     __shared__ float pc[FATHOM_MAX_D / 2], ps[FATHOM_MAX_D / 2];
-    __shared__ float red[2][kEig32Threads / 32];
+    __shared__ float red[kEig32Threads / 32];
     __shared__ float lam_s[FATHOM_MAX_D];
     __shared__ int rank_s[FATHOM_MAX_D];
+    constexpr int NW = kEig32Threads / 32;
     const int u = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int Dp = D + (D & 1), half = Dp / 2;
     double *Vg = vec + (size_t)u * D * D;
-    for (int e = tid; e < Dp * Dp; e += kEig32Threads) {
-        const int x = e / Dp, y = e % Dp;
-        A[x * kEigPad + y] = (x < D && y < D) ? __double2float_rn(Vg[(size_t)x * D + y]) : 0.0f;
-        V[x * kEigPad + y] = (x == y) ? 1.0f : 0.0f;
-    }
+    for (int x = warp; x < Dp; x += NW)
+        for (int y = lane; y < Dp; y += 32) {
+            A[x * kEigPad + y] = (x < D && y < D) ? __double2float_rn(Vg[(size_t)x * D + y]) : 0.0f;
+            V[x * kEigPad + y] = (x == y) ? 1.0f : 0.0f;
+        }
     __syncthreads();
     for (int sweep = 0; sweep < 24; ++sweep) {
-        float off = 0.0f, tot = 0.0f;
-        for (int e = tid; e < Dp * Dp; e += kEig32Threads) {
-            const int x = e / Dp, y = e % Dp;
-            const float v = A[x * kEigPad + y] * A[x * kEigPad + y];
-            tot += v;
-            if (x != y) off += v;
-        }
+        float tot = 0.0f;
+        for (int x = warp; x < Dp; x += NW)
+            for (int y = lane; y < Dp; y += 32) tot = fmaf(A[x * kEigPad + y], A[x * kEigPad + y], tot);
 #pragma unroll
-        for (int o = 16; o; o >>= 1) {
-            off += __shfl_xor_sync(0xffffffffu, off, o);
-            tot += __shfl_xor_sync(0xffffffffu, tot, o);
-        }
-        if (lane == 0) { red[0][warp] = off; red[1][warp] = tot; }
+        for (int o = 16; o; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
+        if (lane == 0) red[warp] = tot;
         __syncthreads();
-        off = 0.0f; tot = 0.0f;
-        for (int w = 0; w < kEig32Threads / 32; ++w) { off += red[0][w]; tot += red[1][w]; }
-        if (off <= 1e-12f * tot || off == 0.0f) break;          // the same decision in every thread
+        tot = 0.0f;
+        for (int w = 0; w < NW; ++w) tot += red[w];
+        const float floor_abs = 2.384185791e-7f * sqrtf(tot);      // 2^-22 ||A||_F
         int rotated = 0;
         for (int t = 0; t < Dp - 1; ++t) {
             if (tid < half) {
@@ -531,7 +527,8 @@ klt_eigh32_kernel(int D, double *__restrict__ vec, float *__restrict__ lambda) {
                 if (p > r) { const int q = p; p = r; r = q; }
                 const float apr = A[p * kEigPad + r], app = A[p * kEigPad + p], arr = A[r * kEigPad + r];
                 float c = 1.0f, sn = 0.0f;
-                if (apr != 0.0f && fabsf(apr) > 1.1920929e-7f * sqrtf(fabsf(app * arr))) {
+                const float aa = fabsf(apr);
+                if (aa > floor_abs && aa > 1.1920929e-7f * sqrtf(fabsf(app * arr))) {
                     const float th = (arr - app) / (2.0f * apr);
                     const float tt = fabsf(th) > 1e18f ? 0.5f / th
                                                        : (th >= 0.0f ? 1.0f : -1.0f) / (fabsf(th) + sqrtf(1.0f + th * th));
@@ -542,25 +539,29 @@ klt_eigh32_kernel(int D, double *__restrict__ vec, float *__restrict__ lambda) {
                 pp[tid] = p; pr[tid] = r; pc[tid] = c; ps[tid] = sn;
             }
             __syncthreads();
-            for (int e = tid; e < half * Dp; e += kEig32Threads) {   // columns p and r of A and V
-                const int x = e % Dp, i = e / Dp;
+            for (int i = warp; i < half; i += NW) {          // columns p and r of A and V
                 const int p = pp[i], r = pr[i];
                 const float c = pc[i], sn = ps[i];
-                const float axp = A[x * kEigPad + p], axr = A[x * kEigPad + r];
-                A[x * kEigPad + p] = c * axp - sn * axr;
-                A[x * kEigPad + r] = sn * axp + c * axr;
-                const float vxp = V[x * kEigPad + p], vxr = V[x * kEigPad + r];
-                V[x * kEigPad + p] = c * vxp - sn * vxr;
-                V[x * kEigPad + r] = sn * vxp + c * vxr;
+                if (sn == 0.0f) continue;                     // uniform across the warp
+                for (int x = lane; x < Dp; x += 32) {
+                    const float axp = A[x * kEigPad + p], axr = A[x * kEigPad + r];
+                    A[x * kEigPad + p] = c * axp - sn * axr;
+                    A[x * kEigPad + r] = sn * axp + c * axr;
+                    const float vxp = V[x * kEigPad + p], vxr = V[x * kEigPad + r];
+                    V[x * kEigPad + p] = c * vxp - sn * vxr;
+                    V[x * kEigPad + r] = sn * vxp + c * vxr;
+                }
             }
             __syncthreads();
-            for (int e = tid; e < half * Dp; e += kEig32Threads) {   // rows p and r of A
-                const int x = e % Dp, i = e / Dp;
+            for (int i = warp; i < half; i += NW) {          // rows p and r of A
                 const int p = pp[i], r = pr[i];
                 const float c = pc[i], sn = ps[i];
-                const float apx = A[p * kEigPad + x], arx = A[r * kEigPad + x];
-                A[p * kEigPad + x] = c * apx - sn * arx;
-                A[r * kEigPad + x] = sn * apx + c * arx;
+                if (sn == 0.0f) continue;
+                for (int x = lane; x < Dp; x += 32) {
+                    const float apx = A[p * kEigPad + x], arx = A[r * kEigPad + x];
+                    A[p * kEigPad + x] = c * apx - sn * arx;
+                    A[r * kEigPad + x] = sn * apx + c * arx;
+                }
             }
             __syncthreads();
         }

@@ -566,3 +566,38 @@ def test_attention_with_fp64_keys_equals_bf16_row_attention():
     q = rng.normal(size=(G, D)).astype(np.float32)
     idx = np.sort(rng.choice(n, size=(G, 9), replace=False), axis=1).astype(np.int32)
     np.testing.assert_array_equal(O.attention_keys(bf16_to_f64(K), V, q, idx), O.attention(K, V, q, idx))
+
+
+# ------------------------------------------------------------------ Appx. A toy, reconstructed K
+def test_toy_reconstruction_reproduces_every_printed_statement():
+    # The page prints only channel 2 of the toy's K.  toy_k_reconstruction.json
+    # holds channels 0, 1 and 3 fitted by tests/golden/fit_toy_k.py (oracle only)
+    # and is labelled a reconstruction: this pins that one K consistent with all
+    # of the page's statements exists under the oracle's quantiser, planner and
+    # scorer, and that on it the oracle's scan ranks as the page says.
+    rec = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "toy_k_reconstruction.json")))
+    assert "RECONSTRUCTION" in rec["what"]
+    K = np.array(rec["K"], np.float32)
+    np.testing.assert_array_equal(K[:, 2], np.array(GOLD["channel2"]["values"], np.float32))
+    v = np.var(K.astype(np.float64), axis=0, ddof=1)
+    assert np.all(np.abs(v - np.array(GOLD["var"])) <= 0.0005)                # printed to 3 decimals
+    q = np.array([GOLD["q_A"], GOLD["q_B"]], np.float32)
+    P, S, C = O.quantize_pack(K)
+    np.testing.assert_array_equal(C[:, 2], GOLD["channel2"]["codes"])          # printed codes of channel 2
+    exact = q.astype(np.float64) @ K.astype(np.float64).T
+    np.testing.assert_allclose(exact[1], GOLD["head_B_scores"]["exact"], rtol=0, atol=0.005)
+
+    def top2(s):
+        return set(sorted(range(6), key=lambda i: (-s[i], i))[:2])
+
+    assert top2(exact[0]) == set(GOLD["top2"]["A"]) and top2(exact[1]) == set(GOLD["top2"]["B"])
+    var = np.array(GOLD["var"], np.float32)
+    d8, _, _ = O.plan(q, var, 8, bracket=GOLD["bracket"])
+    d6, _, _ = O.plan(q, var, 6, bracket=GOLD["bracket"])
+    a8 = O.scores(P[None], S[None], d8[None], q[None], 6)[0]
+    a6 = O.scores(P[None], S[None], d6[None], q[None], 6)[0]
+    np.testing.assert_allclose(a8[1], GOLD["head_B_scores"]["approx"], rtol=0, atol=0.005)
+    assert top2(a8[0]) == set(GOLD["top2"]["A"]) and top2(a8[1]) == set(GOLD["top2"]["B"])   # B = 8 gets both
+    assert top2(a6[1]) != set(GOLD["top2"]["B"])                                             # B = 6 misses B
+    # reading channels 0 and 1 only (the fixed 2-channel rules at 8 bits) ranks {t5, t3} for head B
+    assert top2(q[1, 0] * K[:, 0].astype(np.float64) + q[1, 1] * K[:, 1].astype(np.float64)) == {5, 3}
