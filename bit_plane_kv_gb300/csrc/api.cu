@@ -73,8 +73,8 @@ int device_sm_count() {
 }
 
 ScanGrid scan_grid(const fathom_shape &s) {
-    // Sub-chunks (32 blocks) of a unit are dealt round-robin to its `chunks`
-    // CTAs, so every CTA of a unit has ceil(n_sub / chunks) of them at most.
+    // A unit's `chunks` CTAs share its sub-chunks (32 blocks), about
+    // ceil(n_sub / chunks) each (they take them from a counter as they go).
     // With `slots` CTAs resident at once (SMs x resident scan CTAs per SM;
     // 152 x 3 on GB300 when no device answers) the scan takes about
     // waves x (sub-chunks per CTA + 1) sub-chunk times, the 1 standing for a
@@ -154,7 +154,10 @@ ScanWorkspace scan_workspace_layout(const fathom_shape &s) {
     w.part_cnt_off = align256(w.part_keys_off + uh * w.parts * (size_t)k_sel * sizeof(uint64_t));
     w.ticket_off = align256(w.part_cnt_off + uh * w.parts * sizeof(int32_t));
     w.dirty_off = align256(w.ticket_off + uh * sizeof(uint32_t));
-    w.total = align256(w.dirty_off + uh * sizeof(int32_t));
+    w.sub_ctr_off = align256(w.dirty_off + uh * sizeof(int32_t));
+    const size_t n_sub = ((size_t)num_blocks(s.n) + kSubBlocks - 1) / kSubBlocks;
+    w.sub_owner_off = align256(w.sub_ctr_off + (size_t)s.units * sizeof(int32_t));
+    w.total = align256(w.sub_owner_off + (size_t)s.units * n_sub * sizeof(int32_t));
     return w;
 }
 

@@ -39,8 +39,8 @@ __host__ __device__ inline Forced forced_range(int n, int n_sink, int n_recent) 
     return f;
 }
 
-// Scan decomposition: every unit's 32-block sub-chunks are dealt round-robin
-// to `chunks` CTAs; `chunk_blocks` is the most blocks one CTA gets.
+// Scan decomposition: `chunks` CTAs per unit share its 32-block sub-chunks;
+// `chunk_blocks` is the blocks one CTA gets when they are shared evenly.
 struct ScanGrid {
     int chunks;
     int chunk_blocks;
@@ -71,7 +71,7 @@ int merge_parts(int chunks, int m_sel);
 struct ScanWorkspace {
     int parts;
     size_t cand_off, cnt_off, tau_off, flags_off, forced_off, part_keys_off, part_cnt_off,
-        ticket_off, dirty_off, total;
+        ticket_off, dirty_off, sub_ctr_off, sub_owner_off, total;
 };
 ScanWorkspace scan_workspace_layout(const fathom_shape &s);
 

@@ -4,7 +4,8 @@
 // active channel, token and head).
 //
 // Grid: (chunks, units).  A CTA streams sub-chunks of 32 blocks (2048 tokens)
-// of its unit, dealt round-robin over the unit's CTAs.  For each sub-chunk the planned
+// of its unit, taking the next one from a per-unit counter as it goes (so a
+// CTA that runs faster scores more of them).  For each sub-chunk the planned
 // plane words of the active channels (grouped so that at most 64 planes are
 // staged at a time) and per-block weights are staged in shared memory, then
 // each thread scores 8 tokens of one block for all G heads:
@@ -18,15 +19,18 @@
 //   subtraction of 2^23 + 2^t gives exactly 2 (c_t + 0.5 - 2^(t-1)).  With
 //   the block weight w_hj = q_hj * a_j * 2^-t, one fma per head adds
 //   q_hj * (c_t + 0.5 - 2^(t-1)) * a_j / 2^(t-1), i.e. q_hj times the t-bit
-//   mid-rise value, with no rounding before the multiply.
+//   mid-rise value, with no rounding before the multiply.  Tokens m and m + 4
+//   of a thread share byte lanes, so the subtraction and the fmas run as
+//   packed f32x2 operations (each half an ordinary round-to-nearest fp32 op).
 //
 // Selection never materialises all scores.  Tokens are ordered by a 64-bit
 // key (score, ~index).  Each CTA keeps, per head, a candidate list of keys in
 // the workspace and a threshold key tau; a token is appended only if its key
 // >= tau.  tau starts as a key of the CTA's first sub-chunk (selected straight
-// from registers for all heads at once) with between m1 and 2 m1 of that
-// sub-chunk's keys above it, m1 being four times the winners a sub-chunk
-// holds on average; at the end every list is cut back to m .. 2m keys, m
+// from registers for all heads at once: m1 of the threads' best keys, and so
+// at least m1 of the sub-chunk's keys, lie at or above it), m1 being four
+// times the winners a sub-chunk holds on average; at the end every list is
+// cut back to m .. 2m keys, m
 // being four times the CTA's expected share of the k' winners (a list about
 // to overflow is cut the same way on the way).  The merge kernel streams
 // the lists through shared memory (P CTAs per (unit, head), the last of
@@ -34,7 +38,8 @@
 // exact top-k', adds the forced tokens and writes the kept set in ascending
 // index order.  Any CTA whose tau lies above the k'-th key may have dropped
 // a winner: the merge flags it, and a second pass rescans exactly the
-// flagged chunks (keeping their exact top-k') before a second merge.
+// sub-chunks that CTA scored (keeping their exact top-k') before a second
+// merge.
 #include <cstddef>
 #include <mutex>
 #include <type_traits>
@@ -83,6 +88,10 @@ struct ScanSmem {
     GroupDesc grp[FATHOM_MAX_D / kCHG];
     int wcnt[FATHOM_PLANES + 1][FATHOM_MAX_D / 32];   // channels of each depth per warp
     int n_groups;
+    uint32_t two;                                       // 2, opaque to the compiler (see mad_u32)
+    int sq0[2];                                         // first two sub-chunks of this CTA
+    int sq[2];                                          // next sub-chunk of this CTA (double-buffered)
+    int fix_pos;                                        // second pass: where the owner search resumes
     int cnt[G];
     uint64_t tau[G];
     SelScratch<G> selg;   // first-sub-chunk selection, all heads at once
@@ -91,31 +100,64 @@ struct ScanSmem {
 
 
 // ---------------------------------------------------------------------------
+// Per-thread scores of 8 tokens x G heads.  Token m (m = 0..7, token r + 8 m of
+// the block) lives in v[m & 3][h].x for m < 4 and .y for m >= 4: tokens m and
+// m + 4 come from the same byte lane of the low and the high half of a plane
+// word, so one packed (f32x2) instruction updates both.  Each half of a packed
+// operation is an ordinary IEEE single-precision operation (round to nearest),
+// so the scores are the same as with scalar fmaf.
+template <int G>
+struct Acc8 {
+    float2 v[4][G];
+    __device__ __forceinline__ void zero() {
+#pragma unroll
+        for (int b = 0; b < 4; ++b)
+#pragma unroll
+            for (int h = 0; h < G; ++h) v[b][h] = make_float2(0.0f, 0.0f);
+    }
+    __device__ __forceinline__ float &operator()(int m, int h) { return m < 4 ? v[m][h].x : v[m - 4][h].y; }
+    __device__ __forceinline__ float operator()(int m, int h) const { return m < 4 ? v[m][h].x : v[m - 4][h].y; }
+};
+
+// d = a * b + c in the integer multiply-add unit.  The code prefixes are built
+// with shift-and-add steps; written as multiply-adds by a multiplier the
+// compiler cannot see (it is read from shared memory), they run beside the
+// float multiply-adds instead of in the integer/logic unit, which the bit
+// extraction and byte permutes already keep busy.
+__device__ __forceinline__ uint32_t mad_u32(uint32_t a, uint32_t b, uint32_t c) {
+    uint32_t d;
+    asm("mad.lo.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
+// ---------------------------------------------------------------------------
 // Inner loop: channels [a_lo, a_hi) of depth T of the current group.
 // pwcol points at this thread's block in slot 0 of the staged group: slot s of
 // the block is pwcol[s * kSubBlocks] (the lanes of a warp read 4 adjacent words).
 template <int G, int T>
 __device__ __forceinline__ void accum_depth(const uint2 *__restrict__ pwcol,
                                             const float *__restrict__ wrow, int a_lo, int a_hi,
-                                            int slot, uint32_t r, float (&acc)[8][G]) {
+                                            int slot, uint32_t r, uint32_t two, Acc8<G> &acc) {
     constexpr float K = 8388608.0f + (float)(1 << T);
+    const float2 negK = make_float2(-K, -K);
 #pragma unroll 1
     for (int a = a_lo; a < a_hi; ++a, slot += T) {
         uint32_t ylo = 0, yhi = 0;
 #pragma unroll
         for (int p = 0; p < T; ++p) {
             const uint2 w = pwcol[(slot + p) * kSubBlocks];
-            ylo = (ylo << 1) + ((w.x >> r) & 0x01010101u);
-            yhi = (yhi << 1) + ((w.y >> r) & 0x01010101u);
+            ylo = mad_u32(ylo, two, (w.x >> r) & 0x01010101u);
+            yhi = mad_u32(yhi, two, (w.y >> r) & 0x01010101u);
         }
-        ylo = (ylo << 1) + 0x01010101u;
-        yhi = (yhi << 1) + 0x01010101u;
-        float f[8];
+        ylo = mad_u32(ylo, two, 0x01010101u);
+        yhi = mad_u32(yhi, two, 0x01010101u);
+        // byte b of each half under the exponent of 2^23, minus 2^23 + 2^T (exact)
+        float2 f[4];
 #pragma unroll
-        for (int b = 0; b < 4; ++b) {
-            f[b] = __uint_as_float(__byte_perm(ylo, 0x4B000000u, 0x7650u | b)) - K;
-            f[4 + b] = __uint_as_float(__byte_perm(yhi, 0x4B000000u, 0x7650u | b)) - K;
-        }
+        for (int b = 0; b < 4; ++b)
+            f[b] = __fadd2_rn(make_float2(__uint_as_float(__byte_perm(ylo, 0x4B000000u, 0x7650u | b)),
+                                          __uint_as_float(__byte_perm(yhi, 0x4B000000u, 0x7650u | b))),
+                              negK);
         float wv[G];
         if constexpr (G == 4) {
             const float4 v = *reinterpret_cast<const float4 *>(wrow + a * G);
@@ -132,9 +174,11 @@ __device__ __forceinline__ void accum_depth(const uint2 *__restrict__ pwcol,
             wv[0] = wrow[a];
         }
 #pragma unroll
-        for (int m = 0; m < 8; ++m)
+        for (int h = 0; h < G; ++h) {
+            const float2 w2 = make_float2(wv[h], wv[h]);
 #pragma unroll
-            for (int h = 0; h < G; ++h) acc[m][h] = fmaf(wv[h], f[m], acc[m][h]);
+            for (int b = 0; b < 4; ++b) acc.v[b][h] = __ffma2_rn(w2, f[b], acc.v[b][h]);
+        }
     }
 }
 
@@ -476,7 +520,8 @@ scan_kernel(int n, int cb, int ctok, int D, int chunk_blocks, int source, size_t
             const fathom_run *__restrict__ runs, const float *__restrict__ q, int k_sel, int m_sel,
             int m_first, int ns, int r0, int nf, int cap, int vec, float *__restrict__ scores_opt,
             uint64_t *__restrict__ cand, int *__restrict__ cand_cnt, uint64_t *__restrict__ cand_tau,
-            int *__restrict__ flags, float *__restrict__ forced_scores) {
+            int *__restrict__ flags, float *__restrict__ forced_scores, int *__restrict__ sub_ctr,
+            int *__restrict__ sub_owner) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     ScanSmem<G> &sm = *reinterpret_cast<ScanSmem<G> *>(smem_raw);
     const int tid = threadIdx.x;
@@ -583,7 +628,28 @@ scan_kernel(int n, int cb, int ctok, int D, int chunk_blocks, int source, size_t
         g.n4 = nv[4]; g.n3 = nv[3]; g.n2 = nv[2]; g.n1 = nv[1];
         sm.grp[tid] = g;
     }
-    if (tid == 0) sm.n_groups = n_groups;
+    // Sub-chunks are handed out dynamically: the first pass takes the next one of
+    // its unit from a counter, so CTAs that run faster take more of them, and
+    // records which CTA scored each one; the second pass rescans exactly the
+    // sub-chunks the flagged CTA scored.
+    const int n_sub = (nb + kSubBlocks - 1) / kSubBlocks;
+    auto grab = [&]() -> int {   // thread 0 only
+        if (kFix) {
+            for (int q2 = sm.fix_pos; q2 < n_sub; ++q2)
+                if (sub_owner[(size_t)u * n_sub + q2] == chunk) { sm.fix_pos = q2 + 1; return q2; }
+            sm.fix_pos = n_sub;
+            return n_sub;
+        }
+        const int q2 = atomicAdd(sub_ctr + u, 1);
+        return q2 < n_sub ? q2 : n_sub;
+    };
+    if (tid == 0) {
+        sm.n_groups = n_groups;
+        sm.two = 2u;
+        sm.fix_pos = 0;
+        sm.sq0[0] = grab();
+        sm.sq0[1] = sm.sq0[0] < n_sub ? grab() : n_sub;
+    }
     if constexpr (kRows) {   // every channel, unscaled queries
         for (int e = tid; e < D * G; e += NT) sm.qs[e / G][e % G] = q[((size_t)u * G + e % G) * D + e / G];
     }
@@ -592,16 +658,17 @@ scan_kernel(int n, int cb, int ctok, int D, int chunk_blocks, int source, size_t
     const int ng = sm.n_groups;
     const int bl = tid >> 3;                 // block within the sub-chunk
     const uint32_t r = (uint32_t)(tid & 7);  // token offset within a byte lane
+    const uint32_t two = sm.two;
+    int s_cur = sm.sq0[0], s_next = sm.sq0[1], iter = 0;
 
     uint64_t tau[G];                         // per-head thresholds (same in every thread)
 #pragma unroll
     for (int h = 0; h < G; ++h) tau[h] = 0;
     bool first = true;
 
-    // sub-chunks are dealt round-robin to the unit's CTAs (CTA c takes c, c + S,
-    // c + 2S, ...): all CTAs sweep the sequence together, so the addresses in use
-    // at any moment stay within a narrow band (few pages, few DRAM rows)
-    // The usual plan (one staging group of at most kPG / 2 planes, aligned runs)
+    // The unit's CTAs take sub-chunks in order from the counter, so they sweep the
+    // sequence together and the addresses in use at any moment stay within a
+    // narrow band (few pages, few DRAM rows).  The usual plan (one staging group of at most kPG / 2 planes, aligned runs)
     // is double-buffered: while a sub-chunk is scored, cp.async already moves the
     // next one's plane words and scales into the other half of the staging
     // area, so loads stay in flight the whole time (this is what keeps a store
@@ -625,10 +692,11 @@ scan_kernel(int n, int cb, int ctok, int D, int chunk_blocks, int source, size_t
         }
     };
     int half = 0;
-    if (piped && chunk * kSubBlocks < nb) stage_async(0, chunk * kSubBlocks);
+    if (piped && s_cur < n_sub) stage_async(0, s_cur * kSubBlocks);
     if (piped) cp_async_commit();
 
-    for (int sb = chunk * kSubBlocks; sb < nb; sb += (int)gridDim.x * kSubBlocks) {
+    while (s_cur < n_sub) {
+        const int sb = s_cur * kSubBlocks;
         const int nblk = min(kSubBlocks, nb - sb);
         // (second pass) make room in every head's candidate list before this sub-chunk
         if (kFix && k_sel > 0) {
@@ -647,11 +715,8 @@ scan_kernel(int n, int cb, int ctok, int D, int chunk_blocks, int source, size_t
             for (int h = 0; h < G; ++h) tau[h] = sm.tau[h];
         }
 
-        float acc[8][G];
-#pragma unroll
-        for (int m = 0; m < 8; ++m)
-#pragma unroll
-            for (int h = 0; h < G; ++h) acc[m][h] = 0.0f;
+        Acc8<G> acc;
+        acc.zero();
 
         if constexpr (kRows) {
             // exact scores: 4 channels of q (all heads) at a time from shared memory,
@@ -682,81 +747,74 @@ scan_kernel(int n, int cb, int ctok, int D, int chunk_blocks, int source, size_t
 #pragma unroll
                         for (int c = 0; c < 4; ++c)
 #pragma unroll
-                            for (int h = 0; h < G; ++h) acc[m][h] = fmaf(qv[c][h], kf[c], acc[m][h]);
+                            for (int h = 0; h < G; ++h) acc(m, h) = fmaf(qv[c][h], kf[c], acc(m, h));
                     }
                 }
-            }
-        } else if (piped) {
-            const int sbn = sb + (int)gridDim.x * kSubBlocks;
-            if (sbn < nb) stage_async(half ^ 1, sbn);
-            cp_async_commit();
-            cp_async_wait<1>();                 // this sub-chunk's copies have landed
-            __syncthreads();
-            // block weights w_hj = q_hj * 2^-t_j * a_{beta,j} from the prefetched scales
-            for (int e = tid; e < nch0 * kSubBlocks; e += NT) {
-                const int al = e / kSubBlocks, b = e % kSubBlocks;
-                const float a16 = __half2float(__ushort_as_half(sm.scb[half][al][b]));
-#pragma unroll
-                for (int h = 0; h < G; ++h) sm.w[b][al * G + h] = sm.qs[al][h] * a16;
-            }
-            __syncthreads();
-            if (bl < nblk) {
-                const uint2 *pwcol = &sm.pw[half * (kPG / 2)][bl];
-                const float *wrow = sm.w[bl];
-                int a = 0, slot = 0;
-                accum_depth<G, 4>(pwcol, wrow, a, a + g0.n4, slot, r, acc);
-                a += g0.n4; slot += 4 * g0.n4;
-                accum_depth<G, 3>(pwcol, wrow, a, a + g0.n3, slot, r, acc);
-                a += g0.n3; slot += 3 * g0.n3;
-                accum_depth<G, 2>(pwcol, wrow, a, a + g0.n2, slot, r, acc);
-                a += g0.n2; slot += 2 * g0.n2;
-                accum_depth<G, 1>(pwcol, wrow, a, a + g0.n1, slot, r, acc);
             }
         } else {
-            for (int gi = 0; gi < ng; ++gi) {
-                const GroupDesc g = sm.grp[gi];
+            // one staging group at a time: the pipelined plan has a single group whose
+            // copies were issued one sub-chunk ahead; other plans stage each group here
+            for (int gi = 0; gi < (piped ? 1 : ng); ++gi) {
+                const GroupDesc g = piped ? g0 : sm.grp[gi];
                 const int nch = g.n4 + g.n3 + g.n2 + g.n1;
-                const int npl = 4 * g.n4 + 3 * g.n3 + 2 * g.n2 + g.n1;
-                __syncthreads();
-                // stage plane words (slot-major) and block weights; with aligned runs
-                // and a full sub-chunk every load is 16 bytes
-                if (vec && nblk == kSubBlocks) {
-                    for (int e = tid; e < npl * (kSubBlocks / 2); e += NT) {
-                        const int sl = e / (kSubBlocks / 2), c = e % (kSubBlocks / 2);
-                        *reinterpret_cast<uint4 *>(&sm.pw[sl][2 * c]) =
-                            __ldg(reinterpret_cast<const uint4 *>(planes + sm.plane_src[g.p0 + sl] + sb) + c);
-                    }
-                } else {
-                    for (int e = tid; e < npl * kSubBlocks; e += NT) {
-                        const int sl = e / kSubBlocks, b = e % kSubBlocks;
-                        uint2 v = make_uint2(0u, 0u);
-                        if (b < nblk) {
-                            const uint64_t wd = __ldg(planes + sm.plane_src[g.p0 + sl] + sb + b);
-                            v = make_uint2((uint32_t)wd, (uint32_t)(wd >> 32));
-                        }
-                        sm.pw[sl][b] = v;
-                    }
-                }
-                for (int e = tid; e < nch * kSubBlocks; e += NT) {
-                    const int al = e / kSubBlocks, b = e % kSubBlocks;
-                    const int a = g.a0 + al;
-                    float a16 = 0.0f;
-                    if (b < nblk) a16 = __half2float(__ushort_as_half(__ldg(scales + sm.ch_scale[a] + sb + b)));
+                const uint2 *pwbase;
+                if (piped) {
+                    if (s_next < n_sub) stage_async(half ^ 1, s_next * kSubBlocks);
+                    cp_async_commit();
+                    cp_async_wait<1>();                 // this sub-chunk's copies have landed
+                    __syncthreads();
+                    // block weights w_hj = q_hj * 2^-t_j * a_{beta,j} from the prefetched scales
+                    for (int e = tid; e < nch * kSubBlocks; e += NT) {
+                        const int al = e / kSubBlocks, b = e % kSubBlocks;
+                        const float a16 = __half2float(__ushort_as_half(sm.scb[half][al][b]));
 #pragma unroll
-                    for (int h = 0; h < G; ++h) sm.w[b][al * G + h] = sm.qs[a][h] * a16;
+                        for (int h = 0; h < G; ++h) sm.w[b][al * G + h] = sm.qs[al][h] * a16;
+                    }
+                    pwbase = &sm.pw[half * (kPG / 2)][0];
+                } else {
+                    const int npl = 4 * g.n4 + 3 * g.n3 + 2 * g.n2 + g.n1;
+                    __syncthreads();
+                    // stage plane words (slot-major) and block weights; with aligned runs
+                    // and a full sub-chunk every load is 16 bytes
+                    if (vec && nblk == kSubBlocks) {
+                        for (int e = tid; e < npl * (kSubBlocks / 2); e += NT) {
+                            const int sl = e / (kSubBlocks / 2), c = e % (kSubBlocks / 2);
+                            *reinterpret_cast<uint4 *>(&sm.pw[sl][2 * c]) =
+                                __ldg(reinterpret_cast<const uint4 *>(planes + sm.plane_src[g.p0 + sl] + sb) + c);
+                        }
+                    } else {
+                        for (int e = tid; e < npl * kSubBlocks; e += NT) {
+                            const int sl = e / kSubBlocks, b = e % kSubBlocks;
+                            uint2 v = make_uint2(0u, 0u);
+                            if (b < nblk) {
+                                const uint64_t wd = __ldg(planes + sm.plane_src[g.p0 + sl] + sb + b);
+                                v = make_uint2((uint32_t)wd, (uint32_t)(wd >> 32));
+                            }
+                            sm.pw[sl][b] = v;
+                        }
+                    }
+                    for (int e = tid; e < nch * kSubBlocks; e += NT) {
+                        const int al = e / kSubBlocks, b = e % kSubBlocks;
+                        const int a = g.a0 + al;
+                        float a16 = 0.0f;
+                        if (b < nblk) a16 = __half2float(__ushort_as_half(__ldg(scales + sm.ch_scale[a] + sb + b)));
+#pragma unroll
+                        for (int h = 0; h < G; ++h) sm.w[b][al * G + h] = sm.qs[a][h] * a16;
+                    }
+                    pwbase = &sm.pw[0][0];
                 }
                 __syncthreads();
                 if (bl < nblk) {
-                    const uint2 *pwcol = &sm.pw[0][bl];
+                    const uint2 *pwcol = pwbase + bl;
                     const float *wrow = sm.w[bl];
                     int a = 0, slot = 0;
-                    accum_depth<G, 4>(pwcol, wrow, a, a + g.n4, slot, r, acc);
+                    accum_depth<G, 4>(pwcol, wrow, a, a + g.n4, slot, r, two, acc);
                     a += g.n4; slot += 4 * g.n4;
-                    accum_depth<G, 3>(pwcol, wrow, a, a + g.n3, slot, r, acc);
+                    accum_depth<G, 3>(pwcol, wrow, a, a + g.n3, slot, r, two, acc);
                     a += g.n3; slot += 3 * g.n3;
-                    accum_depth<G, 2>(pwcol, wrow, a, a + g.n2, slot, r, acc);
+                    accum_depth<G, 2>(pwcol, wrow, a, a + g.n2, slot, r, two, acc);
                     a += g.n2; slot += 2 * g.n2;
-                    accum_depth<G, 1>(pwcol, wrow, a, a + g.n1, slot, r, acc);
+                    accum_depth<G, 1>(pwcol, wrow, a, a + g.n1, slot, r, two, acc);
                 }
             }
         }
@@ -772,17 +830,17 @@ scan_kernel(int n, int cb, int ctok, int D, int chunk_blocks, int source, size_t
             if (valid && !forced) cvm |= 1u << m;
             if (kScores && valid) {
 #pragma unroll
-                for (int h = 0; h < G; ++h) scores_opt[((size_t)u * G + h) * n + i] = acc[m][h];
+                for (int h = 0; h < G; ++h) scores_opt[((size_t)u * G + h) * n + i] = acc(m, h);
             }
             if (valid && forced) {
                 const int slot = (i < ns) ? i : ns + (i - r0);
 #pragma unroll
-                for (int h = 0; h < G; ++h) forced_scores[((size_t)u * G + h) * nf + slot] = acc[m][h];
+                for (int h = 0; h < G; ++h) forced_scores[((size_t)u * G + h) * nf + slot] = acc(m, h);
             }
         }
         auto key_of = [&](int m, int h) -> uint64_t {
             const uint32_t i = (uint32_t)(beta * 64 + (int)r + 8 * (m & 3) + 32 * (m >> 2));
-            return ((uint64_t)order_f32(acc[m][h]) << 32) | (uint64_t)(0xffffffffu - i);
+            return ((uint64_t)order_f32(acc(m, h)) << 32) | (uint64_t)(0xffffffffu - i);
         };
         if (k_sel > 0 && first) {
             // a threshold from this first sub-chunk, all heads at once, from registers:
@@ -792,7 +850,7 @@ scan_kernel(int n, int cb, int ctok, int D, int chunk_blocks, int source, size_t
             auto visit = [&](auto f) {
 #pragma unroll
                 for (int m = 0; m < 8; ++m)
-                    static_for<0, G>([&](auto h) { f(h, (cvm >> m) & 1u, acc[m][h], key_of(m, h)); });
+                    static_for<0, G>([&](auto h) { f(h, (cvm >> m) & 1u, acc(m, h), key_of(m, h)); });
             };
             if constexpr (kFix) {
                 int kept[G];
@@ -800,7 +858,27 @@ scan_kernel(int n, int cb, int ctok, int D, int chunk_blocks, int source, size_t
                     visit([&](auto h, bool v, float, uint64_t key) { f(h, v, key); });
                 }, m_first, m_first, T, kept);
             } else {
-                hist_thresholds<G>(sm.selg, visit, m_first, T);
+                // each thread's best key per head (its 8 tokens); the threshold puts
+                // m1 of these maxima at or above it, so at least m1 keys pass
+                float mx[G];
+                uint64_t mk[G];
+                bool any = false;
+#pragma unroll
+                for (int h = 0; h < G; ++h) { mx[h] = -CUDART_INF_F; mk[h] = 0ull; }
+#pragma unroll
+                for (int m = 0; m < 8; ++m) {
+                    if ((cvm >> m) & 1u) {
+                        any = true;
+#pragma unroll
+                        for (int h = 0; h < G; ++h) {
+                            const uint64_t kk = key_of(m, h);
+                            if (kk > mk[h]) { mk[h] = kk; mx[h] = acc(m, h); }
+                        }
+                    }
+                }
+                hist_thresholds<G>(sm.selg, [&](auto f) {
+                    static_for<0, G>([&](auto h) { f(h, any, mx[h], mk[h]); });
+                }, m_first, T);
             }
 #pragma unroll
             for (int h = 0; h < G; ++h) tau[h] = T[h];
@@ -822,14 +900,14 @@ scan_kernel(int n, int cb, int ctok, int D, int chunk_blocks, int source, size_t
                 unsigned hm = 0;
 #pragma unroll
                 for (int h = 0; h < G; ++h)
-                    if (((cvm >> m) & 1u) && acc[m][h] >= tf[h]) hm |= 1u << h;
+                    if (((cvm >> m) & 1u) && acc(m, h) >= tf[h]) hm |= 1u << h;
                 while (hm) {
                     const int h = __ffs(hm) - 1;
                     hm &= hm - 1;
-                    float sc = acc[m][0];
+                    float sc = acc(m, 0);
                     uint64_t th = tau[0];
                     static_for<1, G>([&](auto hh) {
-                        if (h == hh) { sc = acc[m][hh]; th = tau[hh]; }
+                        if (h == hh) { sc = acc(m, hh); th = tau[hh]; }
                     });
                     const uint64_t kk = make_key(sc, (uint32_t)(beta * 64 + (int)r + 8 * (m & 3) + 32 * (m >> 2)));
                     if (kk >= th) {
@@ -839,7 +917,14 @@ scan_kernel(int n, int cb, int ctok, int D, int chunk_blocks, int source, size_t
                 }
             }
         }
+        if (tid == 0) {
+            if (!kFix) sub_owner[(size_t)u * n_sub + s_cur] = chunk;
+            sm.sq[iter & 1] = s_next < n_sub ? grab() : n_sub;
+        }
         __syncthreads();   // staging buffers and counters are reused by the next sub-chunk
+        s_cur = s_next;
+        s_next = sm.sq[iter & 1];
+        ++iter;
         half ^= 1;
     }
     if (piped) cp_async_wait<0>();
@@ -1080,14 +1165,15 @@ __device__ void stream_select(MergeSmem &sm, int nl, Base base, Count count, int
         }
         const int take = min(room, total - done);
         const int c0 = sm.count;
-        for (int e = tid; e < take; e += blockDim.x) {
-            const int g = done + e;
-            int lo = 0, hi = nl;              // list holding flattened index g
-            while (hi - lo > 1) {
-                const int mid = (lo + hi) >> 1;
-                if (sm.off[mid] <= g) lo = mid; else hi = mid;
-            }
-            sm.buf[c0 + e] = base(lo)[g - sm.off[lo]];
+        // one warp per list: the lanes copy consecutive keys of the part of the list
+        // that falls in this window (flattened positions [done, done + take))
+        const int lane = tid & 31, warp = tid >> 5, nwarps = (int)blockDim.x >> 5;
+        for (int l = warp; l < nl; l += nwarps) {
+            const int a = max(sm.off[l], done), b = min(sm.off[l + 1], done + take);
+            if (a >= b) continue;
+            const uint64_t *src = base(l) + (a - sm.off[l]);
+            uint64_t *dst = sm.buf + c0 + (a - done);
+            for (int e = lane; e < b - a; e += 32) dst[e] = src[e];
         }
         __syncthreads();
         if (tid == 0) sm.count = c0 + take;
@@ -1119,12 +1205,15 @@ merge_kernel(int n, int G, int k, int k_sel, int ns, int r0, int nf, int chunks,
              const uint64_t *__restrict__ cand_tau, int *__restrict__ flags, int *__restrict__ dirty,
              const float *__restrict__ forced_scores, uint64_t *__restrict__ part_keys,
              int *__restrict__ part_cnt, unsigned *__restrict__ ticket, int32_t *__restrict__ out_idx,
-             float *__restrict__ out_score) {
+             float *__restrict__ out_score, int *__restrict__ sub_ctr) {
     extern __shared__ __align__(16) unsigned char msmem_raw[];
     MergeSmem &sm = *reinterpret_cast<MergeSmem *>(msmem_raw);
     const int p = blockIdx.x, h = blockIdx.y, u = blockIdx.z;
     const int tid = threadIdx.x;
     const size_t uh = (size_t)u * G + h;
+    // the scan that ran before this merge took all of the unit's sub-chunks: its
+    // counter starts again from zero for the next call
+    if (!second && p == 0 && h == 0 && tid == 0) sub_ctr[u] = 0;
     if (second && !dirty[uh]) return;        // nothing was flagged for this (unit, head)
     int32_t *oi = out_idx + uh * k;
     float *os = out_score + uh * k;
@@ -1251,6 +1340,8 @@ static int launch_g(const fathom_shape &s, const uint64_t *planes, const uint16_
     uint64_t *ctau = (uint64_t *)(w + wl.tau_off);
     int *flags = (int *)(w + wl.flags_off);
     int *dirty = (int *)(w + wl.dirty_off);
+    int *sub_ctr = (int *)(w + wl.sub_ctr_off);
+    int *sub_owner = (int *)(w + wl.sub_owner_off);
     // 16-byte staging loads need every plane-row and scale-row start 16-byte aligned:
     // nb a multiple of 8 (n a multiple of 512), aligned strides and bases
     const int nb = num_blocks(s.n);
@@ -1279,7 +1370,7 @@ static int launch_g(const fathom_shape &s, const uint64_t *planes, const uint16_
                                                         stage_words, stage_scales, planes, scales, runs, q,   \
                                                         k_sel, m_sel, m_first, f.ns, f.r0, nf, cap, vec,      \
                                                         SC ? scores_opt : nullptr, cand, cnt, ctau, flags,    \
-                                                        forced)
+                                                        forced, sub_ctr, sub_owner)
         if (rows_src) {
             if (pass == 1) FATHOM_SCAN_LAUNCH(true, false, true);
             else if (scores_opt) FATHOM_SCAN_LAUNCH(false, true, true);
@@ -1294,7 +1385,7 @@ static int launch_g(const fathom_shape &s, const uint64_t *planes, const uint16_
         if (rc) return rc;
         merge_kernel<<<dim3(wl.parts, s.G, s.units), kMThreads, msmem, st>>>(
             s.n, s.G, s.k, k_sel, f.ns, f.r0, nf, sg.chunks, wl.parts, cap, pass, cand, cnt, ctau,
-            flags, dirty, forced, pkeys, pcnt, ticket, idx, score);
+            flags, dirty, forced, pkeys, pcnt, ticket, idx, score, sub_ctr);
         rc = launch_status("merge_kernel");
         if (rc) return rc;
         if (k_sel == 0) break;   // nothing selected: no second pass needed
