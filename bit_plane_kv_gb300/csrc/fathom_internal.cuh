@@ -106,6 +106,16 @@ __device__ __forceinline__ uint32_t key_index(uint64_t key) {
 }
 __device__ __forceinline__ float key_score(uint64_t key) { return unorder_f32((uint32_t)(key >> 32)); }
 
+// 16-byte asynchronous global -> shared copies (zero-filled when bytes == 0).
+__device__ __forceinline__ void cp_async16(void *smem_dst, const void *gmem_src, int bytes) {
+    const unsigned d = (unsigned)__cvta_generic_to_shared(smem_dst);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(d), "l"(gmem_src), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory"); }
+
 // Raise a kernel's dynamic shared-memory limit once per (kernel, device, size);
 // later launches skip the driver call.
 bool smem_attr_needed(const void *func, size_t bytes);   // thread-safe cache lookup/insert

@@ -182,16 +182,6 @@ __device__ __forceinline__ void accum_depth(const uint2 *__restrict__ pwcol,
     }
 }
 
-// ---------------------------------------------------------------------------
-// 16-byte asynchronous global -> shared copies (zero-filled when bytes == 0).
-__device__ __forceinline__ void cp_async16(void *smem_dst, const void *gmem_src, int bytes) {
-    const unsigned d = (unsigned)__cvta_generic_to_shared(smem_dst);
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(d), "l"(gmem_src), "r"(bytes)
-                 : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory"); }
 
 // ---------------------------------------------------------------------------
 // CTA-wide threshold selection, S selections at once.
@@ -934,13 +924,18 @@ scan_kernel(int n, int cb, int ctok, int D, int chunk_blocks, int source, size_t
     // key this CTA dropped is < its threshold
     if constexpr (!kFix) {
         if (k_sel > 0) {
+            // m: four times this CTA's expected share of the k' winners, for the
+            // sub-chunks it actually scored (a CTA that took more of them may hold
+            // more winners; cutting its list to the average share would raise its
+            // threshold above the k'-th key and force a rescan)
+            const int m_eff = min(k_sel, max(m_sel, (int)(((long long)4 * k_sel * iter + n_sub - 1) / n_sub)));
             int cs[G];
             bool fits = true, any_long = false;
 #pragma unroll
             for (int h = 0; h < G; ++h) {
                 cs[h] = min(sm.cnt[h], cap);
                 fits = fits && cs[h] <= kMultiKPT * NT;
-                any_long = any_long || cs[h] > 2 * m_sel;
+                any_long = any_long || cs[h] > 2 * m_eff;
             }
             if (fits && any_long) {
                 uint64_t *lists = cand + cta * G * (size_t)cap;
@@ -956,7 +951,7 @@ scan_kernel(int n, int cb, int ctok, int D, int chunk_blocks, int source, size_t
 #pragma unroll
                     for (int i = 0; i < kMultiKPT; ++i)
                         static_for<0, G>([&](auto h) { f(h, i * NT + tid < cs[h], key_score(rk[h][i]), rk[h][i]); });
-                }, m_sel, T);
+                }, m_eff, T);
                 if (tid < G) sm.cnt[tid] = 0;
                 __syncthreads();   // every key is in registers: the lists may be overwritten
                 const int lane_ = tid & 31;
