@@ -116,6 +116,34 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory"); }
 
+// Programmatic dependent launch.  The kernels of a decode step (plan, scan,
+// merge, attention) are launched so that the next one may start while the
+// previous one is finishing: every such kernel first waits until the kernel
+// before it in the stream has completed and its writes are visible
+// (griddepcontrol.wait, a no-op when the launch had no such dependency), then
+// allows its own successor to launch.  Stream order is unchanged; only the
+// launch latency between dependent kernels overlaps the previous kernel's
+// tail.
+__device__ __forceinline__ void pdl_enter() {
+    asm volatile("griddepcontrol.wait;\n" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+}
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                              Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, (KArgs)args...);
+}
+
 // Raise a kernel's dynamic shared-memory limit once per (kernel, device, size);
 // later launches skip the driver call.
 bool smem_attr_needed(const void *func, size_t bytes);   // thread-safe cache lookup/insert

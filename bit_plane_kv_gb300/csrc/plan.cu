@@ -178,6 +178,7 @@ plan_kernel(int units, int n, int cb, int D, int G, const float *__restrict__ q,
             const float *__restrict__ var, const int32_t *__restrict__ budget,
             const double *__restrict__ bracket, uint8_t *__restrict__ depth,
             double *__restrict__ theta_out, fathom_run *__restrict__ runs) {
+    pdl_enter();
     const int u = blockIdx.x * kPlanWarps + threadIdx.x / 32;
     const int lane = threadIdx.x & 31;
     if (u >= units) return;
@@ -266,6 +267,7 @@ __global__ void __launch_bounds__(32 * kPlanWarps)
 plan_fixed_kernel(int units, int n, int cb, int D, int G, const float *__restrict__ q,
                   const float *__restrict__ var, int n_sel, int t_fixed,
                   uint8_t *__restrict__ depth, fathom_run *__restrict__ runs) {
+    pdl_enter();
     __shared__ double gs[kPlanWarps][FATHOM_MAX_D];
     const int w = threadIdx.x / 32;
     const int u = blockIdx.x * kPlanWarps + w;
@@ -295,16 +297,18 @@ int launch_plan(const fathom_shape &s, const float *q, const float *var, const i
                 const double *bracket, uint8_t *depth, double *theta, fathom_run *runs,
                 cudaStream_t st) {
     const int grid = (s.units + kPlanWarps - 1) / kPlanWarps;
-    plan_kernel<<<grid, 32 * kPlanWarps, 0, st>>>(s.units, s.n, cap_blocks(s), s.D, s.G, q, var, budget, bracket,
-                                                  depth, theta, runs);
+    const cudaError_t e = launch_pdl(plan_kernel, dim3(grid), dim3(32 * kPlanWarps), 0, st, s.units, s.n,
+                                     cap_blocks(s), s.D, s.G, q, var, budget, bracket, depth, theta, runs);
+    if (e != cudaSuccess) { set_error("plan_kernel: %s", cudaGetErrorString(e)); return FATHOM_ECUDA; }
     return launch_status("plan_kernel");
 }
 
 int launch_plan_fixed(const fathom_shape &s, const float *q, const float *var, int n_sel,
                       int t_fixed, uint8_t *depth, fathom_run *runs, cudaStream_t st) {
     const int grid = (s.units + kPlanWarps - 1) / kPlanWarps;
-    plan_fixed_kernel<<<grid, 32 * kPlanWarps, 0, st>>>(s.units, s.n, cap_blocks(s), s.D, s.G, q, var, n_sel,
-                                                        t_fixed, depth, runs);
+    const cudaError_t e = launch_pdl(plan_fixed_kernel, dim3(grid), dim3(32 * kPlanWarps), 0, st, s.units, s.n,
+                                     cap_blocks(s), s.D, s.G, q, var, n_sel, t_fixed, depth, runs);
+    if (e != cudaSuccess) { set_error("plan_fixed_kernel: %s", cudaGetErrorString(e)); return FATHOM_ECUDA; }
     return launch_status("plan_fixed_kernel");
 }
 

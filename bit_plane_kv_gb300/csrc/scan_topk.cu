@@ -512,6 +512,7 @@ scan_kernel(int n, int cb, int ctok, int D, int chunk_blocks, int source, size_t
             uint64_t *__restrict__ cand, int *__restrict__ cand_cnt, uint64_t *__restrict__ cand_tau,
             int *__restrict__ flags, float *__restrict__ forced_scores, int *__restrict__ sub_ctr,
             int *__restrict__ sub_owner) {
+    pdl_enter();
     extern __shared__ __align__(16) unsigned char smem_raw[];
     ScanSmem<G> &sm = *reinterpret_cast<ScanSmem<G> *>(smem_raw);
     const int tid = threadIdx.x;
@@ -1201,6 +1202,7 @@ merge_kernel(int n, int G, int k, int k_sel, int ns, int r0, int nf, int chunks,
              const float *__restrict__ forced_scores, uint64_t *__restrict__ part_keys,
              int *__restrict__ part_cnt, unsigned *__restrict__ ticket, int32_t *__restrict__ out_idx,
              float *__restrict__ out_score, int *__restrict__ sub_ctr) {
+    pdl_enter();
     extern __shared__ __align__(16) unsigned char msmem_raw[];
     MergeSmem &sm = *reinterpret_cast<MergeSmem *>(msmem_raw);
     const int p = blockIdx.x, h = blockIdx.y, u = blockIdx.z;
@@ -1359,13 +1361,13 @@ static int launch_g(const fathom_shape &s, const uint64_t *planes, const uint16_
     ensure_smem(merge_kernel, msmem);
     const int nf = f.nf > 0 ? f.nf : 1;
     dim3 grid(sg.chunks, s.units);
+    cudaError_t le = cudaSuccess;
     for (int pass = 0; pass < 2; ++pass) {
 #define FATHOM_SCAN_LAUNCH(FIX, SC, RW)                                                                    \
-    scan_kernel<G, FIX, SC, RW><<<grid, NT, smem, st>>>(s.n, cb, cap_tokens(s), s.D, sg.chunk_blocks, source, \
-                                                        stage_words, stage_scales, planes, scales, runs, q,   \
-                                                        k_sel, m_sel, m_first, f.ns, f.r0, nf, cap, vec,      \
-                                                        SC ? scores_opt : nullptr, cand, cnt, ctau, flags,    \
-                                                        forced, sub_ctr, sub_owner)
+    le = launch_pdl(scan_kernel<G, FIX, SC, RW>, grid, dim3(NT), smem, st, s.n, cb, cap_tokens(s), s.D,        \
+                    sg.chunk_blocks, source, stage_words, stage_scales, planes, scales, runs, q, k_sel, m_sel, \
+                    m_first, f.ns, f.r0, nf, cap, vec, SC ? scores_opt : nullptr, cand, cnt, ctau, flags,      \
+                    forced, sub_ctr, sub_owner)
         if (rows_src) {
             if (pass == 1) FATHOM_SCAN_LAUNCH(true, false, true);
             else if (scores_opt) FATHOM_SCAN_LAUNCH(false, true, true);
@@ -1376,11 +1378,14 @@ static int launch_g(const fathom_shape &s, const uint64_t *planes, const uint16_
             else FATHOM_SCAN_LAUNCH(false, false, false);
         }
 #undef FATHOM_SCAN_LAUNCH
+        if (le != cudaSuccess) { set_error("scan_kernel: %s", cudaGetErrorString(le)); return FATHOM_ECUDA; }
         int rc = launch_status("scan_kernel");
         if (rc) return rc;
-        merge_kernel<<<dim3(wl.parts, s.G, s.units), kMThreads, msmem, st>>>(
-            s.n, s.G, s.k, k_sel, f.ns, f.r0, nf, sg.chunks, wl.parts, cap, pass, cand, cnt, ctau,
-            flags, dirty, forced, pkeys, pcnt, ticket, idx, score, sub_ctr);
+        le = launch_pdl(merge_kernel, dim3(wl.parts, s.G, s.units), dim3(kMThreads), msmem, st, s.n, s.G, s.k, k_sel,
+                        f.ns, f.r0, nf, sg.chunks, wl.parts, cap, pass, (const uint64_t *)cand, (const int *)cnt,
+                        (const uint64_t *)ctau, flags, dirty, (const float *)forced, pkeys, pcnt, ticket, idx, score,
+                        sub_ctr);
+        if (le != cudaSuccess) { set_error("merge_kernel: %s", cudaGetErrorString(le)); return FATHOM_ECUDA; }
         rc = launch_status("merge_kernel");
         if (rc) return rc;
         if (k_sel == 0) break;   // nothing selected: no second pass needed

@@ -345,6 +345,7 @@ attn_kernel(int n, int ctok, int D, int k, int rows_cta, int cph, int splits, co
             const uint16_t *__restrict__ vrows, const float *__restrict__ q,
             const int32_t *__restrict__ topk, float *__restrict__ out, float *__restrict__ part,
             unsigned *__restrict__ ticket) {
+    pdl_enter();
     constexpr int RB = AttnBatch<G>::RB;
     extern __shared__ __align__(16) unsigned char asmem_raw[];
     AttnHeader &sm = *reinterpret_cast<AttnHeader *>(asmem_raw);
@@ -518,14 +519,15 @@ static int launch_sparse_attn_src(const fathom_shape &s, const KSource &ks, cons
     do {                                                                                                  \
         if (planes) {                                                                                     \
             ensure_smem(attn_kernel<GG, VV, true>, smem);                                                 \
-            attn_kernel<GG, VV, true><<<grid, NA, smem, st>>>(s.n, cap_tokens(s), s.D, s.k, wl.rows, cph,  \
-                                                              wl.splits, ks, vrows, q, idx, out, part, ticket); \
+            le = launch_pdl(attn_kernel<GG, VV, true>, grid, dim3(NA), smem, st, s.n, cap_tokens(s), s.D, s.k, \
+                            wl.rows, cph, wl.splits, ks, vrows, q, idx, out, part, ticket);               \
         } else {                                                                                          \
             ensure_smem(attn_kernel<GG, VV, false>, smem);                                                \
-            attn_kernel<GG, VV, false><<<grid, NA, smem, st>>>(s.n, cap_tokens(s), s.D, s.k, wl.rows, cph, \
-                                                               wl.splits, ks, vrows, q, idx, out, part, ticket); \
+            le = launch_pdl(attn_kernel<GG, VV, false>, grid, dim3(NA), smem, st, s.n, cap_tokens(s), s.D,  \
+                            s.k, wl.rows, cph, wl.splits, ks, vrows, q, idx, out, part, ticket);          \
         }                                                                                                 \
     } while (0)
+    cudaError_t le = cudaSuccess;
     switch (s.G * 2 + (vec ? 1 : 0)) {
         case 2: FATHOM_ATTN_LAUNCH(1, false); break;
         case 3: FATHOM_ATTN_LAUNCH(1, true); break;
@@ -538,6 +540,7 @@ static int launch_sparse_attn_src(const fathom_shape &s, const KSource &ks, cons
         default: set_error("sparse_attn: unsupported G=%d", s.G); return FATHOM_EINVAL;
     }
 #undef FATHOM_ATTN_LAUNCH
+    if (le != cudaSuccess) { set_error("attn_kernel: %s", cudaGetErrorString(le)); return FATHOM_ECUDA; }
     return launch_status("attn_kernel");
 }
 
