@@ -99,9 +99,11 @@ __device__ __forceinline__ void write_plan(int u, int lane, int D, int nb, int c
 
 // The (B+1)-th largest breakpoint b_{j,m} = g_j * 2^-(2m+1) over the warp's
 // channels (with multiplicity), by an MSD radix select on the bit patterns
-// (positive doubles order like their bit patterns).  `bp` holds the lane's 16
-// patterns (0 for channels past D or g_j <= 0); hist is the warp's 256 bins.
-// Requires more than B positive breakpoints.
+// (positive doubles order like their bit patterns), ranking the last bucket's
+// keys directly once it holds at most 32.  `bp` holds the lane's 16 patterns
+// (0 for channels past D or g_j <= 0); hist is the warp's 256 bins (also the
+// 32 candidate slots of the final ranking).  Requires more than B positive
+// breakpoints.
 __device__ unsigned long long critical_breakpoint(const unsigned long long (&bp)[4 * kCh], int B,
                                                   unsigned *hist) {
     const int lane = threadIdx.x & 31;
@@ -160,13 +162,37 @@ __device__ unsigned long long critical_breakpoint(const unsigned long long (&bp)
         pmask |= dmask << lo;
         need -= above;
         if (lo == 0) return prefix;              // every bit decided: this value
-        if (bucket == 1) {                        // one candidate left: find it exactly
-            unsigned long long v = ~0ull;
+        if (bucket <= 32) {
+            // few candidates left: gather them (lane order) and rank each against
+            // the others; the need-th largest is the one with fewer than `need`
+            // candidates above it and at least `need` at or above it
+            unsigned long long *cand = reinterpret_cast<unsigned long long *>(hist);   // 32 slots
+            int mine = 0;
+#pragma unroll
+            for (int e = 0; e < 4 * kCh; ++e) mine += (bp[e] && (bp[e] & pmask) == prefix) ? 1 : 0;
+            int incl = mine;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += y;
+            }
+            __syncwarp();
+            int pos = incl - mine;
 #pragma unroll
             for (int e = 0; e < 4 * kCh; ++e)
-                if (bp[e] && (bp[e] & pmask) == prefix) v = min(v, bp[e]);
-#pragma unroll
-            for (int o = 16; o; o >>= 1) v = min(v, __shfl_xor_sync(0xffffffffu, v, o));
+                if (bp[e] && (bp[e] & pmask) == prefix) cand[pos++] = bp[e];
+            __syncwarp();
+            const unsigned long long x = lane < bucket ? cand[lane] : 0ull;
+            int gt = 0, ge = 0;
+            for (int j = 0; j < bucket; ++j) {
+                const unsigned long long y = cand[j];
+                gt += y > x ? 1 : 0;
+                ge += y >= x ? 1 : 0;
+            }
+            const bool hit = lane < bucket && gt < need && ge >= need;
+            const unsigned who = __ballot_sync(0xffffffffu, hit);
+            const unsigned long long v = __shfl_sync(0xffffffffu, x, __ffs(who) - 1);
+            __syncwarp();
             return v;
         }
         hi_bit = lo - 1;
@@ -240,7 +266,7 @@ plan_kernel(int units, int n, int cb, int D, int G, const float *__restrict__ q,
         }
         exact_bp = __all_sync(0xffffffffu, exact_bp);
         if (exact_bp) {
-            __shared__ unsigned hist_s[kPlanWarps][256];
+            __shared__ __align__(16) unsigned hist_s[kPlanWarps][256];   // 8-byte slots reuse it
             const double bstar = __longlong_as_double(
                 (long long)critical_breakpoint(bp, B, hist_s[threadIdx.x / 32]));
             for (int it = 0; it < 30; ++it) {
