@@ -39,10 +39,10 @@ METRIC = "decode-step µs/layer and scan GB/s (% of PCIe/HBM roofline) at 1M tok
 CLOCK_FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
                 "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
                 "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
-# Measured DRAM traffic of the first-pass scan over its algorithmic bytes (planned plane
-# runs + active-channel scales), from a full ncu capture of one HBM-resident layer of
-# host_256k: 14.42 MB read for 14.7 MB planned.
-SCAN_DRAM_PER_ALGO_BYTE = 14.42 / 14.70
+# Measured DRAM traffic (read + write) of the first-pass scan over its algorithmic bytes
+# (planned plane runs + active-channel scales), from a full ncu capture of one HBM-resident
+# layer of host_1m: 56.65 MB read + 1.18 MB written (candidate lists) for 56.85 MB planned.
+SCAN_DRAM_PER_ALGO_BYTE = (56.65 + 1.18) / 56.85
 
 
 def log(*a):
@@ -786,7 +786,7 @@ def main():
         roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
                 "traffic": scanned * SCAN_DRAM_PER_ALGO_BYTE, "kernel": "scan_kernel",
                 "traffic_note": "DRAM bytes per layer's first-pass scan launch: the measured DRAM/algorithmic "
-                                "ratio of a one-layer host_256k ncu capture times this run's planned bytes",
+                                "ratio of a one-layer host_1m ncu capture times this run's planned bytes",
                 "peak_source": f"{peak_src} HBM copy peak (MEASURED_PEAKS.json hbm_gbs)",
                 "note": "scanned bytes per layer / the scan_topk call's time (scan + merge kernels)"}
     line = {
