@@ -10,9 +10,13 @@
 // steps of geometric bisection mid = sqrt(lo * hi) that keep hi feasible
 // (sum_j t_j(hi) <= B); the plan is t(hi).  Every fp64 operation is an
 // explicitly rounded IEEE operation (no contraction), so the result is
-// reproducible bit for bit on any IEEE machine.  The whole plan stays on the
+// reproducible bit for bit on any IEEE machine.  The bisection's square roots
+// come from exact_sqrt.cuh (the same bits as the fp64 square root, without its
+// long latency on this part) whenever every lo * hi of the chain is a normal
+// double.  The whole plan stays on the
 // device: the run list has one slot per channel (zero length when t_j = 0),
 // so nothing needs to come back to the host.
+#include "exact_sqrt.cuh"
 #include "fathom_internal.cuh"
 
 namespace fathom {
@@ -269,9 +273,19 @@ plan_kernel(int units, int n, int cb, int D, int G, const float *__restrict__ q,
             __shared__ __align__(16) unsigned hist_s[kPlanWarps][256];   // 8-byte slots reuse it
             const double bstar = __longlong_as_double(
                 (long long)critical_breakpoint(bp, B, hist_s[threadIdx.x / 32]));
-            for (int it = 0; it < 30; ++it) {
-                const double mid = __dsqrt_rn(__dmul_rn(lo, hi));
-                if (mid > bstar) hi = mid; else lo = mid;
+            const long long elo = __double_as_longlong(lo) >> 52, ehi = __double_as_longlong(hi) >> 52;
+            if (elo >= 1023 - 511 && ehi <= 1023 + 510) {
+                // lo * hi stays a normal double on every step: integer square root
+                for (int it = 0; it < 30; ++it) {
+                    const double mid = __longlong_as_double(
+                        (long long)xsqrt::sqrt_rn((uint64_t)__double_as_longlong(__dmul_rn(lo, hi))));
+                    if (mid > bstar) hi = mid; else lo = mid;
+                }
+            } else {
+                for (int it = 0; it < 30; ++it) {
+                    const double mid = __dsqrt_rn(__dmul_rn(lo, hi));
+                    if (mid > bstar) hi = mid; else lo = mid;
+                }
             }
         } else {
             for (int it = 0; it < 30; ++it) {
