@@ -120,11 +120,11 @@ int scan_m_sel(int chunks, int k_sel) {
 
 int scan_m_first(int n_sub, int k_sel, int m_sel) {
     // rank of the threshold taken from a CTA's first sub-chunk: twice the
-    // expected winners of one sub-chunk, at least 16, at most m (a sub-chunk
+    // expected winners of one sub-chunk, at least 8, at most m (a sub-chunk
     // holding more winners than that makes its CTA rescan them exactly)
     if (k_sel <= 0) return 0;
     int m = (2 * k_sel + n_sub - 1) / n_sub;
-    m = m < 16 ? 16 : m;
+    m = m < 8 ? 8 : m;
     return m > m_sel ? m_sel : m;
 }
 
