@@ -28,11 +28,10 @@
 // the workspace and a threshold key tau; a token is appended only if its key
 // >= tau.  tau starts as a key of the CTA's first sub-chunk (selected straight
 // from registers for all heads at once: m1 of the threads' best keys, and so
-// at least m1 of the sub-chunk's keys, lie at or above it), m1 being four
-// times the winners a sub-chunk holds on average; at the end every list is
-// cut back to m .. 2m keys, m
-// being four times the CTA's expected share of the k' winners (a list about
-// to overflow is cut the same way on the way).  The merge kernel streams
+// at least m1 of the sub-chunk's keys, lie at or above it), m1 being twice
+// the winners a sub-chunk holds on average (at least 8); at the end a list
+// longer than 4m is cut back to m .. 2m keys, m being four times the CTA's
+// expected share of the k' winners for the sub-chunks it scored.  The merge kernel streams
 // the lists through shared memory (P CTAs per (unit, head), the last of
 // which, by an atomic ticket, merges the P partial results), selects the
 // exact top-k', adds the forced tokens and writes the kept set in ascending
@@ -920,8 +919,8 @@ scan_kernel(int n, int cb, int ctok, int D, int chunk_blocks, int source, size_t
     }
     if (piped) cp_async_wait<0>();
 
-    // ---- shrink long lists (first pass: to about m .. 2m keys by one histogram
-    // pass; second pass: exactly k'), then publish counts and thresholds: every
+    // ---- shrink long lists (first pass: lists longer than 4m to about m .. 2m keys
+    // by one histogram pass; second pass: exactly k'), then publish counts and thresholds: every
     // key this CTA dropped is < its threshold
     if constexpr (!kFix) {
         if (k_sel > 0) {
@@ -936,7 +935,7 @@ scan_kernel(int n, int cb, int ctok, int D, int chunk_blocks, int source, size_t
             for (int h = 0; h < G; ++h) {
                 cs[h] = min(sm.cnt[h], cap);
                 fits = fits && cs[h] <= kMultiKPT * NT;
-                any_long = any_long || cs[h] > 2 * m_eff;
+                any_long = any_long || cs[h] > 4 * m_eff;
             }
             if (fits && any_long) {
                 uint64_t *lists = cand + cta * G * (size_t)cap;
