@@ -22,7 +22,12 @@
  * - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
  *   stream).  Every call only enqueues work on that stream: no host
  *   synchronisation, no host read of device results.  Results are valid once
- *   the stream reaches them.
+ *   the stream reaches them.  The kernels of fathom_plan, fathom_plan_fixed,
+ *   fathom_scan_topk, fathom_exact_topk, fathom_sparse_attn,
+ *   fathom_sparse_attn_planes and fathom_sparse_attn_noalloc are launched with
+ *   programmatic stream serialisation: each may be scheduled while the work before it on
+ *   the stream is finishing, but it waits for that work to complete before
+ *   it reads or writes memory, so the stream order is unchanged.
  * - Every call returns a fathom_status.  Argument errors return FATHOM_EINVAL
  *   before anything is enqueued; CUDA launch errors return FATHOM_ECUDA.
  *   fathom_last_error() returns the calling thread's last message.  Nothing
