@@ -497,7 +497,21 @@ def workload_config(w: synth.Workload, args) -> dict:
             "basis": "rotated (KLT per layer and KV head)" if w.rotated else "channels",
             "regime": w.regime, "path": path,
             "unit_groups": args.groups if path == "pipelined" else 1,
-            "l2": "inputs larger than L2 (store and rows of all layers > 129 MB)"}
+            "l2": l2_note(w)}
+
+
+L2_BYTES = 129 << 20      # GB300 L2
+
+
+def l2_note(w: synth.Workload) -> str:
+    """Whether the step's inputs exceed L2 (the timing rule: inputs larger than L2,
+    or an L2 flush between timed steps; this bench never flushes)."""
+    store = w.units * w.n * (w.D // 2 + w.D // 32)      # 4 plane bits + a 16-bit scale per 64 tokens
+    rows = w.units * w.n * w.D * 2 * 2                   # bf16 K and V rows
+    mb = (store + rows) / 2**20
+    if store + rows > L2_BYTES:
+        return f"inputs larger than L2 (store and rows of all layers: {mb:.0f} MiB > 129 MiB)"
+    return f"inputs fit in L2 ({mb:.1f} MiB): L2-resident, latency-bound; no HBM roofline claim"
 
 
 def run_reference(args, w, rank, world):
