@@ -2,6 +2,7 @@
 // reporting and workspace layouts.  All arithmetic lives in the kernels.
 #include <stdarg.h>
 #include <stdio.h>
+#include <stdlib.h>
 #include <string.h>
 
 #include <mutex>
@@ -233,6 +234,39 @@ static int check_shape(const fathom_shape *s, bool need_select) {
         if (!(p)) { set_error("%s is NULL", #p); return FATHOM_EINVAL; } \
     } while (0)
 
+// Host-side fault injection, for testing how callers handle a failed launch
+// without faulting a GPU.  FATHOM_FAULT (read once per process) holds a
+// comma-separated list of sites: "launch" makes every call that would enqueue
+// GPU work fail, "launch:<name>" only the named call (e.g.
+// launch:fathom_scan_topk).  A failing call has already validated its
+// arguments; it enqueues nothing and returns FATHOM_ECUDA with a message that
+// names the injected fault.  Unset (the default), nothing is injected.
+static bool fault_injected(const char *entry) {
+    static const char *spec = [] {
+        const char *e = getenv("FATHOM_FAULT");
+        return (e && *e) ? e : (const char *)nullptr;
+    }();
+    if (!spec) return false;
+    const size_t n = strlen(entry);
+    for (const char *p = spec; *p;) {
+        const char *end = strchr(p, ',');
+        const size_t len = end ? (size_t)(end - p) : strlen(p);
+        if (len == 6 && strncmp(p, "launch", 6) == 0) return true;
+        if (len == 7 + n && strncmp(p, "launch:", 7) == 0 && strncmp(p + 7, entry, n) == 0) return true;
+        if (!end) break;
+        p = end + 1;
+    }
+    return false;
+}
+
+#define FAULT_POINT(name)                                                              \
+    do {                                                                               \
+        if (fault_injected(name)) {                                                    \
+            set_error("%s: injected launch failure (FATHOM_FAULT)", name);             \
+            return FATHOM_ECUDA;                                                       \
+        }                                                                              \
+    } while (0)
+
 extern "C" {
 
 const char *fathom_last_error(void) { return g_err; }
@@ -248,6 +282,7 @@ int fathom_calibrate(int32_t units, int32_t m, int32_t D, const float *calib, fl
     }
     NONNULL(calib);
     NONNULL(var_out);
+    FAULT_POINT("fathom_calibrate");
     return launch_calibrate(units, m, D, calib, mean_out, var_out, (cudaStream_t)stream);
 }
 
@@ -262,6 +297,7 @@ int fathom_calibrate_klt(int32_t groups, int32_t m, int32_t D, const float *cali
     NONNULL(mean);
     NONNULL(V);
     NONNULL(lambda);
+    FAULT_POINT("fathom_calibrate_klt");
     return launch_calibrate_klt(groups, m, D, calib, mean, V, lambda, (cudaStream_t)stream);
 }
 
@@ -278,6 +314,7 @@ int fathom_rotate_keys(const fathom_shape *shape, const void *keys, int keys_dty
     NONNULL(mean);
     NONNULL(V);
     NONNULL(out);
+    FAULT_POINT("fathom_rotate_keys");
     return launch_rotate_keys(*shape, keys, keys_dtype, groups, mean, V, out, (cudaStream_t)stream);
 }
 
@@ -291,6 +328,7 @@ int fathom_rotate_query(const fathom_shape *shape, const float *q, int32_t group
     NONNULL(q);
     NONNULL(V);
     NONNULL(q_rot);
+    FAULT_POINT("fathom_rotate_query");
     return launch_rotate_query(*shape, q, groups, V, q_rot, (cudaStream_t)stream);
 }
 
@@ -310,6 +348,7 @@ int fathom_append_block(const fathom_shape *shape, const void *keys, int keys_dt
     NONNULL(keys);
     NONNULL(planes);
     NONNULL(scales);
+    FAULT_POINT("fathom_append_block");
     return launch_append(*shape, keys, keys_dtype, block, count, planes, scales, (cudaStream_t)stream);
 }
 
@@ -324,6 +363,7 @@ int fathom_quantize_pack(const fathom_shape *shape, const void *keys, int keys_d
     NONNULL(keys);
     NONNULL(planes);
     NONNULL(scales);
+    FAULT_POINT("fathom_quantize_pack");
     return launch_quantize(*shape, keys, keys_dtype, planes, scales, (cudaStream_t)stream);
 }
 
@@ -339,6 +379,7 @@ int fathom_plan(const fathom_shape *shape, const float *q, const float *var, con
     NONNULL(depth);
     NONNULL(theta);
     NONNULL(runs);
+    FAULT_POINT("fathom_plan");
     return launch_plan(*shape, q, var, budget, bracket, depth, theta, runs, (cudaStream_t)stream);
 }
 
@@ -356,6 +397,7 @@ int fathom_plan_fixed(const fathom_shape *shape, const float *q, const float *va
     NONNULL(var);
     NONNULL(depth);
     NONNULL(runs);
+    FAULT_POINT("fathom_plan_fixed");
     return launch_plan_fixed(*shape, q, var, n_channels, depth_each, depth, runs,
                              (cudaStream_t)stream);
 }
@@ -372,6 +414,7 @@ int fathom_gather(const fathom_shape *shape, const uint64_t *store_planes,
     NONNULL(stage_planes);
     NONNULL(stage_scales);
     if (stage_words < 1 || stage_scales_n < 1) { set_error("empty staging area"); return FATHOM_EINVAL; }
+    FAULT_POINT("fathom_gather");
     return launch_gather(*shape, store_planes, store_scales, runs, stage_planes, stage_scales,
                          stage_words, stage_scales_n, (cudaStream_t)stream);
 }
@@ -414,6 +457,7 @@ int fathom_scan_topk(const fathom_shape *shape, const uint64_t *planes, const ui
         return FATHOM_ENOMEM;
     }
     if (((uintptr_t)workspace & 255) != 0) { set_error("workspace must be 256-byte aligned"); return FATHOM_EINVAL; }
+    FAULT_POINT("fathom_scan_topk");
     return launch_scan_topk(*shape, planes, scales, source, stage_words, stage_scales_n, runs, q,
                             topk_idx, topk_score, scores_opt, workspace, (cudaStream_t)stream);
 }
@@ -435,6 +479,7 @@ int fathom_exact_topk(const fathom_shape *shape, const uint16_t *k_rows, const f
         return FATHOM_ENOMEM;
     }
     if (((uintptr_t)workspace & 255) != 0) { set_error("workspace must be 256-byte aligned"); return FATHOM_EINVAL; }
+    FAULT_POINT("fathom_exact_topk");
     return launch_scan_topk(*shape, (const uint64_t *)k_rows, nullptr, FATHOM_SRC_ROWS, 0, 0, nullptr, q,
                             topk_idx, topk_score, scores_opt, workspace, (cudaStream_t)stream);
 }
@@ -458,6 +503,7 @@ int fathom_sparse_attn_planes(const fathom_shape *shape, const uint64_t *planes,
         return FATHOM_ENOMEM;
     }
     if (((uintptr_t)workspace & 255) != 0) { set_error("workspace must be 256-byte aligned"); return FATHOM_EINVAL; }
+    FAULT_POINT("fathom_sparse_attn_planes");
     return launch_sparse_attn_planes(*shape, planes, scales, v_rows, q, topk_idx, out, workspace,
                                      (cudaStream_t)stream);
 }
@@ -478,6 +524,7 @@ int fathom_dense_attn(const fathom_shape *shape, const uint16_t *k_rows, const u
         return FATHOM_ENOMEM;
     }
     if (((uintptr_t)workspace & 255) != 0) { set_error("workspace must be 256-byte aligned"); return FATHOM_EINVAL; }
+    FAULT_POINT("fathom_dense_attn");
     return launch_dense_attn(*shape, k_rows, v_rows, q, out, workspace, (cudaStream_t)stream);
 }
 
@@ -498,6 +545,7 @@ int fathom_klt_online(const fathom_shape *shape, const uint16_t *k_rows, double 
         return FATHOM_ENOMEM;
     }
     if (((uintptr_t)workspace & 255) != 0) { set_error("workspace must be 256-byte aligned"); return FATHOM_EINVAL; }
+    FAULT_POINT("fathom_klt_online");
     return launch_klt_online(*shape, k_rows, mean, V, lambda, workspace, (cudaStream_t)stream);
 }
 
@@ -508,6 +556,7 @@ int fathom_rel_err(int32_t rows, int32_t D, const float *a, const float *ref, do
     NONNULL(a);
     NONNULL(ref);
     NONNULL(err);
+    FAULT_POINT("fathom_rel_err");
     return launch_rel_err(rows, D, a, ref, err, (cudaStream_t)stream);
 }
 
@@ -519,6 +568,7 @@ int fathom_set_overlap(int32_t rows, int32_t k, const int32_t *a, const int32_t 
     NONNULL(a);
     NONNULL(b);
     NONNULL(count);
+    FAULT_POINT("fathom_set_overlap");
     return launch_set_overlap(rows, k, a, b, count, (cudaStream_t)stream);
 }
 
@@ -560,6 +610,7 @@ int fathom_sparse_attn(const fathom_shape *shape, const uint16_t *k_rows, const 
         return FATHOM_ENOMEM;
     }
     if (((uintptr_t)workspace & 255) != 0) { set_error("workspace must be 256-byte aligned"); return FATHOM_EINVAL; }
+    FAULT_POINT("fathom_sparse_attn");
     return launch_sparse_attn(*shape, k_rows, v_rows, q, topk_idx, out, workspace,
                               (cudaStream_t)stream);
 }
@@ -575,6 +626,7 @@ int fathom_sparse_attn_noalloc(const fathom_shape *shape, const uint16_t *k_rows
     NONNULL(q);
     NONNULL(topk_idx);
     NONNULL(out);
+    FAULT_POINT("fathom_sparse_attn_noalloc");
     return launch_sparse_attn_noalloc(*shape, k_rows, v_rows, q, topk_idx, out, (cudaStream_t)stream);
 }
 

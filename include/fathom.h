@@ -33,6 +33,13 @@
  *   fathom_last_error() returns the calling thread's last message.  Nothing
  *   throws across this ABI and nothing aborts the process.
  * - Inputs are never modified.  Outputs may not alias inputs.
+ * - Fault injection (for testing a caller's error handling without a GPU
+ *   fault): the environment variable FATHOM_FAULT, read once per process,
+ *   holds a comma-separated list of sites.  "launch" makes every call that
+ *   would enqueue GPU work return FATHOM_ECUDA after its argument checks,
+ *   with nothing enqueued; "launch:<call name>" (e.g.
+ *   launch:fathom_scan_topk) does so for that call only.  The message names
+ *   the injected fault.  Unset, nothing is injected.
  *
  * Capacity
  * --------
