@@ -136,6 +136,18 @@ def test_prefix_identity_exhaustive(a):
     assert O.dequant(5, 0, a) == 0.0
 
 
+@pytest.mark.parametrize("a", [1.0, 0.5, 0.37109375, 3.0])
+def test_prefix_value_is_a_signed_binary_expansion(a):
+    # Each plane read halves the cell: the t-plane value is the sum over the read
+    # planes p = 0..t-1 (0 = MSB) of +a/2^(p+1) where the plane's bit is 1 and
+    # -a/2^(p+1) where it is 0 (a bisection of [-a, a) that starts at 0).
+    for c in range(16):
+        for t in range(0, 5):
+            bits = [(c >> (3 - p)) & 1 for p in range(t)]
+            x = sum((1 if b else -1) * a / 2 ** (p + 1) for p, b in enumerate(bits))
+            assert O.dequant(c >> (4 - t), t, a) == x, (c, t)
+
+
 def test_error_law_a2_over_3_4t():
     rng = np.random.default_rng(7)
     nblk = 16384
