@@ -39,10 +39,6 @@ METRIC = "decode-step µs/layer and scan GB/s (% of PCIe/HBM roofline) at 1M tok
 CLOCK_FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
                 "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
                 "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
-# Measured DRAM traffic (read + write) of the first-pass scan over its algorithmic bytes
-# (planned plane runs + active-channel scales), from a full ncu capture of one HBM-resident
-# layer of host_1m: 56.65 MB read + 1.18 MB written (candidate lists) for 56.85 MB planned.
-SCAN_DRAM_PER_ALGO_BYTE = (56.65 + 1.18) / 56.85
 
 
 def log(*a):
@@ -828,9 +824,10 @@ def main():
         hbm = peaks["hbm_gbs"]
         achieved = scanned / kern_avg / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-                "traffic": scanned * SCAN_DRAM_PER_ALGO_BYTE, "kernel": "scan_kernel",
-                "traffic_note": "DRAM bytes per layer's first-pass scan launch: the measured DRAM/algorithmic "
-                                "ratio of a one-layer host_1m ncu capture times this run's planned bytes",
+                "traffic": None, "kernel": "scan_kernel",
+                "traffic_note": "no DRAM counters of the current scan kernel: the last full ncu capture (one "
+                                "HBM-resident host_1m layer, an earlier build of the kernel) read 56.65 MB and "
+                                "wrote 1.18 MB for 56.85 MB of planned bytes",
                 "peak_source": f"{peak_src} HBM copy peak (MEASURED_PEAKS.json hbm_gbs)",
                 "note": "scanned bytes per layer / the scan_topk call's time (scan + merge kernels)"}
     line = {
