@@ -584,10 +584,12 @@ def main():
         st.step(s)
     torch.cuda.synchronize()
     plan_bytes = [0] * st.L
+    active = [0.0] * st.L                 # mean active channels (t_j > 0) per unit, per layer
     for l in range(st.L):
         st.layer(l, st.Q[0, l])
         torch.cuda.synchronize()
         plan_bytes[l] = st.planned_bytes()
+        active[l] = float((st.depth > 0).sum().item()) / st.H
 
     # CPU time to issue one eager step (the Python binding's per-call cost)
     torch.cuda.synchronize()
@@ -839,6 +841,7 @@ def main():
         "scan_gbs": scan_gbs,
         "scanned_bytes_per_layer": scanned,
         "scanned_bits_per_token": bits_per_token,
+        "active_channels_per_unit": statistics.mean(active),
         "roofline": roof,
         "e2e": {"value": e2e_us_layer, "unit": "µs/layer",
                 "h2d_bytes_per_step": int(st.Q[0].numel() * 4), "d2h_bytes_per_step": int(st.out.numel() * 4)},
