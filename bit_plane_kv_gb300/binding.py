@@ -115,18 +115,50 @@ def _stream(stream=None):
     return ctypes.c_void_p(stream.cuda_stream)
 
 
-def _check(t, name, dtypes, shape=None, dev=True):
+def _check(t, name, dtypes, shape=None, dev=True, min_numel=None):
+    """Dtype, shape (exact), size (at least min_numel elements: the library sees only
+    a pointer, so a shorter tensor would be read or written past its end),
+    contiguity, and memory the GPU can reach, in that order."""
     if t is None:
         raise ValueError(f"{name} is required")
     if dtypes and t.dtype not in dtypes:
         raise TypeError(f"{name}: dtype {t.dtype} not in {dtypes}")
-    if not t.is_contiguous():
-        raise ValueError(f"{name} must be contiguous")
-    if dev and not (t.is_cuda or t.is_pinned()):
-        raise ValueError(f"{name} must be a CUDA tensor or pinned host memory")
     if shape is not None and tuple(t.shape) != tuple(shape):
         raise ValueError(f"{name}: shape {tuple(t.shape)} != {tuple(shape)}")
+    if min_numel is not None and t.numel() < min_numel:
+        raise ValueError(f"{name}: {t.numel()} elements, the call needs at least {min_numel}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dev and not _reachable(t):
+        raise ValueError(f"{name} must be a CUDA tensor or pinned host memory")
     return t
+
+
+def _reachable(t) -> bool:
+    """Memory the GPU can load from and store to: device memory or pinned host memory."""
+    return t.is_cuda or t.is_pinned()
+
+
+def _check_out(t, name, dtypes, min_numel):
+    """A caller-provided output (None: the binding allocates it)."""
+    if t is not None:
+        _check(t, name, dtypes, min_numel=min_numel)
+    return t
+
+
+def _store_words(shape: Shape) -> int:
+    """Elements of a bit-plane store [units][D][4][cap blocks]."""
+    return shape.units * shape.D * 4 * nblocks(shape.cap)
+
+
+def _store_scales(shape: Shape) -> int:
+    """Elements of the store's scales [units][D][cap blocks]."""
+    return shape.units * shape.D * nblocks(shape.cap)
+
+
+def _rows(shape: Shape) -> int:
+    """Elements of per-unit rows [units][cap][D]."""
+    return shape.units * shape.cap * shape.D
 
 
 def make_shape(units, n, D=128, G=4, k=1, n_sink=4, n_recent=32, n_cap=0) -> Shape:
@@ -156,7 +188,11 @@ def alloc_workspace(shape: Shape, which: int, device="cuda") -> torch.Tensor:
 def fathom_calibrate(calib, mean=None, var=None, stream=None):
     """calib [U][m][D] fp32 -> (mean [U][D], var [U][D]) fp32 (ddof = 1)."""
     _check(calib, "calib", (torch.float32,))
+    if calib.dim() != 3:
+        raise ValueError(f"calib: shape {tuple(calib.shape)} is not [units][m][D]")
     U, m, D = calib.shape
+    _check_out(mean, "mean", (torch.float32,), U * D)
+    _check_out(var, "var", (torch.float32,), U * D)
     if var is None:
         var = torch.empty(U, D, dtype=torch.float32, device=calib.device)
     if mean is None:
@@ -169,8 +205,13 @@ def fathom_calibrate_klt(calib, mean=None, V=None, lam=None, stream=None):
     """calib [groups][m][D] fp32 -> (mean [groups][D] fp64, V [groups][D][D] fp64 (eigenvectors
     as columns, eigenvalues descending), lambda [groups][D] fp32)."""
     _check(calib, "calib", (torch.float32,))
+    if calib.dim() != 3:
+        raise ValueError(f"calib: shape {tuple(calib.shape)} is not [groups][m][D]")
     Gr, m, D = calib.shape
     dev = calib.device
+    _check_out(mean, "mean", (torch.float64,), Gr * D)
+    _check_out(V, "V", (torch.float64,), Gr * D * D)
+    _check_out(lam, "lam", (torch.float32,), Gr * D)
     if mean is None:
         mean = torch.empty(Gr, D, dtype=torch.float64, device=dev)
     if V is None:
@@ -183,9 +224,10 @@ def fathom_calibrate_klt(calib, mean=None, V=None, lam=None, stream=None):
 
 def fathom_rotate_keys(shape: Shape, keys, groups, mean, V, out=None, stream=None):
     """keys [U][n][D] fp32 or bf16 -> (k - mu_g) V_g [U][n][D] fp32, g = u % groups."""
-    _check(keys, "keys", (torch.float32, torch.bfloat16, torch.int16))
+    _check(keys, "keys", (torch.float32, torch.bfloat16, torch.int16), min_numel=_rows(shape))
     _check(mean, "mean", (torch.float64,), (groups, shape.D))
     _check(V, "V", (torch.float64,), (groups, shape.D, shape.D))
+    _check_out(out, "out", (torch.float32,), _rows(shape))
     dt = F32 if keys.dtype == torch.float32 else BF16
     if out is None:
         out = torch.empty(shape.units, shape.cap, shape.D, dtype=torch.float32, device=keys.device)
@@ -198,6 +240,7 @@ def fathom_rotate_query(shape: Shape, q, groups, V, out=None, stream=None):
     """q [U][G][D] fp32 -> q V_g [U][G][D] fp32, g = u % groups."""
     _check(q, "q", (torch.float32,), (shape.units, shape.G, shape.D))
     _check(V, "V", (torch.float64,), (groups, shape.D, shape.D))
+    _check_out(out, "out", (torch.float32,), shape.units * shape.G * shape.D)
     if out is None:
         out = torch.empty_like(q)
     _call("fathom_rotate_query", ctypes.byref(shape), _p(q), int(groups), _p(V), _p(out), _stream(stream))
@@ -207,7 +250,9 @@ def fathom_rotate_query(shape: Shape, q, groups, V, out=None, stream=None):
 def fathom_quantize_pack(shape: Shape, keys, planes=None, scales=None, stream=None):
     """keys [U][n][D] fp32 or bf16 -> planes [U][D][4][nb] (int64 storage of u64),
     scales [U][D][nb] (int16 storage of fp16 bits)."""
-    _check(keys, "keys", (torch.float32, torch.bfloat16, torch.int16))
+    _check(keys, "keys", (torch.float32, torch.bfloat16, torch.int16), min_numel=_rows(shape))
+    _check_out(planes, "planes", (torch.int64,), _store_words(shape))
+    _check_out(scales, "scales", (torch.int16,), _store_scales(shape))
     dt = F32 if keys.dtype == torch.float32 else BF16
     nb = nblocks(shape.cap)
     dev = keys.device
@@ -241,6 +286,9 @@ def fathom_plan(shape: Shape, q, var, budget, bracket=None, depth=None, theta=No
     _check(budget, "budget", (torch.int32,), (shape.units,))
     if bracket is not None:
         _check(bracket, "bracket", (torch.float64,), (shape.units, 2))
+    _check_out(depth, "depth", (torch.uint8,), shape.units * shape.D)
+    _check_out(theta, "theta", (torch.float64,), shape.units)
+    _check_out(runs, "runs", (torch.int32,), shape.units * shape.D * 6)
     dev = q.device
     if depth is None:
         depth = torch.empty(shape.units, shape.D, dtype=torch.uint8, device=dev)
@@ -257,6 +305,8 @@ def fathom_plan_fixed(shape: Shape, q, var, n_channels, depth_each, depth=None, 
                       stream=None):
     _check(q, "q", (torch.float32,), (shape.units, shape.G, shape.D))
     _check(var, "var", (torch.float32,), (shape.units, shape.D))
+    _check_out(depth, "depth", (torch.uint8,), shape.units * shape.D)
+    _check_out(runs, "runs", (torch.int32,), shape.units * shape.D * 6)
     dev = q.device
     if depth is None:
         depth = torch.empty(shape.units, shape.D, dtype=torch.uint8, device=dev)
@@ -270,13 +320,13 @@ def fathom_plan_fixed(shape: Shape, q, var, n_channels, depth_each, depth=None, 
 def fathom_gather(shape: Shape, store_planes, store_scales, runs, stage_planes, stage_scales,
                   stream=None):
     """stage_planes [U][W] int64, stage_scales [U][S] int16 (per-unit strides W, S)."""
-    _check(store_planes, "store_planes", (torch.int64,))
-    _check(store_scales, "store_scales", (torch.int16,))
+    _check(store_planes, "store_planes", (torch.int64,), min_numel=_store_words(shape))
+    _check(store_scales, "store_scales", (torch.int16,), min_numel=_store_scales(shape))
     _check(runs, "runs", (torch.int32,), (shape.units, shape.D, 6))
-    _check(stage_planes, "stage_planes", (torch.int64,))
-    _check(stage_scales, "stage_scales", (torch.int16,))
-    W = stage_planes.shape[-1]
-    S = stage_scales.shape[-1]
+    W = stage_planes.shape[-1] if stage_planes is not None and stage_planes.dim() else 0
+    S = stage_scales.shape[-1] if stage_scales is not None and stage_scales.dim() else 0
+    _check(stage_planes, "stage_planes", (torch.int64,), min_numel=shape.units * W)
+    _check(stage_scales, "stage_scales", (torch.int16,), min_numel=shape.units * S)
     _call("fathom_gather", ctypes.byref(shape), _p(store_planes), _p(store_scales), _p(runs),
           _p(stage_planes), _p(stage_scales), W, S, _stream(stream))
     return stage_planes, stage_scales
@@ -286,11 +336,20 @@ def fathom_scan_topk(shape: Shape, planes, scales, runs, q, workspace, source=SR
                      topk_idx=None, topk_score=None, scores=None, stream=None):
     """-> topk_idx [U][G][k] int32 ascending, topk_score [U][G][k] fp32 (scores, if given,
     receives every token's score [U][G][n])."""
-    _check(planes, "planes", (torch.int64,))
-    _check(scales, "scales", (torch.int16,))
+    if source == SRC_STAGING:      # [units][W] and [units][S]: the last dimension is the per-unit stride
+        W = planes.shape[-1] if planes is not None and planes.dim() else 0
+        S = scales.shape[-1] if scales is not None and scales.dim() else 0
+        need_p, need_s = shape.units * W, shape.units * S
+    else:
+        W = S = 0
+        need_p, need_s = _store_words(shape), _store_scales(shape)
+    _check(planes, "planes", (torch.int64,), min_numel=need_p)
+    _check(scales, "scales", (torch.int16,), min_numel=need_s)
     _check(runs, "runs", (torch.int32,), (shape.units, shape.D, 6))
     _check(q, "q", (torch.float32,), (shape.units, shape.G, shape.D))
     _check(workspace, "workspace", (torch.uint8,))
+    _check_out(topk_idx, "topk_idx", (torch.int32,), shape.units * shape.G * shape.k)
+    _check_out(topk_score, "topk_score", (torch.float32,), shape.units * shape.G * shape.k)
     dev = q.device
     if topk_idx is None:
         topk_idx = torch.empty(shape.units, shape.G, shape.k, dtype=torch.int32, device=dev)
@@ -298,8 +357,6 @@ def fathom_scan_topk(shape: Shape, planes, scales, runs, q, workspace, source=SR
         topk_score = torch.empty(shape.units, shape.G, shape.k, dtype=torch.float32, device=dev)
     if scores is not None:
         _check(scores, "scores", (torch.float32,), (shape.units, shape.G, shape.n))
-    W = planes.shape[-1] if source == SRC_STAGING else 0
-    S = scales.shape[-1] if source == SRC_STAGING else 0
     _call("fathom_scan_topk", ctypes.byref(shape), _p(planes), _p(scales), int(source), W, S,
           _p(runs), _p(q), _p(topk_idx), _p(topk_score), _p(scores), _p(workspace),
           workspace.numel(), _stream(stream))
@@ -315,6 +372,8 @@ def fathom_exact_topk(shape: Shape, k_rows, q, workspace, topk_idx=None, topk_sc
     _check(k_rows, "k_rows", (torch.bfloat16, torch.int16), (shape.units, shape.cap, shape.D))
     _check(q, "q", (torch.float32,), (shape.units, shape.G, shape.D))
     _check(workspace, "workspace", (torch.uint8,))
+    _check_out(topk_idx, "topk_idx", (torch.int32,), shape.units * shape.G * shape.k)
+    _check_out(topk_score, "topk_score", (torch.float32,), shape.units * shape.G * shape.k)
     dev = q.device
     if topk_idx is None:
         topk_idx = torch.empty(shape.units, shape.G, shape.k, dtype=torch.int32, device=dev)
@@ -335,6 +394,7 @@ def fathom_dense_attn(shape: Shape, k_rows, v_rows, q, workspace, out=None, stre
     _check(v_rows, "v_rows", (torch.bfloat16, torch.int16), (shape.units, shape.cap, shape.D))
     _check(q, "q", (torch.float32,), (shape.units, shape.G, shape.D))
     _check(workspace, "workspace", (torch.uint8,))
+    _check_out(out, "out", (torch.float32,), shape.units * shape.G * shape.D)
     if out is None:
         out = torch.empty(shape.units, shape.G, shape.D, dtype=torch.float32, device=q.device)
     _call("fathom_dense_attn", ctypes.byref(shape), _p(k_rows), _p(v_rows), _p(q), _p(out),
@@ -346,6 +406,9 @@ def fathom_klt_online(shape: Shape, k_rows, workspace=None, mean=None, V=None, l
     """Per-unit rotated basis from the unit's own key rows [U][cap][D] bf16 ->
     (mean [U][D] f64, V [U][D][D] f64, lambda [U][D] f32)."""
     _check(k_rows, "k_rows", (torch.bfloat16, torch.int16), (shape.units, shape.cap, shape.D))
+    _check_out(mean, "mean", (torch.float64,), shape.units * shape.D)
+    _check_out(V, "V", (torch.float64,), shape.units * shape.D * shape.D)
+    _check_out(lam, "lam", (torch.float32,), shape.units * shape.D)
     dev = "cuda"
     if workspace is None:
         workspace = alloc_workspace(shape, WS_KLT_ONLINE, device=dev)
@@ -411,6 +474,7 @@ def fathom_sparse_attn_planes(shape: Shape, planes, scales, v_rows, q, topk_idx,
     _check(q, "q", (torch.float32,), (shape.units, shape.G, shape.D))
     _check(topk_idx, "topk_idx", (torch.int32,), (shape.units, shape.G, shape.k))
     _check(workspace, "workspace", (torch.uint8,))
+    _check_out(out, "out", (torch.float32,), shape.units * shape.G * shape.D)
     if out is None:
         out = torch.empty(shape.units, shape.G, shape.D, dtype=torch.float32, device=q.device)
     _call("fathom_sparse_attn_planes", ctypes.byref(shape), _p(planes), _p(scales), _p(v_rows), _p(q),
@@ -439,6 +503,7 @@ def fathom_sparse_attn(shape: Shape, k_rows, v_rows, q, topk_idx, workspace, out
     _check(q, "q", (torch.float32,), (shape.units, shape.G, shape.D))
     _check(topk_idx, "topk_idx", (torch.int32,), (shape.units, shape.G, shape.k))
     _check(workspace, "workspace", (torch.uint8,))
+    _check_out(out, "out", (torch.float32,), shape.units * shape.G * shape.D)
     if out is None:
         out = torch.empty(shape.units, shape.G, shape.D, dtype=torch.float32, device=q.device)
     _call("fathom_sparse_attn", ctypes.byref(shape), _p(k_rows), _p(v_rows), _p(q), _p(topk_idx),
