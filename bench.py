@@ -432,13 +432,11 @@ def unit_budget(w: synth.Workload, budget: int, unit: int) -> int:
     return budget
 
 
-def oracle_layer_sample(w: synth.Workload, budget: int, unit: int):
-    """Time the CPU oracle on one unit of the workload (the whole per-unit step:
-    query rotation for a rotated store, plan, gather, scores, selection,
-    attention); returns seconds."""
+def _oracle_inputs(w: synth.Workload, budget: int, unit: int) -> dict:
+    """One unit's inputs to the oracle's decode step, with its store built (the
+    store build is not part of the step and is not timed)."""
     from oracle import oracle as O
     O.build()
-    n = w.n
     keys = synth.unit_keys(w, unit, "cpu").to(torch.bfloat16)
     k32 = keys.float().numpy()
     kb = keys.view(torch.int16).numpy().view(np.uint16)
@@ -446,7 +444,7 @@ def oracle_layer_sample(w: synth.Workload, budget: int, unit: int):
     q = synth.unit_query(w, unit, "cpu", step=1).numpy()
     calib = synth.unit_calib(w, unit, "cpu").numpy()
     V = None
-    if w.rotated:                              # store build, not part of the step
+    if w.rotated:
         mean, _, cov = O.calibrate(calib, with_cov=True)
         lam, V = O.eigh(cov)
         var = lam.astype(np.float32)
@@ -454,21 +452,34 @@ def oracle_layer_sample(w: synth.Workload, budget: int, unit: int):
     else:
         _, var = O.calibrate(calib)
         var = var.astype(np.float32)
-    P, S, _ = O.quantize_pack(k32)            # store build: not part of the step
-    b = unit_budget(w, budget, unit)
+    P, S, _ = O.quantize_pack(k32)
+    return {"kb": kb, "vb": vb, "q": q, "V": V, "var": var, "P": P, "S": S,
+            "budget": unit_budget(w, budget, unit)}
+
+
+def _oracle_step(w: synth.Workload, inp: dict) -> float:
+    """The oracle's whole per-unit decode step (query rotation for a rotated
+    store, plan, gather, scores, selection, attention); returns seconds."""
+    from oracle import oracle as O
+    n = w.n
     t0 = time.perf_counter()
-    qs = O.rotate_query(q, V).astype(np.float32) if w.rotated else q
-    depth, theta, _ = O.plan(qs, var, b)
+    qs = O.rotate_query(inp["q"], inp["V"]).astype(np.float32) if w.rotated else inp["q"]
+    depth, theta, _ = O.plan(qs, inp["var"], inp["budget"])
     runs = O.runs(depth, n)
     if w.regime == "host":
         nb = (n + 63) // 64
-        sp, ss = O.gather(runs, P, S, int(depth.sum()) * nb, int((depth > 0).sum()) * nb)
+        sp, ss = O.gather(runs, inp["P"], inp["S"], int(depth.sum()) * nb, int((depth > 0).sum()) * nb)
         s = O.scores_staged(runs, sp, ss, depth, qs, n)
     else:
-        s = O.scores(P[None], S[None], depth[None], qs[None], n)[0]
+        s = O.scores(inp["P"][None], inp["S"][None], depth[None], qs[None], n)[0]
     idx, _ = O.select(s, w.k, w.n_sink, w.n_recent)
-    O.attention(kb, vb, q, idx)
+    O.attention(inp["kb"], inp["vb"], inp["q"], idx)
     return time.perf_counter() - t0
+
+
+def oracle_layer_sample(w: synth.Workload, budget: int, unit: int):
+    """Time the CPU oracle on one unit of the workload; returns seconds."""
+    return _oracle_step(w, _oracle_inputs(w, budget, unit))
 
 
 def cpu_baseline(w, budget, reps=1):
@@ -478,6 +489,88 @@ def cpu_baseline(w, budget, reps=1):
     return {"value": us_layer, "unit": "µs/layer", "cores": 1, "kind": "oracle",
             "sample": f"{reps} unit(s) of layer 0 at n={w.n} (plan, gather, scores, top-k, attention; "
                       f"single-threaded C), scaled x{w.units_per_layer()} units per layer"}
+
+
+def _parallel_worker(w: synth.Workload, budget: int, unit: int, barrier, wait_s: float, results):
+    """One worker process of the all-cores baseline: build the unit's inputs,
+    wait for the other workers, then time the unit's step (monotonic clock,
+    comparable across the processes of one host).  Puts (unit, t0, t1) or
+    (unit, error) on `results`."""
+    try:
+        torch.set_num_threads(1)
+        inp = _oracle_inputs(w, budget, unit)
+        barrier.wait(timeout=wait_s)
+        t0 = time.monotonic()
+        _oracle_step(w, inp)
+        results.put((unit, t0, time.monotonic()))
+    except BaseException as exc:   # the parent reports it; never hang the barrier's other parties
+        try:
+            barrier.abort()
+        finally:
+            results.put((unit, repr(exc)[:200]))
+
+
+def host_cores() -> int:
+    """Cores this process may run on (its affinity set)."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def cpu_baseline_parallel(w: synth.Workload, budget: int, max_workers: int = 0, mem_bytes: int = 8 << 30,
+                          wait_s: float = 600.0) -> dict:
+    """The oracle on several units of layer 0 at once, one single-threaded process per
+    unit ("spawn" processes: this process already holds a CUDA context).  Workers are
+    limited by the host's cores, the layer's units and a host-memory budget for their
+    inputs (about 14 bytes per token and channel).  The layer's time is the wall time
+    of one round (first start to last end, after a barrier) times the rounds a layer
+    needs on that many workers.  A worker that fails or does not report within
+    2 * wait_s is terminated and the call raises."""
+    import math
+    import multiprocessing as mp
+    import queue as queue_mod
+    per_unit = 14 * w.n * w.D
+    P = min(host_cores(), w.units_per_layer(), max(1, mem_bytes // per_unit))
+    if max_workers:
+        P = min(P, max_workers)
+    P = max(1, P)
+    units = w.layer_units(0)[:P]
+    ctx = mp.get_context("spawn")
+    barrier, results = ctx.Barrier(P), ctx.Queue()
+    procs = [ctx.Process(target=_parallel_worker, args=(w, budget, u, barrier, wait_s, results), daemon=True)
+             for u in units]
+    spans, errors = [], []
+    try:
+        for pr in procs:
+            pr.start()
+        deadline = time.monotonic() + 2 * wait_s
+        while len(spans) + len(errors) < P:
+            try:
+                r = results.get(timeout=2.0)
+            except queue_mod.Empty:
+                dead = [pr.exitcode for pr in procs if not pr.is_alive() and pr.exitcode not in (0, None)]
+                if dead:
+                    raise RuntimeError(f"all-cores baseline: a worker exited with code {dead[0]}")
+                if time.monotonic() > deadline:
+                    raise TimeoutError(f"all-cores baseline: {P - len(spans) - len(errors)} worker(s) "
+                                       "did not report")
+                continue
+            (spans if len(r) == 3 else errors).append(r)
+    finally:
+        for pr in procs:
+            pr.join(timeout=10)
+            if pr.is_alive():
+                pr.terminate()
+                pr.join(timeout=10)
+    if errors:
+        raise RuntimeError(f"all-cores baseline: worker error {errors[0]}")
+    wall = max(t1 for _, _, t1 in spans) - min(t0 for _, t0, _ in spans)
+    rounds = math.ceil(w.units_per_layer() / P)
+    return {"value": wall * rounds * 1e6, "unit": "µs/layer", "cores": P, "kind": "oracle",
+            "sample": f"{P} unit(s) of layer 0 at n={w.n} in {P} single-threaded processes at once "
+                      f"(wall time of the round), x{rounds} rounds for the layer's "
+                      f"{w.units_per_layer()} units; {host_cores()} cores available"}
 
 
 # ---------------------------------------------------------------- main
@@ -865,6 +958,11 @@ def main():
         line["link_roofline_frac_of_step"] = (scanned / (link_gbs * 1e9)) / (elapsed / (args.steps * L))
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, args.budget)
+        try:
+            line["cpu_baseline"]["all_cores"] = cpu_baseline_parallel(w, args.budget)
+        except Exception as exc:   # reported as missing, never as a number
+            log(f"[bench] all-cores CPU baseline unavailable: {exc}")
+            line["cpu_baseline"]["all_cores"] = {"error": str(exc)[:200]}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -72,3 +72,26 @@ def test_l2_note_follows_the_workload_size():
     assert "L2-resident" in bench.l2_note(synth.WORKLOADS["single_4k"])
     # one layer of 8 heads at 1024 tokens: 8 x 1024 x (68 + 512) B = 4.6 MiB
     assert "L2-resident" in bench.l2_note(synth.shrink(synth.WORKLOADS["host_1m"], n=1024, layers=1))
+
+
+def test_all_cores_cpu_baseline_runs_units_in_parallel_processes():
+    sys.path.insert(0, ROOT)
+    import bench
+    from bit_plane_kv_gb300 import synth
+    w = synth.shrink(synth.WORKLOADS["qwen3_32k"], n=2048, layers=1)     # 8 units per layer
+    res = bench.cpu_baseline_parallel(w, 48, max_workers=2, wait_s=120.0)
+    assert res["kind"] == "oracle" and res["unit"] == "µs/layer" and res["value"] > 0
+    assert res["cores"] == min(2, bench.host_cores())
+    assert f"x{-(-8 // res['cores'])} rounds" in res["sample"]
+    # the single-process sample times the same step
+    assert bench.oracle_layer_sample(w, 48, 0) > 0
+
+
+def test_all_cores_cpu_baseline_reports_a_failing_worker():
+    sys.path.insert(0, ROOT)
+    import bench
+    from bit_plane_kv_gb300 import synth
+    # k larger than n: the oracle's selection rejects it inside the workers
+    w = synth.shrink(synth.WORKLOADS["qwen3_32k"], n=256, layers=1, k=512)
+    with pytest.raises(RuntimeError, match="worker"):
+        bench.cpu_baseline_parallel(w, 48, max_workers=2, wait_s=60.0)
