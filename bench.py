@@ -949,6 +949,7 @@ def main():
         "timing": "one CUDA graph replay per step" if use_graph else "eager launches",
         "graph_warmup_replays": graph_warmup,
         "step_ms_min_median_max": [min(step_ms), statistics.median(step_ms), max(step_ms)],
+        "wall_ms_per_step": (wall1 - wall0) * 1e3 / args.steps,
         "eager_issue_us_per_layer": issue_s * 1e6 / st.L,
         "clocks": clk,
     }
