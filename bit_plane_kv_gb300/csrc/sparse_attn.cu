@@ -562,9 +562,14 @@ static void *noalloc_scratch_ptr(int *status) {
     static void *ptrs[64] = {nullptr};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess || dev < 0 || dev >= 64) {
+    if (e != cudaSuccess) {
         set_error("sparse_attn_noalloc: cudaGetDevice: %s", cudaGetErrorString(e));
         *status = FATHOM_ECUDA;
+        return nullptr;
+    }
+    if (dev < 0 || dev >= 64) {
+        set_error("sparse_attn_noalloc: device %d is beyond the 64 devices this call supports", dev);
+        *status = FATHOM_EINVAL;
         return nullptr;
     }
     std::lock_guard<std::mutex> lock(mu);
