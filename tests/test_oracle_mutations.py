@@ -94,6 +94,15 @@ MUTANTS = [
     ("queries rotated by V transposed", "for (int j = 0; j < D; ++j) s += (double)q[(size_t)h * D + j] * V[(size_t)j * D + c];",
      "for (int j = 0; j < D; ++j) s += (double)q[(size_t)h * D + j] * V[(size_t)c * D + j];"),
     ("auto bracket too narrow", "lo = gmin / 512.0;", "lo = gmin / 8.0;"),
+    ("staging offsets skip a word", "dst_w += r[1];", "dst_w += r[1] + (r[1] > 0);"),
+    ("scales staged for inactive channels", "r[4] = t > 0 ? nb : 0;", "r[4] = nb;"),
+    ("one winner too few", "for (int r = 0; r < k - nf; ++r) out[o++] = c[r].i;",
+     "for (int r = 0; r + 1 < k - nf; ++r) out[o++] = c[r].i;\n        if (k - nf > 0) out[o++] = c[m - 1].i;"),
+    ("softmax not normalised", "for (int j = 0; j < D; ++j) out[(size_t)h * D + j] /= den;", ""),
+    ("fixed plan ignores its depth", "depth[j] = (uint8_t)(better < n_sel ? t_fixed : 0);",
+     "depth[j] = (uint8_t)(better < n_sel ? 4 : 0);"),
+    ("greedy ties to the higher layer", "if (best == -1 || drop > best_drop) { best = l; best_drop = drop; }",
+     "if (best == -1 || drop >= best_drop) { best = l; best_drop = drop; }"),
 ]
 
 CHILD = r"""

@@ -286,11 +286,12 @@ def test_plan_fixed_is_top_channels_by_g():
     var[3] = var[5]
     q[:, 3] = q[:, 5]                                   # an exact tie
     g = O.importance(q, var)
-    depth = O.plan_fixed(q, var, 5, 4)
     order = np.lexsort((np.arange(16), -g))             # g desc, index asc
-    ref = np.zeros(16, np.uint8)
-    ref[order[:5]] = 4
-    assert depth.tolist() == ref.tolist()
+    for n_sel, t in ((5, 4), (7, 2), (16, 1)):
+        depth = O.plan_fixed(q, var, n_sel, t)
+        ref = np.zeros(16, np.uint8)
+        ref[order[:n_sel]] = t
+        assert depth.tolist() == ref.tolist()
 
 
 def test_dense_reduction_B_equals_4D():
