@@ -101,6 +101,11 @@ MUTANTS = [
     ("softmax not normalised", "for (int j = 0; j < D; ++j) out[(size_t)h * D + j] /= den;", ""),
     ("fixed plan ignores its depth", "depth[j] = (uint8_t)(better < n_sel ? t_fixed : 0);",
      "depth[j] = (uint8_t)(better < n_sel ? 4 : 0);"),
+    ("depth ties round down", "if (g >= theta * ldexp(1.0, 2 * m + 1)) ++t;", "if (g > theta * ldexp(1.0, 2 * m + 1)) ++t;"),
+    ("eigenvector sign rule inverted", "if (V[(size_t)arg * D + c] < 0.0)", "if (V[(size_t)arg * D + c] > 0.0)"),
+    ("sink tokens not forced", "if (i < n_sink || i >= n - n_recent) { forced[i] = 1; ++nf; }",
+     "if (i >= n - n_recent) { forced[i] = 1; ++nf; }"),
+    ("budget-not-binding case ignored", "if (total_depth(D, g, lo) <= B) {  /* budget not binding */", "if (0) {"),
     ("greedy ties to the higher layer", "if (best == -1 || drop > best_drop) { best = l; best_drop = drop; }",
      "if (best == -1 || drop >= best_drop) { best = l; best_drop = drop; }"),
 ]

@@ -279,6 +279,20 @@ def test_plan_degenerate_cases():
     assert depth.tolist() == [0, 4, 0, 0] and steps == 0
 
 
+def test_depth_rounds_half_up_at_exact_breakpoints():
+    # t = clip(round(log4(g / theta)), 0, 4): at g / theta = 2^(2m+1), log4 is m + 1/2 and the
+    # depth is m + 1 (round half up, the depth reading); just below it, m.  Exact in fp64.
+    for theta in (1.0, 0.0625, 3.0, 1e-7):
+        for m in range(4):
+            g = theta * 2.0 ** (2 * m + 1)
+            assert O.depth_of(g, theta) == m + 1, (theta, m)
+            assert O.depth_of(float(np.nextafter(g, 0.0)), theta) == m, (theta, m)
+            away = theta * 4.0 ** (m + 0.25)                # log4 = m + 1/4: rounds to m
+            assert O.depth_of(away, theta) == m, (theta, m)
+        assert O.depth_of(theta * 2.0 ** 20, theta) == 4     # clipped at 4
+        assert O.depth_of(0.0, theta) == 0
+
+
 def test_plan_fixed_is_top_channels_by_g():
     rng = np.random.default_rng(9)
     q = rng.normal(size=(4, 16)).astype(np.float32)
