@@ -106,6 +106,20 @@ MUTANTS = [
     ("sink tokens not forced", "if (i < n_sink || i >= n - n_recent) { forced[i] = 1; ++nf; }",
      "if (i >= n - n_recent) { forced[i] = 1; ++nf; }"),
     ("budget-not-binding case ignored", "if (total_depth(D, g, lo) <= B) {  /* budget not binding */", "if (0) {"),
+    ("exact scores miss the last channel",
+     "for (int j = 0; j < D; ++j)\n                d += (double)q[(size_t)h * D + j] * (double)keys[(size_t)i * D + j];",
+     "for (int j = 0; j + 1 < D; ++j)\n                d += (double)q[(size_t)h * D + j] * (double)keys[(size_t)i * D + j];"),
+    ("importance over one head", "for (int h = 0; h < G; ++h) {\n            double x",
+     "for (int h = 0; h < 1; ++h) {\n            double x"),
+    ("channels with g = 0 read", "if (g >= theta * ldexp(1.0, 2 * m + 1)) ++t;",
+     "if (g >= theta * ldexp(1.0, 2 * m + 1) || g == 0.0) ++t;"),
+    ("selection keeps the lowest scores", "if (a->s > b->s) return -1;          /* score descending */",
+     "if (a->s < b->s) return -1;"),
+    ("attention with head 0's query", "d += (double)q[(size_t)h * D + j] * oracle_bf16_value(krows[(size_t)i * D + j]);",
+     "d += (double)q[j] * oracle_bf16_value(krows[(size_t)i * D + j]);"),
+    ("rotated keys scaled", "out[(size_t)i * D + c] = (float)s;", "out[(size_t)i * D + c] = (float)(s * (1.0 + 1e-6));"),
+    ("greedy starts one level up", "int *lev = (int *)calloc((size_t)layers, sizeof(int));",
+     "int *lev = (int *)calloc((size_t)layers, sizeof(int));\n    for (int l = 0; l < layers && levels > 1; ++l) lev[l] = 1;"),
     ("greedy ties to the higher layer", "if (best == -1 || drop > best_drop) { best = l; best_drop = drop; }",
      "if (best == -1 || drop >= best_drop) { best = l; best_drop = drop; }"),
 ]
