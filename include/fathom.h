@@ -345,7 +345,9 @@ int fathom_greedy_budgets(int32_t layers, int32_t levels, const double *err, int
  *   o_h = sum_{i in S_h} softmax_i(q_h . k_i / sqrt(D)) v_i
  * with fp32 accumulation and no mass for unselected tokens.
  *   k_rows, v_rows [units][C][D] bf16 bit patterns (device or pinned host)
- *   q [units][G][D] fp32, topk_idx [units][G][k] int32, each row ascending
+ *   q [units][G][D] fp32, topk_idx [units][G][k] int32, each row strictly
+ *   ascending as fathom_scan_topk writes it (other rows give an unspecified
+ *   result; entries outside [0, n) are skipped, never read)
  *   out [units][G][D] fp32 (out)
  *   workspace: at least fathom_workspace_size(shape, FATHOM_WS_SPARSE_ATTN)
  *   bytes, same rules as fathom_scan_topk's. */
