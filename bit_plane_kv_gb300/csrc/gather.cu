@@ -49,7 +49,19 @@ gather_kernel(int D, int nb, int cb, int x_planes, int x_total, const uint64_t *
               size_t stage_words, size_t stage_scales_n, int vec_planes, int vec_scales) {
     __shared__ fathom_run r[FATHOM_MAX_D];
     const int u = blockIdx.y;
-    for (int j = threadIdx.x; j < D; j += kGThreads) r[j] = runs[(size_t)u * D + j];
+    for (int j = threadIdx.x; j < D; j += kGThreads) {
+        fathom_run v = runs[(size_t)u * D + j];
+        // The source fields must be the ones the plan writes for channel j: the run
+        // starts at the channel's own planes and scales, covers whole planes (at most
+        // four) and at most one scale per block.  Any other run would read outside
+        // channel j's part of the store, so it copies nothing.
+        const bool ok = v.src_word == (uint32_t)j * FATHOM_PLANES * (uint32_t)cb &&
+                        v.src_scale == (uint32_t)j * (uint32_t)cb &&
+                        v.n_words <= (uint32_t)FATHOM_PLANES * (uint32_t)nb && v.n_words % (uint32_t)nb == 0 &&
+                        v.n_scales <= (uint32_t)nb;
+        if (!ok) { v.n_words = 0; v.n_scales = 0; }
+        r[j] = v;
+    }
     __syncthreads();
     // grid-stride over the unit's destination windows: plane windows, then scale windows
     for (int x = blockIdx.x; x < x_total; x += gridDim.x) {
@@ -106,7 +118,9 @@ int launch_gather(const fathom_shape &s, const uint64_t *sp, const uint16_t *ss,
     // a copy over the host link needs enough bytes in flight (each thread keeps
     // 4 x 16 B outstanding) but not every SM: about two CTAs per SM in all, which
     // leaves room for kernels that run beside the gather
-    int per_unit = (2 * 152 + s.units - 1) / s.units;
+    int sms = device_sm_count();
+    if (sms <= 0) sms = 152;   // no device answered: the GB300's count
+    int per_unit = (2 * sms + s.units - 1) / s.units;
     if (per_unit > xp + xs) per_unit = xp + xs;
     dim3 grid(per_unit, s.units);
     gather_kernel<<<grid, kGThreads, 0, st>>>(s.D, nb, cb, xp, xp + xs, sp, ss, runs, dp, ds, stage_words,
