@@ -555,11 +555,12 @@ static int launch_sparse_attn_src(const fathom_shape &s, const KSource &ks, cons
 constexpr size_t kNoAllocScratchBytes = (size_t)8 << 20;   // 8 MiB
 static __device__ __align__(256) unsigned char g_attn_scratch[kNoAllocScratchBytes];
 
-// The array's device address, looked up once per device with that device
-// current (in host code the symbol is only a host-side stand-in).
+// The array's device address on the current device.  In host code the symbol
+// is only a host-side stand-in, so the address is looked up with the device
+// current, on every call: the lookup is a host-side query, and a cached address
+// would go stale after cudaDeviceReset or under another primary context.  The
+// first lookup on a device may load the library's device code there.
 static void *noalloc_scratch_ptr(int *status) {
-    static std::mutex mu;
-    static void *ptrs[64] = {nullptr};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) {
@@ -567,24 +568,15 @@ static void *noalloc_scratch_ptr(int *status) {
         *status = FATHOM_ECUDA;
         return nullptr;
     }
-    if (dev < 0 || dev >= 64) {
-        set_error("sparse_attn_noalloc: device %d is beyond the 64 devices this call supports", dev);
-        *status = FATHOM_EINVAL;
+    void *p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_attn_scratch);
+    if (e != cudaSuccess || !p) {
+        set_error("sparse_attn_noalloc: cudaGetSymbolAddress on device %d: %s", dev, cudaGetErrorString(e));
+        *status = FATHOM_ECUDA;
         return nullptr;
     }
-    std::lock_guard<std::mutex> lock(mu);
-    if (!ptrs[dev]) {
-        void *p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_attn_scratch);
-        if (e != cudaSuccess || !p) {
-            set_error("sparse_attn_noalloc: cudaGetSymbolAddress: %s", cudaGetErrorString(e));
-            *status = FATHOM_ECUDA;
-            return nullptr;
-        }
-        ptrs[dev] = p;
-    }
     *status = FATHOM_OK;
-    return ptrs[dev];
+    return p;
 }
 
 int launch_sparse_attn_noalloc(const fathom_shape &s, const uint16_t *krows, const uint16_t *vrows,
