@@ -279,8 +279,10 @@ def fathom_append_block(shape: Shape, keys, block, count, planes, scales, stream
 
 
 def fathom_plan(shape: Shape, q, var, budget, bracket=None, depth=None, theta=None, runs=None,
-                stream=None):
-    """-> depth [U][D] u8, theta [U] f64, runs [U][D][6] (int32 storage of u32)."""
+                stream=None, want_theta=True):
+    """-> depth [U][D] u8, theta [U] f64 (None when want_theta is False: the call
+    then passes no theta buffer and the depths and runs are the same), runs
+    [U][D][6] (int32 storage of u32)."""
     _check(q, "q", (torch.float32,), (shape.units, shape.G, shape.D))
     _check(var, "var", (torch.float32,), (shape.units, shape.D))
     _check(budget, "budget", (torch.int32,), (shape.units,))
@@ -292,7 +294,9 @@ def fathom_plan(shape: Shape, q, var, budget, bracket=None, depth=None, theta=No
     dev = q.device
     if depth is None:
         depth = torch.empty(shape.units, shape.D, dtype=torch.uint8, device=dev)
-    if theta is None:
+    if not want_theta:
+        theta = None
+    elif theta is None:
         theta = torch.empty(shape.units, dtype=torch.float64, device=dev)
     if runs is None:
         runs = torch.empty(shape.units, shape.D, 6, dtype=torch.int32, device=dev)

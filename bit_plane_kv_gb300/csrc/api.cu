@@ -120,11 +120,27 @@ int scan_m_sel(int chunks, int k_sel) {
 }
 
 int scan_m_first(int n_sub, int k_sel, int m_sel) {
-    // rank of the threshold taken from a CTA's first sub-chunk: twice the
-    // expected winners of one sub-chunk, at least 8, at most m (a sub-chunk
-    // holding more winners than that makes its CTA rescan them exactly)
+    // Rank of the threshold taken from a CTA's first sub-chunk.  A sub-chunk that
+    // holds at least this many of the unit's k' winners sets a threshold above the
+    // k'-th key, and its CTA is rescanned exactly, so the rank is a tail bound of
+    // the winners one sub-chunk holds: with the winners spread over the sequence
+    // (lambda = k' / n_sub per sub-chunk on average, Poisson), the smallest m with
+    // P(X >= m) <= 1e-6, at least 8, at most m_sel.  (Twice the mean, the earlier
+    // rule, flagged about one (CTA, head) in twenty at lambda ~ 4.)
     if (k_sel <= 0) return 0;
-    int m = (2 * k_sel + n_sub - 1) / n_sub;
+    const double lam = (double)k_sel / (double)(n_sub > 0 ? n_sub : 1);
+    int m;
+    if (lam > 200.0) {
+        m = (int)std::ceil(lam + 5.0 * std::sqrt(lam) + 5.0);   // normal tail, about 3e-7
+    } else {
+        double p = std::exp(-lam), cdf = p;   // P(X = 0), P(X <= m - 1) with m = 1
+        m = 1;
+        while (1.0 - cdf > 1e-6 && m < m_sel) {
+            p *= lam / m;
+            cdf += p;
+            ++m;
+        }
+    }
     m = m < 8 ? 8 : m;
     return m > m_sel ? m_sel : m;
 }
@@ -377,7 +393,6 @@ int fathom_plan(const fathom_shape *shape, const float *q, const float *var, con
     NONNULL(var);
     NONNULL(budget);
     NONNULL(depth);
-    NONNULL(theta);
     NONNULL(runs);
     FAULT_POINT("fathom_plan");
     return launch_plan(*shape, q, var, budget, bracket, depth, theta, runs, (cudaStream_t)stream);

@@ -28,8 +28,9 @@
 // the workspace and a threshold key tau; a token is appended only if its key
 // >= tau.  tau starts as a key of the CTA's first sub-chunk (selected straight
 // from registers for all heads at once: m1 of the threads' best keys, and so
-// at least m1 of the sub-chunk's keys, lie at or above it), m1 being twice
-// the winners a sub-chunk holds on average (at least 8); at the end a list
+// at least m1 of the sub-chunk's keys, lie at or above it), m1 being a tail
+// bound of the winners a sub-chunk holds (P <= 1e-6 that it holds more, for
+// winners spread over the sequence; at least 8); at the end a list
 // longer than 4m is cut back to m .. 2m keys, m being four times the CTA's
 // expected share of the k' winners for the sub-chunks it scored.  The merge kernel streams
 // the lists through shared memory (P CTAs per (unit, head), the last of
@@ -834,8 +835,8 @@ scan_kernel(int n, int cb, int ctok, int D, int chunk_blocks, int source, size_t
         };
         if (k_sel > 0 && first) {
             // a threshold from this first sub-chunk, all heads at once, from registers:
-            // at least m1 of its keys are >= it (m1: four times the winners one
-            // sub-chunk holds on average; the second pass: exactly k' .. 2k')
+            // at least m1 of its keys are >= it (m1: a tail bound of the winners one
+            // sub-chunk holds; the second pass: exactly k' .. 2k')
             uint64_t T[G];
             auto visit = [&](auto f) {
 #pragma unroll

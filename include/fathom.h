@@ -208,8 +208,16 @@ int fathom_append_block(const fathom_shape *shape, const void *keys, int keys_dt
  * Every decision uses only IEEE-exact fp64 operations in a fixed order, so the
  * plan is reproducible bit for bit.
  *   q [units][G][D] fp32, var [units][D] fp32, budget [units] int32 >= 0
- *   depth [units][D] uint8 (out), theta [units] fp64 (out),
+ *   depth [units][D] uint8 (out), theta [units] fp64 (out, or NULL),
  *   runs [units][D] fathom_run (out; see fathom_run).
+ * theta NULL: theta is not written, and the depths and runs are the same as
+ * with it.  Without an explicit bracket the call then skips the 30 dependent
+ * bisection steps wherever they cannot change the depths: theta fits the
+ * budget exactly when it lies above b*, the (budget + 1)-th largest of the
+ * breakpoints g_j / 2^(2m+1), and the final theta lies within a factor
+ * 1 + 4x of b* (x = (e + 1) ln2 / 2^30 + 2^-51, e the exponent span of the
+ * bracket); when no breakpoint lies in that range the depths are those at the
+ * next breakpoint above b*.  Otherwise the bisection runs as above.
  * All pointers device. */
 int fathom_plan(const fathom_shape *shape, const float *q, const float *var,
                 const int32_t *budget, const double *bracket, uint8_t *depth,
@@ -383,8 +391,11 @@ int fathom_sparse_attn_planes(const fathom_shape *shape, const uint64_t *planes,
  *   loads the library until the process exits; shapes whose
  *   fathom_workspace_size(shape, FATHOM_WS_SPARSE_ATTN) exceeds 8 MiB are
  *   rejected with FATHOM_EINVAL and nothing is enqueued.
- *   The first call on a device looks up the array's device address (with
- *   that device current); make that first call before any stream capture.
+ *   Every call looks up the array's device address with the calling thread's
+ *   current device (a host-side query; nothing is cached, so the address stays
+ *   right after cudaDeviceReset).  The first call on a device may load the
+ *   library's device code there: make that first call before any stream
+ *   capture.
  *   Every call clears the array's ticket words on `stream` and then uses the
  *   one shared array, so calls whose work overlaps on the GPU (other streams,
  *   other threads) race and must be serialised by the caller.
