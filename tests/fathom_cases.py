@@ -58,24 +58,68 @@ class Inputs:
         self.calib = torch.stack([synth.unit_calib(w, u, device) for u in self.units]).contiguous()
 
 
+class Canaries:
+    """Device buffers with guard bytes on both sides (the stand-in for a memory
+    checker, which is closed on this machine): every buffer a call writes is the
+    middle of a larger allocation whose first and last 256 bytes hold a fixed
+    pattern, and check() asserts after the calls that no guard byte changed."""
+
+    PAD = 256
+    PATTERN = 0xA5
+
+    def __init__(self):
+        self.bufs = []
+
+    def alloc(self, name, shape, dtype, fill=None):
+        shape = tuple(int(x) for x in shape)
+        numel = int(np.prod(shape)) if shape else 1
+        es = torch.empty((), dtype=dtype).element_size()
+        pad = self.PAD // es
+        raw = torch.empty(numel + 2 * pad, dtype=dtype, device="cuda")
+        raw.view(torch.uint8).fill_(self.PATTERN)
+        body = raw[pad:pad + numel].view(shape)
+        if fill is not None:
+            body.fill_(fill)
+        self.bufs.append((name, raw, pad * es, numel * es))
+        return body
+
+    def check(self):
+        torch.cuda.synchronize()
+        for name, raw, pad, nbytes in self.bufs:
+            b = raw.view(torch.uint8)
+            head, tail = b[:pad], b[pad + nbytes:]
+            assert bool((head == self.PATTERN).all()), f"{name}: bytes before the buffer were written"
+            assert bool((tail == self.PATTERN).all()), f"{name}: bytes after the buffer were written"
+        return len(self.bufs)
+
+
 def run_gpu(inp: Inputs, k, budget, n_sink=4, n_recent=32, regime="hbm", bracket=None,
             fixed=None, want_scores=True):
     w = inp.w
     U = len(inp.units)
     shape = B.make_shape(U, inp.n, w.D, w.G, k, n_sink, n_recent)
-    r = {"shape": shape}
-    r["mean"], r["var"] = B.fathom_calibrate(inp.calib)
-    r["planes"], r["scales"] = B.fathom_quantize_pack(shape, inp.keys_in)
+    cz = Canaries()
+    r = {"shape": shape, "canaries": cz}
+    nb = B.nblocks(inp.n)
+    r["mean"], r["var"] = B.fathom_calibrate(inp.calib, mean=cz.alloc("mean", (U, w.D), torch.float32),
+                                             var=cz.alloc("var", (U, w.D), torch.float32))
+    r["planes"], r["scales"] = B.fathom_quantize_pack(
+        shape, inp.keys_in, planes=cz.alloc("planes", (U, w.D, 4, nb), torch.int64),
+        scales=cz.alloc("scales", (U, w.D, nb), torch.int16))
     bud = torch.as_tensor(np.broadcast_to(np.asarray(budget, np.int32), (U,)).copy(), device="cuda")
+    depth_b = cz.alloc("depth", (U, w.D), torch.uint8)
+    runs_b = cz.alloc("runs", (U, w.D, 6), torch.int32)
     if fixed is not None:
-        r["depth"], r["runs"] = B.fathom_plan_fixed(shape, inp.q, r["var"], fixed[0], fixed[1])
+        r["depth"], r["runs"] = B.fathom_plan_fixed(shape, inp.q, r["var"], fixed[0], fixed[1],
+                                                    depth=depth_b, runs=runs_b)
         r["theta"] = None
     else:
         br = None if bracket is None else torch.as_tensor(np.tile(np.asarray(bracket, np.float64), (U, 1)), device="cuda")
-        r["depth"], r["theta"], r["runs"] = B.fathom_plan(shape, inp.q, r["var"], bud, bracket=br)
-    ws = B.alloc_workspace(shape, B.WS_SCAN_TOPK)
-    scores = torch.full((U, w.G, inp.n), float("nan"), device="cuda") if want_scores else None
-    nb = B.nblocks(inp.n)
+        r["depth"], r["theta"], r["runs"] = B.fathom_plan(shape, inp.q, r["var"], bud, bracket=br, depth=depth_b,
+                                                          theta=cz.alloc("theta", (U,), torch.float64),
+                                                          runs=runs_b)
+    ws = cz.alloc("scan workspace", (B.workspace_size(shape, B.WS_SCAN_TOPK),), torch.uint8, fill=0)
+    scores = cz.alloc("scores", (U, w.G, inp.n), torch.float32, fill=float("nan")) if want_scores else None
     if regime == "fused":
         # host-resident store read by the scan straight from pinned memory (the bench's default path)
         hp = r["planes"].cpu().pin_memory()
@@ -89,21 +133,25 @@ def run_gpu(inp: Inputs, k, budget, n_sink=4, n_recent=32, regime="hbm", bracket
         W += W % 2
         S = min(bmax, w.D) * nb
         S = (S + 7) // 8 * 8
-        r["stage_planes"] = torch.zeros(U, W, dtype=torch.int64, device="cuda")
-        r["stage_scales"] = torch.zeros(U, S, dtype=torch.int16, device="cuda")
+        r["stage_planes"] = cz.alloc("staging planes", (U, W), torch.int64, fill=0)
+        r["stage_scales"] = cz.alloc("staging scales", (U, S), torch.int16, fill=0)
         B.fathom_gather(shape, hp, hs, r["runs"], r["stage_planes"], r["stage_scales"])
         src_p, src_s, source = r["stage_planes"], r["stage_scales"], B.SRC_STAGING
     else:
         src_p, src_s, source = r["planes"], r["scales"], B.SRC_STORE
     r["idx"], r["sel"] = B.fathom_scan_topk(shape, src_p, src_s, r["runs"], inp.q, ws, source=source,
-                                            scores=scores)
+                                            scores=scores,
+                                            topk_idx=cz.alloc("topk_idx", (U, w.G, k), torch.int32),
+                                            topk_score=cz.alloc("topk_score", (U, w.G, k), torch.float32))
     r["scores"] = scores
-    aws = B.alloc_workspace(shape, B.WS_SPARSE_ATTN)
+    aws = cz.alloc("attention workspace", (B.workspace_size(shape, B.WS_SPARSE_ATTN),), torch.uint8, fill=0)
     kr, vr = inp.krows, inp.vrows
     if regime in ("host", "fused"):
         kr, vr = kr.cpu().pin_memory(), vr.cpu().pin_memory()
-    r["out"] = B.fathom_sparse_attn(shape, kr, vr, inp.q, r["idx"], aws)
+    r["out"] = B.fathom_sparse_attn(shape, kr, vr, inp.q, r["idx"], aws,
+                                    out=cz.alloc("out", (U, w.G, w.D), torch.float32))
     torch.cuda.synchronize()
+    assert cz.check() >= 10
     return r
 
 

@@ -12,6 +12,7 @@ from bit_plane_kv_gb300 import binding as B
 from bit_plane_kv_gb300 import synth
 from oracle import oracle as O
 
+import fathom_cases
 from fathom_cases import Inputs, check_unit, run_gpu, u16, u32, u64
 
 pytestmark = pytest.mark.gpu
@@ -75,6 +76,46 @@ def test_toy_channel2_codes_and_full_path():
     assert codes == GOLD["channel2"]["codes"]
     assert u16(r["scales"][0, 2])[0] == np.float16(0.5).view(np.uint16)
     check_unit(toy, r, 0, 2, 8, n_sink=0, n_recent=0)
+
+
+def test_toy_reconstructed_k_printed_top2_on_the_gpu():
+    # The toy's full K is not printed (only channel 2); tests/golden holds a K
+    # reconstructed under the oracle so that every printed statement holds.  On
+    # it the CUDA path must reproduce the printed outcomes: with the printed Var
+    # and bracket, B = 8 keeps {t0, t3} for head A and {t5, t0} for head B, head
+    # B's approximate scores match the printed ones to their 2 decimals, and
+    # B = 6 misses head B's pair.
+    rec = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "toy_k_reconstruction.json")))
+    K = np.array(rec["K"], np.float32)
+    keys = torch.tensor(K[None], device="cuda")
+    q = torch.tensor([[GOLD["q_A"], GOLD["q_B"]]], dtype=torch.float32, device="cuda")
+    var = torch.tensor([GOLD["var"]], dtype=torch.float32, device="cuda")
+    br = torch.tensor([GOLD["bracket"]], dtype=torch.float64, device="cuda")
+    shape = B.make_shape(1, 6, 4, 2, 2, 0, 0)
+    planes, scales = B.fathom_quantize_pack(shape, keys)
+    ws = B.alloc_workspace(shape, B.WS_SCAN_TOPK)
+    P, S, C = O.quantize_pack(K)
+    qn = q[0].cpu().numpy()
+    for Bud in (8, 6):
+        bud = torch.tensor([Bud], dtype=torch.int32, device="cuda")
+        depth, theta, runs = B.fathom_plan(shape, q, var, bud, bracket=br)
+        scores = torch.full((1, 2, 6), float("nan"), device="cuda")
+        idx, sel = B.fathom_scan_topk(shape, planes, scales, runs, q, ws, scores=scores)
+        torch.cuda.synchronize()
+        od, _, _ = O.plan(qn, np.array(GOLD["var"], np.float32), Bud, bracket=GOLD["bracket"])
+        np.testing.assert_array_equal(depth[0].cpu().numpy(), od)
+        got = scores[0].cpu().numpy().astype(np.float64)
+        ref = O.scores(P[None], S[None], od[None], qn[None], 6)[0]
+        mag = fathom_cases.khat_magnitude(C, S, od, qn, 6)
+        assert np.all(np.abs(got - ref) <= fathom_cases.SCORE_RTOL * mag + 1e-30)
+        kept = [set(idx[0, h].tolist()) for h in range(2)]
+        if Bud == 8:
+            assert depth[0].tolist() == GOLD["B8"]["depth"]
+            assert kept[0] == set(GOLD["top2"]["A"]) and kept[1] == set(GOLD["top2"]["B"])
+            np.testing.assert_allclose(got[1], GOLD["head_B_scores"]["approx"], rtol=0, atol=0.005)
+        else:
+            assert depth[0].tolist() == GOLD["B6"]["depth"]
+            assert kept[1] != set(GOLD["top2"]["B"])
 
 
 # ------------------------------------------------------------------ store / calibration
@@ -172,6 +213,44 @@ def test_plan_bit_exact_across_magnitudes():
         assert th[u] == oth, (u, th[u], oth)
 
 
+def test_plan_without_theta_gives_the_same_depths_and_runs():
+    # theta not requested: the kernel may take the depths straight from the
+    # breakpoint above b*; over budgets, magnitudes and near-coincident
+    # breakpoints the depths and runs must equal the oracle's (and the call with
+    # theta), bit for bit
+    w = W("qwen3_32k")
+    U = 448
+    gen = torch.Generator(device="cpu").manual_seed(20260311)
+    q = torch.stack([synth.unit_query(w, u % 64, "cuda") for u in range(U)])
+    _, var = B.fathom_calibrate(torch.stack([synth.unit_calib(w, u % 64, "cuda") for u in range(U)]))
+    sq = 10.0 ** torch.randint(-15, 16, (U, 1, 1), generator=gen).double()
+    sv = 10.0 ** torch.randint(-30, 31, (U, 1), generator=gen).double()
+    sq[:64] = 1.0
+    sv[:64] = 1.0
+    q = (q.double().cpu() * sq).float()
+    var = (var.double().cpu() * sv).float()
+    # units 64..127: pairs of channels with importances a few ulps apart
+    # (q one fp32 ulp up, var 2^-22 down), so breakpoints nearly coincide
+    q[64:128, :, 1::2] = torch.nextafter(q[64:128, :, 0::2], torch.full_like(q[64:128, :, 0::2], 1e30))
+    var[64:128, 1::2] = var[64:128, 0::2] * (1.0 - 2.0 ** -22)
+    q[5] = 0.0
+    q, var = q.cuda().contiguous(), var.cuda().contiguous()
+    budgets = np.array([0, 1, 7, 8, 24, 48, 64, 100, 200, 400, 512, 600], np.int32)[np.arange(U) % 12]
+    bt = torch.tensor(budgets, device="cuda")
+    shape = B.make_shape(U, 65536, 128, 4, 1, 0, 0)
+    d1, t1, r1 = B.fathom_plan(shape, q, var, bt)
+    d0, t0, r0 = B.fathom_plan(shape, q, var, bt, want_theta=False)
+    torch.cuda.synchronize()
+    assert t0 is None
+    torch.testing.assert_close(d0, d1, rtol=0, atol=0)
+    torch.testing.assert_close(r0, r1, rtol=0, atol=0)
+    qn, vn, dn = q.cpu().numpy(), var.cpu().numpy(), d0.cpu().numpy()
+    for u in range(U):
+        od, _, _ = O.plan(qn[u], vn[u], int(budgets[u]))
+        np.testing.assert_array_equal(dn[u], od)
+        np.testing.assert_array_equal(u32(r0[u]), O.runs(od, 65536))
+
+
 def test_plan_explicit_bracket_and_fixed():
     w = W("qwen3_32k")
     U = 16
@@ -191,6 +270,43 @@ def test_plan_explicit_bracket_and_fixed():
         fd = O.plan_fixed(qn, vn, 32, 4)
         np.testing.assert_array_equal(fdepth[u].cpu().numpy(), fd)
         np.testing.assert_array_equal(u32(fruns[u]), O.runs(fd, 1 << 20))
+
+
+def test_gather_copies_nothing_for_a_corrupted_run():
+    # a run whose source fields are not the ones the plan writes for its channel
+    # (another channel's planes, more than four planes, a partial plane, another
+    # channel's scales, more scales than blocks) would read outside the channel's
+    # part of the store: the gather copies nothing for it, and every other
+    # channel exactly as the oracle does
+    w = W("qwen3_32k", n=4096)
+    inp = Inputs(w, [0], 4096)
+    shape = B.make_shape(1, 4096, 128, 4, 1, 0, 0)
+    planes, scales = B.fathom_quantize_pack(shape, inp.keys_in)
+    _, var = B.fathom_calibrate(inp.calib)
+    depth, _, runs = B.fathom_plan(shape, inp.q, var, torch.tensor([48], dtype=torch.int32, device="cuda"))
+    torch.cuda.synchronize()
+    nb = B.nblocks(4096)
+    r = u32(runs[0]).copy()
+    act = np.nonzero(depth[0].cpu().numpy())[0]
+    assert len(act) >= 5
+    bad = act[:5]
+    r[bad[0], 0] = (bad[0] + 1) * 4 * nb          # src_word of the next channel
+    r[bad[1], 1] = 5 * nb                          # five planes
+    r[bad[2], 1] = r[bad[2], 1] + 1                # not whole planes
+    r[bad[3], 3] = (bad[3] + 1) * nb               # src_scale of the next channel
+    r[bad[4], 4] = nb + 1                          # more scales than blocks
+    runs_bad = torch.tensor(r.view(np.int32)[None], device="cuda").contiguous()
+    W_, S_ = 48 * nb, 48 * nb
+    sp = torch.zeros(1, W_, dtype=torch.int64, device="cuda")
+    ss = torch.zeros(1, S_, dtype=torch.int16, device="cuda")
+    B.fathom_gather(shape, planes.cpu().pin_memory(), scales.cpu().pin_memory(), runs_bad, sp, ss)
+    torch.cuda.synchronize()
+    ref_runs = u32(runs[0]).copy()
+    ref_runs[bad, 1] = 0                           # nothing copied for the corrupted channels
+    ref_runs[bad, 4] = 0
+    rp, rs = O.gather(ref_runs, u64(planes[0]), u16(scales[0]), W_, S_)
+    np.testing.assert_array_equal(u64(sp[0]), rp)
+    np.testing.assert_array_equal(u16(ss[0]), rs)
 
 
 # ------------------------------------------------------------------ whole path, small
