@@ -54,7 +54,7 @@ def dist_setup(n_gpus):
         import torch.distributed as dist
         backend = "nccl" if torch.cuda.is_available() else "gloo"
         dist.init_process_group(backend)
-    if torch.cuda.is_available():
+    if torch.cuda.is_available() and local < torch.cuda.device_count():
         torch.cuda.set_device(local)
     return rank, world
 
@@ -155,10 +155,13 @@ class Setup:
     """Builds the store and rows of one session on this rank (untimed)."""
 
     def __init__(self, w: synth.Workload, budget: int, rank: int, steps_total: int, fixed: bool,
-                 path: str = "fused", groups: int = 4):
+                 path: str = "fused", groups: int = 4, want_theta: bool = False):
         from bit_plane_kv_gb300 import binding as B
         self.B = B
         self.w, self.budget, self.fixed = w, budget, fixed
+        # the decode step needs the depths and the run list; theta (the water level)
+        # is a diagnostic, requested only with --plan-theta
+        self.want_theta = want_theta
         w = rank_workload(w, rank)
         self.L, self.H = w.layers, w.units_per_layer()
         self.n, self.G, self.D, self.k = w.n, w.G, w.D, w.k
@@ -260,7 +263,7 @@ class Setup:
             B.fathom_plan_fixed(self.shape, q, self.var[l], 32, 4, depth=self.depth, runs=self.runs)
         else:
             B.fathom_plan(self.shape, q, self.var[l], self.budget_t[l], depth=self.depth, theta=self.theta,
-                          runs=self.runs)
+                          runs=self.runs, want_theta=self.want_theta)
         if self.host and self.path == "pipelined":
             self._gather_scan_pipelined(l, q, ev)
         elif self.host and self.path == "staged":
@@ -315,8 +318,11 @@ class Setup:
         if self.rotated:
             nh = self.w.kv_heads
             q = B.fathom_rotate_query(self.shape, qa, nh, self.kV[l * nh:(l + 1) * nh], out=self.qrot[l])
-        B.fathom_plan(self.shape, q, self.var[l], self.budget_t[l], depth=self.depth, theta=self.theta,
-                      runs=self.runs)
+        if self.fixed:
+            B.fathom_plan_fixed(self.shape, q, self.var[l], 32, 4, depth=self.depth, runs=self.runs)
+        else:
+            B.fathom_plan(self.shape, q, self.var[l], self.budget_t[l], depth=self.depth, theta=self.theta,
+                          runs=self.runs, want_theta=self.want_theta)
         ev[1].record()
         if self.host and self.path == "staged":
             B.fathom_gather(self.shape, self.planes[l], self.scales[l], self.runs, self.stage_p, self.stage_sc)
@@ -415,6 +421,89 @@ def measure_sm_read_peak(st):
         best = min(best, e0.elapsed_time(e1) / 1e3)
     del sp, ss
     return nbytes / best / 1e9
+
+
+# Thread instructions the first-pass scan kernel issues per scored token, from the
+# ncu capture of one HBM-resident host_1m layer (8 units x 2^20 tokens, B = 48) of
+# the current kernel; the bench multiplies it by the tokens a call scores to
+# estimate how close the HBM-resident scan runs to the instruction-issue bound.
+SCAN_PROFILE = {"thread_instructions_per_token": 76.77e6 * 32 / (8 << 20),
+                "dram_bytes_per_layer": 57.03e6 + 0.97e6,
+                "source": "profiles/scan_kernel_host1m_hbm.md"}
+
+
+def measure_hbm_scan(st, args, peaks, sm_mhz):
+    """The scan + top-k call on layer 0's store copied into HBM (the HBM-resident
+    regime), with each timed step's plan; L2 (129 MB) is flushed by a 256 MiB write
+    before every call, and CUDA events bracket the call on its stream."""
+    B = st.B
+    planes = st.planes[0].to("cuda")
+    scales = st.scales[0].to("cuda")
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    times, nbytes = [], []
+    for i in range(args.warmup + args.steps):
+        q = st.Q[i, 0]
+        if st.fixed:
+            B.fathom_plan_fixed(st.shape, q, st.var[0], 32, 4, depth=st.depth, runs=st.runs)
+        else:
+            B.fathom_plan(st.shape, q, st.var[0], st.budget_t[0], depth=st.depth, runs=st.runs, want_theta=False)
+        flush.fill_(i & 0xFF)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        B.fathom_scan_topk(st.shape, planes, scales, st.runs, q, st.ws, topk_idx=st.idx, topk_score=st.sel)
+        e1.record()
+        torch.cuda.synchronize()
+        if i >= args.warmup:
+            times.append(e0.elapsed_time(e1) / 1e3)
+            nbytes.append(st.planned_bytes())
+    del planes, scales, flush
+    t = statistics.mean(times)
+    gbs = statistics.mean(nbytes) / t / 1e9
+    hbm = peaks["hbm_gbs"]
+    res = {"us": t * 1e6, "gbs": gbs, "peak_gbs": hbm, "frac": gbs / hbm,
+           "scanned_bytes": statistics.mean(nbytes), "calls": len(times),
+           "traffic": SCAN_PROFILE["dram_bytes_per_layer"],
+           "note": "fathom_scan_topk (first-pass scan, merge, exact second pass, second merge) on layer 0's "
+                   "store copied to HBM, the plan of each timed step's queries, L2 flushed before each call; "
+                   "traffic = DRAM read + write bytes of the first-pass scan kernel on this layer "
+                   f"({SCAN_PROFILE['source']})"}
+    ipt = SCAN_PROFILE["thread_instructions_per_token"]
+    if ipt:
+        sms = torch.cuda.get_device_properties(0).multi_processor_count
+        mhz = sm_mhz or 2070.0
+        tokens = st.H * st.n
+        res["issue_bound_frac"] = ipt * tokens / 32.0 / (sms * 4 * mhz * 1e6 * t)
+        res["issue_note"] = (f"{ipt:.0f} thread instructions per token (profiled) x {tokens} tokens / 32 = warp "
+                             f"instructions, over {sms} SMs x 4 issue slots x {mhz:.0f} MHz x the call's time")
+    return res
+
+
+def measure_fixed_plan(st, args):
+    """The byte-equivalent 136-bit comparison (32 channels at depth 4, the same kernels),
+    timed as the main step: one graph replay per step, each with its own queries."""
+    st.fixed = True
+    try:
+        graph = st.capture(None)
+        gw = max(args.warmup, 10)
+        for i in range(gw):
+            st.qcur.copy_(st.Q[i], non_blocking=True)
+            graph.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for i in range(args.steps):
+            st.qcur.copy_(st.Q[gw + i], non_blocking=True)
+            graph.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        us_layer = e0.elapsed_time(e1) * 1e3 / (args.steps * st.L)
+        st.layer(0, st.Q[0, 0])
+        torch.cuda.synchronize()
+        nbytes = st.planned_bytes()
+        del graph
+    finally:
+        st.fixed = False
+    return {"us_per_layer": us_layer, "scanned_bytes_per_layer": nbytes}
 
 
 def measured_peaks():
@@ -604,7 +693,10 @@ def l2_note(w: synth.Workload) -> str:
 
 
 def run_reference(args, w, rank, world):
-    """The CPU oracle on the same workload, as the reference arm."""
+    """The CPU oracle on the same workload, as the reference arm.  One step is one
+    (layer, KV head) unit's decode step, which is what is timed: ms_per_step is that
+    unit's time, and value scales it to a layer (x units per layer) so that it
+    reads in the same unit as the GPU arm's value."""
     if rank != 0:
         return
     for _ in range(args.warmup):
@@ -616,7 +708,10 @@ def run_reference(args, w, rank, world):
     per_unit = statistics.mean(secs)
     us_layer = per_unit * w.units_per_layer() * 1e6
     line = {"impl": "reference", "metric": METRIC, "value": us_layer, "unit": "µs/layer",
-            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": us_layer * w.layers / 1e3,
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_unit * 1e3,
+            "step": f"one unit (one KV head of one layer) at n={w.n}; value = the unit's time x "
+                    f"{w.units_per_layer()} units per layer",
+            "unit_step_ms_min_median_max": [min(secs) * 1e3, statistics.median(secs) * 1e3, max(secs) * 1e3],
             "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded Qwen3-8B-shaped keys/queries/values)",
             "config": workload_config(w, args),
@@ -624,6 +719,26 @@ def run_reference(args, w, rank, world):
                              "sample": f"one unit per step at n={w.n}, scaled x{w.units_per_layer()} units per layer"},
             "e2e": {"value": us_layer, "unit": "µs/layer", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
+
+
+def spawn_ranks(n):
+    """`--gpus N` without a launcher: start N copies of this command as ranks
+    0..N-1 of one job on this node (RANK, LOCAL_RANK, WORLD_SIZE and a free
+    MASTER_PORT on 127.0.0.1 in their environment), pass rank 0's output
+    through, and return the largest exit code."""
+    import socket
+    with socket.socket() as so:
+        so.bind(("127.0.0.1", 0))
+        port = so.getsockname()[1]
+    procs = []
+    for r in range(n):
+        env = dict(os.environ, RANK=str(r), LOCAL_RANK=str(r), WORLD_SIZE=str(n),
+                   LOCAL_WORLD_SIZE=str(n), MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+        out = None if r == 0 else subprocess.DEVNULL
+        procs.append(subprocess.Popen([sys.executable, os.path.abspath(__file__), *sys.argv[1:]], env=env,
+                                      stdout=out))
+    rcs = [p.wait() for p in procs]
+    return max(abs(rc) for rc in rcs)
 
 
 def main():
@@ -646,8 +761,17 @@ def main():
                     help="override where the store and rows live (default: the workload's)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-fidelity", action="store_true", help="skip the (untimed) fidelity measurement")
+    ap.add_argument("--plan-theta", action="store_true",
+                    help="have the plan also write theta (the decode step needs only the depths and runs)")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the HBM-resident scan and 136-bit comparison measurements")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
+    if "WORLD_SIZE" not in os.environ and args.gpus > 1:
+        sys.exit(spawn_ranks(args.gpus))
+    if int(os.environ.get("WORLD_SIZE", "1")) != args.gpus:
+        log(f"[bench] --gpus {args.gpus} but WORLD_SIZE={os.environ.get('WORLD_SIZE')}: launch one rank per GPU")
+        sys.exit(2)
     rank, world = dist_setup(args.gpus)
     w = synth.WORKLOADS[args.workload]
     if args.budget is None:
@@ -663,8 +787,9 @@ def main():
     from bit_plane_kv_gb300 import binding as B
     import __graft_entry__
     __graft_entry__.build()
-    total_steps = args.warmup + 2 * args.steps + max(args.warmup, 10)   # + distinct graph warm-up queries
-    st = Setup(w, args.budget, rank, total_steps, args.fixed, args.path, args.groups)
+    # queries: warm-up, timed, e2e, graph warm-up and 50 spread steps, all distinct
+    total_steps = args.warmup + 2 * args.steps + max(args.warmup, 10) + 50
+    st = Setup(w, args.budget, rank, total_steps, args.fixed, args.path, args.groups, args.plan_theta)
     link_gbs = measure_link_peak() if st.host else None
     sm_link_gbs = measure_sm_read_peak(st) if st.host else None
     link_src = "measured in this run: pinned host->device copy, 1 GiB, best of 10"
@@ -752,16 +877,33 @@ def main():
         kern = [e[0].elapsed_time(e[1]) / 1e3 for row in evs for e in row]
     kern_avg = statistics.mean(kern)
 
-    # end to end through the public calls with host buffers
+    # end to end through the public calls with host buffers, on the host clock: each
+    # step issues its query copy, every layer's calls and the output copy, and waits
+    # for the output (a decode loop reads it before the next step)
     barrier(world)
     torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
+    e2e_steps = []
     for s in range(args.steps):
+        h0 = time.perf_counter()
         st.step_e2e(args.warmup + args.steps + s)
-    e1.record()
-    torch.cuda.synchronize()
-    e2e_elapsed = max_over_ranks(e0.elapsed_time(e1) / 1e3, world)
+        torch.cuda.current_stream().synchronize()
+        e2e_steps.append(time.perf_counter() - h0)
+    e2e_elapsed = max_over_ranks(sum(e2e_steps), world)
+
+    # per-step spread over more steps than the timed region (graph replays, each with
+    # its own queries; events between replays), reported beside the timed value
+    spread_ms = []
+    if use_graph:
+        n_spread = 50
+        sp_ev = [torch.cuda.Event(enable_timing=True) for _ in range(n_spread + 1)]
+        q_sp = args.warmup + 2 * args.steps + graph_warmup
+        sp_ev[0].record()
+        for i in range(n_spread):
+            st.qcur.copy_(st.Q[q_sp + i], non_blocking=True)
+            graph.replay()
+            sp_ev[i + 1].record()
+        torch.cuda.synchronize()
+        spread_ms = sorted(sp_ev[i].elapsed_time(sp_ev[i + 1]) for i in range(n_spread))
 
     # decode-time append: coding the block of a new token into the store (the step before
     # the scan in a decode loop); timed on layer 0's store for its last block, which codes
@@ -791,6 +933,23 @@ def main():
         append_us = a0.elapsed_time(a1) * 1e3 / args.steps
     except Exception as exc:   # reported as missing, never as a number
         log(f"[bench] append timing unavailable: {exc}")
+
+    # the HBM-resident scan and the 136-bit comparison (host-resident runs)
+    hbm_scan, fixed136 = None, None
+    if st.host and not args.no_extras:
+        try:
+            hbm_scan = measure_hbm_scan(st, args, peaks, clk.get("sm_mhz"))
+            log(f"[bench] HBM-resident scan: {hbm_scan}")
+        except Exception as exc:   # reported as missing, never as a number
+            log(f"[bench] HBM-resident scan unavailable: {exc}")
+            hbm_scan = {"error": str(exc)[:200]}
+        if not st.fixed and st.path == "fused":
+            try:
+                fixed136 = measure_fixed_plan(st, args)
+                log(f"[bench] 136-bit plan: {fixed136}")
+            except Exception as exc:   # reported as missing, never as a number
+                log(f"[bench] 136-bit plan unavailable: {exc}")
+                fixed136 = {"error": str(exc)[:200]}
 
     # per-stage breakdown (separate pass, events between the calls)
     stage_ev = []
@@ -918,14 +1077,15 @@ def main():
     else:
         hbm = peaks["hbm_gbs"]
         achieved = scanned / kern_avg / 1e9
+        same_as_profile = w.name == "host_1m" and args.budget == 48 and not args.fixed
         roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-                "traffic": None, "kernel": "scan_kernel",
-                "traffic_note": "no DRAM counters of the current scan kernel: the last full ncu capture (one "
-                                "HBM-resident host_1m layer, an earlier build of the kernel) read 56.65 MB and "
-                                "wrote 1.18 MB for 56.85 MB of planned bytes",
+                "traffic": SCAN_PROFILE["dram_bytes_per_layer"] if same_as_profile else None,
+                "kernel": "scan_kernel",
+                "traffic_note": (f"DRAM read + write bytes of the first-pass scan kernel on one layer of this "
+                                 f"workload ({SCAN_PROFILE['source']})" if same_as_profile else
+                                 "no ncu capture of this workload's scan layer"),
                 "peak_source": f"{peak_src} HBM copy peak (MEASURED_PEAKS.json hbm_gbs)",
-                "binding_resource": "instruction issue (last full ncu capture of the scan: 64% issue-active, "
-                                    "6% of peak DRAM throughput)",
+                "binding_resource": f"instruction issue ({SCAN_PROFILE['source']})",
                 "note": "scanned bytes per layer / the scan_topk call's time (scan + merge kernels); the HBM "
                         "roofline is the denominator the target is stated against, not the scan's bound"}
     line = {
@@ -940,7 +1100,10 @@ def main():
         "active_channels_per_unit": statistics.mean(active),
         "roofline": roof,
         "e2e": {"value": e2e_us_layer, "unit": "µs/layer",
-                "h2d_bytes_per_step": int(st.Q[0].numel() * 4), "d2h_bytes_per_step": int(st.out.numel() * 4)},
+                "h2d_bytes_per_step": int(st.Q[0].numel() * 4), "d2h_bytes_per_step": int(st.out.numel() * 4),
+                "how": "host wall clock (perf_counter) per step around the query copy from pinned host memory, "
+                       "every layer's C-ABI calls (eager, through the Python binding) and the output copy back, "
+                       "ending at the stream's synchronisation"},
         "gpu_launches": launches_per_layer * L * args.steps,
         "stages_us_per_layer": stages,
         "append_us_per_layer": append_us,
@@ -949,10 +1112,27 @@ def main():
         "timing": "one CUDA graph replay per step" if use_graph else "eager launches",
         "graph_warmup_replays": graph_warmup,
         "step_ms_min_median_max": [min(step_ms), statistics.median(step_ms), max(step_ms)],
+        "step_spread_50": ({"ms_min_p10_median_p90_max": [spread_ms[0], spread_ms[len(spread_ms) // 10],
+                                                           statistics.median(spread_ms),
+                                                           spread_ms[(9 * len(spread_ms)) // 10], spread_ms[-1]],
+                            "us_per_layer_median": statistics.median(spread_ms) * 1e3 / st.L,
+                            "note": "50 more graph replays after the timed region, each with its own queries"}
+                           if spread_ms else None),
+        "e2e_step_ms_min_median_max": [min(e2e_steps) * 1e3, statistics.median(e2e_steps) * 1e3,
+                                       max(e2e_steps) * 1e3],
         "wall_ms_per_step": (wall1 - wall0) * 1e3 / args.steps,
         "eager_issue_us_per_layer": issue_s * 1e6 / st.L,
         "clocks": clk,
     }
+    if hbm_scan is not None:
+        line["hbm_scan"] = hbm_scan
+    if fixed136 is not None:
+        if "us_per_layer" in fixed136:
+            fixed136["speedup_of_fathom"] = fixed136["us_per_layer"] / us_layer
+            fixed136["note"] = ("the 32 channels of largest g at depth 4 (128 code bits + 8 scale bits per token) "
+                                "through the same kernels and path; the pages report 1.67x at 1M tokens on an "
+                                "A100 with PCIe 4.0 (Tab. 2), context only")
+        line["vs_136bit"] = fixed136
     if st.host:
         line["link_gbs_peak"] = link_gbs
         line["link_gbs_sm_loads"] = sm_link_gbs

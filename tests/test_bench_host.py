@@ -63,6 +63,43 @@ def test_reference_arm_under_torchrun_prints_on_rank_0_only():
     _check_reference_line(lines[0], 2)
 
 
+def test_gpus_flag_without_a_launcher_spawns_the_ranks():
+    # `bench.py --gpus 2` with no torchrun: the bench starts two ranks itself
+    # (gloo here, no GPU), rank 0 prints the one line, and it reports n_gpus 2
+    env = dict(os.environ, CUDA_VISIBLE_DEVICES="")
+    for k in ("RANK", "WORLD_SIZE", "LOCAL_RANK", "MASTER_ADDR", "MASTER_PORT"):
+        env.pop(k, None)
+    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--gpus", "2", "--steps", "1",
+                        "--warmup", "3", "--workload", "single_4k"],
+                       cwd=ROOT, capture_output=True, text=True, timeout=900, env=env)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = _json_lines(r.stdout)
+    assert len(lines) == 1
+    _check_reference_line(lines[0], 2)
+
+
+def test_gpus_flag_must_match_the_launcher_world_size():
+    env = dict(os.environ, CUDA_VISIBLE_DEVICES="", WORLD_SIZE="1", RANK="0", LOCAL_RANK="0")
+    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--gpus", "2", "--steps", "1",
+                        "--warmup", "3", "--workload", "single_4k"],
+                       cwd=ROOT, capture_output=True, text=True, timeout=300, env=env)
+    assert r.returncode != 0
+    assert not _json_lines(r.stdout)
+
+
+def test_reference_step_is_the_timed_unit():
+    # ms_per_step is what one timed step took (one unit), value the unit scaled to a layer
+    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--steps", "2",
+                        "--warmup", "0", "--workload", "single_4k"],
+                       cwd=ROOT, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    line = _json_lines(r.stdout)[0]
+    lo, med, hi = line["unit_step_ms_min_median_max"]
+    assert lo <= line["ms_per_step"] <= hi
+    assert abs(line["value"] - line["ms_per_step"] * 1e3 * 1) < 1e-6 * line["value"]   # single_4k: 1 unit per layer
+    assert "one unit" in line["step"]
+
+
 def test_l2_note_follows_the_workload_size():
     sys.path.insert(0, ROOT)
     import bench
