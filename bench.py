@@ -679,6 +679,11 @@ def workload_config(w: synth.Workload, args) -> dict:
 
 
 L2_BYTES = 129 << 20      # GB300 L2
+# Graph replays before the timed region.  On a host-resident store the first
+# replays run slower (up to 1.4x over the first ten or so, in every run) while
+# the pinned pages' translations warm up; a decode loop runs in the steady state
+# that follows.
+GRAPH_WARMUP = 40
 
 
 def l2_note(w: synth.Workload) -> str:
@@ -788,7 +793,7 @@ def main():
     import __graft_entry__
     __graft_entry__.build()
     # queries: warm-up, timed, e2e, graph warm-up and 50 spread steps, all distinct
-    total_steps = args.warmup + 2 * args.steps + max(args.warmup, 10) + 50
+    total_steps = args.warmup + 2 * args.steps + max(args.warmup, GRAPH_WARMUP) + 50
     st = Setup(w, args.budget, rank, total_steps, args.fixed, args.path, args.groups, args.plan_theta)
     link_gbs = measure_link_peak() if st.host else None
     sm_link_gbs = measure_sm_read_peak(st) if st.host else None
@@ -831,9 +836,9 @@ def main():
     clocks.start()                              # running (first sample taken) before the timed region
     # graph warm-up: the first replays upload the graph, and a host-resident store needs
     # several steps with different queries (different planned channels) before its reads
-    # reach their steady rate, as in a decode loop: at least 10 replays, each with its own
+    # reach their steady rate, as in a decode loop: at least GRAPH_WARMUP replays, each with its own
     # queries (none of them used by the timed steps)
-    graph_warmup = max(args.warmup, 10) if use_graph else 0
+    graph_warmup = max(args.warmup, GRAPH_WARMUP) if use_graph else 0
     q_gw = args.warmup + 2 * args.steps         # first query index reserved for the graph warm-up
     if use_graph:
         for s in range(graph_warmup):
