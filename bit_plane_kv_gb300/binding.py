@@ -14,7 +14,9 @@ import os
 import torch
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_PKG, "_build", "libfathom.so")
+# FATHOM_LIB names another build of the same library (e.g. the debug build with
+# bounds checks, libfathom_debug.so) to load instead of the default one.
+LIB_PATH = os.environ.get("FATHOM_LIB") or os.path.join(_PKG, "_build", "libfathom.so")
 
 F32, BF16 = 0, 1
 WS_SCAN_TOPK, WS_SPARSE_ATTN, WS_DENSE_ATTN, WS_KLT_ONLINE = 0, 1, 2, 3
@@ -68,6 +70,7 @@ SIGNATURES = {
     "fathom_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(Shape), ctypes.c_int]),
     "fathom_last_error": (ctypes.c_char_p, []),
     "fathom_version": (ctypes.c_char_p, []),
+    "fathom_debug_status": (ctypes.c_int, [ctypes.c_int, ctypes.c_void_p]),
 }
 
 
@@ -513,3 +516,12 @@ def fathom_sparse_attn(shape: Shape, k_rows, v_rows, q, topk_idx, workspace, out
     _call("fathom_sparse_attn", ctypes.byref(shape), _p(k_rows), _p(v_rows), _p(q), _p(topk_idx),
           _p(out), _p(workspace), workspace.numel(), _stream(stream))
     return out
+
+
+def fathom_debug_status(mode=0):
+    """Debug build only: the first failed bounds check of the scan, gather and
+    attention kernels, as three integers (site << 48 | index; 0: none).  mode 1
+    also clears them; mode 2 plants a self-test record first."""
+    out = (ctypes.c_uint64 * 3)()
+    _call("fathom_debug_status", int(mode), ctypes.cast(out, ctypes.c_void_p))
+    return [int(x) for x in out]

@@ -44,17 +44,26 @@ def _stale(target, deps):
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False, ptxas_verbose: bool = False) -> str:
-    os.makedirs(OUT_DIR, exist_ok=True)
+DEBUG_LIB = os.path.join(OUT_DIR, "libfathom_debug.so")
+
+
+def build(force: bool = False, verbose: bool = False, ptxas_verbose: bool = False, debug: bool = False) -> str:
+    """Build libfathom.so, or with debug=True libfathom_debug.so: the same sources
+    compiled with -DFATHOM_DEBUG, whose kernels check every data-derived index
+    (see fathom_debug_status in include/fathom.h)."""
+    out_dir = os.path.join(OUT_DIR, "debug") if debug else OUT_DIR
+    lib_path = DEBUG_LIB if debug else LIB
+    os.makedirs(out_dir, exist_ok=True)
     headers = glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(ROOT, "include", "*.h"))
     srcs = sources()
-    objs = [os.path.join(OUT_DIR, os.path.basename(s)[:-3] + ".o") for s in srcs]
+    objs = [os.path.join(out_dir, os.path.basename(s)[:-3] + ".o") for s in srcs]
     cc = nvcc()
+    extra = ["-DFATHOM_DEBUG"] if debug else []
 
     def compile_one(src, obj):
         if not force and not _stale(obj, [src, *headers]):
             return ""
-        cmd = [cc, *ARCH, *FLAGS, "-c", src, "-o", obj]
+        cmd = [cc, *ARCH, *FLAGS, *extra, "-c", src, "-o", obj]
         if ptxas_verbose:
             cmd.insert(1, "-Xptxas=-v")
         r = subprocess.run(cmd, capture_output=True, text=True)
@@ -68,15 +77,16 @@ def build(force: bool = False, verbose: bool = False, ptxas_verbose: bool = Fals
         for src, log in zip(srcs, logs):
             if log:
                 sys.stderr.write(f"--- {os.path.basename(src)}\n{log}")
-    if force or _stale(LIB, objs):
-        tmp = LIB + f".tmp{os.getpid()}"
+    if force or _stale(lib_path, objs):
+        tmp = lib_path + f".tmp{os.getpid()}"
         cmd = [cc, *ARCH, "-shared", "-cudart", "shared", "-Xlinker", "-rpath", "-Xlinker", _cuda_libdir(cc), "-o", tmp, *objs]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-        os.replace(tmp, LIB)
-    return LIB
+        os.replace(tmp, lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose=True, ptxas_verbose="-v" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose=True, ptxas_verbose="-v" in sys.argv,
+                debug="--debug" in sys.argv))

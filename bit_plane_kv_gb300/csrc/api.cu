@@ -289,6 +289,29 @@ const char *fathom_last_error(void) { return g_err; }
 
 const char *fathom_version(void) { return "fathom-gb300 0.2 (sm_103a)"; }
 
+int fathom_debug_status(int mode, uint64_t *first_failure) {
+    g_err[0] = 0;
+    NONNULL(first_failure);
+    if (mode < 0 || mode > 2) { set_error("debug_status: mode must be 0, 1 or 2"); return FATHOM_EINVAL; }
+#ifdef FATHOM_DEBUG
+    if (mode == 2) {   // plant a self-test record in every file's word first
+        debug_read_scan_plant();
+        debug_read_gather_plant();
+        debug_read_attn_plant();
+    }
+    const cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) { set_error("debug_status: %s", cudaGetErrorString(e)); return FATHOM_ECUDA; }
+    first_failure[0] = debug_read_scan(mode == 1);
+    first_failure[1] = debug_read_gather(mode == 1);
+    first_failure[2] = debug_read_attn(mode == 1);
+    return launch_status("debug_status");
+#else
+    first_failure[0] = first_failure[1] = first_failure[2] = 0;
+    set_error("debug_status: this library was built without the debug checks (-DFATHOM_DEBUG)");
+    return FATHOM_EINVAL;
+#endif
+}
+
 int fathom_calibrate(int32_t units, int32_t m, int32_t D, const float *calib, float *mean_out,
                      float *var_out, void *stream) {
     g_err[0] = 0;

@@ -16,6 +16,56 @@ namespace fathom {
 void set_error(const char *fmt, ...);
 int launch_status(const char *what);   // FATHOM_OK or FATHOM_ECUDA (+ message)
 
+// ---------------------------------------------------------------- debug checks
+// A build with -DFATHOM_DEBUG checks, before each load or store whose index
+// comes from data (run lists, kept lists, staged offsets), that the index lies
+// inside the buffer the call was given.  A failed check records its site and
+// the offending index in this translation unit's debug word (the first failure
+// wins), and the access is skipped, so a bad index never reaches memory and
+// the kernel still ends normally.  fathom_debug_status() reads the words.  In
+// the default build every check is the constant true and costs nothing.
+enum DebugSite : unsigned {
+    kDbgScanStagePlanes = 1,   // scan: a staged plane word outside the store or staging area
+    kDbgScanStageScales = 2,   // scan: a staged scale outside it
+    kDbgScanLoadPlanes = 3,    // scan (synchronous staging): a plane word outside it
+    kDbgScanLoadScales = 4,    // scan (synchronous staging): a scale outside it
+    kDbgScanForced = 5,        // scan: a forced token's slot outside [0, |forced|)
+    kDbgGatherSrc = 6,         // gather: a source word or scale outside the store
+    kDbgGatherDst = 7,         // gather: a destination outside the staging area
+    kDbgAttnRow = 8,           // attention: a kept row outside [0, n)
+    kDbgSelfTest = 15          // a record planted on request, to test the reporting path
+};
+#ifdef FATHOM_DEBUG
+static __device__ unsigned long long g_fathom_dbg;   // one per translation unit
+__device__ __forceinline__ bool debug_check(bool ok, unsigned site, unsigned long long value) {
+    if (!ok) atomicCAS(&g_fathom_dbg, 0ull, ((unsigned long long)site << 48) | (value & 0xffffffffffffull));
+    return ok;
+}
+#define FATHOM_CHECK(cond, site, value) ::fathom::debug_check((cond), (site), (unsigned long long)(value))
+// Each translation unit that checks defines its reader with this macro, and a
+// one-thread kernel that plants a self-test record (no memory access).
+#define FATHOM_DEBUG_READER(name)                                                        \
+    __global__ void name##_plant_kernel() { FATHOM_CHECK(false, kDbgSelfTest, 0x5e1f); } \
+    void name##_plant() { name##_plant_kernel<<<1, 1>>>(); }                            \
+    unsigned long long name(bool reset) {                                               \
+        unsigned long long v = 0;                                                       \
+        cudaMemcpyFromSymbol(&v, g_fathom_dbg, sizeof v);                               \
+        if (reset) { const unsigned long long z = 0; cudaMemcpyToSymbol(g_fathom_dbg, &z, sizeof z); } \
+        return v;                                                                       \
+    }
+#else
+#define FATHOM_CHECK(cond, site, value) (true)
+#define FATHOM_DEBUG_READER(name)
+#endif
+#ifdef FATHOM_DEBUG
+unsigned long long debug_read_scan(bool reset);
+unsigned long long debug_read_gather(bool reset);
+unsigned long long debug_read_attn(bool reset);
+void debug_read_scan_plant();
+void debug_read_gather_plant();
+void debug_read_attn_plant();
+#endif
+
 // ---------------------------------------------------------------- geometry
 __host__ __device__ inline int num_blocks(int n) { return (n + FATHOM_BLOCK - 1) / FATHOM_BLOCK; }
 

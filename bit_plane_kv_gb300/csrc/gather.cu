@@ -85,20 +85,28 @@ gather_kernel(int D, int nb, int cb, int x_planes, int x_total, const uint64_t *
                     const size_t p = (d - rs) / nb, o = (d - rs) - p * nb;
                     const size_t seg = (cb == nb) ? hi - d : min(hi - d, nb - o);
                     const size_t src0 = p * cb + o;
-                    copy_span<uint64_t, uint4>(sbase + src0, stage_planes + (size_t)u * stage_words + d,
-                                               (uint32_t)seg,
-                                               vec_planes && (((r[j].src_word + src0) | d) % 2 == 0));
+                    const size_t sidx = (size_t)u * D * FATHOM_PLANES * cb + r[j].src_word + src0;
+                    if (FATHOM_CHECK(sidx + seg <= (size_t)gridDim.y * D * FATHOM_PLANES * cb, kDbgGatherSrc, sidx) &&
+                        FATHOM_CHECK(d + seg <= stage_words, kDbgGatherDst, d + seg))
+                        copy_span<uint64_t, uint4>(sbase + src0, stage_planes + (size_t)u * stage_words + d,
+                                                   (uint32_t)seg,
+                                                   vec_planes && (((r[j].src_word + src0) | d) % 2 == 0));
                     d += seg;
                 }
             } else {
                 const size_t src0 = r[j].src_scale + (lo - rs);
-                copy_span<uint16_t, uint4>(store_scales + (size_t)u * D * cb + src0,
-                                           stage_scales + (size_t)u * stage_scales_n + lo,
-                                           (uint32_t)(hi - lo), vec_scales && ((src0 | lo) % 8 == 0));
+                const size_t sidx = (size_t)u * D * cb + src0;
+                if (FATHOM_CHECK(sidx + (hi - lo) <= (size_t)gridDim.y * D * cb, kDbgGatherSrc, sidx) &&
+                    FATHOM_CHECK(hi <= stage_scales_n, kDbgGatherDst, hi))
+                    copy_span<uint16_t, uint4>(store_scales + (size_t)u * D * cb + src0,
+                                               stage_scales + (size_t)u * stage_scales_n + lo,
+                                               (uint32_t)(hi - lo), vec_scales && ((src0 | lo) % 8 == 0));
             }
         }
     }
 }
+
+FATHOM_DEBUG_READER(debug_read_gather)
 
 int launch_gather(const fathom_shape &s, const uint64_t *sp, const uint16_t *ss,
                   const fathom_run *runs, uint64_t *dp, uint16_t *ds, size_t stage_words,

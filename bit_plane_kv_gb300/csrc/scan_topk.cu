@@ -668,16 +668,27 @@ scan_kernel(int n, int cb, int ctok, int D, int chunk_blocks, int source, size_t
     const int nch0 = g0.n4 + g0.n3 + g0.n2 + g0.n1;
     const int npl0 = 4 * g0.n4 + 3 * g0.n3 + 2 * g0.n2 + g0.n1;
     const bool piped = vec && ng == 1 && npl0 <= kPG / 2;
+    // words and scales of the buffer the scan reads (store or staging), for the debug checks
+    const uint64_t src_words = (source == FATHOM_SRC_STORE) ? (uint64_t)gridDim.y * D * FATHOM_PLANES * cb
+                                                             : (uint64_t)gridDim.y * stage_words;
+    const uint64_t src_scales = (source == FATHOM_SRC_STORE) ? (uint64_t)gridDim.y * D * cb
+                                                              : (uint64_t)gridDim.y * stage_scales;
+    (void)src_words;
+    (void)src_scales;
     auto stage_async = [&](int half, int sbx) {
         for (int e = tid; e < npl0 * (kSubBlocks / 2); e += NT) {
             const int sl = e / (kSubBlocks / 2), c = e % (kSubBlocks / 2);
-            const bool ok = sbx + 2 * c < nb;                 // nb even: both words in range or neither
+            const bool ok = sbx + 2 * c < nb &&              // nb even: both words in range or neither
+                            FATHOM_CHECK(sm.plane_src[sl] + sbx + 2 * c + 2 <= src_words, kDbgScanStagePlanes,
+                                         sm.plane_src[sl] + sbx + 2 * c);
             const uint64_t *src = ok ? planes + sm.plane_src[sl] + sbx + 2 * c : planes;
             cp_async16(&sm.pw[half * (kPG / 2) + sl][2 * c], src, ok ? 16 : 0);
         }
         for (int e = tid; e < nch0 * (kSubBlocks / 8); e += NT) {
             const int al = e / (kSubBlocks / 8), c = e % (kSubBlocks / 8);
-            const bool ok = sbx + 8 * c < nb;                 // nb % 8 == 0 on this path
+            const bool ok = sbx + 8 * c < nb &&              // nb % 8 == 0 on this path
+                            FATHOM_CHECK(sm.ch_scale[al] + sbx + 8 * c + 8 <= src_scales, kDbgScanStageScales,
+                                         sm.ch_scale[al] + sbx + 8 * c);
             const uint16_t *src = ok ? scales + sm.ch_scale[al] + sbx + 8 * c : scales;
             cp_async16(&sm.scb[half][al][8 * c], src, ok ? 16 : 0);
         }
@@ -770,14 +781,18 @@ scan_kernel(int n, int cb, int ctok, int D, int chunk_blocks, int source, size_t
                     if (vec && nblk == kSubBlocks) {
                         for (int e = tid; e < npl * (kSubBlocks / 2); e += NT) {
                             const int sl = e / (kSubBlocks / 2), c = e % (kSubBlocks / 2);
+                            const uint64_t w0 = sm.plane_src[g.p0 + sl] + sb + 2 * c;
                             *reinterpret_cast<uint4 *>(&sm.pw[sl][2 * c]) =
-                                __ldg(reinterpret_cast<const uint4 *>(planes + sm.plane_src[g.p0 + sl] + sb) + c);
+                                FATHOM_CHECK(w0 + 2 <= src_words, kDbgScanLoadPlanes, w0)
+                                    ? __ldg(reinterpret_cast<const uint4 *>(planes + w0))
+                                    : make_uint4(0u, 0u, 0u, 0u);
                         }
                     } else {
                         for (int e = tid; e < npl * kSubBlocks; e += NT) {
                             const int sl = e / kSubBlocks, b = e % kSubBlocks;
                             uint2 v = make_uint2(0u, 0u);
-                            if (b < nblk) {
+                            if (b < nblk && FATHOM_CHECK(sm.plane_src[g.p0 + sl] + sb + b < src_words,
+                                                         kDbgScanLoadPlanes, sm.plane_src[g.p0 + sl] + sb + b)) {
                                 const uint64_t wd = __ldg(planes + sm.plane_src[g.p0 + sl] + sb + b);
                                 v = make_uint2((uint32_t)wd, (uint32_t)(wd >> 32));
                             }
@@ -788,7 +803,9 @@ scan_kernel(int n, int cb, int ctok, int D, int chunk_blocks, int source, size_t
                         const int al = e / kSubBlocks, b = e % kSubBlocks;
                         const int a = g.a0 + al;
                         float a16 = 0.0f;
-                        if (b < nblk) a16 = __half2float(__ushort_as_half(__ldg(scales + sm.ch_scale[a] + sb + b)));
+                        if (b < nblk && FATHOM_CHECK(sm.ch_scale[a] + sb + b < src_scales, kDbgScanLoadScales,
+                                                     sm.ch_scale[a] + sb + b))
+                            a16 = __half2float(__ushort_as_half(__ldg(scales + sm.ch_scale[a] + sb + b)));
 #pragma unroll
                         for (int h = 0; h < G; ++h) sm.w[b][al * G + h] = sm.qs[a][h] * a16;
                     }
@@ -825,8 +842,10 @@ scan_kernel(int n, int cb, int ctok, int D, int chunk_blocks, int source, size_t
             }
             if (valid && forced) {
                 const int slot = (i < ns) ? i : ns + (i - r0);
+                if (FATHOM_CHECK(slot >= 0 && slot < nf, kDbgScanForced, slot)) {
 #pragma unroll
-                for (int h = 0; h < G; ++h) forced_scores[((size_t)u * G + h) * nf + slot] = acc(m, h);
+                    for (int h = 0; h < G; ++h) forced_scores[((size_t)u * G + h) * nf + slot] = acc(m, h);
+                }
             }
         }
         auto key_of = [&](int m, int h) -> uint64_t {
@@ -1417,6 +1436,8 @@ static int resident_g() {
     }
     return cache[dev];
 }
+
+FATHOM_DEBUG_READER(debug_read_scan)
 
 int scan_resident_ctas(int G) {
     switch (G) {

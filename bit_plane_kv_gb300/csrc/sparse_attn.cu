@@ -405,6 +405,7 @@ attn_kernel(int n, int ctok, int D, int k, int rows_cta, int cph, int splits, co
                 m = sm.rmask[rr];
                 i = sm.rows[rr];
                 if (!((m >> hown) & 1u) || (m & below)) m = 0;   // invalid, or a lower head owns it
+                if (m && !FATHOM_CHECK(i >= 0 && i < n, kDbgAttnRow, (unsigned)i)) m = 0;
             }
             mask[r] = m;
             ti[r] = i;
@@ -543,6 +544,8 @@ static int launch_sparse_attn_src(const fathom_shape &s, const KSource &ks, cons
     if (le != cudaSuccess) { set_error("attn_kernel: %s", cudaGetErrorString(le)); return FATHOM_ECUDA; }
     return launch_status("attn_kernel");
 }
+
+FATHOM_DEBUG_READER(debug_read_attn)
 
 // ---------------------------------------------------------------------------
 // Allocation-free variant.  Some callers cannot hand the library a workspace

@@ -413,6 +413,23 @@ const char *fathom_last_error(void);
 /* Library version string. */
 const char *fathom_version(void);
 
+/* Bounds checks of a debug build (compiled with -DFATHOM_DEBUG; the paper has no
+ * counterpart: they stand in for a memory checker).  In such a build every
+ * load or store of the scan, gather and attention kernels whose index comes
+ * from data (run lists, staged offsets, kept lists) first checks that the
+ * index lies inside the buffer the call was given; a failed check skips the
+ * access and records, per kernel file, the first failure as
+ * (site << 48) | index, the sites being: 1-4 scan staging and loads of plane
+ * words and scales, 5 a forced token's slot, 6-7 gather source and
+ * destination, 8 an attention row.  This call synchronises the calling
+ * thread's device and writes the records of the scan, gather and attention
+ * files to first_failure[0..2] (0: no failure).  mode 0 reads them, mode 1
+ * reads and clears them, mode 2 first plants a self-test record (site 15,
+ * index 0x5e1f, no memory access) in each file and then reads, to test the
+ * reporting path.  A build without the checks writes zeros and returns
+ * FATHOM_EINVAL. */
+int fathom_debug_status(int mode, uint64_t *first_failure);
+
 #ifdef __cplusplus
 }
 #endif

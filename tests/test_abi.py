@@ -185,3 +185,14 @@ def test_fidelity_helpers_validate_and_greedy_matches_oracle(lib):
         B.fathom_greedy_budgets(np.full((2, 14), np.nan), 24, 8, 48)
     with pytest.raises(B.FathomError):
         B.fathom_greedy_budgets(np.zeros((2, 3)), 24, 8, 48)            # above the top level (40)
+
+
+def test_debug_status_reports_a_build_without_checks(lib):
+    # the default build compiles every bounds check away: the call says so and writes zeros
+    out = (ctypes.c_uint64 * 3)(7, 7, 7)
+    rc = lib.fathom_debug_status(0, ctypes.cast(out, ctypes.c_void_p))
+    code, msg = rc_msg(lib, rc)
+    assert code == 1 and "without the debug checks" in msg
+    assert list(out) == [0, 0, 0]
+    assert rc_msg(lib, lib.fathom_debug_status(3, ctypes.cast(out, ctypes.c_void_p)))[0] == 1
+    assert rc_msg(lib, lib.fathom_debug_status(0, None)) == (1, "first_failure is NULL")
