@@ -30,11 +30,12 @@ _vp, _i32, _sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
 class Shape(ctypes.Structure):
     _fields_ = [("units", ctypes.c_int32), ("n", ctypes.c_int32), ("D", ctypes.c_int32),
                 ("G", ctypes.c_int32), ("k", ctypes.c_int32), ("n_sink", ctypes.c_int32),
-                ("n_recent", ctypes.c_int32), ("n_cap", ctypes.c_int32)]
+                ("n_recent", ctypes.c_int32), ("n_cap", ctypes.c_int32), ("scan_ctas_per_sm", ctypes.c_int32)]
 
     def __repr__(self):
         return (f"Shape(units={self.units}, n={self.n}, D={self.D}, G={self.G}, k={self.k}, "
-                f"n_sink={self.n_sink}, n_recent={self.n_recent}, n_cap={self.n_cap})")
+                f"n_sink={self.n_sink}, n_recent={self.n_recent}, n_cap={self.n_cap}, "
+                f"scan_ctas_per_sm={self.scan_ctas_per_sm})")
 
     @property
     def cap(self) -> int:
@@ -57,6 +58,10 @@ SIGNATURES = {
     "fathom_gather": (ctypes.c_int, [ctypes.POINTER(Shape), _vp, _vp, _vp, _vp, _vp, _sz, _sz, _vp]),
     "fathom_scan_topk": (ctypes.c_int, [ctypes.POINTER(Shape), _vp, _vp, ctypes.c_int, _sz, _sz, _vp,
                                         _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "fathom_scan": (ctypes.c_int, [ctypes.POINTER(Shape), _vp, _vp, ctypes.c_int, _sz, _sz, _vp, _vp, _vp, _vp,
+                                   _sz, _vp]),
+    "fathom_select": (ctypes.c_int, [ctypes.POINTER(Shape), _vp, _vp, ctypes.c_int, _sz, _sz, _vp, _vp, _vp, _vp,
+                                     _vp, _sz, _vp]),
     "fathom_exact_topk": (ctypes.c_int, [ctypes.POINTER(Shape), _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "fathom_sparse_attn": (ctypes.c_int, [ctypes.POINTER(Shape), _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "fathom_dense_attn": (ctypes.c_int, [ctypes.POINTER(Shape), _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
@@ -164,8 +169,8 @@ def _rows(shape: Shape) -> int:
     return shape.units * shape.cap * shape.D
 
 
-def make_shape(units, n, D=128, G=4, k=1, n_sink=4, n_recent=32, n_cap=0) -> Shape:
-    return Shape(units, n, D, G, k, n_sink, n_recent, n_cap)
+def make_shape(units, n, D=128, G=4, k=1, n_sink=4, n_recent=32, n_cap=0, scan_ctas_per_sm=0) -> Shape:
+    return Shape(units, n, D, G, k, n_sink, n_recent, n_cap, scan_ctas_per_sm)
 
 
 def nblocks(n: int) -> int:
@@ -367,6 +372,47 @@ def fathom_scan_topk(shape: Shape, planes, scales, runs, q, workspace, source=SR
     _call("fathom_scan_topk", ctypes.byref(shape), _p(planes), _p(scales), int(source), W, S,
           _p(runs), _p(q), _p(topk_idx), _p(topk_score), _p(scores), _p(workspace),
           workspace.numel(), _stream(stream))
+    return topk_idx, topk_score
+
+
+def _scan_inputs(shape, planes, scales, runs, q, workspace, source):
+    if source == SRC_STAGING:
+        W = planes.shape[-1] if planes is not None and planes.dim() else 0
+        S = scales.shape[-1] if scales is not None and scales.dim() else 0
+        need_p, need_s = shape.units * W, shape.units * S
+    else:
+        W = S = 0
+        need_p, need_s = _store_words(shape), _store_scales(shape)
+    _check(planes, "planes", (torch.int64,), min_numel=need_p)
+    _check(scales, "scales", (torch.int16,), min_numel=need_s)
+    _check(runs, "runs", (torch.int32,), (shape.units, shape.D, 6))
+    _check(q, "q", (torch.float32,), (shape.units, shape.G, shape.D))
+    _check(workspace, "workspace", (torch.uint8,))
+    return W, S
+
+
+def fathom_scan(shape: Shape, planes, scales, runs, q, workspace, source=SRC_STORE, scores=None, stream=None):
+    """The scan half of fathom_scan_topk: candidate lists in the workspace (scores, if
+    given, receives every token's score [U][G][n])."""
+    W, S = _scan_inputs(shape, planes, scales, runs, q, workspace, source)
+    if scores is not None:
+        _check(scores, "scores", (torch.float32,), (shape.units, shape.G, shape.n))
+    _call("fathom_scan", ctypes.byref(shape), _p(planes), _p(scales), int(source), W, S, _p(runs), _p(q),
+          _p(scores), _p(workspace), workspace.numel(), _stream(stream))
+
+
+def fathom_select(shape: Shape, planes, scales, runs, q, workspace, source=SRC_STORE, topk_idx=None,
+                  topk_score=None, stream=None):
+    """The selection half: -> topk_idx [U][G][k] int32 ascending, topk_score [U][G][k] fp32."""
+    W, S = _scan_inputs(shape, planes, scales, runs, q, workspace, source)
+    _check_out(topk_idx, "topk_idx", (torch.int32,), shape.units * shape.G * shape.k)
+    _check_out(topk_score, "topk_score", (torch.float32,), shape.units * shape.G * shape.k)
+    if topk_idx is None:
+        topk_idx = torch.empty(shape.units, shape.G, shape.k, dtype=torch.int32, device=q.device)
+    if topk_score is None:
+        topk_score = torch.empty(shape.units, shape.G, shape.k, dtype=torch.float32, device=q.device)
+    _call("fathom_select", ctypes.byref(shape), _p(planes), _p(scales), int(source), W, S, _p(runs), _p(q),
+          _p(topk_idx), _p(topk_score), _p(workspace), workspace.numel(), _stream(stream))
     return topk_idx, topk_score
 
 

@@ -85,6 +85,7 @@ ScanGrid scan_grid(const fathom_shape &s) {
     if (sms <= 0) sms = 152;
     int res = scan_resident_ctas(s.G);
     if (res <= 0) res = (s.G <= 4) ? 3 : 1;
+    if (s.scan_ctas_per_sm > 0 && s.scan_ctas_per_sm < res) res = s.scan_ctas_per_sm;
     const long long slots = (long long)sms * res;
     const int nb = num_blocks(s.n);
     const int n_sub = (nb + kSubBlocks - 1) / kSubBlocks;
@@ -225,6 +226,9 @@ static int check_shape(const fathom_shape *s, bool need_select) {
     if (!(s->G == 1 || s->G == 2 || s->G == 4 || s->G == 8)) { set_error("G must be 1, 2, 4 or 8 (got %d)", s->G); return FATHOM_EINVAL; }
     if (s->n_cap != 0 && (s->n_cap < s->n || s->n_cap > (1 << 28))) {
         set_error("n_cap must be 0 or in [n, 2^28] (got n_cap=%d, n=%d)", s->n_cap, s->n); return FATHOM_EINVAL;
+    }
+    if (s->scan_ctas_per_sm < 0 || s->scan_ctas_per_sm > 8) {
+        set_error("scan_ctas_per_sm must be in [0, 8] (got %d)", s->scan_ctas_per_sm); return FATHOM_EINVAL;
     }
     if ((size_t)s->units * s->D * FATHOM_PLANES * (size_t)cap_blocks(*s) >= ((size_t)1 << 40) ||
         (size_t)s->D * FATHOM_PLANES * (size_t)cap_blocks(*s) >= ((size_t)1 << 32)) {
@@ -469,11 +473,9 @@ size_t fathom_workspace_size(const fathom_shape *shape, int which) {
     return 0;
 }
 
-int fathom_scan_topk(const fathom_shape *shape, const uint64_t *planes, const uint16_t *scales,
-                     int source, size_t stage_words, size_t stage_scales_n, const fathom_run *runs,
-                     const float *q, int32_t *topk_idx, float *topk_score, float *scores_opt,
-                     void *workspace, size_t workspace_bytes, void *stream) {
-    g_err[0] = 0;
+static int check_scan_args(const fathom_shape *shape, const uint64_t *planes, const uint16_t *scales, int source,
+                           size_t stage_words, size_t stage_scales_n, const fathom_run *runs, const float *q,
+                           void *workspace, size_t workspace_bytes) {
     int rc = check_shape(shape, true);
     if (rc) return rc;
     if (source != FATHOM_SRC_STORE && source != FATHOM_SRC_STAGING) {
@@ -486,8 +488,6 @@ int fathom_scan_topk(const fathom_shape *shape, const uint64_t *planes, const ui
     NONNULL(scales);
     NONNULL(runs);
     NONNULL(q);
-    NONNULL(topk_idx);
-    NONNULL(topk_score);
     NONNULL(workspace);
     size_t need = scan_workspace_layout(*shape).total;
     if (workspace_bytes < need) {
@@ -495,9 +495,48 @@ int fathom_scan_topk(const fathom_shape *shape, const uint64_t *planes, const ui
         return FATHOM_ENOMEM;
     }
     if (((uintptr_t)workspace & 255) != 0) { set_error("workspace must be 256-byte aligned"); return FATHOM_EINVAL; }
+    return FATHOM_OK;
+}
+
+int fathom_scan_topk(const fathom_shape *shape, const uint64_t *planes, const uint16_t *scales,
+                     int source, size_t stage_words, size_t stage_scales_n, const fathom_run *runs,
+                     const float *q, int32_t *topk_idx, float *topk_score, float *scores_opt,
+                     void *workspace, size_t workspace_bytes, void *stream) {
+    g_err[0] = 0;
+    int rc = check_scan_args(shape, planes, scales, source, stage_words, stage_scales_n, runs, q, workspace,
+                             workspace_bytes);
+    if (rc) return rc;
+    NONNULL(topk_idx);
+    NONNULL(topk_score);
     FAULT_POINT("fathom_scan_topk");
     return launch_scan_topk(*shape, planes, scales, source, stage_words, stage_scales_n, runs, q,
-                            topk_idx, topk_score, scores_opt, workspace, (cudaStream_t)stream);
+                            topk_idx, topk_score, scores_opt, workspace, (cudaStream_t)stream, SCAN_PART_ALL);
+}
+
+int fathom_scan(const fathom_shape *shape, const uint64_t *planes, const uint16_t *scales, int source,
+                size_t stage_words, size_t stage_scales_n, const fathom_run *runs, const float *q,
+                float *scores_opt, void *workspace, size_t workspace_bytes, void *stream) {
+    g_err[0] = 0;
+    int rc = check_scan_args(shape, planes, scales, source, stage_words, stage_scales_n, runs, q, workspace,
+                             workspace_bytes);
+    if (rc) return rc;
+    FAULT_POINT("fathom_scan");
+    return launch_scan_topk(*shape, planes, scales, source, stage_words, stage_scales_n, runs, q, nullptr,
+                            nullptr, scores_opt, workspace, (cudaStream_t)stream, SCAN_PART_SCAN);
+}
+
+int fathom_select(const fathom_shape *shape, const uint64_t *planes, const uint16_t *scales, int source,
+                  size_t stage_words, size_t stage_scales_n, const fathom_run *runs, const float *q,
+                  int32_t *topk_idx, float *topk_score, void *workspace, size_t workspace_bytes, void *stream) {
+    g_err[0] = 0;
+    int rc = check_scan_args(shape, planes, scales, source, stage_words, stage_scales_n, runs, q, workspace,
+                             workspace_bytes);
+    if (rc) return rc;
+    NONNULL(topk_idx);
+    NONNULL(topk_score);
+    FAULT_POINT("fathom_select");
+    return launch_scan_topk(*shape, planes, scales, source, stage_words, stage_scales_n, runs, q, topk_idx,
+                            topk_score, nullptr, workspace, (cudaStream_t)stream, SCAN_PART_SELECT);
 }
 
 int fathom_exact_topk(const fathom_shape *shape, const uint16_t *k_rows, const float *q,

@@ -224,10 +224,13 @@ int launch_plan_fixed(const fathom_shape &s, const float *q, const float *var, i
 int launch_gather(const fathom_shape &s, const uint64_t *sp, const uint16_t *ss,
                   const fathom_run *runs, uint64_t *dp, uint16_t *ds, size_t stage_words,
                   size_t stage_scales, cudaStream_t st);
+// Which launches of scan + top-k to enqueue: all of them, the first-pass scan
+// only, or the selection only (merge, exact second pass, second merge).
+enum ScanPart { SCAN_PART_ALL = 0, SCAN_PART_SCAN = 1, SCAN_PART_SELECT = 2 };
 int launch_scan_topk(const fathom_shape &s, const uint64_t *planes, const uint16_t *scales,
                      int source, size_t stage_words, size_t stage_scales, const fathom_run *runs,
                      const float *q, int32_t *idx, float *score, float *scores_opt, void *ws,
-                     cudaStream_t st);
+                     cudaStream_t st, int part = SCAN_PART_ALL);
 int launch_sparse_attn(const fathom_shape &s, const uint16_t *krows, const uint16_t *vrows,
                        const float *q, const int32_t *idx, float *out, void *ws, cudaStream_t st);
 int launch_dense_attn(const fathom_shape &s, const uint16_t *krows, const uint16_t *vrows, const float *q,

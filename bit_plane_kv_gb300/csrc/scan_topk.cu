@@ -1337,7 +1337,7 @@ template <int G>
 static int launch_g(const fathom_shape &s, const uint64_t *planes, const uint16_t *scales,
                     int source, size_t stage_words, size_t stage_scales, const fathom_run *runs,
                     const float *q, int32_t *idx, float *score, float *scores_opt, void *ws,
-                    cudaStream_t st) {
+                    cudaStream_t st, int part) {
     const ScanGrid sg = scan_grid(s);
     const Forced f = forced_range(s.n, s.n_sink, s.n_recent);
     const ScanWorkspace wl = scan_workspace_layout(s);
@@ -1382,30 +1382,36 @@ static int launch_g(const fathom_shape &s, const uint64_t *planes, const uint16_
     dim3 grid(sg.chunks, s.units);
     cudaError_t le = cudaSuccess;
     for (int pass = 0; pass < 2; ++pass) {
+        // part SCAN: the first-pass scan only; part SELECT: everything after it
+        const bool do_scan = pass == 1 ? part != SCAN_PART_SCAN : part != SCAN_PART_SELECT;
+        const bool do_merge = part != SCAN_PART_SCAN;
 #define FATHOM_SCAN_LAUNCH(FIX, SC, RW)                                                                    \
     le = launch_pdl(scan_kernel<G, FIX, SC, RW>, grid, dim3(NT), smem, st, s.n, cb, cap_tokens(s), s.D,        \
                     sg.chunk_blocks, source, stage_words, stage_scales, planes, scales, runs, q, k_sel, m_sel, \
                     m_first, f.ns, f.r0, nf, cap, vec, SC ? scores_opt : nullptr, cand, cnt, ctau, flags,      \
                     forced, sub_ctr, sub_owner)
-        if (rows_src) {
-            if (pass == 1) FATHOM_SCAN_LAUNCH(true, false, true);
-            else if (scores_opt) FATHOM_SCAN_LAUNCH(false, true, true);
-            else FATHOM_SCAN_LAUNCH(false, false, true);
-        } else {
-            if (pass == 1) FATHOM_SCAN_LAUNCH(true, false, false);
-            else if (scores_opt) FATHOM_SCAN_LAUNCH(false, true, false);
-            else FATHOM_SCAN_LAUNCH(false, false, false);
+        if (do_scan) {
+            if (rows_src) {
+                if (pass == 1) FATHOM_SCAN_LAUNCH(true, false, true);
+                else if (scores_opt) FATHOM_SCAN_LAUNCH(false, true, true);
+                else FATHOM_SCAN_LAUNCH(false, false, true);
+            } else {
+                if (pass == 1) FATHOM_SCAN_LAUNCH(true, false, false);
+                else if (scores_opt) FATHOM_SCAN_LAUNCH(false, true, false);
+                else FATHOM_SCAN_LAUNCH(false, false, false);
+            }
+            if (le != cudaSuccess) { set_error("scan_kernel: %s", cudaGetErrorString(le)); return FATHOM_ECUDA; }
+            const int rc0 = launch_status("scan_kernel");
+            if (rc0) return rc0;
         }
 #undef FATHOM_SCAN_LAUNCH
-        if (le != cudaSuccess) { set_error("scan_kernel: %s", cudaGetErrorString(le)); return FATHOM_ECUDA; }
-        int rc = launch_status("scan_kernel");
-        if (rc) return rc;
+        if (!do_merge) break;
         le = launch_pdl(merge_kernel, dim3(wl.parts, s.G, s.units), dim3(kMThreads), msmem, st, s.n, s.G, s.k, k_sel,
                         f.ns, f.r0, nf, sg.chunks, wl.parts, cap, pass, (const uint64_t *)cand, (const int *)cnt,
                         (const uint64_t *)ctau, flags, dirty, (const float *)forced, pkeys, pcnt, ticket, idx, score,
                         sub_ctr);
         if (le != cudaSuccess) { set_error("merge_kernel: %s", cudaGetErrorString(le)); return FATHOM_ECUDA; }
-        rc = launch_status("merge_kernel");
+        const int rc = launch_status("merge_kernel");
         if (rc) return rc;
         if (k_sel == 0) break;   // nothing selected: no second pass needed
     }
@@ -1452,12 +1458,12 @@ int scan_resident_ctas(int G) {
 int launch_scan_topk(const fathom_shape &s, const uint64_t *planes, const uint16_t *scales,
                      int source, size_t stage_words, size_t stage_scales, const fathom_run *runs,
                      const float *q, int32_t *idx, float *score, float *scores_opt, void *ws,
-                     cudaStream_t st) {
+                     cudaStream_t st, int part) {
     switch (s.G) {
-        case 1: return launch_g<1>(s, planes, scales, source, stage_words, stage_scales, runs, q, idx, score, scores_opt, ws, st);
-        case 2: return launch_g<2>(s, planes, scales, source, stage_words, stage_scales, runs, q, idx, score, scores_opt, ws, st);
-        case 4: return launch_g<4>(s, planes, scales, source, stage_words, stage_scales, runs, q, idx, score, scores_opt, ws, st);
-        case 8: return launch_g<8>(s, planes, scales, source, stage_words, stage_scales, runs, q, idx, score, scores_opt, ws, st);
+        case 1: return launch_g<1>(s, planes, scales, source, stage_words, stage_scales, runs, q, idx, score, scores_opt, ws, st, part);
+        case 2: return launch_g<2>(s, planes, scales, source, stage_words, stage_scales, runs, q, idx, score, scores_opt, ws, st, part);
+        case 4: return launch_g<4>(s, planes, scales, source, stage_words, stage_scales, runs, q, idx, score, scores_opt, ws, st, part);
+        case 8: return launch_g<8>(s, planes, scales, source, stage_words, stage_scales, runs, q, idx, score, scores_opt, ws, st, part);
         default: set_error("unsupported G=%d", s.G); return FATHOM_EINVAL;
     }
 }

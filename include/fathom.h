@@ -23,7 +23,7 @@
  *   stream).  Every call only enqueues work on that stream: no host
  *   synchronisation, no host read of device results.  Results are valid once
  *   the stream reaches them.  The kernels of fathom_plan, fathom_plan_fixed,
- *   fathom_scan_topk, fathom_exact_topk, fathom_sparse_attn,
+ *   fathom_scan_topk, fathom_scan, fathom_select, fathom_exact_topk, fathom_sparse_attn,
  *   fathom_sparse_attn_planes and fathom_sparse_attn_noalloc are launched with
  *   programmatic stream serialisation: each may be scheduled while the work before it on
  *   the stream is finishing, but it waits for that work to complete before
@@ -115,6 +115,10 @@ typedef struct {
     int32_t n_recent; /* last tokens always kept (the pages use 32) */
     int32_t n_cap;    /* tokens the per-unit arrays are laid out for: 0 means n, else n <= n_cap
                          (a store that grows during decoding; see "Capacity" above) */
+    int32_t scan_ctas_per_sm; /* 0: the scan's grid fills every SM with as many CTAs as fit (3 for
+                         G <= 4); 1..3: at most this many per SM, which leaves room on every SM for
+                         kernels that other streams run beside the scan (a host-resident scan is
+                         bound by the host link, not by its CTAs).  The workspace size follows it. */
 } fathom_shape;
 
 /* ---------------------------------------------------------------------- */
@@ -273,6 +277,26 @@ int fathom_scan_topk(const fathom_shape *shape, const uint64_t *planes,
                      size_t stage_nscales, const fathom_run *runs, const float *q,
                      int32_t *topk_idx, float *topk_score, float *scores_opt,
                      void *workspace, size_t workspace_bytes, void *stream);
+
+/* The two halves of fathom_scan_topk, for callers that overlap one group of
+ * units' selection with the next group's scan on another stream.
+ * fathom_scan (§3.2, §3.3) scores every token for all G heads and leaves each
+ * CTA's candidate keys, threshold and the forced tokens' scores in the
+ * workspace (scores_opt as in fathom_scan_topk).  fathom_select (§2) merges
+ * those lists into the kept sets, rescans exactly any chunk whose threshold may
+ * have dropped a winner (reading planes, scales, runs and q again), and writes
+ * topk_idx and topk_score.  Together, with the same arguments and workspace and
+ * fathom_select ordered after fathom_scan, they compute exactly what
+ * fathom_scan_topk computes; until fathom_select has run, the workspace must
+ * not be given to another scan.  Arguments, layouts and errors as in
+ * fathom_scan_topk. */
+int fathom_scan(const fathom_shape *shape, const uint64_t *planes, const uint16_t *scales, int source,
+                size_t stage_words, size_t stage_nscales, const fathom_run *runs, const float *q,
+                float *scores_opt, void *workspace, size_t workspace_bytes, void *stream);
+int fathom_select(const fathom_shape *shape, const uint64_t *planes, const uint16_t *scales, int source,
+                  size_t stage_words, size_t stage_nscales, const fathom_run *runs, const float *q,
+                  int32_t *topk_idx, float *topk_score, void *workspace, size_t workspace_bytes,
+                  void *stream);
 
 /* Rotated basis without calibration data (Appx. D: the mean, eigenbasis and
  * eigenvalues of a session's own keys; the pages report this under 1 ms at

@@ -36,7 +36,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 def test_version_and_struct_sizes(lib):
     assert "sm_103a" in B.version()
-    assert ctypes.sizeof(B.Shape) == 8 * 4
+    assert ctypes.sizeof(B.Shape) == 9 * 4
     assert B.RUN_BYTES == 24
 
 
@@ -47,7 +47,7 @@ def rc_msg(lib, rc):
 @pytest.mark.parametrize("field,value,frag", [
     ("units", 0, "units"), ("n", 0, "n must"), ("D", 0, "D must"), ("D", 129, "D must"),
     ("G", 3, "G must"), ("k", 0, "k must"), ("k", 5000, "k must"), ("n_sink", -1, "n_sink"),
-    ("n_cap", 100, "n_cap"),
+    ("n_cap", 100, "n_cap"), ("scan_ctas_per_sm", -1, "scan_ctas_per_sm"), ("scan_ctas_per_sm", 9, "scan_ctas_per_sm"),
 ])
 def test_shape_validation(lib, field, value, frag):
     s = B.make_shape(2, 4096, 128, 4, 64)

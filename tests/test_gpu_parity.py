@@ -327,6 +327,41 @@ def test_ragged_multi_tile_multi_unit():
         check_unit(inp, r, ui, 300, [40, 48, 56])
 
 
+@pytest.mark.parametrize("regime", ["hbm", "host", "fused"])
+def test_scan_and_select_halves_equal_scan_topk(regime):
+    # fathom_scan then fathom_select (here on two streams, ordered by an event)
+    # give exactly fathom_scan_topk's kept sets and scores, for grids that fill
+    # every SM and for grids limited to 1 or 2 scan CTAs per SM
+    w = W("qwen3_32k", n=40000)
+    inp = Inputs(w, [0, 1, 2, 3], 40000)
+    r = run_gpu(inp, k=512, budget=48, regime=regime)
+    if regime == "host":
+        src_p, src_s, source = r["stage_planes"], r["stage_scales"], B.SRC_STAGING
+    elif regime == "fused":
+        src_p, src_s, source = r["planes"].cpu().pin_memory(), r["scales"].cpu().pin_memory(), B.SRC_STORE
+    else:
+        src_p, src_s, source = r["planes"], r["scales"], B.SRC_STORE
+    side = torch.cuda.Stream()
+    for per_sm in (0, 1, 2):
+        shape = B.make_shape(4, 40000, 128, 4, 512, 4, 32, 0, per_sm)
+        ws = B.alloc_workspace(shape, B.WS_SCAN_TOPK)
+        scores = torch.full((4, 4, 40000), float("nan"), device="cuda")
+        B.fathom_scan(shape, src_p, src_s, r["runs"], inp.q, ws, source=source, scores=scores)
+        ev = torch.cuda.Event()
+        ev.record()
+        side.wait_event(ev)
+        with torch.cuda.stream(side):
+            idx, sel = B.fathom_select(shape, src_p, src_s, r["runs"], inp.q, ws, source=source)
+        torch.cuda.synchronize()
+        torch.testing.assert_close(idx, r["idx"], rtol=0, atol=0)
+        torch.testing.assert_close(sel, r["sel"], rtol=0, atol=0)
+        torch.testing.assert_close(scores, r["scores"], rtol=0, atol=0)
+        # and the one-call form with the limited grid
+        idx2, sel2 = B.fathom_scan_topk(shape, src_p, src_s, r["runs"], inp.q, ws, source=source)
+        torch.cuda.synchronize()
+        torch.testing.assert_close(idx2, r["idx"], rtol=0, atol=0)
+
+
 def test_long_chunks_exercise_pruning():
     # 152 units x 64k tokens: a few chunks per unit (one full wave of CTAs over
     # 152 units), each of 8 or more sub-chunks -> in-CTA prunes
