@@ -653,8 +653,16 @@ scan_kernel(int n, int cb, int ctok, int D, int chunk_blocks, int source, size_t
     int s_cur = sm.sq0[0], s_next = sm.sq0[1], iter = 0;
 
     uint64_t tau[G];                         // per-head thresholds (same in every thread)
+    float tf[G];                             // the score part of tau (-inf: keep everything)
 #pragma unroll
-    for (int h = 0; h < G; ++h) tau[h] = 0;
+    for (int h = 0; h < G; ++h) { tau[h] = 0; tf[h] = -CUDART_INF_F; }
+    auto refresh_tf = [&]() {
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+            const uint32_t thi = (uint32_t)(tau[h] >> 32);
+            tf[h] = (thi <= order_f32(-CUDART_INF_F)) ? -CUDART_INF_F : unorder_f32(thi);
+        }
+    };
     bool first = true;
 
     // The unit's CTAs take sub-chunks in order from the counter, so they sweep the
@@ -715,6 +723,7 @@ scan_kernel(int n, int cb, int ctok, int D, int chunk_blocks, int source, size_t
             }
 #pragma unroll
             for (int h = 0; h < G; ++h) tau[h] = sm.tau[h];
+            refresh_tf();
         }
 
         Acc8<G> acc;
@@ -830,8 +839,11 @@ scan_kernel(int n, int cb, int ctok, int D, int chunk_blocks, int source, size_t
         // ---- epilogue: debug scores, forced tokens, then the candidates' keys
         const int beta = sb + bl;
         unsigned cvm = 0;                        // bit m: a candidate (valid, not forced)
+        // a block inside the sequence and clear of the forced tokens: all 8 are candidates
+        const bool interior = !kScores && bl < nblk && beta * 64 >= ns && beta * 64 + 64 <= r0 && beta * 64 + 64 <= n;
+        if (interior) cvm = 0xffu;
 #pragma unroll
-        for (int m = 0; m < 8; ++m) {
+        for (int m = 0; m < 8 && !interior; ++m) {
             const int i = beta * 64 + (int)r + 8 * (m & 3) + 32 * (m >> 2);
             const bool valid = (bl < nblk) && (i < n);
             const bool forced = (i < ns || i >= r0);
@@ -892,6 +904,7 @@ scan_kernel(int n, int cb, int ctok, int D, int chunk_blocks, int source, size_t
             }
 #pragma unroll
             for (int h = 0; h < G; ++h) tau[h] = T[h];
+            refresh_tf();
             if (tid < G) sm.tau[tid] = T[tid];
             first = false;
         }
@@ -899,12 +912,6 @@ scan_kernel(int n, int cb, int ctok, int D, int chunk_blocks, int source, size_t
             // append every key >= tau (few, about m1 .. 2 m1 per sub-chunk and head):
             // a mask of the heads whose score reaches tau's score (one float compare
             // each; tau = 0 keeps everything), then per token a short loop over them
-            float tf[G];
-#pragma unroll
-            for (int h = 0; h < G; ++h) {
-                const uint32_t thi = (uint32_t)(tau[h] >> 32);
-                tf[h] = (thi <= order_f32(-CUDART_INF_F)) ? -CUDART_INF_F : unorder_f32(thi);
-            }
 #pragma unroll
             for (int m = 0; m < 8; ++m) {
                 unsigned hm = 0;
