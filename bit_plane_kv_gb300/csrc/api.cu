@@ -5,7 +5,11 @@
 #include <stdlib.h>
 #include <string.h>
 
+#include <functional>
 #include <mutex>
+#include <queue>
+#include <utility>
+#include <vector>
 
 #include <cmath>
 
@@ -73,14 +77,51 @@ int device_sm_count() {
     return cache[dev];
 }
 
+// Makespan, in sub-chunk times, of a scan whose CTAs start in launch order as
+// resident slots free up, CTA i working on unit i % units (unit_fast) or
+// i / chunks.  A running CTA takes its unit's sub-chunks one at a time from a
+// counter it shares with the unit's other CTAs (one time unit each) and ends
+// with its fixed work (one unit: plan prologue, first threshold, final
+// shrink); a CTA that finds the counter exhausted ends at once (0.1).
+static double scan_makespan(long long units, int n_sub, int chunks, long long slots, bool unit_fast) {
+    const long long total = units * chunks;
+    std::vector<int> ctr((size_t)units, 0);
+    std::vector<char> took((size_t)total, 0);
+    using Ev = std::pair<double, long long>;
+    std::priority_queue<Ev, std::vector<Ev>, std::greater<Ev>> q;
+    long long next = 0;
+    for (; next < total && next < slots; ++next) q.push({0.0, next});
+    double end = 0.0;
+    while (!q.empty()) {
+        const Ev e = q.top();
+        q.pop();
+        const long long i = e.second;
+        const long long u = unit_fast ? i % units : i / chunks;
+        if (ctr[(size_t)u] < n_sub) {
+            ++ctr[(size_t)u];
+            took[(size_t)i] = 1;
+            q.push({e.first + 1.0, i});
+            continue;
+        }
+        const double t = e.first + (took[(size_t)i] ? 1.0 : 0.1);
+        end = t > end ? t : end;
+        if (next < total) q.push({t, next++});
+    }
+    return end;
+}
+
 ScanGrid scan_grid(const fathom_shape &s) {
-    // A unit's `chunks` CTAs share its sub-chunks (32 blocks), about
-    // ceil(n_sub / chunks) each (they take them from a counter as they go).
-    // With `slots` CTAs resident at once (SMs x resident scan CTAs per SM;
-    // 152 x 3 on GB300 when no device answers) the scan takes about
-    // waves x (sub-chunks per CTA + 1) sub-chunk times, the 1 standing for a
-    // CTA's fixed work (plan prologue, first threshold, final shrink).  Take
-    // the chunk count that minimises it (ties: fewer CTAs).
+    // A unit's `chunks` CTAs share its sub-chunks (32 blocks) through a counter,
+    // so a CTA that runs faster scores more of them.  With `slots` CTAs resident
+    // at once (SMs x resident scan CTAs per SM; 152 x 3 on GB300 when no device
+    // answers), the CTAs start in launch order as slots free up.  Launched
+    // chunk-fastest, a unit's CTAs run together and the scan takes about
+    // waves x (sub-chunks per CTA + 1) sub-chunk times.  With fewer units than
+    // slots and no chunk count that fills the slots exactly, a unit-fastest
+    // launch starts every unit at once and lets the later CTAs join the units
+    // still running (the others find their counter spent and end at once):
+    // its makespan comes from simulating that schedule.  Take the order and
+    // chunk count with the smallest time (ties: chunk-fastest, fewer CTAs).
     int sms = device_sm_count();
     if (sms <= 0) sms = 152;
     int res = scan_resident_ctas(s.G);
@@ -89,15 +130,42 @@ ScanGrid scan_grid(const fathom_shape &s) {
     const long long slots = (long long)sms * res;
     const int nb = num_blocks(s.n);
     const int n_sub = (nb + kSubBlocks - 1) / kSubBlocks;
+    const int max_chunks = n_sub < kScanMaxChunks ? n_sub : kScanMaxChunks;
     int best = 1;
-    long long best_cost = -1;
-    for (int c = 1; c <= n_sub; ++c) {
+    double best_cost = -1.0;
+    for (int c = 1; c <= max_chunks; ++c) {
         const long long waves = ((long long)s.units * c + slots - 1) / slots;
-        const long long cost = waves * ((n_sub + c - 1) / c + 1);
+        const double cost = (double)(waves * ((n_sub + c - 1) / c + 1));
         if (best_cost < 0 || cost < best_cost) { best_cost = cost; best = c; }
         if ((long long)s.units * c >= 8 * slots) break;   // more CTAs than this never pay
     }
     ScanGrid g;
+    g.unit_fast = 0;
+    if ((long long)s.units < slots && slots % s.units != 0 && (long long)s.units * n_sub <= 1000000) {
+        static std::mutex mu;
+        static long long key[16][3];
+        static int val[16];
+        static int used = 0, next_slot = 0;
+        std::lock_guard<std::mutex> lock(mu);
+        int hit = -1;
+        for (int i = 0; i < used; ++i)
+            if (key[i][0] == s.units && key[i][1] == n_sub && key[i][2] == slots) hit = i;
+        int uf_best = 0;
+        if (hit >= 0) {
+            uf_best = val[hit];
+        } else {
+            double uf_cost = best_cost;
+            const int q0 = (int)(slots / s.units) + 1;
+            for (int c = q0; c <= 4 * q0 && c <= max_chunks; ++c) {
+                const double t = scan_makespan(s.units, n_sub, c, slots, true);
+                if (t < uf_cost) { uf_cost = t; uf_best = c; }
+            }
+            const int slot_i = used < 16 ? used++ : next_slot++ % 16;
+            key[slot_i][0] = s.units; key[slot_i][1] = n_sub; key[slot_i][2] = slots;
+            val[slot_i] = uf_best;
+        }
+        if (uf_best > 0) { best = uf_best; g.unit_fast = 1; }
+    }
     g.chunks = best;
     g.chunk_blocks = ((n_sub + best - 1) / best) * kSubBlocks;   // blocks per CTA, at most
     return g;

@@ -505,7 +505,7 @@ constexpr int kMultiKPT = 4;   // register keys per thread and head for the fina
 // planes; the selection is the same.  The exact top-k of a fidelity check.
 template <int G, bool kFix, bool kScores, bool kRows>
 __global__ void __launch_bounds__(NT, (G <= 4) ? 3 : 1)
-scan_kernel(int n, int cb, int ctok, int D, int chunk_blocks, int source, size_t stage_words, size_t stage_scales,
+scan_kernel(int n, int cb, int ctok, int D, int chunks, int unit_fast, int source, size_t stage_words, size_t stage_scales,
             const uint64_t *__restrict__ planes, const uint16_t *__restrict__ scales,
             const fathom_run *__restrict__ runs, const float *__restrict__ q, int k_sel, int m_sel,
             int m_first, int ns, int r0, int nf, int cap, int vec, float *__restrict__ scores_opt,
@@ -516,17 +516,33 @@ scan_kernel(int n, int cb, int ctok, int D, int chunk_blocks, int source, size_t
     extern __shared__ __align__(16) unsigned char smem_raw[];
     ScanSmem<G> &sm = *reinterpret_cast<ScanSmem<G> *>(smem_raw);
     const int tid = threadIdx.x;
-    const int u = blockIdx.y;
-    const int chunk = blockIdx.x;
+    const int units = (int)(gridDim.x / (unsigned)chunks);
+    const int u = unit_fast ? (int)(blockIdx.x % (unsigned)units) : (int)(blockIdx.x / (unsigned)chunks);
+    const int chunk = unit_fast ? (int)(blockIdx.x / (unsigned)units) : (int)(blockIdx.x % (unsigned)chunks);
     const int nb = num_blocks(n);
-    (void)chunk_blocks;
-    const size_t cta = (size_t)u * gridDim.x + chunk;
+    const int n_sub = (nb + kSubBlocks - 1) / kSubBlocks;
+    const size_t cta = (size_t)u * chunks + chunk;
     if (kFix) {
         // second pass: only chunks the merge flagged run again, keeping their exact top-k'
         bool any = false;
         for (int h = 0; h < G; ++h) any |= flags[cta * G + h] != 0;
         if (!any) return;
         m_sel = m_first = k_sel;
+    } else {
+        // the first sub-chunk is taken before the prologue: a CTA that starts after
+        // its unit's sub-chunks are all taken publishes an empty list and ends
+        if (tid == 0) {
+            const int q0 = atomicAdd(sub_ctr + u, 1);
+            sm.sq0[0] = q0 < n_sub ? q0 : n_sub;
+        }
+        __syncthreads();
+        if (sm.sq0[0] >= n_sub) {
+            if (tid < G) {
+                cand_cnt[cta * G + tid] = 0;
+                cand_tau[cta * G + tid] = 0ull;
+            }
+            return;
+        }
     }
 
     // ---- prologue: active channels sorted by depth (desc), ties by channel:
@@ -623,7 +639,6 @@ scan_kernel(int n, int cb, int ctok, int D, int chunk_blocks, int source, size_t
     // its unit from a counter, so CTAs that run faster take more of them, and
     // records which CTA scored each one; the second pass rescans exactly the
     // sub-chunks the flagged CTA scored.
-    const int n_sub = (nb + kSubBlocks - 1) / kSubBlocks;
     auto grab = [&]() -> int {   // thread 0 only
         if (kFix) {
             for (int q2 = sm.fix_pos; q2 < n_sub; ++q2)
@@ -638,7 +653,7 @@ scan_kernel(int n, int cb, int ctok, int D, int chunk_blocks, int source, size_t
         sm.n_groups = n_groups;
         sm.two = 2u;
         sm.fix_pos = 0;
-        sm.sq0[0] = grab();
+        if (kFix) sm.sq0[0] = grab();   // (the first pass took its first sub-chunk above)
         sm.sq0[1] = sm.sq0[0] < n_sub ? grab() : n_sub;
     }
     if constexpr (kRows) {   // every channel, unscaled queries
@@ -677,10 +692,10 @@ scan_kernel(int n, int cb, int ctok, int D, int chunk_blocks, int source, size_t
     const int npl0 = 4 * g0.n4 + 3 * g0.n3 + 2 * g0.n2 + g0.n1;
     const bool piped = vec && ng == 1 && npl0 <= kPG / 2;
     // words and scales of the buffer the scan reads (store or staging), for the debug checks
-    const uint64_t src_words = (source == FATHOM_SRC_STORE) ? (uint64_t)gridDim.y * D * FATHOM_PLANES * cb
-                                                             : (uint64_t)gridDim.y * stage_words;
-    const uint64_t src_scales = (source == FATHOM_SRC_STORE) ? (uint64_t)gridDim.y * D * cb
-                                                              : (uint64_t)gridDim.y * stage_scales;
+    const uint64_t src_words = (source == FATHOM_SRC_STORE) ? (uint64_t)units * D * FATHOM_PLANES * cb
+                                                             : (uint64_t)units * stage_words;
+    const uint64_t src_scales = (source == FATHOM_SRC_STORE) ? (uint64_t)units * D * cb
+                                                              : (uint64_t)units * stage_scales;
     (void)src_words;
     (void)src_scales;
     auto stage_async = [&](int half, int sbx) {
@@ -1376,7 +1391,7 @@ static int launch_g(const fathom_shape &s, const uint64_t *planes, const uint16_
                              : (nb % 8 == 0) && (source != FATHOM_SRC_STORE || cb % 8 == 0) && aligned_src &&
                                    ((uintptr_t)planes % 16 == 0) && ((uintptr_t)scales % 16 == 0);
     const size_t smem = sizeof(ScanSmem<G>);
-    if (s.units > 65535) { set_error("scan: too many units for one launch"); return FATHOM_EINVAL; }
+    if ((long long)s.units * sg.chunks > 0x7fffffffLL) { set_error("scan: too many units for one launch"); return FATHOM_EINVAL; }
     ensure_smem(scan_kernel<G, false, false, false>, smem);
     ensure_smem(scan_kernel<G, false, true, false>, smem);
     ensure_smem(scan_kernel<G, true, false, false>, smem);
@@ -1386,7 +1401,7 @@ static int launch_g(const fathom_shape &s, const uint64_t *planes, const uint16_
     const size_t msmem = sizeof(MergeSmem);
     ensure_smem(merge_kernel, msmem);
     const int nf = f.nf > 0 ? f.nf : 1;
-    dim3 grid(sg.chunks, s.units);
+    dim3 grid((unsigned)(s.units * sg.chunks));
     cudaError_t le = cudaSuccess;
     for (int pass = 0; pass < 2; ++pass) {
         // part SCAN: the first-pass scan only; part SELECT: everything after it
@@ -1394,7 +1409,7 @@ static int launch_g(const fathom_shape &s, const uint64_t *planes, const uint16_
         const bool do_merge = part != SCAN_PART_SCAN;
 #define FATHOM_SCAN_LAUNCH(FIX, SC, RW)                                                                    \
     le = launch_pdl(scan_kernel<G, FIX, SC, RW>, grid, dim3(NT), smem, st, s.n, cb, cap_tokens(s), s.D,        \
-                    sg.chunk_blocks, source, stage_words, stage_scales, planes, scales, runs, q, k_sel, m_sel, \
+                    sg.chunks, sg.unit_fast, source, stage_words, stage_scales, planes, scales, runs, q, k_sel, m_sel, \
                     m_first, f.ns, f.r0, nf, cap, vec, SC ? scores_opt : nullptr, cand, cnt, ctau, flags,      \
                     forced, sub_ctr, sub_owner)
         if (do_scan) {
