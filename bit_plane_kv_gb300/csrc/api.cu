@@ -215,8 +215,9 @@ int scan_m_first(int n_sub, int k_sel, int m_sel) {
 }
 
 int merge_parts(int chunks, int m_sel) {
-    // lists hold between m and 2m keys after the scan's final shrink (about 1.5 m)
-    long long keys = (long long)chunks * 3 * (m_sel > 0 ? m_sel : 1) / 2;
+    // a list holds at most about 8m keys after the scan's final shrink, and
+    // typically about 3m (the first threshold lets m1 .. 2 m1 keys per sub-chunk in)
+    long long keys = (long long)chunks * 3 * (m_sel > 0 ? m_sel : 1);
     int p = (int)((keys + 8191) / 8192);
     if (p > chunks) p = chunks;
     if (p > FATHOM_MERGE_MAX_LISTS) p = FATHOM_MERGE_MAX_LISTS;

@@ -88,7 +88,6 @@ struct ScanSmem {
     GroupDesc grp[FATHOM_MAX_D / kCHG];
     int wcnt[FATHOM_PLANES + 1][FATHOM_MAX_D / 32];   // channels of each depth per warp
     int n_groups;
-    uint32_t two;                                       // 2, opaque to the compiler (see mad_u32)
     int sq0[2];                                         // first two sub-chunks of this CTA
     int sq[2];                                          // next sub-chunk of this CTA (double-buffered)
     int fix_pos;                                        // second pass: where the owner search resumes
@@ -119,38 +118,37 @@ struct Acc8 {
     __device__ __forceinline__ float operator()(int m, int h) const { return m < 4 ? v[m][h].x : v[m - 4][h].y; }
 };
 
-// d = a * b + c in the integer multiply-add unit.  The code prefixes are built
-// with shift-and-add steps; written as multiply-adds by a multiplier the
-// compiler cannot see (it is read from shared memory), they run beside the
-// float multiply-adds instead of in the integer/logic unit, which the bit
-// extraction and byte permutes already keep busy.
-__device__ __forceinline__ uint32_t mad_u32(uint32_t a, uint32_t b, uint32_t c) {
-    uint32_t d;
-    asm("mad.lo.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
-    return d;
-}
+// Rotation amounts of thread r: rot[k] = (r - k) mod 32, so that rotating a
+// plane half-word right by rot[k] moves token r + 8m (bit r + 8m) to bit
+// 8m + k, for the four tokens m = 0..3 at once.
+struct DecodeRot {
+    uint32_t rot[FATHOM_PLANES + 1];
+};
 
 // ---------------------------------------------------------------------------
 // Inner loop: channels [a_lo, a_hi) of depth T of the current group.
 // pwcol points at this thread's block in slot 0 of the staged group: slot s of
 // the block is pwcol[s * kSubBlocks] (the lanes of a warp read 4 adjacent words).
+// Byte m of y is built as 1 + sum_p b_p 2^(T - p): plane p's bit of token
+// r + 8m is rotated to bit T - p of byte m and merged in (one funnel shift and
+// one three-input logic op per plane and half word), so y's bytes are
+// 2 c_T + 1 with c_T the T-bit code prefix (at most 31: no carries).
 template <int G, int T>
 __device__ __forceinline__ void accum_depth(const uint2 *__restrict__ pwcol,
                                             const float *__restrict__ wrow, int a_lo, int a_hi,
-                                            int slot, uint32_t r, uint32_t two, Acc8<G> &acc) {
+                                            int slot, const DecodeRot &dr, Acc8<G> &acc) {
     constexpr float K = 8388608.0f + (float)(1 << T);
     const float2 negK = make_float2(-K, -K);
 #pragma unroll 1
     for (int a = a_lo; a < a_hi; ++a, slot += T) {
-        uint32_t ylo = 0, yhi = 0;
+        uint32_t ylo = 0x01010101u, yhi = 0x01010101u;
 #pragma unroll
         for (int p = 0; p < T; ++p) {
             const uint2 w = pwcol[(slot + p) * kSubBlocks];
-            ylo = mad_u32(ylo, two, (w.x >> r) & 0x01010101u);
-            yhi = mad_u32(yhi, two, (w.y >> r) & 0x01010101u);
+            const uint32_t m = 0x01010101u << (T - p);
+            ylo |= __funnelshift_r(w.x, w.x, dr.rot[T - p]) & m;
+            yhi |= __funnelshift_r(w.y, w.y, dr.rot[T - p]) & m;
         }
-        ylo = mad_u32(ylo, two, 0x01010101u);
-        yhi = mad_u32(yhi, two, 0x01010101u);
         // byte b of each half under the exponent of 2^23, minus 2^23 + 2^T (exact)
         float2 f[4];
 #pragma unroll
@@ -494,6 +492,11 @@ __device__ int prune_list(SelScratch<1> &sm, uint64_t *lst, int count, int targe
 // ---------------------------------------------------------------------------
 constexpr int kListKPT = 26;   // register keys per thread for list prunes (cap <= 26 * 256)
 constexpr int kMultiKPT = 4;   // register keys per thread and head for the final shrink
+// A first-pass list is cut back at the end only when it is longer than this many
+// times m: the merge streams longer lists for less than the cut costs (a cut at
+// 4m took 6 us of a 105 us scan of eight 1M-token units, and the merge was no
+// faster for the shorter lists).
+constexpr int kShrinkAbove = 8;
 
 // kFix = false: the first pass (histogram thresholds, no exact selection; a
 // list that would overflow publishes tau = max so that the merge flags it).
@@ -651,7 +654,6 @@ scan_kernel(int n, int cb, int ctok, int D, int chunks, int unit_fast, int sourc
     };
     if (tid == 0) {
         sm.n_groups = n_groups;
-        sm.two = 2u;
         sm.fix_pos = 0;
         if (kFix) sm.sq0[0] = grab();   // (the first pass took its first sub-chunk above)
         sm.sq0[1] = sm.sq0[0] < n_sub ? grab() : n_sub;
@@ -664,7 +666,9 @@ scan_kernel(int n, int cb, int ctok, int D, int chunks, int unit_fast, int sourc
     const int ng = sm.n_groups;
     const int bl = tid >> 3;                 // block within the sub-chunk
     const uint32_t r = (uint32_t)(tid & 7);  // token offset within a byte lane
-    const uint32_t two = sm.two;
+    DecodeRot dr;
+#pragma unroll
+    for (int k = 0; k <= FATHOM_PLANES; ++k) dr.rot[k] = (r - (uint32_t)k) & 31u;
     int s_cur = sm.sq0[0], s_next = sm.sq0[1], iter = 0;
 
     uint64_t tau[G];                         // per-head thresholds (same in every thread)
@@ -840,13 +844,13 @@ scan_kernel(int n, int cb, int ctok, int D, int chunks, int unit_fast, int sourc
                     const uint2 *pwcol = pwbase + bl;
                     const float *wrow = sm.w[bl];
                     int a = 0, slot = 0;
-                    accum_depth<G, 4>(pwcol, wrow, a, a + g.n4, slot, r, two, acc);
+                    accum_depth<G, 4>(pwcol, wrow, a, a + g.n4, slot, dr, acc);
                     a += g.n4; slot += 4 * g.n4;
-                    accum_depth<G, 3>(pwcol, wrow, a, a + g.n3, slot, r, two, acc);
+                    accum_depth<G, 3>(pwcol, wrow, a, a + g.n3, slot, dr, acc);
                     a += g.n3; slot += 3 * g.n3;
-                    accum_depth<G, 2>(pwcol, wrow, a, a + g.n2, slot, r, two, acc);
+                    accum_depth<G, 2>(pwcol, wrow, a, a + g.n2, slot, dr, acc);
                     a += g.n2; slot += 2 * g.n2;
-                    accum_depth<G, 1>(pwcol, wrow, a, a + g.n1, slot, r, two, acc);
+                    accum_depth<G, 1>(pwcol, wrow, a, a + g.n1, slot, dr, acc);
                 }
             }
         }
@@ -961,7 +965,7 @@ scan_kernel(int n, int cb, int ctok, int D, int chunks, int unit_fast, int sourc
     }
     if (piped) cp_async_wait<0>();
 
-    // ---- shrink long lists (first pass: lists longer than 4m to about m .. 2m keys
+    // ---- shrink long lists (first pass: lists longer than 8m to about m .. 2m keys
     // by one histogram pass; second pass: exactly k'), then publish counts and thresholds: every
     // key this CTA dropped is < its threshold
     if constexpr (!kFix) {
@@ -977,7 +981,7 @@ scan_kernel(int n, int cb, int ctok, int D, int chunks, int unit_fast, int sourc
             for (int h = 0; h < G; ++h) {
                 cs[h] = min(sm.cnt[h], cap);
                 fits = fits && cs[h] <= kMultiKPT * NT;
-                any_long = any_long || cs[h] > 4 * m_eff;
+                any_long = any_long || cs[h] > kShrinkAbove * m_eff;
             }
             if (fits && any_long) {
                 uint64_t *lists = cand + cta * G * (size_t)cap;

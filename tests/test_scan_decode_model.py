@@ -3,14 +3,16 @@ checked against the oracle's prefix dequantisation (CPU).
 
 The kernel's thread (block b, r in 0..7) takes tokens r + 8m + 32h of the block
 (m = 0..3, h = 0 for the low and 1 for the high 32-bit half of each plane
-word).  For a channel of depth t it forms y = (...((x_0) * 2 + x_1) * 2 ...) *
-2 + 0x01010101 with x_p = (half-word of plane p >> r) & 0x01010101, so byte m
-of y is 2 c_t + 1 for token r + 8m + 32h (at most 31: no carries between
-bytes).  A byte permute puts byte m under the exponent of 2^23, and one fp32
-subtraction of 2^23 + 2^t leaves 2 (c_t + 1/2 - 2^(t-1)) exactly; the block
-weight q * a * 2^-t then gives q times the t-plane value.  This test runs those
-integer and fp32 steps on real plane words and compares every token with the
-oracle's codes and dequantised values."""
+word).  For a channel of depth t it starts from y = 0x01010101 and, for every
+plane p < t, rotates the plane's half-word right by (r - (t - p)) mod 32 (token
+r + 8m's bit lands on bit t - p of byte m), masks bit t - p of every byte and
+ORs it into y; so byte m of y is 1 + sum_p b_p 2^(t - p) = 2 c_t + 1 for token
+r + 8m + 32h (at most 31: no carries between bytes).  A byte permute puts byte
+m under the exponent of 2^23, and one fp32 subtraction of 2^23 + 2^t leaves
+2 (c_t + 1/2 - 2^(t-1)) exactly; the block weight q * a * 2^-t then gives q
+times the t-plane value.  This test runs those integer and fp32 steps on real
+plane words and compares every token with the oracle's codes and dequantised
+values."""
 import numpy as np
 import pytest
 
@@ -19,12 +21,19 @@ from oracle import oracle as O
 MASK = np.uint32(0x01010101)
 
 
+def rotr32(x, s):
+    s = int(s) % 32
+    x = int(x)
+    return np.uint32(((x >> s) | (x << (32 - s))) & 0xFFFFFFFF) if s else np.uint32(x)
+
+
 def model_bytes(words_half, r, t):
     """y for one channel: words_half [t] uint32 half-words of planes 0..t-1."""
-    y = np.uint32(0)
+    y = MASK
     for p in range(t):
-        y = np.uint32(y * np.uint32(2) + ((words_half[p] >> np.uint32(r)) & MASK))
-    return np.uint32(y * np.uint32(2) + MASK)
+        k = t - p
+        y = np.uint32(y | (rotr32(words_half[p], (r - k) % 32) & np.uint32(int(MASK) << k)))
+    return y
 
 
 def byte_under_exponent(y, m):
@@ -60,7 +69,7 @@ def test_decode_steps_give_the_prefix_value(t):
 
 
 def test_bytes_never_carry():
-    # the largest byte after t = 4 shift-adds and the final step is 2 * 15 + 1 = 31
+    # the largest byte after t = 4 planes is 1 + 2 + 4 + 8 + 16 = 2 * 15 + 1 = 31
     w = np.full(4, 0xFFFFFFFF, np.uint32)
     y = model_bytes(w, 0, 4)
     assert int(y) == 0x1F1F1F1F
