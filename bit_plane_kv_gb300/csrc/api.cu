@@ -253,10 +253,14 @@ AttnWorkspace attn_workspace_layout(const fathom_shape &s) {
     AttnWorkspace w;
     // 128 entries of a head's kept list per CTA; 256 (fewer CTAs, each list
     // loaded and searched fewer times) once 128 would need more than two waves
+    // of two CTAs per SM; 512 (one CTA per unit and head) once that alone fills
+    // two waves (a 256-unit layer: 113 against 123 us per layer; with few
+    // units it leaves the host link under-used: 115 against 56 us for 8 units)
     int sms = device_sm_count();
     if (sms <= 0) sms = 152;
     const long long ctas128 = (long long)s.units * s.G * ((s.k + 127) / 128);
-    w.rows = ctas128 > 2LL * 2 * sms ? 256 : 128;
+    const long long ctas512 = (long long)s.units * s.G * ((s.k + 511) / 512);
+    w.rows = ctas512 >= 2LL * 2 * sms ? 512 : (ctas128 > 2LL * 2 * sms ? 256 : 128);
     w.splits = s.G * ((s.k + w.rows - 1) / w.rows);
     if (w.splits < 1) w.splits = 1;
     w.part_off = 0;

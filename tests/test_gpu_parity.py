@@ -461,3 +461,36 @@ def test_concentrated_winners_force_the_exact_second_pass():
     idx = r["idx"][0].cpu().numpy()
     free = idx[:, 4:-32]
     assert np.mean((free >= 40960) & (free < 43008)) > 0.9
+
+
+@pytest.mark.parametrize("rows", [128, 256, 512])
+def test_attention_for_each_rows_per_cta_choice(rows):
+    # The attention takes 128, 256 or 512 kept-list entries per CTA depending on how
+    # many (unit, head) pairs the call has (more pairs: fewer, longer CTAs).  Unit
+    # counts that select each choice on this device; random strictly ascending kept
+    # lists (one entry out of range per head: skipped) checked on every unit.
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    G, k, n, D = 4, 512, 2048, 128
+    per_unit128, per_unit512 = G * (k // 128), G * (k // 512)
+    units = {128: 8,
+             256: 4 * sms // per_unit128 + 1,
+             512: -(-4 * sms // per_unit512)}[rows]
+    shape = B.make_shape(units, n, D, G, k, 4, 32)
+    rng = np.random.default_rng(900 + rows)
+    kr = torch.from_numpy(rng.standard_normal((units, n, D)).astype(np.float32)).to(torch.bfloat16).cuda()
+    vr = torch.from_numpy(rng.standard_normal((units, n, D)).astype(np.float32)).to(torch.bfloat16).cuda()
+    q = torch.from_numpy(rng.standard_normal((units, G, D)).astype(np.float32)).cuda()
+    idx = np.empty((units, G, k), np.int32)
+    for u in range(units):
+        for h in range(G):
+            sel = np.sort(rng.choice(n, size=k - 1, replace=False)).astype(np.int32)
+            idx[u, h] = np.concatenate([sel, [n + 5]])       # the last entry lies outside [0, n)
+    out = B.fathom_sparse_attn(shape, kr, vr, q, torch.from_numpy(idx).cuda(),
+                               B.alloc_workspace(shape, B.WS_SPARSE_ATTN))
+    torch.cuda.synchronize()
+    for u in range(units):
+        # the oracle over the in-range entries (it reads every entry it is given)
+        ref = O.attention(u16(kr[u]), u16(vr[u]), q[u].cpu().numpy(), np.ascontiguousarray(idx[u][:, :k - 1]))
+        got = out[u].cpu().numpy().astype(np.float64)
+        rel = np.linalg.norm(got - ref, axis=1) / np.linalg.norm(ref, axis=1)
+        assert np.all(rel <= fathom_cases.ATTN_RTOL), (u, rel)
