@@ -427,8 +427,8 @@ def measure_sm_read_peak(st):
 # ncu capture of one HBM-resident host_1m layer (8 units x 2^20 tokens, B = 48) of
 # the current kernel; the bench multiplies it by the tokens a call scores to
 # estimate how close the HBM-resident scan runs to the instruction-issue bound.
-SCAN_PROFILE = {"thread_instructions_per_token": 73.03e6 * 32 / (8 << 20),
-                "dram_bytes_per_layer": 57.03e6 + 1.07e6,
+SCAN_PROFILE = {"thread_instructions_per_token": 71.59e6 * 32 / (8 << 20),
+                "dram_bytes_per_layer": 56.98e6 + 0.87e6,
                 "source": "profiles/scan_kernel_host1m_hbm.md"}
 
 
