@@ -1056,16 +1056,26 @@ scan_kernel(int n, int cb, int ctok, int D, int chunks, int unit_fast, int sourc
 // part to finish streams the P partial lists the same way, sorts the exact
 // top-k' by token index and writes it between the forced sink and recent
 // tokens.  With P = 1 the single part finishes directly.
+// Two builds of the merge: 512 threads and an 8192-key buffer (one CTA per SM:
+// for calls with few (unit, head) pairs), and 256 threads with a 2048-key
+// buffer and at most 64 registers a thread (four CTAs per SM: for calls with
+// many pairs, such as a 256-unit layer's 1024, whose merges would otherwise
+// run in seven waves).  Both compute the same result; a buffer that fills is
+// cut to its exact top-k' and streaming goes on.
 constexpr int kMThreads = 512;
 constexpr int kMBuf = 8192;                  // keys in the shared-memory buffer
-constexpr int kMKPT = kMBuf / kMThreads;     // register keys per thread for a buffer prune
+constexpr int kMThreadsS = 256;
+constexpr int kMBufS = 2048;
 
 constexpr int kMSmall = 1024;              // keys of the boundary bin ranked directly, at most
+template <int NTH, int MBUF>
 struct MergeSmem {
+    static constexpr int kThreads = NTH, kBuf = MBUF;
+    static constexpr int kKPT = MBUF / NTH;  // register keys per thread for a buffer prune
     SelScratch<1> sel;
-    uint64_t buf[kMBuf];
+    uint64_t buf[MBUF];
     uint64_t small[kMSmall];                 // the boundary bin's keys (exact selection)
-    float fred[2][kMThreads / 32];
+    float fred[2][NTH / 32];
     int bin_sel, bin_above, n_small;
     int off[FATHOM_MERGE_MAX_LISTS + 1];     // prefix sums of the streamed lists' counts
     int count;
@@ -1080,7 +1090,8 @@ struct MergeSmem {
 // bins are fine where the k-th key falls) are ranked against each other to
 // find the k-th exactly.  A bin of more than kMSmall keys (scores bunched
 // together) takes the radix select instead.  Requires count > k.
-__device__ uint64_t merge_exact_top(MergeSmem &sm, int count, int k) {
+template <class SM>
+__device__ uint64_t merge_exact_top(SM &sm, int count, int k) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
     float lo = CUDART_INF_F, hi = -CUDART_INF_F;
     for (int e = tid; e < count; e += blockDim.x) {
@@ -1128,7 +1139,7 @@ __device__ uint64_t merge_exact_top(MergeSmem &sm, int count, int k) {
     const int b = sm.bin_sel, above = sm.bin_above;
     if ((int)sm.sel.hist[0][b] > kMSmall) {   // bunched scores: radix select
         uint64_t T;
-        const int nc = prune_list<kMKPT>(sm.sel, sm.buf, count, k, 0, &T);
+        const int nc = prune_list<SM::kKPT>(sm.sel, sm.buf, count, k, 0, &T);
         __syncthreads();
         if (tid == 0) { sm.count = nc; sm.thresh = T; }
         __syncthreads();
@@ -1149,17 +1160,17 @@ __device__ uint64_t merge_exact_top(MergeSmem &sm, int count, int k) {
     __syncthreads();
     const uint64_t T = sm.thresh;
     // every key is >= T or not: keep the k keys >= T, compacted in place through registers
-    uint64_t r[kMKPT];
+    uint64_t r[SM::kKPT];
     const int used = (count + (int)blockDim.x - 1) / (int)blockDim.x;
 #pragma unroll
-    for (int i = 0; i < kMKPT; ++i) {
+    for (int i = 0; i < SM::kKPT; ++i) {
         const int e = i * (int)blockDim.x + tid;
         r[i] = (i < used && e < count) ? sm.buf[e] : 0ull;
     }
     if (tid == 0) sm.sel.new_cnt = 0;
     __syncthreads();
 #pragma unroll
-    for (int i = 0; i < kMKPT; ++i)
+    for (int i = 0; i < SM::kKPT; ++i)
         if (i < used) append_if<1>(sm.sel, (i * (int)blockDim.x + tid < count) && r[i] >= T, r[i], sm.buf, count);
     __syncthreads();
     if (tid == 0) sm.count = sm.sel.new_cnt;
@@ -1169,8 +1180,8 @@ __device__ uint64_t merge_exact_top(MergeSmem &sm, int count, int k) {
 
 // Streams `nl` lists (list l: base(l), count(l)) into sm.buf and leaves the
 // exact top-k' (or everything, if fewer) in sm.buf[0 .. sm.count).
-template <typename Base, typename Count>
-__device__ void stream_select(MergeSmem &sm, int nl, Base base, Count count, int k_sel) {
+template <class SM, typename Base, typename Count>
+__device__ void stream_select(SM &sm, int nl, Base base, Count count, int k_sel) {
     const int tid = threadIdx.x;
     // all list counts in one round of loads, then an exclusive scan by warp 0
     // (lane l sums a run of ceil(nl / 32) consecutive counts)
@@ -1199,10 +1210,10 @@ __device__ void stream_select(MergeSmem &sm, int nl, Base base, Count count, int
     const int total = sm.off[nl];
     int done = 0;
     while (done < total) {
-        int room = kMBuf - sm.count;
-        if (room < kMThreads) {              // make room: cut the buffer to its exact top-k'
+        int room = SM::kBuf - sm.count;
+        if (room < SM::kThreads) {           // make room: cut the buffer to its exact top-k'
             merge_exact_top(sm, sm.count, k_sel);
-            room = kMBuf - sm.count;
+            room = SM::kBuf - sm.count;
         }
         const int take = min(room, total - done);
         const int c0 = sm.count;
@@ -1240,7 +1251,8 @@ __device__ void stream_select(MergeSmem &sm, int nl, Base base, Count count, int
     __syncthreads();
 }
 
-__global__ void __launch_bounds__(kMThreads)
+template <int NTH, int MBUF>
+__global__ void __launch_bounds__(NTH, (NTH <= 256 ? 4 : 1))
 merge_kernel(int n, int G, int k, int k_sel, int ns, int r0, int nf, int chunks, int parts, int cap,
              int second, const uint64_t *__restrict__ cand, const int *__restrict__ cand_cnt,
              const uint64_t *__restrict__ cand_tau, int *__restrict__ flags, int *__restrict__ dirty,
@@ -1249,7 +1261,7 @@ merge_kernel(int n, int G, int k, int k_sel, int ns, int r0, int nf, int chunks,
              float *__restrict__ out_score, int *__restrict__ sub_ctr) {
     pdl_enter();
     extern __shared__ __align__(16) unsigned char msmem_raw[];
-    MergeSmem &sm = *reinterpret_cast<MergeSmem *>(msmem_raw);
+    MergeSmem<NTH, MBUF> &sm = *reinterpret_cast<MergeSmem<NTH, MBUF> *>(msmem_raw);
     const int p = blockIdx.x, h = blockIdx.y, u = blockIdx.z;
     const int tid = threadIdx.x;
     const size_t uh = (size_t)u * G + h;
@@ -1308,12 +1320,12 @@ merge_kernel(int n, int G, int k, int k_sel, int ns, int r0, int nf, int chunks,
     // bitonic sort of the k' winners by token index; padding keys 0 (index 0xffffffff) sort last
     int P2 = 1;
     while (P2 < k_sel) P2 <<= 1;
-    if (P2 <= kMThreads) {
+    if (P2 <= NTH) {
         // one key per thread: compare-exchange partners within a warp by shuffles,
         // farther ones through two alternating shared-memory buffers
         uint64_t x = (tid < sm.count) ? sm.buf[tid] : 0ull;
         __syncthreads();
-        uint64_t *xb[2] = {sm.buf, sm.buf + kMThreads};
+        uint64_t *xb[2] = {sm.buf, sm.buf + NTH};
         int pb = 0;
         for (int size = 2; size <= P2; size <<= 1) {
             for (int stride = size >> 1; stride > 0; stride >>= 1) {
@@ -1402,8 +1414,15 @@ static int launch_g(const fathom_shape &s, const uint64_t *planes, const uint16_
     ensure_smem(scan_kernel<G, false, false, true>, smem);
     ensure_smem(scan_kernel<G, false, true, true>, smem);
     ensure_smem(scan_kernel<G, true, false, true>, smem);
-    const size_t msmem = sizeof(MergeSmem);
-    ensure_smem(merge_kernel, msmem);
+    // the merge build: four 256-thread CTAs per SM once the (unit, head) pairs (times
+    // the parts of each) would fill two waves of one 512-thread CTA per SM
+    int sms = device_sm_count();
+    if (sms <= 0) sms = 152;
+    // (and k' at most half its buffer, so that a cut buffer keeps room to stream)
+    const bool small_merge = (long long)s.units * s.G * wl.parts >= 2LL * sms && k_sel <= kMBufS / 2;
+    const size_t msmem = small_merge ? sizeof(MergeSmem<kMThreadsS, kMBufS>) : sizeof(MergeSmem<kMThreads, kMBuf>);
+    if (small_merge) ensure_smem(merge_kernel<kMThreadsS, kMBufS>, msmem);
+    else ensure_smem(merge_kernel<kMThreads, kMBuf>, msmem);
     const int nf = f.nf > 0 ? f.nf : 1;
     dim3 grid((unsigned)(s.units * sg.chunks));
     cudaError_t le = cudaSuccess;
@@ -1432,10 +1451,14 @@ static int launch_g(const fathom_shape &s, const uint64_t *planes, const uint16_
         }
 #undef FATHOM_SCAN_LAUNCH
         if (!do_merge) break;
-        le = launch_pdl(merge_kernel, dim3(wl.parts, s.G, s.units), dim3(kMThreads), msmem, st, s.n, s.G, s.k, k_sel,
-                        f.ns, f.r0, nf, sg.chunks, wl.parts, cap, pass, (const uint64_t *)cand, (const int *)cnt,
-                        (const uint64_t *)ctau, flags, dirty, (const float *)forced, pkeys, pcnt, ticket, idx, score,
-                        sub_ctr);
+#define FATHOM_MERGE_LAUNCH(NTH, MBUF)                                                                    \
+    le = launch_pdl(merge_kernel<NTH, MBUF>, dim3(wl.parts, s.G, s.units), dim3(NTH), msmem, st, s.n, s.G, s.k, k_sel, \
+                    f.ns, f.r0, nf, sg.chunks, wl.parts, cap, pass, (const uint64_t *)cand, (const int *)cnt,     \
+                    (const uint64_t *)ctau, flags, dirty, (const float *)forced, pkeys, pcnt, ticket, idx, score,  \
+                    sub_ctr)
+        if (small_merge) FATHOM_MERGE_LAUNCH(kMThreadsS, kMBufS);
+        else FATHOM_MERGE_LAUNCH(kMThreads, kMBuf);
+#undef FATHOM_MERGE_LAUNCH
         if (le != cudaSuccess) { set_error("merge_kernel: %s", cudaGetErrorString(le)); return FATHOM_ECUDA; }
         const int rc = launch_status("merge_kernel");
         if (rc) return rc;

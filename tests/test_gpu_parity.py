@@ -494,3 +494,16 @@ def test_attention_for_each_rows_per_cta_choice(rows):
         got = out[u].cpu().numpy().astype(np.float64)
         rel = np.linalg.norm(got - ref, axis=1) / np.linalg.norm(ref, axis=1)
         assert np.all(rel <= fathom_cases.ATTN_RTOL), (u, rel)
+
+
+@pytest.mark.parametrize("k", [512, 36])
+def test_many_units_use_the_small_merge(k):
+    # enough (unit, head) pairs for the 256-thread merge build (four CTAs per SM):
+    # every unit's store, plan, scores, kept set and attention against the oracle
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    units = -(-2 * sms // 4)                     # 2 x SMs pairs at G = 4
+    w = W("qwen3_32k", n=4096)
+    inp = Inputs(w, range(units), 4096)
+    r = run_gpu(inp, k=k, budget=48)
+    for ui in range(units):
+        check_unit(inp, r, ui, k, 48)
