@@ -249,23 +249,42 @@ ScanWorkspace scan_workspace_layout(const fathom_shape &s) {
     return w;
 }
 
-AttnWorkspace attn_workspace_layout(const fathom_shape &s) {
-    AttnWorkspace w;
-    // 128 entries of a head's kept list per CTA; 256 (fewer CTAs, each list
-    // loaded and searched fewer times) once 128 would need more than two waves
-    // of two CTAs per SM; 512 (one CTA per unit and head) once that alone fills
-    // two waves (a 256-unit layer: 113 against 123 us per layer; with few
-    // units it leaves the host link under-used: 115 against 56 us for 8 units)
+bool is_device_memory(const void *p) {
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    return a.type == cudaMemoryTypeDevice;
+}
+
+// Kept-list entries per attention CTA for `pairs` grid rows of one head's list
+// (G heads each): 128; 256 (fewer CTAs, each list loaded and searched fewer
+// times) once 128 would need more than two waves of two CTAs per SM; 512 (one
+// CTA per grid row and head) once that alone fills two waves (a 256-unit layer:
+// 113 against 123 us; with few units it leaves the host link under-used: 115
+// against 56 us for 8 units).
+static int attn_rows_per_cta(long long units, int G, int k) {
     int sms = device_sm_count();
     if (sms <= 0) sms = 152;
-    const long long ctas128 = (long long)s.units * s.G * ((s.k + 127) / 128);
-    const long long ctas512 = (long long)s.units * s.G * ((s.k + 511) / 512);
-    w.rows = ctas512 >= 2LL * 2 * sms ? 512 : (ctas128 > 2LL * 2 * sms ? 256 : 128);
+    const long long ctas128 = units * G * ((k + 127) / 128);
+    const long long ctas512 = units * G * ((k + 511) / 512);
+    return ctas512 >= 2LL * 2 * sms ? 512 : (ctas128 > 2LL * 2 * sms ? 256 : 128);
+}
+
+AttnWorkspace attn_workspace_layout(const fathom_shape &s) {
+    AttnWorkspace w;
+    w.rows = attn_rows_per_cta(s.units, s.G, s.k);
     w.splits = s.G * ((s.k + w.rows - 1) / w.rows);
     if (w.splits < 1) w.splits = 1;
+    w.ph_rows = attn_rows_per_cta((long long)s.units * s.G, 1, s.k);
+    w.ph_splits = (s.k + w.ph_rows - 1) / w.ph_rows;
+    if (w.ph_splits < 1) w.ph_splits = 1;
+    const size_t part_union = (size_t)s.units * w.splits * s.G * (s.D + 2);
+    const size_t part_head = (size_t)s.units * s.G * w.ph_splits * (s.D + 2);
     w.part_off = 0;
-    w.ticket_off = align256((size_t)s.units * w.splits * s.G * (s.D + 2) * sizeof(float));
-    w.total = align256(w.ticket_off + (size_t)s.units * sizeof(uint32_t));
+    w.ticket_off = align256((part_union > part_head ? part_union : part_head) * sizeof(float));
+    w.total = align256(w.ticket_off + (size_t)s.units * s.G * sizeof(uint32_t));
     return w;
 }
 
@@ -281,6 +300,8 @@ AttnWorkspace dense_workspace_layout(const fathom_shape &s) {
     splits = splits > max_splits ? max_splits : splits;
     w.rows = ((s.n + splits - 1) / splits + 63) / 64 * 64;
     w.splits = (s.n + w.rows - 1) / w.rows;
+    w.ph_rows = w.rows;
+    w.ph_splits = w.splits;
     w.part_off = 0;
     w.ticket_off = align256((size_t)s.units * w.splits * s.G * (s.D + 2) * sizeof(float));
     w.total = align256(w.ticket_off + (size_t)s.units * sizeof(uint32_t));

@@ -102,6 +102,7 @@ struct ScanGrid {
 constexpr int kScanMaxChunks = 4096;
 ScanGrid scan_grid(const fathom_shape &s);
 int device_sm_count();
+bool is_device_memory(const void *p);   // device memory of some GPU (not host, not managed)
 int scan_resident_ctas(int G);   // resident scan CTAs per SM (0: no device)
 
 constexpr int kScanThreads = 256;
@@ -132,9 +133,16 @@ ScanWorkspace scan_workspace_layout(const fathom_shape &s);
 
 constexpr int kAttnThreads = 256;
 constexpr int kAttnRowsMax = 512;   // kept-list entries per CTA, at most
+// Two launch forms share one workspace: the union form (a unit's G heads in one
+// grid row: every kept row fetched once, all G dot products computed for it) and
+// the per-head form (each (unit, head) its own grid row: one dot product per
+// fetched row, rows kept by several heads fetched once per head).  The partial
+// states and the tickets are sized for whichever needs more.
 struct AttnWorkspace {
-    int rows;     // kept-list entries per CTA
+    int rows;     // kept-list entries per CTA (union form)
     int splits;
+    int ph_rows;  // the same for the per-head form (units x G rows of one head each)
+    int ph_splits;
     size_t part_off, ticket_off, total;
 };
 AttnWorkspace attn_workspace_layout(const fathom_shape &s);

@@ -341,7 +341,7 @@ __device__ __forceinline__ void attn_batch(const unsigned (&mask)[AttnBatch<G>::
 // of V per row) or channels l + 32 e (any D <= 128).
 template <int G, bool kVec, bool kPlanes>
 __global__ void __launch_bounds__(NA, G >= 8 ? 1 : 2)
-attn_kernel(int n, int ctok, int D, int k, int rows_cta, int cph, int splits, const KSource ks,
+attn_kernel(int n, int ctok, int D, int k, int rows_cta, int cph, int splits, int hdiv, const KSource ks,
             const uint16_t *__restrict__ vrows, const float *__restrict__ q,
             const int32_t *__restrict__ topk, float *__restrict__ out, float *__restrict__ part,
             unsigned *__restrict__ ticket) {
@@ -410,7 +410,8 @@ attn_kernel(int n, int ctok, int D, int k, int rows_cta, int cph, int splits, co
             mask[r] = m;
             ti[r] = i;
         }
-        attn_batch<G, kVec, kPlanes>(mask, ti, ks, vrows, u, (size_t)u * ctok, D, scale, qv, m_h, l_h, o_h, pb);
+        attn_batch<G, kVec, kPlanes>(mask, ti, ks, vrows, u / hdiv, (size_t)(u / hdiv) * ctok, D, scale, qv, m_h,
+                                     l_h, o_h, pb);
     }
     attn_finish<G, kVec>(sm, asmem_raw, lay, D, s, u, splits, m_h, l_h, o_h, out, part, ticket);
 }
@@ -511,25 +512,36 @@ static int launch_sparse_attn_src(const fathom_shape &s, const KSource &ks, cons
     char *w = (char *)ws;
     float *part = (float *)(w + wl.part_off);
     unsigned *ticket = (unsigned *)(w + wl.ticket_off);
-    if (s.units > 65535) { set_error("sparse_attn: too many units for one launch"); return FATHOM_EINVAL; }
-    const size_t smem = attn_smem_layout(s.G, s.k, s.D, wl.splits).total;
-    const int cph = (s.k + wl.rows - 1) / wl.rows;   // CTAs per head
     const bool vec = s.D == 128 && (planes || (uintptr_t)ks.rows % 8 == 0) && ((uintptr_t)vrows % 8 == 0);
-    const dim3 grid(wl.splits, s.units);
+    // Rows in device memory: one head per grid row (each (unit, head) attends its own
+    // list, one dot product per fetched row; a row kept by several heads is read once
+    // per head, which HBM affords).  Rows in host memory, or keys rebuilt from the
+    // store: the union form, every kept row fetched once for all G heads.
+    const bool per_head = !planes && s.G > 1 && (long long)s.units * s.G <= 65535 &&
+                          is_device_memory(ks.rows) && is_device_memory(vrows);
+    const int gg = per_head ? 1 : s.G;
+    const int units = per_head ? s.units * s.G : s.units;
+    const int rows = per_head ? wl.ph_rows : wl.rows;
+    const int splits = per_head ? wl.ph_splits : wl.splits;
+    const int hdiv = per_head ? s.G : 1;
+    if (units > 65535) { set_error("sparse_attn: too many units for one launch"); return FATHOM_EINVAL; }
+    const size_t smem = attn_smem_layout(gg, s.k, s.D, splits).total;
+    const int cph = (s.k + rows - 1) / rows;   // CTAs per head
+    const dim3 grid(splits, units);
 #define FATHOM_ATTN_LAUNCH(GG, VV)                                                                        \
     do {                                                                                                  \
         if (planes) {                                                                                     \
             ensure_smem(attn_kernel<GG, VV, true>, smem);                                                 \
             le = launch_pdl(attn_kernel<GG, VV, true>, grid, dim3(NA), smem, st, s.n, cap_tokens(s), s.D, s.k, \
-                            wl.rows, cph, wl.splits, ks, vrows, q, idx, out, part, ticket);               \
+                            rows, cph, splits, hdiv, ks, vrows, q, idx, out, part, ticket);               \
         } else {                                                                                          \
             ensure_smem(attn_kernel<GG, VV, false>, smem);                                                \
             le = launch_pdl(attn_kernel<GG, VV, false>, grid, dim3(NA), smem, st, s.n, cap_tokens(s), s.D,  \
-                            s.k, wl.rows, cph, wl.splits, ks, vrows, q, idx, out, part, ticket);          \
+                            s.k, rows, cph, splits, hdiv, ks, vrows, q, idx, out, part, ticket);          \
         }                                                                                                 \
     } while (0)
     cudaError_t le = cudaSuccess;
-    switch (s.G * 2 + (vec ? 1 : 0)) {
+    switch (gg * 2 + (vec ? 1 : 0)) {
         case 2: FATHOM_ATTN_LAUNCH(1, false); break;
         case 3: FATHOM_ATTN_LAUNCH(1, true); break;
         case 4: FATHOM_ATTN_LAUNCH(2, false); break;

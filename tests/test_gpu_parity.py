@@ -463,12 +463,15 @@ def test_concentrated_winners_force_the_exact_second_pass():
     assert np.mean((free >= 40960) & (free < 43008)) > 0.9
 
 
+@pytest.mark.parametrize("where", ["device", "host"])
 @pytest.mark.parametrize("rows", [128, 256, 512])
-def test_attention_for_each_rows_per_cta_choice(rows):
+def test_attention_for_each_rows_per_cta_choice(rows, where):
     # The attention takes 128, 256 or 512 kept-list entries per CTA depending on how
-    # many (unit, head) pairs the call has (more pairs: fewer, longer CTAs).  Unit
-    # counts that select each choice on this device; random strictly ascending kept
-    # lists (one entry out of range per head: skipped) checked on every unit.
+    # many (unit, head) pairs the call has (more pairs: fewer, longer CTAs), with one
+    # head per grid row when the rows are device memory and the union of the heads'
+    # rows per grid row when they are pinned host memory.  Unit counts that select
+    # each choice on this device; random strictly ascending kept lists (one entry out
+    # of range per head: skipped) checked on every unit.
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     G, k, n, D = 4, 512, 2048, 128
     per_unit128, per_unit512 = G * (k // 128), G * (k // 512)
@@ -485,6 +488,8 @@ def test_attention_for_each_rows_per_cta_choice(rows):
         for h in range(G):
             sel = np.sort(rng.choice(n, size=k - 1, replace=False)).astype(np.int32)
             idx[u, h] = np.concatenate([sel, [n + 5]])       # the last entry lies outside [0, n)
+    if where == "host":
+        kr, vr = kr.cpu().pin_memory(), vr.cpu().pin_memory()
     out = B.fathom_sparse_attn(shape, kr, vr, q, torch.from_numpy(idx).cuda(),
                                B.alloc_workspace(shape, B.WS_SPARSE_ATTN))
     torch.cuda.synchronize()
