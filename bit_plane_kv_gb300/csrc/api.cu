@@ -249,15 +249,6 @@ ScanWorkspace scan_workspace_layout(const fathom_shape &s) {
     return w;
 }
 
-bool is_device_memory(const void *p) {
-    cudaPointerAttributes a;
-    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
-        cudaGetLastError();
-        return false;
-    }
-    return a.type == cudaMemoryTypeDevice;
-}
-
 // Kept-list entries per attention CTA for `pairs` grid rows of one head's list
 // (G heads each): 128; 256 (fewer CTAs, each list loaded and searched fewer
 // times) once 128 would need more than two waves of two CTAs per SM; 512 (one

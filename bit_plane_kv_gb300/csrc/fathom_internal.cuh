@@ -102,7 +102,6 @@ struct ScanGrid {
 constexpr int kScanMaxChunks = 4096;
 ScanGrid scan_grid(const fathom_shape &s);
 int device_sm_count();
-bool is_device_memory(const void *p);   // device memory of some GPU (not host, not managed)
 int scan_resident_ctas(int G);   // resident scan CTAs per SM (0: no device)
 
 constexpr int kScanThreads = 256;

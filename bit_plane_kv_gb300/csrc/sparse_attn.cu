@@ -513,12 +513,15 @@ static int launch_sparse_attn_src(const fathom_shape &s, const KSource &ks, cons
     float *part = (float *)(w + wl.part_off);
     unsigned *ticket = (unsigned *)(w + wl.ticket_off);
     const bool vec = s.D == 128 && (planes || (uintptr_t)ks.rows % 8 == 0) && ((uintptr_t)vrows % 8 == 0);
-    // Rows in device memory: one head per grid row (each (unit, head) attends its own
-    // list, one dot product per fetched row; a row kept by several heads is read once
-    // per head, which HBM affords).  Rows in host memory, or keys rebuilt from the
-    // store: the union form, every kept row fetched once for all G heads.
-    const bool per_head = !planes && s.G > 1 && (long long)s.units * s.G <= 65535 &&
-                          is_device_memory(ks.rows) && is_device_memory(vrows);
+    // One head per grid row: each (unit, head) attends its own list with one dot
+    // product per fetched row; a row kept by several heads (about a tenth of them) is
+    // read once per head.  Faster for rows in HBM (a 256-unit layer: 72 against 113
+    // us) and in pinned host memory (an 8-unit 1M-token layer: 54 against 60-73 us),
+    // where the union form's G dot products per row delayed the next rows' loads.  The
+    // union form (every kept row fetched once for all G heads) stays for keys rebuilt
+    // from the store, whose rebuild costs more than the arithmetic, and for calls
+    // with more than 65535 (unit, head) pairs.
+    const bool per_head = !planes && s.G > 1 && (long long)s.units * s.G <= 65535;
     const int gg = per_head ? 1 : s.G;
     const int units = per_head ? s.units * s.G : s.units;
     const int rows = per_head ? wl.ph_rows : wl.rows;

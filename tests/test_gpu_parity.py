@@ -467,11 +467,10 @@ def test_concentrated_winners_force_the_exact_second_pass():
 @pytest.mark.parametrize("rows", [128, 256, 512])
 def test_attention_for_each_rows_per_cta_choice(rows, where):
     # The attention takes 128, 256 or 512 kept-list entries per CTA depending on how
-    # many (unit, head) pairs the call has (more pairs: fewer, longer CTAs), with one
-    # head per grid row when the rows are device memory and the union of the heads'
-    # rows per grid row when they are pinned host memory.  Unit counts that select
-    # each choice on this device; random strictly ascending kept lists (one entry out
-    # of range per head: skipped) checked on every unit.
+    # many (unit, head) pairs the call has (more pairs: fewer, longer CTAs).  Unit
+    # counts that select each choice on this device, rows in device and in pinned
+    # host memory; random strictly ascending kept lists (one entry out of range per
+    # head: skipped) checked on every unit.
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     G, k, n, D = 4, 512, 2048, 128
     per_unit128, per_unit512 = G * (k // 128), G * (k // 512)
@@ -512,3 +511,25 @@ def test_many_units_use_the_small_merge(k):
     r = run_gpu(inp, k=k, budget=48)
     for ui in range(units):
         check_unit(inp, r, ui, k, 48)
+
+
+def test_attention_union_form_beyond_the_grid_limit():
+    # more than 65535 (unit, head) pairs: the attention falls back to one grid row
+    # per unit (the union of its heads' kept rows, fetched once for all G heads)
+    G, k, n, D = 4, 40, 64, 128
+    units = 65536 // G + 3
+    shape = B.make_shape(units, n, D, G, k, 4, 4)
+    g = torch.Generator(device="cuda").manual_seed(31)
+    kr = torch.randn(units, n, D, device="cuda", generator=g).to(torch.bfloat16)
+    vr = torch.randn(units, n, D, device="cuda", generator=g).to(torch.bfloat16)
+    q = torch.randn(units, G, D, device="cuda", generator=g)
+    idx = torch.stack([torch.stack([torch.randperm(n, device="cuda", generator=g)[:k].sort().values
+                                    for _ in range(G)]) for _ in range(8)]).int()
+    idx = idx.repeat((units + 7) // 8, 1, 1)[:units].contiguous()
+    out = B.fathom_sparse_attn(shape, kr, vr, q, idx, B.alloc_workspace(shape, B.WS_SPARSE_ATTN))
+    torch.cuda.synchronize()
+    for u in (0, 1, units // 2, units - 1):
+        ref = O.attention(u16(kr[u]), u16(vr[u]), q[u].cpu().numpy(), idx[u].cpu().numpy())
+        got = out[u].cpu().numpy().astype(np.float64)
+        rel = np.linalg.norm(got - ref, axis=1) / np.linalg.norm(ref, axis=1)
+        assert np.all(rel <= fathom_cases.ATTN_RTOL), (u, rel)
