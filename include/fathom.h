@@ -371,11 +371,14 @@ int fathom_set_overlap(int32_t rows, int32_t k, const int32_t *a, const int32_t 
 int fathom_greedy_budgets(int32_t layers, int32_t levels, const double *err, int32_t b_min,
                           int32_t step, int32_t b_mean, int32_t *budgets);
 
-/* Exact sparse attention over the winners (§1, §2, §3.1).  Per unit, the
- * union of the G heads' kept sets is fetched once at full precision (bf16 K
- * and V rows; at most G * k rows), and per head
+/* Exact sparse attention over the winners (§1, §2, §3.1).  The winners' rows
+ * are fetched at full precision (bf16 K and V rows; at most G * k per unit),
+ * and per head
  *   o_h = sum_{i in S_h} softmax_i(q_h . k_i / sqrt(D)) v_i
- * with fp32 accumulation and no mass for unselected tokens.
+ * with fp32 accumulation and no mass for unselected tokens.  Each head reads
+ * the rows of its own kept set, so a row kept by several heads is read once
+ * per head (calls with more than 65535 (unit, head) pairs read the union of a
+ * unit's kept sets once instead).
  *   k_rows, v_rows [units][C][D] bf16 bit patterns (device or pinned host)
  *   q [units][G][D] fp32, topk_idx [units][G][k] int32, each row strictly
  *   ascending as fathom_scan_topk writes it (other rows give an unspecified
