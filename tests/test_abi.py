@@ -98,6 +98,31 @@ def test_workspace_sizes_scale_with_shape(lib):
     assert B.workspace_size(big, 4) == 0
 
 
+def _attn_rows(pairs, k, sms=152):
+    # kept-list entries per attention CTA for `pairs` grid rows of one head (the
+    # library's rule; without a device it assumes 152 SMs)
+    ctas128 = pairs * -(-k // 128)
+    ctas512 = pairs * -(-k // 512)
+    return 512 if ctas512 >= 4 * sms else (256 if ctas128 > 4 * sms else 128)
+
+
+@pytest.mark.parametrize("units,G,k,D", [(1, 4, 64, 128), (8, 4, 512, 128), (39, 4, 512, 128), (152, 4, 512, 128),
+                                         (256, 4, 512, 128), (16387, 4, 40, 128), (3, 8, 2048, 98), (5, 2, 300, 64)])
+def test_attention_workspace_covers_both_launch_forms(lib, units, G, k, D):
+    # the union form (one grid row per unit, G heads) and the per-head form (one grid
+    # row per unit and head) share one workspace: partial states of whichever needs
+    # more, then a ticket per (unit, head)
+    shape = B.make_shape(units, 4096, D, G, k)
+    ru = _attn_rows(units * G, k)                  # union form: units rows of G heads each
+    rh = _attn_rows(units * G, k)                  # per-head form: units x G rows of one head
+    splits_union = G * -(-k // ru)
+    splits_head = -(-k // rh)
+    part = max(units * splits_union * G, units * G * splits_head) * (D + 2) * 4
+    align = lambda x: (x + 255) // 256 * 256
+    need = align(align(part) + units * G * 4)
+    assert B.workspace_size(shape, 1) == need
+
+
 def test_fidelity_reference_calls_validate_arguments(lib):
     d = ctypes.c_void_p(256)
     s = B.make_shape(2, 4096, 128, 4, 64)
