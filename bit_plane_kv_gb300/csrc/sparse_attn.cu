@@ -33,10 +33,12 @@ struct KSource {
     int cb;
 };
 
-// Rows per warp batch: RB rows x G heads = S dot products, reduced together.
+// Rows per warp batch: RB rows x G heads = S dot products, reduced together
+// (16 rows for one head per grid row: twice the loads in flight, and the
+// batch's reduction and softmax update spread over twice the rows).
 template <int G>
 struct AttnBatch {
-    static constexpr int RB = (32 / G) < 8 ? (32 / G) : 8;
+    static constexpr int RB = G == 1 ? 16 : ((32 / G) < 8 ? (32 / G) : 8);
     static constexpr int S = RB * G;   // <= 32, a power of two
 };
 
