@@ -221,3 +221,92 @@ def test_debug_status_reports_a_build_without_checks(lib):
     assert list(out) == [0, 0, 0]
     assert rc_msg(lib, lib.fathom_debug_status(3, ctypes.cast(out, ctypes.c_void_p)))[0] == 1
     assert rc_msg(lib, lib.fathom_debug_status(0, None)) == (1, "first_failure is NULL")
+
+
+# ---- the scan's grid choice, seen through the workspace size (host logic, no device:
+# the library then assumes 152 SMs with 3 resident scan CTAs each)
+def _scan_makespan(units, n_sub, chunks, slots, unit_fast):
+    import heapq
+    total = units * chunks
+    ctr = [0] * units
+    took = [False] * total
+    q = [(0.0, i) for i in range(min(total, slots))]
+    heapq.heapify(q)
+    nxt, end = min(total, slots), 0.0
+    while q:
+        t, i = heapq.heappop(q)
+        u = i % units if unit_fast else i // chunks
+        if ctr[u] < n_sub:
+            ctr[u] += 1
+            took[i] = True
+            heapq.heappush(q, (t + 1.0, i))
+            continue
+        t2 = t + (1.0 if took[i] else 0.1)
+        end = max(end, t2)
+        if nxt < total:
+            heapq.heappush(q, (t2, nxt))
+            nxt += 1
+    return end
+
+
+def _scan_chunks(units, n, slots=152 * 3):
+    n_sub = -(-(-(-n // 64)) // 32)
+    best, best_cost = 1, None
+    for c in range(1, min(n_sub, 4096) + 1):
+        waves = -(-(units * c) // slots)
+        cost = waves * (-(-n_sub // c) + 1)
+        if best_cost is None or cost < best_cost:
+            best, best_cost = c, cost
+        if units * c >= 8 * slots:
+            break
+    if units < slots and slots % units and units * n_sub <= 1000000:
+        q0 = slots // units + 1
+        uf_cost, uf_best = best_cost, 0
+        for c in range(q0, min(4 * q0, n_sub, 4096) + 1):
+            t = _scan_makespan(units, n_sub, c, slots, True)
+            if t < uf_cost:
+                uf_cost, uf_best = t, c
+        if uf_best:
+            best = uf_best
+    return best
+
+
+def _scan_ws(units, n, G, k, chunks, n_sink=4, n_recent=32):
+    a = lambda x: (x + 255) // 256 * 256
+    ns = min(n_sink, n)
+    r0 = max(ns, n - n_recent)
+    nf = ns + n - r0
+    ksel = max(k - nf, 0)
+    cap = a(ksel + 256 + 2 * 2048)
+    ks1 = max(ksel, 1)
+    m = min(max(-(-4 * ks1 // chunks), 32), ks1)
+    parts = max(min(-(-(chunks * 3 * m) // 8192), chunks, 1024), 1)
+    ctas, uh = units * chunks, units * G
+    off = a(ctas * G * cap * 8)
+    off = a(off + ctas * G * 4)
+    off = a(off + ctas * G * 8)
+    off = a(off + ctas * G * 4)
+    off = a(off + uh * max(nf, 1) * 4)
+    off = a(off + uh * parts * ks1 * 8)
+    off = a(off + uh * parts * 4)
+    off = a(off + uh * 4)
+    off = a(off + uh * 4)
+    n_sub = -(-(-(-n // 64)) // 32)
+    off = a(off + units * 4)
+    return a(off + units * n_sub * 4)
+
+
+@pytest.mark.parametrize("units,n", [(8, 1 << 20), (8, 1 << 15), (256, 1 << 16), (300, 1 << 16), (100, 1 << 17),
+                                     (2048, 1 << 16), (1, 4096), (24, 1 << 20)])
+def test_scan_grid_choice_matches_a_simulation_of_the_schedule(lib, units, n):
+    # the chunk count behind the workspace size is the one a direct simulation of
+    # the shared sub-chunk counters picks (unit-fastest launch only where the units
+    # do not fill the resident slots evenly); for 256 units of 64k tokens it is the
+    # unit-fastest launch with 8 CTAs per unit
+    G, k = 4, 512
+    shape = B.make_shape(units, n, 128, G, k)
+    got = B.workspace_size(shape, 0)
+    c = _scan_chunks(units, n)
+    assert got == _scan_ws(units, n, G, k, c), (units, n, c)
+    if (units, n) == (256, 1 << 16):
+        assert c == 8
