@@ -3,7 +3,9 @@
 // by the G query heads, §2 forced sink/recent tokens, §7 one multiply-add per
 // active channel, token and head).
 //
-// Grid: (chunks, units).  A CTA streams sub-chunks of 32 blocks (2048 tokens)
+// Grid: units x chunks CTAs, one-dimensional (chunk-fastest, or unit-fastest
+// when the units do not fill the resident slots evenly; see scan_grid).  A CTA
+// streams sub-chunks of 32 blocks (2048 tokens)
 // of its unit, taking the next one from a per-unit counter as it goes (so a
 // CTA that runs faster scores more of them).  For each sub-chunk the planned
 // plane words of the active channels (grouped so that at most 64 planes are
@@ -11,10 +13,11 @@
 // each thread scores 8 tokens of one block for all G heads:
 //
 //   thread (block b, r in 0..7) takes tokens r, r+8, r+16, r+24 from the low
-//   and the high 32-bit half of every plane word.  (w >> r) & 0x01010101
-//   puts those four tokens' bits in four byte lanes; t shift-and-add steps
-//   over a channel's t planes build the t-bit code prefixes c_t byte-wise,
-//   one more step makes every byte 2 c_t + 1 (at most 31, so no carries);
+//   and the high 32-bit half of every plane word.  Rotating plane p's half
+//   word right by (r - (t - p)) mod 32 puts those four tokens' bits on bit
+//   t - p of four byte lanes; merged under a mask into 0x01010101, the t planes
+//   make every byte 2 c_t + 1 (c_t the t-bit code prefix; at most 31, so no
+//   carries);
 //   a byte permute drops one byte under the exponent of 2^23 and one fp32
 //   subtraction of 2^23 + 2^t gives exactly 2 (c_t + 0.5 - 2^(t-1)).  With
 //   the block weight w_hj = q_hj * a_j * 2^-t, one fma per head adds
@@ -31,7 +34,7 @@
 // at least m1 of the sub-chunk's keys, lie at or above it), m1 being a tail
 // bound of the winners a sub-chunk holds (P <= 1e-6 that it holds more, for
 // winners spread over the sequence; at least 8); at the end a list
-// longer than 4m is cut back to m .. 2m keys, m being four times the CTA's
+// longer than 8m is cut back to m .. 2m keys, m being four times the CTA's
 // expected share of the k' winners for the sub-chunks it scored.  The merge kernel streams
 // the lists through shared memory (P CTAs per (unit, head), the last of
 // which, by an atomic ticket, merges the P partial results), selects the

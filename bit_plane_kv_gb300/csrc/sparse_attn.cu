@@ -1,19 +1,24 @@
 // sparse_attn.cu -- exact attention over the winners (Fathom §1 / §3.1: the
-// union of the G heads' winners, k_union <= G k rows, is fetched once at full
-// precision; §2: each head attends exactly over its own selected set, with no
-// mass redistribution for the rest).
+// winners' rows at full precision; §2: each head attends exactly over its own
+// selected set, with no mass redistribution for the rest).
 //
-// Grid: (G * ceil(k / R), units).  CTA (h, c) takes entries
-// [c R, c R + R) of head h's sorted kept list and handles the rows that h
-// owns -- the rows no lower head lists -- so every row of the union is
-// fetched exactly once.  The CTA first finds, for its R rows, which other
-// heads list them (one binary search per (row, head) pair, all threads at
-// once).  Each warp then loads a batch of rows (K and V, bf16) and computes
-// the G dot products of every row in the batch with one transpose reduction
-// across the warp, updates an online softmax state (running max, sum,
-// weighted V) per head, and the CTA merges its warps into one partial state
-// per head.  The last CTA of the unit (an atomic ticket, no waiting) merges
-// the partial states of all CTAs of the unit and writes o_h.
+// Two launch forms of one kernel.  One head per grid row (the usual one): the
+// kernel runs with G = 1 over units x G grid rows, row (u, h) reading unit u's
+// K and V rows with head h's query and kept list; CTA c of a row takes entries
+// [c R, c R + R) of the list, and a row kept by several heads is read once per
+// head.  The union form (keys rebuilt from the store, or more than 65535
+// (unit, head) pairs): grid (G * ceil(k / R), units), CTA (h, c) takes entries
+// [c R, c R + R) of head h's list and handles the rows that h owns -- the rows
+// no lower head lists -- so every row of the union is fetched exactly once; the
+// CTA first finds, for its R rows, which other heads list them (one binary
+// search per (row, head) pair, all threads at once).  In both forms each warp
+// loads a batch of rows (K and V, bf16) and computes the dot products of every
+// (row, head) slot of the batch with one transpose reduction across the warp,
+// updates an online softmax state (running max, sum, weighted V) per head, and
+// the CTA merges its warps into one partial state per head.  The last CTA of
+// the grid row (an atomic ticket, no waiting) merges the partial states of all
+// CTAs of the row and writes o_h.
+
 #include <mutex>
 
 #include "fathom_internal.cuh"
