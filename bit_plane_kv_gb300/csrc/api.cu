@@ -167,7 +167,6 @@ ScanGrid scan_grid(const fathom_shape &s) {
         if (uf_best > 0) { best = uf_best; g.unit_fast = 1; }
     }
     g.chunks = best;
-    g.chunk_blocks = ((n_sub + best - 1) / best) * kSubBlocks;   // blocks per CTA, at most
     return g;
 }
 

@@ -89,14 +89,12 @@ __host__ __device__ inline Forced forced_range(int n, int n_sink, int n_recent) 
     return f;
 }
 
-// Scan decomposition: `chunks` CTAs per unit share its 32-block sub-chunks;
-// `chunk_blocks` is the blocks one CTA gets when they are shared evenly.  The
+// Scan decomposition: `chunks` CTAs per unit share its 32-block sub-chunks.  The
 // grid is one-dimensional, units x chunks CTAs; CTA i works on unit i / chunks
 // (chunk i % chunks), or with unit_fast on unit i % units (chunk i / units),
 // so that every unit has a CTA among the first to start.
 struct ScanGrid {
     int chunks;
-    int chunk_blocks;
     int unit_fast;
 };
 constexpr int kScanMaxChunks = 4096;

@@ -86,6 +86,7 @@ gather_kernel(int D, int nb, int cb, int x_planes, int x_total, const uint64_t *
                     const size_t seg = (cb == nb) ? hi - d : min(hi - d, nb - o);
                     const size_t src0 = p * cb + o;
                     const size_t sidx = (size_t)u * D * FATHOM_PLANES * cb + r[j].src_word + src0;
+                    (void)sidx;   // read by the debug build's checks only
                     if (FATHOM_CHECK(sidx + seg <= (size_t)gridDim.y * D * FATHOM_PLANES * cb, kDbgGatherSrc, sidx) &&
                         FATHOM_CHECK(d + seg <= stage_words, kDbgGatherDst, d + seg))
                         copy_span<uint64_t, uint4>(sbase + src0, stage_planes + (size_t)u * stage_words + d,
@@ -96,6 +97,7 @@ gather_kernel(int D, int nb, int cb, int x_planes, int x_total, const uint64_t *
             } else {
                 const size_t src0 = r[j].src_scale + (lo - rs);
                 const size_t sidx = (size_t)u * D * cb + src0;
+                (void)sidx;   // read by the debug build's checks only
                 if (FATHOM_CHECK(sidx + (hi - lo) <= (size_t)gridDim.y * D * cb, kDbgGatherSrc, sidx) &&
                     FATHOM_CHECK(hi <= stage_scales_n, kDbgGatherDst, hi))
                     copy_span<uint16_t, uint4>(store_scales + (size_t)u * D * cb + src0,
